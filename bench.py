@@ -1,0 +1,491 @@
+"""Benchmark of segment-relocated MLA attention (RedKnot-MLA online step).
+
+One step = one forward of the whole path (plan built once, outside the timed
+region) over the 128K long-context workload: 48 shuffled 2048-row document
+latents + a 32768-row recomputed tail, H = 128 (112 Local / 16 Global),
+d_nope = 512, d_rope = 64, sink 4, window 256, 25 % protected budget.
+
+Prints ONE JSON line.  `value` is algorithmic attention TFLOP/s (2 d_k +
+2 d_v FLOP per attended query-key pair); the decode-shaped batch (64
+requests, split over segments) is reported alongside in HBM GB/s.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("seg-relocated MLA attention TFLOP/s & % bf16 peak (1×GB300); "
+          "decode HBM GB/s")
+WORKLOAD = "ctx128k"
+WORKLOAD_DESC = ("128K long context: 48 x 2048-row latents (shuffled) + 32768 new rows, "
+                 "H=128 (112 Local/16 Global), d_nope=512, d_rope=64, sink=4, w=256, "
+                 "protected budget 25%, bf16 N(0,1)/sqrt(576), seed 0")
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return dict(FALLBACK), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "position_independent_kv_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        d = json.load(open(p))
+        e = d.get(f"{kernel}:{workload}")
+        if e and e.get("source_hash") == kernel_source_hash():
+            return e.get("dram_bytes_per_launch")
+    except Exception:
+        return None
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.f = None
+
+    def _bus_id(self):
+        import torch
+        try:
+            pr = torch.cuda.get_device_properties(self.dev)
+            return "%08x:%02x:%02x.0" % (pr.pci_domain_id, pr.pci_bus_id, pr.pci_device_id)
+        except Exception:
+            return None
+
+    def start(self):
+        try:
+            self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            cmd = ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                   "-lms", "200"]
+            bus = self._bus_id()
+            if bus:
+                cmd += ["-i", bus]
+            self.proc = subprocess.Popen(cmd, stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.flush()
+        self.f.seek(0)
+        rows = [l.strip().split(",") for l in self.f.read().splitlines() if l.strip()]
+        os.unlink(self.f.name)
+        sm, smax, pw, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+                pw.append(float(r[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "power_w_max": max(pw), "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# --------------------------------------------------------------------------
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def setup(args):
+    import torch
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def prefill_flops(info, d_nope, d_rope):
+    per_pair = 2 * (d_nope + d_rope) + 2 * d_nope
+    return per_pair * (info["pairs_global"] + info["pairs_local"]), per_pair * info["performed_pairs"]
+
+
+def decode_bytes(wl):
+    tot = 0
+    for r in wl.requests:
+        tot += r.T * wl.d_k * 2
+        tot += wl.H * (wl.d_k * 2 + wl.d_v * 2 + 4)
+    return tot
+
+
+def bench_prefill(args, ws, local, pk):
+    import torch
+    from position_independent_kv_gb300 import binding as B
+    from position_independent_kv_gb300.protected import build_bitmap
+    from position_independent_kv_gb300.workloads import make_workload
+
+    dev = torch.device("cuda", local)
+    wl = make_workload(args.workload, seed=0, device=dev)
+    bm, _ = build_bitmap(wl)
+    stream = torch.cuda.current_stream(dev)
+    plan = B.SegAttnPlan.from_workload(wl, bitmap=bm, stream=stream)
+    info = plan.info
+    ws_buf = None
+    if plan.workspace_bytes:
+        ws_buf = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
+    out, lse = wl.out_init, wl.lse_init          # forward overwrites in place
+    alg_flops, perf_flops = prefill_flops(info, wl.d_nope, wl.d_rope)
+
+    for _ in range(args.warmup):
+        plan.forward(wl.q, out, lse, ws_buf, stream=stream)
+    torch.cuda.synchronize(dev)
+    if plan.device_status(stream=stream) != 0:
+        raise RuntimeError("device status error during warm-up")
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(ws)
+    torch.cuda.synchronize(dev)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        plan.forward(wl.q, out, lse, ws_buf, stream=stream)
+        ev[i][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    clk = clocks.stop()
+    total_ms = t0.elapsed_time(t1)
+    launch_ms = [a.elapsed_time(b) for a, b in ev]
+    if plan.device_status(stream=stream) != 0:
+        raise RuntimeError("device status error in the timed region")
+
+    res = dict(total_ms=total_ms, launch_ms=launch_ms, info=info, alg_flops=alg_flops,
+               perf_flops=perf_flops, clocks=clk,
+               launches_per_step=(1 if info["dense_tiles"] else 0) + (1 if info["split_chunks"] else 0))
+
+    # end to end through the C ABI with host buffers (pinned), copies inside
+    if not args.no_e2e:
+        h_q = torch.empty(wl.q.shape, dtype=wl.q.dtype, pin_memory=True)
+        h_q.copy_(wl.q)
+        h_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        h_out.copy_(out)
+        h_lse = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+        h_lse.copy_(lse)
+        h_lat = torch.empty(wl.latent_pool.shape, dtype=wl.latent_pool.dtype, pin_memory=True)
+        h_lat.copy_(wl.latent_pool)
+        torch.cuda.synchronize(dev)
+        h2d = sum(t.numel() * t.element_size() for t in (h_q, h_out, h_lse, h_lat))
+        d2h = out.numel() * out.element_size() + lse.numel() * lse.element_size()
+        steps = max(1, min(args.steps, 3))
+        barrier(ws)
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            wl.q.copy_(h_q, non_blocking=True)
+            out.copy_(h_out, non_blocking=True)
+            lse.copy_(h_lse, non_blocking=True)
+            wl.latent_pool.copy_(h_lat, non_blocking=True)
+            plan.forward(wl.q, out, lse, ws_buf, stream=stream)
+            h_out.copy_(out, non_blocking=True)
+            h_lse.copy_(lse, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(ws)
+        res["e2e_ms"] = e0.elapsed_time(e1) / steps
+        res["h2d"] = h2d
+        res["d2h"] = d2h
+        del h_q, h_out, h_lse, h_lat
+    plan.close()
+    res["wl"] = wl
+    return res
+
+
+def bench_decode(args, local):
+    import torch
+    from position_independent_kv_gb300 import binding as B
+    from position_independent_kv_gb300.protected import build_bitmap
+    from position_independent_kv_gb300.workloads import make_workload
+
+    dev = torch.device("cuda", local)
+    wl = make_workload("decode", seed=0, device=dev)
+    bm, _ = build_bitmap(wl)
+    stream = torch.cuda.current_stream(dev)
+    plan = B.SegAttnPlan.from_workload(wl, bitmap=bm, stream=stream)
+    ws_buf = torch.empty(max(16, plan.workspace_bytes), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    out, lse = wl.out_init, wl.lse_init
+    for _ in range(5):
+        plan.forward(wl.q, out, lse, ws_buf, stream=stream)
+    torch.cuda.synchronize(dev)
+    times = []
+    for _ in range(20):
+        flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        plan.forward(wl.q, out, lse, ws_buf, stream=stream)
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        times.append(a.elapsed_time(b))
+    ok = plan.device_status(stream=stream) == 0
+    byt = decode_bytes(wl)
+    ms = statistics.median(times)
+    info = plan.info
+    plan.close()
+    del flush
+    return dict(ms=ms, bytes=byt, gbs=byt / (ms * 1e-3) / 1e9, ok=ok, info=info)
+
+
+def cpu_baseline(wl, budget_s: float = 20.0):
+    """The fp64 oracle on a bounded, stratified sample of the workload's rows
+    (host cores; relocation of all keys included in the time)."""
+    import torch
+    import oracle as O
+    from position_independent_kv_gb300.protected import build_bitmap
+    bm, prot_rows = build_bitmap(wl)
+    req = wl.requests[0]
+    rng = np.random.default_rng(0)
+    t_start = time.perf_counter()
+    segs = [(s.latent.double().cpu().numpy(), s.delta, s.is_new) for s in req.segments]
+    allp = np.arange(req.q_row_begin, req.T)
+    order = rng.permutation(allp)
+    rows_done, pairs, i = 0, 0, 0
+    K, V = O.relocate([(l, d) for l, d, _ in segs], req.T, wl.d_nope, wl.rope_base)
+    t_reloc = time.perf_counter() - t_start
+    glob = np.nonzero(wl.head_role)[0]
+    loc = np.nonzero(wl.head_role == 0)[0]
+    new = np.zeros(req.T, bool)
+    for s in req.segments:
+        if s.is_new:
+            new[s.delta:s.delta + s.n] = True
+    prot = prot_rows[0] | new
+    while time.perf_counter() - t_start < budget_s and i < len(order):
+        p = int(order[i])
+        i += 1
+        q = wl.q[p - req.q_row_begin].double().cpu().numpy()
+        O.attend(q[glob], K[:p + 1], V[:p + 1], wl.scale)
+        pairs += len(glob) * (p + 1)
+        if prot[p] and len(loc):
+            keys = O.visible_keys(p, False, wl.sink, wl.window)
+            O.attend(q[loc], K[keys], V[keys], wl.scale)
+            pairs += len(loc) * len(keys)
+        rows_done += 1
+    el = time.perf_counter() - t_start
+    per_pair = 2 * wl.d_k + 2 * wl.d_v
+    return {"value": pairs * per_pair / el / 1e12, "unit": "TFLOP/s",
+            "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{rows_done} random rows of the {wl.name} workload (all heads each), "
+                      f"fp64 NumPy, key relocation ({t_reloc:.1f}s) included, {el:.1f}s"}
+
+
+def run_ours(args):
+    import torch
+    ws, rank, local = setup(args)
+    pk, pk_kind = peaks()
+    if rank == 0:
+        from position_independent_kv_gb300 import build as BUILD
+        BUILD.build()
+    barrier(ws)
+    res = bench_prefill(args, ws, local, pk)
+    ms_step = max_over_ranks(res["total_ms"] / args.steps, ws)
+    flops_all = sum_over_ranks(res["alg_flops"], ws)
+    value = flops_all / (ms_step * 1e-3) / 1e12
+    perf_value = sum_over_ranks(res["perf_flops"], ws) / (ms_step * 1e-3) / 1e12
+    launch_ms = statistics.mean(res["launch_ms"])
+    achieved = res["alg_flops"] / (launch_ms * 1e-3) / 1e12
+    e2e = None
+    if "e2e_ms" in res:
+        e2e_ms = max_over_ranks(res["e2e_ms"], ws)
+        e2e = {"value": flops_all / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": int(res["h2d"]), "d2h_bytes_per_step": int(res["d2h"]),
+               "ms_per_step": e2e_ms}
+    wl = res.pop("wl")
+    dec = None
+    if not args.no_decode:
+        dec = bench_decode(args, local)
+    line = None
+    if rank == 0:
+        info = res["info"]
+        kernel = "tcgen05" if info["kernel"] == 1 else "mma_sync"
+        peak = pk["bf16_tflops"]
+        line = {
+            "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD_DESC, "name": args.workload,
+                       "parallelism": f"replicas{ws}",
+                       "l2": "inputs larger than L2 (Q 19.3 GB + O 17.2 GB per step), no flush",
+                       "kernel": kernel, "dense_tiles": info["dense_tiles"],
+                       "pairs_global": info["pairs_global"], "pairs_local": info["pairs_local"],
+                       "performed_pairs": info["performed_pairs"]},
+            "performed_tflops": round(perf_value, 3),
+            "performed_frac_of_peak": round(perf_value / ws / peak, 4),
+            "pairs_per_s": (info["pairs_global"] + info["pairs_local"]) * ws / (ms_step * 1e-3),
+            "roofline": {"bound": "tensor", "achieved": round(achieved, 3), "peak": peak,
+                         "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                         "peak_kind": f"{pk_kind} bf16 burst",
+                         "frac_of_sustained": round(achieved / pk.get("bf16_tflops_sustained", peak), 4),
+                         "traffic": recorded_traffic(kernel, args.workload),
+                         "kernel": f"{kernel} dense tiles"},
+            "gpu_launches": res["launches_per_step"] * args.steps,
+            "clocks": res["clocks"],
+        }
+        if e2e:
+            line["e2e"] = e2e
+        if dec:
+            line["decode"] = {"workload": "64 requests x 1 row, 4-32 segments, 8K-64K keys, "
+                                          "H=64 (56/8), split over segments + fused LSE merge",
+                              "GB/s": round(dec["gbs"], 1), "ms": round(dec["ms"], 4),
+                              "bytes": dec["bytes"], "frac_of_hbm": round(dec["gbs"] / pk["hbm_gbs"], 4),
+                              "hbm_peak": pk["hbm_gbs"], "split_chunks": dec["info"]["split_chunks"],
+                              "l2": "256 MB flush between iterations"}
+        if not args.no_cpu:
+            line["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_seconds)
+        print(json.dumps(line), flush=True)
+    barrier(ws)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    """The oracle, as it stands, on the host cores: each step is a bounded
+    sample of the same workload (rows of the 128K request)."""
+    ws, rank, local = dist_env()
+    if rank != 0:
+        return
+    import torch
+    from position_independent_kv_gb300.workloads import make_workload
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    if dev == "cuda":
+        torch.cuda.set_device(local)
+    wl = make_workload(args.workload, seed=0, device=dev, with_out=False)
+    per = max(2.0, args.cpu_seconds / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        cpu_baseline(wl, budget_s=per)
+    vals = []
+    t0 = time.perf_counter()
+    last = None
+    for _ in range(args.steps):
+        last = cpu_baseline(wl, budget_s=per)
+        vals.append(last["value"])
+    el = time.perf_counter() - t0
+    v = statistics.mean(vals)
+    line = {"metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": WORKLOAD_DESC, "name": args.workload},
+            "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": last["cores"],
+                             "kind": "oracle", "sample": last["sample"]},
+            "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,215 @@
+/*
+ * rk_seg_attn.h - C ABI of the segment-relocated MLA attention library.
+ *
+ * The operation is the online attention step of RedKnot-MLA (arXiv
+ * 2609.07008, "RedKnot-MLA: Multi-Head Offline-Online Reuse for DeepSeek-V4
+ * Long-Context Serving"):
+ *
+ *   - every immutable document i is a canonical packed MLA latent C_i built
+ *     alone at positions 0..n_i-1 (artifacts paragraph) and placed at request
+ *     offset delta_i;
+ *   - the runtime rotates the query's RoPE slice by -delta_i, attends the
+ *     canonical latent in place (K = [c_nope | k_rope], V = c_nope, the one
+ *     packed latent shared by every logical head), and combines the
+ *     per-segment statistics with a numerically stable log-sum-exp merge
+ *     (RoPE-orthogonality paragraph);
+ *   - logical heads have two roles (head-partition paragraph, eq. (1)):
+ *     Global heads attend causally to the whole request; Local heads see the
+ *     sink and the window [p - w, p] only (RedKnot blog "RedKnot, explained",
+ *     "Insight 1", window W(i));
+ *   - the Local rows of the protected set are replaced by the recomputed
+ *     values, never added (protected-set paragraph).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * bf16     IEEE bfloat16 stored as uint16.
+ * d_k      d_nope + d_rope;  d_v = d_nope.
+ * RoPE     interleaved pairs (2j, 2j+1) of the rope slice, theta_j =
+ *          rope_base^(-2j/d_rope); R(phi) turns (x, y) into
+ *          (x cos - y sin, x sin + y cos) with angle phi * theta_j.
+ * rows     The rows a forward computes are, per request r in order, the
+ *          absolute positions q_row_begin[r] .. T_r - 1 (T_r = sum of the
+ *          request's segment lengths).  Q, out and lse are indexed by this
+ *          flattened "computed row" index.
+ * scores   x = softmax_scale * q.k; lse is the natural-log LSE of x.
+ * streams  `stream` is a cudaStream_t passed as void*; NULL is the legacy
+ *          default stream.  Entry points that take a stream enqueue work and
+ *          return without synchronising unless stated otherwise.
+ * errors   Every argument or geometry error is returned synchronously before
+ *          any launch and leaves all buffers untouched.  A failed CUDA call
+ *          returns RK_ERR_CUDA.  There is no fallback path of any kind.
+ */
+#ifndef RK_SEG_ATTN_H
+#define RK_SEG_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  RK_OK = 0,
+  RK_ERR_NULL = 1,              /* a required pointer is NULL */
+  RK_ERR_INVALID_ARG = 2,       /* a count, size or value is out of range */
+  RK_ERR_SEGMENT_OVERLAP = 3,   /* two segments of a request share a row */
+  RK_ERR_SEGMENT_GAP = 4,       /* segments do not tile [0, T_r) */
+  RK_ERR_UNSUPPORTED_DIMS = 5,  /* (d_nope, d_rope) not compiled in */
+  RK_ERR_CAPACITY = 6,          /* a size exceeds an int32 index or a fixed limit */
+  RK_ERR_CUDA = 7,              /* a CUDA runtime/driver call failed */
+  RK_ERR_DEVICE_TIMEOUT = 8,    /* a bounded device-side wait expired */
+  RK_ERR_PLAN_MISMATCH = 9,     /* the plan was built host-only or for another device */
+  RK_ERR_ALIGNMENT = 10,        /* a device pointer is not 16-byte aligned */
+  RK_ERR_WORKSPACE = 11         /* workspace missing or smaller than required */
+} rk_status_t;
+
+/* Segment flag: the request's own new rows (always protected, causal among
+ * themselves like every other row). */
+#define RK_SEG_NEW 1u
+
+/* Plan flags. */
+#define RK_PLAN_HOST_ONLY 1u    /* build and validate on the host only: no
+                                   device memory, forward refuses the plan */
+#define RK_PLAN_LEGACY_MMA 2u   /* run the prefill tiles on the mma.sync
+                                   kernel instead of the tcgen05 kernel */
+
+/* One document segment of a request.
+ * latent  device pointer, bf16 [n, d_k] row-major (row stride d_k elements),
+ *         16-byte aligned, row j = [c_nope | k_rope] with k_rope rotated at
+ *         canonical position j.  Owned by the caller; it must stay valid and
+ *         unchanged while any forward using the plan is in flight.
+ * n       rows (>= 1).
+ * delta   request offset of row 0 (>= 0).
+ * flags   0 or RK_SEG_NEW. */
+typedef struct {
+  const void* latent;
+  int64_t n;
+  int64_t delta;
+  uint32_t flags;
+  uint32_t reserved;  /* must be 0 */
+} rk_segment_t;
+
+/* Request geometry and head roles.  Every pointer here is a HOST pointer and
+ * is only read during rk_seg_attn_plan.
+ * num_requests     R >= 1.
+ * seg_begin        [R + 1] prefix offsets into segs (seg_begin[0] == 0).
+ * segs             segment table, any order within a request; the segments
+ *                  of a request must tile [0, T_r) exactly.
+ * q_row_begin      [R] first computed row of each request (0 for a prefill
+ *                  that recomputes every row; T_r - 1 for a decode step).
+ * num_heads        H, a multiple of 8, at most 256.
+ * d_nope, d_rope   (512, 64) or (128, 32).
+ * rope_base        theta base (> 1).
+ * softmax_scale    s > 0, usually 1/sqrt(d_k).
+ * head_role        [H] 0 = Local, 1 = Global.
+ * sink, window     Local visibility: keys k <= p with k < sink or k >= p - window.
+ * protected_bitmap concatenated per-request bitmaps of ceil(T_r / 32) uint32
+ *                  words each, bit p % 32 of word p / 32 (LSB first) set when
+ *                  absolute row p is protected; NULL means no protected rows
+ *                  besides the RK_SEG_NEW rows, which are always protected.
+ * flags            RK_PLAN_* bits. */
+typedef struct {
+  int32_t num_requests;
+  const int32_t* seg_begin;
+  const rk_segment_t* segs;
+  const int64_t* q_row_begin;
+  int32_t num_heads;
+  int32_t d_nope;
+  int32_t d_rope;
+  double rope_base;
+  float softmax_scale;
+  const uint8_t* head_role;
+  int32_t sink;
+  int32_t window;
+  const uint32_t* protected_bitmap;
+  uint32_t flags;
+} rk_seg_attn_desc_t;
+
+typedef struct rk_seg_attn_plan_s* rk_seg_attn_plan_t;
+
+/* Host-side counts of a plan (for reports and tests). */
+typedef struct {
+  int64_t rows;              /* computed rows (leading dimension of q/out/lse) */
+  int32_t num_heads, d_nope, d_rope;
+  int32_t num_global_heads, num_local_heads;
+  int64_t protected_local_rows;   /* computed rows whose Local heads are recomputed */
+  int64_t dense_tiles;       /* prefill-style work tiles */
+  int64_t split_chunks;      /* split-over-segments chunks (decode) */
+  int64_t pairs_global;      /* attended (row, Global head, key) pairs */
+  int64_t pairs_local;       /* attended (row, Local head, key) pairs */
+  int64_t performed_pairs;   /* M_tile x N_tile summed over issued key tiles */
+  int64_t latent_bytes;      /* bytes of every segment latent */
+  int32_t kernel;            /* 0 = mma.sync tiles, 1 = tcgen05 tiles */
+  int32_t reserved;
+} rk_plan_info_t;
+
+/* Build an immutable, reusable plan for one request bundle geometry
+ * (paper, TP8 fast-path paragraph: repeated document bundles reuse compact
+ * segment-pointer geometry).  Validates the descriptor, sorts segments by
+ * offset, computes the fp64 cos/sin(delta_i theta_j) table (stored fp32),
+ * compacts the protected rows, enumerates the work tiles (fully masked tiles
+ * are never listed) longest first, and uploads everything on `stream`.
+ * Owns copies of all host inputs; the descriptor may be freed on return.
+ * The segment latent pointers are recorded, not copied.
+ * Errors: RK_ERR_NULL, RK_ERR_INVALID_ARG, RK_ERR_SEGMENT_OVERLAP,
+ * RK_ERR_SEGMENT_GAP, RK_ERR_UNSUPPORTED_DIMS, RK_ERR_CAPACITY,
+ * RK_ERR_ALIGNMENT (a latent not 16-byte aligned), RK_ERR_CUDA.  On error
+ * *out is set to NULL and nothing is allocated. */
+rk_status_t rk_seg_attn_plan(const rk_seg_attn_desc_t* desc, void* stream,
+                             rk_seg_attn_plan_t* out);
+
+/* Release a plan (synchronises the device first; NULL is ignored). */
+void rk_seg_attn_plan_destroy(rk_seg_attn_plan_t plan);
+
+/* Fill *info with the plan's counts.  Host only; errors: RK_ERR_NULL. */
+rk_status_t rk_seg_attn_plan_info(rk_seg_attn_plan_t plan, rk_plan_info_t* info);
+
+/* Bytes of device workspace rk_seg_attn_forward needs (0 if none). */
+size_t rk_seg_attn_workspace_bytes(rk_seg_attn_plan_t plan);
+
+/* Segment-relocated attention over the plan's segments (paper,
+ * RoPE-orthogonality and protected-set paragraphs; blog "Insight 1").
+ * q          device bf16 [rows, H, d_k], q_rope rotated at the row's absolute
+ *            position, 16-byte aligned.
+ * out        device bf16 [rows, H, d_nope], in/out.  Global heads: written on
+ *            every computed row.  Local heads: written only on protected
+ *            rows (bitmap bit set or RK_SEG_NEW row); every other element
+ *            keeps its bytes.
+ * lse        device fp32 [rows, H], in/out, written exactly where out is.
+ * workspace  device scratch of rk_seg_attn_workspace_bytes(plan) bytes,
+ *            16-byte aligned (may be NULL when that is 0); its contents on
+ *            entry are irrelevant.  Forwards that share a workspace must be
+ *            ordered on one stream.
+ * Asynchronous on `stream`.  Errors: RK_ERR_NULL, RK_ERR_ALIGNMENT,
+ * RK_ERR_WORKSPACE, RK_ERR_PLAN_MISMATCH, RK_ERR_CUDA (launch failure).
+ * Device-side wait expiries are reported by rk_seg_attn_last_device_status. */
+rk_status_t rk_seg_attn_forward(rk_seg_attn_plan_t plan, const void* q, void* out,
+                                float* lse, void* workspace, size_t workspace_bytes,
+                                void* stream);
+
+/* Stand-alone segment LSE merge (paper, RoPE-orthogonality paragraph).
+ * o_parts    device fp32 [P, rows, H, d_v]   partial outputs (normalised)
+ * lse_parts  device fp32 [P, rows, H]        partial LSEs; -inf = empty part
+ * out        device bf16 [rows, H, d_v]      merged output (round to nearest even)
+ * lse_out    device fp32 [rows, H]           lse = ln sum_j exp(lse_j)
+ * Parts with lse = -inf carry weight 0; if all are -inf the result is
+ * out = 0, lse = -inf.  P >= 1, rows >= 0, 1 <= H, 1 <= d_v <= 1024.
+ * Asynchronous on `stream`.  Errors: RK_ERR_NULL, RK_ERR_INVALID_ARG,
+ * RK_ERR_ALIGNMENT, RK_ERR_CUDA. */
+rk_status_t rk_lse_merge(const float* o_parts, const float* lse_parts, int32_t P,
+                         int64_t rows, int32_t H, int32_t d_v, void* out, float* lse_out,
+                         void* stream);
+
+/* Synchronise `stream`, return and clear the plan's device status word
+ * (RK_OK, or RK_ERR_DEVICE_TIMEOUT if a bounded wait expired). */
+rk_status_t rk_seg_attn_last_device_status(rk_seg_attn_plan_t plan, void* stream);
+
+/* Static description of a status code (never NULL). */
+const char* rk_status_string(rk_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RK_SEG_ATTN_H */

@@ -129,7 +129,7 @@ def attend(qh: np.ndarray, K: np.ndarray, V: np.ndarray, scale: float):
 def seg_attn_request(q: np.ndarray, segments, T: int, q_row_begin: int,
                      head_role, d_nope: int, base: float, scale: float,
                      sink: int, window: int, protected: np.ndarray,
-                     out_init: np.ndarray, lse_init: np.ndarray, rows=None):
+                     out_init: np.ndarray, lse_init: np.ndarray, rows=None, sampled=False):
     """One request.
 
     q         fp64 [T - q_row_begin, H, d_k]  (row i = absolute row q_row_begin + i)
@@ -137,6 +137,8 @@ def seg_attn_request(q: np.ndarray, segments, T: int, q_row_begin: int,
     protected bool [T]  protected rows (new rows are added here as well)
     out_init  [T - q_row_begin, H, d_nope] cached values;  lse_init likewise
     rows      absolute rows to evaluate (default: every computed row)
+    sampled   if True, q / out_init / lse_init hold only the evaluated rows,
+              in the order of `rows`
 
     Returns (O, lse) for the evaluated rows, already assembled: Global heads
     computed, Local heads computed on protected rows and copied otherwise.
@@ -156,7 +158,8 @@ def seg_attn_request(q: np.ndarray, segments, T: int, q_row_begin: int,
     O = np.empty((len(rows), H, d_nope), dtype=np.float64)
     L = np.empty((len(rows), H), dtype=np.float64)
     for i, p in enumerate(rows):
-        r = p - q_row_begin
+        assert q_row_begin <= p < T
+        r = i if sampled else p - q_row_begin
         O[i] = out_init[r]
         L[i] = lse_init[r]
         if len(gh):

@@ -1,0 +1,217 @@
+"""Python binding of the C ABI in include/rk_seg_attn.h (ctypes).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of librk_seg_attn.so.  PyTorch supplies device memory and streams.
+If the shared library has not been built, every entry point raises; there is
+no other implementation to fall back to.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import numpy as np
+
+from .build import LIB
+
+RK_SEG_NEW = 1
+RK_PLAN_HOST_ONLY = 1
+RK_PLAN_LEGACY_MMA = 2
+
+EXPORTS = ["rk_seg_attn_plan", "rk_seg_attn_plan_destroy", "rk_seg_attn_plan_info",
+           "rk_seg_attn_workspace_bytes", "rk_seg_attn_forward", "rk_lse_merge",
+           "rk_seg_attn_last_device_status", "rk_status_string"]
+
+STATUS = {0: "RK_OK", 1: "RK_ERR_NULL", 2: "RK_ERR_INVALID_ARG", 3: "RK_ERR_SEGMENT_OVERLAP",
+          4: "RK_ERR_SEGMENT_GAP", 5: "RK_ERR_UNSUPPORTED_DIMS", 6: "RK_ERR_CAPACITY",
+          7: "RK_ERR_CUDA", 8: "RK_ERR_DEVICE_TIMEOUT", 9: "RK_ERR_PLAN_MISMATCH",
+          10: "RK_ERR_ALIGNMENT", 11: "RK_ERR_WORKSPACE"}
+
+
+class RkSegment(C.Structure):
+    _fields_ = [("latent", C.c_void_p), ("n", C.c_int64), ("delta", C.c_int64),
+                ("flags", C.c_uint32), ("reserved", C.c_uint32)]
+
+
+class RkDesc(C.Structure):
+    _fields_ = [("num_requests", C.c_int32), ("seg_begin", C.POINTER(C.c_int32)),
+                ("segs", C.POINTER(RkSegment)), ("q_row_begin", C.POINTER(C.c_int64)),
+                ("num_heads", C.c_int32), ("d_nope", C.c_int32), ("d_rope", C.c_int32),
+                ("rope_base", C.c_double), ("softmax_scale", C.c_float),
+                ("head_role", C.POINTER(C.c_uint8)), ("sink", C.c_int32), ("window", C.c_int32),
+                ("protected_bitmap", C.POINTER(C.c_uint32)), ("flags", C.c_uint32)]
+
+
+class RkPlanInfo(C.Structure):
+    _fields_ = [("rows", C.c_int64), ("num_heads", C.c_int32), ("d_nope", C.c_int32),
+                ("d_rope", C.c_int32), ("num_global_heads", C.c_int32),
+                ("num_local_heads", C.c_int32), ("protected_local_rows", C.c_int64),
+                ("dense_tiles", C.c_int64), ("split_chunks", C.c_int64),
+                ("pairs_global", C.c_int64), ("pairs_local", C.c_int64),
+                ("performed_pairs", C.c_int64), ("latent_bytes", C.c_int64),
+                ("kernel", C.c_int32), ("reserved", C.c_int32)]
+
+    def as_dict(self) -> dict:
+        return {k: getattr(self, k) for k, _ in self._fields_ if k != "reserved"}
+
+
+class RkError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)}")
+
+
+_lib = None
+
+
+def lib() -> C.CDLL:
+    """The loaded library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB):
+            raise RuntimeError(f"{LIB} is missing: run position_independent_kv_gb300.build.build()")
+        try:
+            import torch  # noqa: F401  (loads the CUDA runtime torch was built with)
+        except ImportError:
+            pass
+        L = C.CDLL(LIB)
+        L.rk_seg_attn_plan.argtypes = [C.POINTER(RkDesc), C.c_void_p, C.POINTER(C.c_void_p)]
+        L.rk_seg_attn_plan.restype = C.c_int
+        L.rk_seg_attn_plan_destroy.argtypes = [C.c_void_p]
+        L.rk_seg_attn_plan_destroy.restype = None
+        L.rk_seg_attn_plan_info.argtypes = [C.c_void_p, C.POINTER(RkPlanInfo)]
+        L.rk_seg_attn_plan_info.restype = C.c_int
+        L.rk_seg_attn_workspace_bytes.argtypes = [C.c_void_p]
+        L.rk_seg_attn_workspace_bytes.restype = C.c_size_t
+        L.rk_seg_attn_forward.argtypes = [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
+                                          C.c_void_p, C.c_size_t, C.c_void_p]
+        L.rk_seg_attn_forward.restype = C.c_int
+        L.rk_lse_merge.argtypes = [C.c_void_p, C.c_void_p, C.c_int32, C.c_int64, C.c_int32,
+                                   C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p]
+        L.rk_lse_merge.restype = C.c_int
+        L.rk_seg_attn_last_device_status.argtypes = [C.c_void_p, C.c_void_p]
+        L.rk_seg_attn_last_device_status.restype = C.c_int
+        L.rk_status_string.argtypes = [C.c_int]
+        L.rk_status_string.restype = C.c_char_p
+        _lib = L
+    return _lib
+
+
+def _ptr(x) -> int:
+    if x is None:
+        return 0
+    if isinstance(x, int):
+        return x
+    return int(x.data_ptr())
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        import torch
+        return int(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return stream
+    return int(stream.cuda_stream)
+
+
+def _check(st: int, where: str):
+    if st != 0:
+        raise RkError(st, where)
+
+
+class SegAttnPlan:
+    """rk_seg_attn_plan / rk_seg_attn_forward.
+
+    segments: list of (latent tensor or device address, n, delta, is_new)
+    seg_begin: [R + 1] prefix offsets; q_row_begin: [R]
+    bitmap: uint32 words per request (concatenated) or None
+    """
+
+    def __init__(self, segments, seg_begin, q_row_begin, num_heads, d_nope, d_rope,
+                 rope_base, softmax_scale, head_role, sink, window, bitmap=None, flags=0,
+                 stream=None):
+        L = lib()
+        R = len(seg_begin) - 1
+        segs = (RkSegment * max(1, len(segments)))()
+        for i, (lat, n, delta, is_new) in enumerate(segments):
+            segs[i] = RkSegment(_ptr(lat), int(n), int(delta), RK_SEG_NEW if is_new else 0, 0)
+        self._keep = [segments]
+        sb = np.ascontiguousarray(seg_begin, dtype=np.int32)
+        qb = np.ascontiguousarray(q_row_begin, dtype=np.int64)
+        role = np.ascontiguousarray(head_role, dtype=np.uint8)
+        bm = None if bitmap is None else np.ascontiguousarray(bitmap, dtype=np.uint32)
+        desc = RkDesc()
+        desc.num_requests = R
+        desc.seg_begin = sb.ctypes.data_as(C.POINTER(C.c_int32))
+        desc.segs = segs
+        desc.q_row_begin = qb.ctypes.data_as(C.POINTER(C.c_int64))
+        desc.num_heads = int(num_heads)
+        desc.d_nope = int(d_nope)
+        desc.d_rope = int(d_rope)
+        desc.rope_base = float(rope_base)
+        desc.softmax_scale = float(softmax_scale)
+        desc.head_role = role.ctypes.data_as(C.POINTER(C.c_uint8))
+        desc.sink = int(sink)
+        desc.window = int(window)
+        desc.protected_bitmap = (bm.ctypes.data_as(C.POINTER(C.c_uint32)) if bm is not None
+                                 else C.POINTER(C.c_uint32)())
+        desc.flags = int(flags)
+        host_only = bool(flags & RK_PLAN_HOST_ONLY)
+        handle = C.c_void_p()
+        st = L.rk_seg_attn_plan(C.byref(desc), 0 if host_only else _stream(stream),
+                                C.byref(handle))
+        _check(st, "rk_seg_attn_plan")
+        self._h = handle
+        self.num_heads, self.d_nope, self.d_rope = int(num_heads), int(d_nope), int(d_rope)
+
+    @classmethod
+    def from_workload(cls, wl, bitmap=None, flags=0, stream=None, addresses=None):
+        from .workloads import segments_for_abi
+        flat, begins = segments_for_abi(wl)
+        if addresses is not None:
+            flat = [(addresses(i, s), s[1], s[2], s[3]) for i, s in enumerate(flat)]
+        return cls(flat, begins, [r.q_row_begin for r in wl.requests], wl.H, wl.d_nope,
+                   wl.d_rope, wl.rope_base, wl.scale, wl.head_role, wl.sink, wl.window,
+                   bitmap=bitmap, flags=flags, stream=stream)
+
+    @property
+    def info(self) -> dict:
+        inf = RkPlanInfo()
+        _check(lib().rk_seg_attn_plan_info(self._h, C.byref(inf)), "rk_seg_attn_plan_info")
+        return inf.as_dict()
+
+    @property
+    def workspace_bytes(self) -> int:
+        return int(lib().rk_seg_attn_workspace_bytes(self._h))
+
+    def forward(self, q, out, lse, workspace=None, stream=None):
+        ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+        st = lib().rk_seg_attn_forward(self._h, _ptr(q), _ptr(out), _ptr(lse), _ptr(workspace),
+                                       ws_bytes, _stream(stream))
+        _check(st, "rk_seg_attn_forward")
+
+    def device_status(self, stream=None) -> int:
+        return int(lib().rk_seg_attn_last_device_status(self._h, _stream(stream)))
+
+    def close(self):
+        if getattr(self, "_h", None):
+            lib().rk_seg_attn_plan_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def lse_merge(o_parts, lse_parts, out, lse_out, stream=None):
+    """rk_lse_merge: o_parts fp32 [P, rows, H, d_v], lse_parts fp32 [P, rows, H]."""
+    P, rows, H, d_v = (int(x) for x in o_parts.shape)
+    st = lib().rk_lse_merge(_ptr(o_parts), _ptr(lse_parts), P, rows, H, d_v, _ptr(out),
+                            _ptr(lse_out), _stream(stream))
+    _check(st, "rk_lse_merge")
+
+
+def status_string(st: int) -> str:
+    return lib().rk_status_string(int(st)).decode()

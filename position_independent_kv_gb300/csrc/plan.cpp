@@ -1,0 +1,511 @@
+// Host plan and C-ABI entry points of the segment-relocated MLA attention
+// library.  The plan validates a request bundle, compacts the protected rows,
+// builds the RoPE table and the work lists once; forward only launches.
+// RedKnot-MLA paper (arXiv 2609.07008): TP8 fast-path paragraph (compact,
+// reusable segment-pointer geometry), protected-set paragraph (which Local
+// rows are recomputed), RoPE-orthogonality paragraph (query rotation by
+// -delta and the log-sum-exp merge).
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <numeric>
+
+#include "rk_internal.h"
+
+using rk::DenseTile;
+using rk::DevReq;
+using rk::DevSeg;
+using rk::SplitChunk;
+
+namespace {
+
+constexpr int kMmaTileM = 64;     // query pairs per mma.sync tile
+constexpr int kMmaTileN = 32;     // keys per mma.sync key tile
+constexpr int kSplitHeads = 8;    // Global heads per split chunk
+
+bool dims_supported(int d_nope, int d_rope) {
+  return (d_nope == 512 && d_rope == 64) || (d_nope == 128 && d_rope == 32);
+}
+
+template <typename T>
+rk_status_t upload(const std::vector<T>& v, T** dptr, cudaStream_t s) {
+  *dptr = nullptr;
+  if (v.empty()) return RK_OK;
+  if (cudaMalloc(reinterpret_cast<void**>(dptr), v.size() * sizeof(T)) != cudaSuccess) {
+    *dptr = nullptr;
+    return RK_ERR_CUDA;
+  }
+  if (cudaMemcpyAsync(*dptr, v.data(), v.size() * sizeof(T), cudaMemcpyHostToDevice, s) !=
+      cudaSuccess)
+    return RK_ERR_CUDA;
+  return RK_OK;
+}
+
+void free_device(rk_seg_attn_plan_s* p) {
+  cudaFree(p->d_segs);
+  cudaFree(p->d_reqs);
+  cudaFree(p->d_rope_cs);
+  cudaFree(p->d_tiles);
+  cudaFree(p->d_local_rows);
+  cudaFree(p->d_global_heads);
+  cudaFree(p->d_local_heads);
+  cudaFree(p->d_chunks);
+  cudaFree(p->d_status);
+  p->d_segs = nullptr;
+  p->d_reqs = nullptr;
+  p->d_rope_cs = nullptr;
+  p->d_tiles = nullptr;
+  p->d_local_rows = nullptr;
+  p->d_global_heads = p->d_local_heads = nullptr;
+  p->d_chunks = nullptr;
+  p->d_status = nullptr;
+}
+
+// Number of keys a tile visits in segment [d, d + n): the union
+// [0, sink_hi) u [win_lo, key_hi) clipped to the segment, rounded up to key
+// tiles of width `tn` per range.
+int64_t key_tiles_in_segment(const DenseTile& t, int64_t d, int64_t n, int tn) {
+  int64_t tiles = 0;
+  auto add = [&](int64_t lo, int64_t hi) {
+    lo = std::max(lo, d);
+    hi = std::min(hi, d + n);
+    if (hi > lo) tiles += (hi - lo + tn - 1) / tn;
+  };
+  add(0, t.sink_hi);
+  add(t.win_lo, t.key_hi);
+  return tiles;
+}
+
+int64_t keys_visible_local(int64_t p, int64_t sink, int64_t window) {
+  int64_t lo = std::max<int64_t>(0, p - window);
+  if (lo <= sink) return p + 1;
+  return std::min<int64_t>(sink, p + 1) + (p - lo + 1);
+}
+
+}  // namespace
+
+extern "C" const char* rk_status_string(rk_status_t s) {
+  switch (s) {
+    case RK_OK: return "ok";
+    case RK_ERR_NULL: return "a required pointer is NULL";
+    case RK_ERR_INVALID_ARG: return "invalid argument";
+    case RK_ERR_SEGMENT_OVERLAP: return "segments of a request overlap";
+    case RK_ERR_SEGMENT_GAP: return "segments of a request leave a gap";
+    case RK_ERR_UNSUPPORTED_DIMS: return "unsupported (d_nope, d_rope)";
+    case RK_ERR_CAPACITY: return "size exceeds a fixed limit";
+    case RK_ERR_CUDA: return "CUDA call failed";
+    case RK_ERR_DEVICE_TIMEOUT: return "bounded device-side wait expired";
+    case RK_ERR_PLAN_MISMATCH: return "plan is host-only or belongs to another device";
+    case RK_ERR_ALIGNMENT: return "device pointer not 16-byte aligned";
+    case RK_ERR_WORKSPACE: return "workspace missing or too small";
+  }
+  return "unknown status";
+}
+
+static rk_status_t build_plan(const rk_seg_attn_desc_t* d, rk_seg_attn_plan_s* p) {
+  // ---------------- validation (no CUDA call before this block ends) -----
+  if (!d->seg_begin || !d->segs || !d->q_row_begin || !d->head_role) return RK_ERR_NULL;
+  const int R = d->num_requests;
+  if (R < 1) return RK_ERR_INVALID_ARG;
+  if (d->num_heads < 8 || d->num_heads > 256 || d->num_heads % 8) return RK_ERR_INVALID_ARG;
+  if (!dims_supported(d->d_nope, d->d_rope)) return RK_ERR_UNSUPPORTED_DIMS;
+  if (!(d->rope_base > 1.0) || !std::isfinite(d->rope_base)) return RK_ERR_INVALID_ARG;
+  if (!(d->softmax_scale > 0.f) || !std::isfinite(d->softmax_scale)) return RK_ERR_INVALID_ARG;
+  if (d->sink < 0 || d->window < 0) return RK_ERR_INVALID_ARG;
+  if (d->flags & ~(RK_PLAN_HOST_ONLY | RK_PLAN_LEGACY_MMA)) return RK_ERR_INVALID_ARG;
+  if (d->seg_begin[0] != 0) return RK_ERR_INVALID_ARG;
+  for (int r = 0; r < R; ++r)
+    if (d->seg_begin[r + 1] <= d->seg_begin[r]) return RK_ERR_INVALID_ARG;
+  const int64_t nseg = d->seg_begin[R];
+  if (nseg > (1 << 24)) return RK_ERR_CAPACITY;
+  const int H = d->num_heads;
+  for (int h = 0; h < H; ++h)
+    if (d->head_role[h] > 1) return RK_ERR_INVALID_ARG;
+  for (int64_t i = 0; i < nseg; ++i) {
+    const rk_segment_t& s = d->segs[i];
+    if (!s.latent) return RK_ERR_NULL;
+    if (reinterpret_cast<uintptr_t>(s.latent) & 15) return RK_ERR_ALIGNMENT;
+    if (s.n < 1 || s.delta < 0) return RK_ERR_INVALID_ARG;
+    if ((s.flags & ~RK_SEG_NEW) || s.reserved) return RK_ERR_INVALID_ARG;
+    if (s.n > INT32_MAX || s.delta > INT32_MAX) return RK_ERR_CAPACITY;
+  }
+  p->H = H;
+  p->d_nope = d->d_nope;
+  p->d_rope = d->d_rope;
+  p->sink = d->sink;
+  p->window = d->window;
+  p->softmax_scale = d->softmax_scale;
+  p->host_only = (d->flags & RK_PLAN_HOST_ONLY) != 0;
+  p->kernel = 0;
+  p->tile_m = kMmaTileM;
+
+  // segments, sorted by offset inside each request; contiguity check
+  std::vector<int64_t> T(R), word_off(R + 1, 0);
+  int64_t rows_total = 0;
+  p->segs.resize(nseg);
+  p->reqs.resize(R);
+  for (int r = 0; r < R; ++r) {
+    const int b = d->seg_begin[r], e = d->seg_begin[r + 1];
+    std::vector<int> idx(e - b);
+    std::iota(idx.begin(), idx.end(), b);
+    std::stable_sort(idx.begin(), idx.end(),
+                     [&](int x, int y) { return d->segs[x].delta < d->segs[y].delta; });
+    int64_t pos = 0;
+    for (int j = 0; j < e - b; ++j) {
+      const rk_segment_t& s = d->segs[idx[j]];
+      if (s.delta < pos) return RK_ERR_SEGMENT_OVERLAP;
+      if (s.delta > pos) return RK_ERR_SEGMENT_GAP;
+      pos = s.delta + s.n;
+      if (pos > INT32_MAX) return RK_ERR_CAPACITY;
+      DevSeg& ds = p->segs[b + j];
+      ds.latent = static_cast<const uint16_t*>(s.latent);
+      ds.n = static_cast<int32_t>(s.n);
+      ds.delta = static_cast<int32_t>(s.delta);
+      ds.is_new = (s.flags & RK_SEG_NEW) ? 1 : 0;
+      ds.pad = 0;
+    }
+    T[r] = pos;
+    const int64_t qb = d->q_row_begin[r];
+    if (qb < 0 || qb >= pos) return RK_ERR_INVALID_ARG;
+    DevReq& rq = p->reqs[r];
+    rq.seg_first = b;
+    rq.seg_count = e - b;
+    rq.T = static_cast<int32_t>(pos);
+    rq.q_row_begin = static_cast<int32_t>(qb);
+    rq.row_base = rows_total;
+    rows_total += pos - qb;
+    word_off[r + 1] = word_off[r] + (pos + 31) / 32;
+  }
+  if (rows_total * H > (int64_t(1) << 40)) return RK_ERR_CAPACITY;
+
+  // heads
+  for (int h = 0; h < H; ++h) (d->head_role[h] ? p->global_heads : p->local_heads).push_back(h);
+  const int HG = static_cast<int>(p->global_heads.size());
+  const int HL = static_cast<int>(p->local_heads.size());
+
+  // RoPE table: cos/sin(delta * theta_j) in fp64, stored fp32
+  const int half = d->d_rope / 2;
+  p->rope_cs.resize(static_cast<size_t>(nseg) * half * 2);
+  for (int64_t i = 0; i < nseg; ++i) {
+    for (int j = 0; j < half; ++j) {
+      const double theta = std::pow(d->rope_base, -2.0 * j / d->d_rope);
+      const double ang = static_cast<double>(p->segs[i].delta) * theta;
+      p->rope_cs[(i * half + j) * 2 + 0] = static_cast<float>(std::cos(ang));
+      p->rope_cs[(i * half + j) * 2 + 1] = static_cast<float>(std::sin(ang));
+    }
+  }
+
+  // work lists
+  rk_plan_info_t& info = p->info;
+  std::memset(&info, 0, sizeof(info));
+  info.rows = rows_total;
+  info.num_heads = H;
+  info.d_nope = d->d_nope;
+  info.d_rope = d->d_rope;
+  info.num_global_heads = HG;
+  info.num_local_heads = HL;
+  info.kernel = p->kernel;
+  for (int64_t i = 0; i < nseg; ++i)
+    info.latent_bytes += p->segs[i].n * int64_t(d->d_nope + d->d_rope) * 2;
+
+  const int TM = p->tile_m;
+  const int TN = kMmaTileN;
+  const int64_t sink = d->sink, window = d->window;
+  std::vector<std::pair<int64_t, DenseTile>> tiles;  // (cost, tile)
+  int64_t mgroups = 0, parts = 0;
+  const int groups = (HG + kSplitHeads - 1) / kSplitHeads;
+  for (int r = 0; r < R; ++r) {
+    const DevReq& rq = p->reqs[r];
+    const int64_t qb = rq.q_row_begin, Tr = rq.T;
+    // protected computed rows
+    std::vector<uint8_t> prot(Tr, 0);
+    if (d->protected_bitmap) {
+      const uint32_t* w = d->protected_bitmap + word_off[r];
+      for (int64_t q = 0; q < Tr; ++q) prot[q] = (w[q >> 5] >> (q & 31)) & 1u;
+    }
+    for (int j = 0; j < rq.seg_count; ++j) {
+      const DevSeg& s = p->segs[rq.seg_first + j];
+      if (s.is_new) std::fill(prot.begin() + s.delta, prot.begin() + s.delta + s.n, 1);
+    }
+    const size_t lr_first = p->local_rows.size();
+    for (int64_t q = qb; q < Tr; ++q)
+      if (prot[q]) p->local_rows.push_back(static_cast<int32_t>(q));
+    const int64_t nprot = static_cast<int64_t>(p->local_rows.size() - lr_first);
+    if (HL) info.protected_local_rows += nprot;
+
+    // algorithmic pairs
+    for (int64_t q = qb; q < Tr; ++q) info.pairs_global += int64_t(HG) * (q + 1);
+    if (HL)
+      for (size_t i = lr_first; i < p->local_rows.size(); ++i)
+        info.pairs_local += int64_t(HL) * keys_visible_local(p->local_rows[i], sink, window);
+
+    // Global heads
+    const bool split = (Tr - qb == 1) && HG > 0;
+    if (split) {
+      // one row: split the keys [0, T) over segments and chunks
+      const int64_t keys = Tr;
+      int64_t C = (keys + 3) / 4;  // at least a few chunks per request
+      C = std::max<int64_t>(256, std::min<int64_t>(4096, ((C + 63) / 64) * 64));
+      for (int g = 0; g < groups; ++g) {
+        const int64_t first = parts;
+        std::vector<SplitChunk> cs;
+        for (int j = 0; j < rq.seg_count; ++j) {
+          const DevSeg& s = p->segs[rq.seg_first + j];
+          for (int64_t k0 = s.delta; k0 < int64_t(s.delta) + s.n; k0 += C) {
+            SplitChunk c{};
+            c.req = r;
+            c.seg = rq.seg_first + j;
+            c.k0 = static_cast<int32_t>(k0);
+            c.k1 = static_cast<int32_t>(std::min<int64_t>(k0 + C, int64_t(s.delta) + s.n));
+            c.group = g;
+            c.mgroup = static_cast<int32_t>(mgroups);
+            cs.push_back(c);
+          }
+        }
+        for (auto& c : cs) {
+          c.part = static_cast<int32_t>(parts++);
+          c.part_first = static_cast<int32_t>(first);
+          c.nparts = static_cast<int32_t>(cs.size());
+          p->chunks.push_back(c);
+          info.performed_pairs += int64_t(kSplitHeads) * ((c.k1 - c.k0 + 63) / 64) * 64;
+        }
+        ++mgroups;
+      }
+    } else if (HG) {
+      const int rows_per = std::max(1, TM / HG);
+      for (int64_t q0 = qb; q0 < Tr; q0 += rows_per) {
+        DenseTile t{};
+        t.req = r;
+        t.kind = 0;
+        t.first = static_cast<int32_t>(q0);
+        t.count = static_cast<int32_t>(std::min<int64_t>(rows_per, Tr - q0));
+        t.key_hi = t.first + t.count;
+        t.win_lo = 0;
+        t.sink_hi = 0;
+        int64_t kt = 0;
+        for (int j = 0; j < rq.seg_count; ++j) {
+          const DevSeg& s = p->segs[rq.seg_first + j];
+          kt += key_tiles_in_segment(t, s.delta, s.n, TN);
+        }
+        info.performed_pairs += kt * TN * TM;
+        tiles.push_back({kt, t});
+      }
+    }
+    // Local heads on protected rows
+    if (HL && nprot) {
+      const int64_t npairs = nprot * HL;
+      const int64_t pair_base = static_cast<int64_t>(lr_first) * HL;
+      int64_t i = 0;
+      while (i < npairs) {
+        const int64_t p_first = p->local_rows[lr_first + i / HL];
+        int64_t e = std::min<int64_t>(npairs, i + TM);
+        // cut the tile where the next row is too far away to share a window
+        for (int64_t k = i + 1; k < e; ++k) {
+          if ((k % HL) == 0 && p->local_rows[lr_first + k / HL] - p_first > window / 2 + 1) {
+            e = k;
+            break;
+          }
+        }
+        const int64_t p_last = p->local_rows[lr_first + (e - 1) / HL];
+        DenseTile t{};
+        t.req = r;
+        t.kind = 1;
+        t.first = static_cast<int32_t>(pair_base + i);
+        t.count = static_cast<int32_t>(e - i);
+        t.key_hi = static_cast<int32_t>(p_last + 1);
+        int64_t wl = std::max<int64_t>(0, p_first - window);
+        if (wl <= sink) {
+          t.win_lo = 0;
+          t.sink_hi = 0;
+        } else {
+          t.win_lo = static_cast<int32_t>(wl);
+          t.sink_hi = static_cast<int32_t>(sink);
+        }
+        int64_t kt = 0;
+        for (int j = 0; j < rq.seg_count; ++j) {
+          const DevSeg& s = p->segs[rq.seg_first + j];
+          kt += key_tiles_in_segment(t, s.delta, s.n, TN);
+        }
+        info.performed_pairs += kt * TN * TM;
+        tiles.push_back({kt, t});
+        i = e;
+      }
+    }
+  }
+  if (static_cast<int64_t>(p->local_rows.size()) * std::max(HL, 1) > INT32_MAX)
+    return RK_ERR_CAPACITY;
+  if (tiles.size() > INT32_MAX / 2 || p->chunks.size() > INT32_MAX / 2) return RK_ERR_CAPACITY;
+  // longest first
+  std::stable_sort(tiles.begin(), tiles.end(),
+                   [](const auto& a, const auto& b) { return a.first > b.first; });
+  p->tiles.reserve(tiles.size());
+  for (auto& t : tiles) p->tiles.push_back(t.second);
+  info.dense_tiles = static_cast<int64_t>(p->tiles.size());
+  info.split_chunks = static_cast<int64_t>(p->chunks.size());
+  p->num_parts = parts;
+  p->num_mgroups = mgroups;
+  if (parts) {
+    const size_t dv = d->d_nope;
+    size_t bytes = 0;
+    bytes += static_cast<size_t>(parts) * kSplitHeads * dv * sizeof(float);
+    bytes += static_cast<size_t>(parts) * kSplitHeads * sizeof(float);
+    bytes = (bytes + 255) & ~size_t(255);
+    bytes += static_cast<size_t>(mgroups) * sizeof(int32_t);
+    p->workspace_bytes = (bytes + 255) & ~size_t(255);
+  }
+  return RK_OK;
+}
+
+extern "C" rk_status_t rk_seg_attn_plan(const rk_seg_attn_desc_t* desc, void* stream,
+                                        rk_seg_attn_plan_t* out) {
+  if (!out) return RK_ERR_NULL;
+  *out = nullptr;
+  if (!desc) return RK_ERR_NULL;
+  rk_seg_attn_plan_s* p = new (std::nothrow) rk_seg_attn_plan_s();
+  if (!p) return RK_ERR_CAPACITY;
+  rk_status_t st = build_plan(desc, p);
+  if (st != RK_OK) {
+    delete p;
+    return st;
+  }
+  if (!p->host_only) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaGetDevice(&p->device) != cudaSuccess) st = RK_ERR_CUDA;
+    if (st == RK_OK) st = upload(p->segs, &p->d_segs, s);
+    if (st == RK_OK) st = upload(p->reqs, &p->d_reqs, s);
+    if (st == RK_OK) st = upload(p->rope_cs, &p->d_rope_cs, s);
+    if (st == RK_OK) st = upload(p->tiles, &p->d_tiles, s);
+    if (st == RK_OK) st = upload(p->local_rows, &p->d_local_rows, s);
+    if (st == RK_OK) st = upload(p->global_heads, &p->d_global_heads, s);
+    if (st == RK_OK) st = upload(p->local_heads, &p->d_local_heads, s);
+    if (st == RK_OK) st = upload(p->chunks, &p->d_chunks, s);
+    if (st == RK_OK) {
+      if (cudaMalloc(reinterpret_cast<void**>(&p->d_status), sizeof(int32_t)) != cudaSuccess)
+        st = RK_ERR_CUDA;
+      else if (cudaMemsetAsync(p->d_status, 0, sizeof(int32_t), s) != cudaSuccess)
+        st = RK_ERR_CUDA;
+    }
+    // host vectors are pageable: make the uploads complete before returning
+    if (st == RK_OK && cudaStreamSynchronize(s) != cudaSuccess) st = RK_ERR_CUDA;
+    if (st != RK_OK) {
+      free_device(p);
+      delete p;
+      return st;
+    }
+  }
+  *out = p;
+  return RK_OK;
+}
+
+extern "C" void rk_seg_attn_plan_destroy(rk_seg_attn_plan_t p) {
+  if (!p) return;
+  if (!p->host_only) {
+    int cur = -1;
+    cudaGetDevice(&cur);
+    if (cur != p->device) cudaSetDevice(p->device);
+    cudaDeviceSynchronize();
+    free_device(p);
+    if (cur != p->device && cur >= 0) cudaSetDevice(cur);
+  }
+  delete p;
+}
+
+extern "C" rk_status_t rk_seg_attn_plan_info(rk_seg_attn_plan_t p, rk_plan_info_t* info) {
+  if (!p || !info) return RK_ERR_NULL;
+  *info = p->info;
+  return RK_OK;
+}
+
+extern "C" size_t rk_seg_attn_workspace_bytes(rk_seg_attn_plan_t p) {
+  return p ? p->workspace_bytes : 0;
+}
+
+extern "C" rk_status_t rk_seg_attn_forward(rk_seg_attn_plan_t p, const void* q, void* out,
+                                           float* lse, void* workspace, size_t ws_bytes,
+                                           void* stream) {
+  if (!p || !q || !out || !lse) return RK_ERR_NULL;
+  if (p->host_only) return RK_ERR_PLAN_MISMATCH;
+  auto mis = [](const void* x) { return (reinterpret_cast<uintptr_t>(x) & 15) != 0; };
+  if (mis(q) || mis(out) || (reinterpret_cast<uintptr_t>(lse) & 3)) return RK_ERR_ALIGNMENT;
+  if (p->workspace_bytes) {
+    if (!workspace || ws_bytes < p->workspace_bytes) return RK_ERR_WORKSPACE;
+    if (mis(workspace)) return RK_ERR_ALIGNMENT;
+  }
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess) return RK_ERR_CUDA;
+  if (cur != p->device) return RK_ERR_PLAN_MISMATCH;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  rk::KernelArgs a{};
+  a.q = static_cast<const uint16_t*>(q);
+  a.out = static_cast<uint16_t*>(out);
+  a.lse = lse;
+  a.segs = p->d_segs;
+  a.reqs = p->d_reqs;
+  a.rope_cs = p->d_rope_cs;
+  a.tiles = p->d_tiles;
+  a.num_tiles = static_cast<int32_t>(p->tiles.size());
+  a.local_rows = p->d_local_rows;
+  a.global_heads = p->d_global_heads;
+  a.local_heads = p->d_local_heads;
+  a.num_global = static_cast<int32_t>(p->global_heads.size());
+  a.num_local = static_cast<int32_t>(p->local_heads.size());
+  a.H = p->H;
+  a.sink = p->sink;
+  a.window = p->window;
+  a.scale_log2 = p->softmax_scale * 1.4426950408889634f;
+  a.chunks = p->d_chunks;
+  a.num_chunks = static_cast<int32_t>(p->chunks.size());
+  a.status = p->d_status;
+  if (p->num_parts) {
+    char* w = static_cast<char*>(workspace);
+    a.ws_o = reinterpret_cast<float*>(w);
+    size_t off = static_cast<size_t>(p->num_parts) * kSplitHeads * p->d_nope * sizeof(float);
+    a.ws_lse = reinterpret_cast<float*>(w + off);
+    off += static_cast<size_t>(p->num_parts) * kSplitHeads * sizeof(float);
+    off = (off + 255) & ~size_t(255);
+    a.ws_ticket = reinterpret_cast<int32_t*>(w + off);
+    if (cudaMemsetAsync(a.ws_ticket, 0, p->num_mgroups * sizeof(int32_t), s) != cudaSuccess)
+      return RK_ERR_CUDA;
+  }
+  if (a.num_chunks) {
+    if (rk::launch_split_decode(*p, a, s) != cudaSuccess) return RK_ERR_CUDA;
+  }
+  if (a.num_tiles) {
+    if (rk::launch_dense_mma(*p, a, s) != cudaSuccess) return RK_ERR_CUDA;
+  }
+  return RK_OK;
+}
+
+extern "C" rk_status_t rk_lse_merge(const float* o_parts, const float* lse_parts, int32_t P,
+                                    int64_t rows, int32_t H, int32_t d_v, void* out,
+                                    float* lse_out, void* stream) {
+  if (!o_parts || !lse_parts || !out || !lse_out) return RK_ERR_NULL;
+  if (P < 1 || rows < 0 || H < 1 || d_v < 1 || d_v > 1024) return RK_ERR_INVALID_ARG;
+  if (rows * H > (int64_t(1) << 40)) return RK_ERR_CAPACITY;
+  if ((reinterpret_cast<uintptr_t>(o_parts) | reinterpret_cast<uintptr_t>(lse_parts) |
+       reinterpret_cast<uintptr_t>(lse_out)) & 3)
+    return RK_ERR_ALIGNMENT;
+  if (reinterpret_cast<uintptr_t>(out) & 1) return RK_ERR_ALIGNMENT;
+  if (rows == 0) return RK_OK;
+  cudaError_t e = rk::launch_lse_merge(o_parts, lse_parts, P, rows, H, d_v,
+                                       static_cast<uint16_t*>(out), lse_out,
+                                       static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? RK_OK : RK_ERR_CUDA;
+}
+
+extern "C" rk_status_t rk_seg_attn_last_device_status(rk_seg_attn_plan_t p, void* stream) {
+  if (!p) return RK_ERR_NULL;
+  if (p->host_only) return RK_ERR_PLAN_MISMATCH;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t h = 0;
+  if (cudaMemcpyAsync(&h, p->d_status, sizeof(h), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return RK_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return RK_ERR_CUDA;
+  if (cudaMemsetAsync(p->d_status, 0, sizeof(int32_t), s) != cudaSuccess) return RK_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return RK_ERR_CUDA;
+  return h ? static_cast<rk_status_t>(h) : RK_OK;
+}

@@ -1,0 +1,130 @@
+// Internal types shared by the host plan and the CUDA kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <vector>
+
+#include "rk_seg_attn.h"
+
+namespace rk {
+
+// One segment as the kernels see it; segments of a request are stored
+// contiguously, sorted by offset.
+struct DevSeg {
+  const uint16_t* latent;  // bf16 [n, d_k]
+  int32_t n;
+  int32_t delta;
+  int32_t is_new;
+  int32_t pad;
+};
+
+struct DevReq {
+  int32_t seg_first;   // index of the request's first DevSeg
+  int32_t seg_count;
+  int32_t T;           // rows of the request
+  int32_t q_row_begin; // first computed absolute row
+  int64_t row_base;    // flattened computed-row index of q_row_begin
+};
+
+// A prefill-style work tile: a set of (row, head) query pairs that share
+// one key range.  kind 0: rows [first, first + count) x every Global head.
+// kind 1: pairs [first, first + count) of the flattened (protected row,
+// Local head) list, pair i -> (local_rows[i / HL], local_heads[i % HL]).
+// Keys visited: [0, sink_hi) u [win_lo, key_hi), clipped to each segment.
+struct DenseTile {
+  int32_t req;
+  int32_t kind;
+  int32_t first;
+  int32_t count;
+  int32_t key_hi;
+  int32_t win_lo;
+  int32_t sink_hi;
+  int32_t pad;
+};
+
+// A split-over-segments chunk (single computed row, Global heads): keys
+// [k0, k1) (absolute) inside segment `seg`, head group `group` (8 Global
+// heads), partial slot `part` of the merge group `mgroup` whose parts are
+// [part_first, part_first + nparts).
+struct SplitChunk {
+  int32_t req;
+  int32_t seg;       // global DevSeg index
+  int32_t k0, k1;
+  int32_t group;
+  int32_t part;
+  int32_t mgroup;
+  int32_t part_first;
+  int32_t nparts;
+  int32_t pad[3];
+};
+
+struct KernelArgs {
+  const uint16_t* q;
+  uint16_t* out;
+  float* lse;
+  const DevSeg* segs;
+  const DevReq* reqs;
+  const float* rope_cs;       // [num_segs][d_rope/2][2] cos, sin of delta * theta
+  const DenseTile* tiles;
+  int32_t num_tiles;
+  const int32_t* local_rows;  // compacted protected computed rows (absolute)
+  const int32_t* global_heads;
+  const int32_t* local_heads;
+  int32_t num_global, num_local;
+  int32_t H;
+  int32_t sink, window;
+  float scale_log2;           // softmax_scale * log2(e)
+  const SplitChunk* chunks;
+  int32_t num_chunks;
+  float* ws_o;                // [parts][8][d_v]
+  float* ws_lse;              // [parts][8]
+  int32_t* ws_ticket;         // [mgroups]
+  int32_t* status;            // device status word
+};
+
+}  // namespace rk
+
+struct rk_seg_attn_plan_s {
+  int device = -1;
+  bool host_only = false;
+  int32_t H = 0, d_nope = 0, d_rope = 0;
+  int32_t sink = 0, window = 0;
+  float softmax_scale = 0.f;
+  int kernel = 0;          // 0 mma.sync tiles, 1 tcgen05 tiles
+  int tile_m = 64;         // query pairs per dense tile
+  rk_plan_info_t info{};
+  // host copies
+  std::vector<rk::DevSeg> segs;
+  std::vector<rk::DevReq> reqs;
+  std::vector<float> rope_cs;
+  std::vector<rk::DenseTile> tiles;
+  std::vector<int32_t> local_rows;
+  std::vector<int32_t> global_heads, local_heads;
+  std::vector<rk::SplitChunk> chunks;
+  int64_t num_parts = 0;
+  int64_t num_mgroups = 0;
+  // device copies
+  rk::DevSeg* d_segs = nullptr;
+  rk::DevReq* d_reqs = nullptr;
+  float* d_rope_cs = nullptr;
+  rk::DenseTile* d_tiles = nullptr;
+  int32_t* d_local_rows = nullptr;
+  int32_t* d_global_heads = nullptr;
+  int32_t* d_local_heads = nullptr;
+  rk::SplitChunk* d_chunks = nullptr;
+  int32_t* d_status = nullptr;
+  size_t workspace_bytes = 0;
+};
+
+namespace rk {
+// Kernel launchers (defined in the .cu files).
+cudaError_t launch_dense_mma(const rk_seg_attn_plan_s& plan, const KernelArgs& a,
+                             cudaStream_t stream);
+cudaError_t launch_split_decode(const rk_seg_attn_plan_s& plan, const KernelArgs& a,
+                                cudaStream_t stream);
+cudaError_t launch_lse_merge(const float* o_parts, const float* lse_parts, int32_t P,
+                             int64_t rows, int32_t H, int32_t d_v, uint16_t* out,
+                             float* lse_out, cudaStream_t stream);
+}  // namespace rk

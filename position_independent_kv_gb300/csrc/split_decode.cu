@@ -1,0 +1,363 @@
+// Split-over-segments attention for single-row (decode) requests, Global
+// heads, with a fused log-sum-exp merge.
+//
+// Each CTA takes one chunk: up to a few thousand keys of ONE segment of one
+// request, for a group of 8 Global heads.  It rotates the 8 query RoPE
+// slices by the segment's -delta once (RedKnot-MLA paper, RoPE-orthogonality
+// paragraph), streams the canonical latent rows through shared memory, and
+// keeps a running (max, sum, output) per head.  The chunk's normalised
+// partial output and LSE go to the workspace; the last CTA of the request
+// (atomic ticket) merges all partials with a numerically stable
+// log-sum-exp and writes bf16 output and fp32 LSE.
+//
+// The contraction is laid out transposed: keys and d_v rows are the 16-row
+// side of the mma.sync tile and the 8 heads are the 8-column side, so no
+// tile padding is wasted on 8 heads.  The work is bound by HBM reads of the
+// latent; the tensor path only keeps arithmetic off the critical path.
+
+#include "common.cuh"
+
+namespace rk {
+namespace {
+
+constexpr int THREADS = 128;
+constexpr int TK = 64;        // keys per shared-memory tile (16 per warp)
+constexpr int NH = 8;         // heads per chunk
+
+template <int DN, int DR>
+struct SCfg {
+  static constexpr int DK = DN + DR;
+  static constexpr int QS = DN + 2 * DR + 8;
+  static constexpr int KS = DK + 8;
+  static constexpr int PS = TK + 8;
+  static constexpr int DVW = DN / 4;       // d_v rows per warp
+  static constexpr int MT = DVW / 16;      // output m-tiles per warp
+  static constexpr int KSTEPS = (DN + 2 * DR) / 16;
+  static constexpr size_t Q_BYTES = size_t(NH) * QS * 2;
+  static constexpr size_t QRO_BYTES = size_t(NH) * DR * 2;
+  static constexpr size_t K_BYTES = size_t(TK) * KS * 2;
+  static constexpr size_t P_BYTES = size_t(NH) * PS * 2;
+  static constexpr size_t SMEM = Q_BYTES + QRO_BYTES + 2 * K_BYTES + P_BYTES + 2 * 4 * NH * 4 + 16;
+};
+
+template <int DN, int DR>
+__global__ void __launch_bounds__(THREADS, 1) split_decode_kernel(const KernelArgs a) {
+  using C = SCfg<DN, DR>;
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint16_t* Qs = reinterpret_cast<uint16_t*>(smem);
+  uint16_t* Qro = reinterpret_cast<uint16_t*>(smem + C::Q_BYTES);
+  uint16_t* Ks = reinterpret_cast<uint16_t*>(smem + C::Q_BYTES + C::QRO_BYTES);
+  uint16_t* Ps = reinterpret_cast<uint16_t*>(smem + C::Q_BYTES + C::QRO_BYTES + 2 * C::K_BYTES);
+  float* red_m = reinterpret_cast<float*>(smem + C::Q_BYTES + C::QRO_BYTES + 2 * C::K_BYTES +
+                                          C::P_BYTES);
+  float* red_l = red_m + 4 * NH;
+  int* flag = reinterpret_cast<int*>(red_l + 4 * NH);
+
+  const SplitChunk ch = a.chunks[blockIdx.x];
+  const DevReq rq = a.reqs[ch.req];
+  const DevSeg sg = a.segs[ch.seg];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t4 = lane & 3;
+  const int hbase = ch.group * NH;
+  const int nh = min(NH, a.num_global - hbase);
+  const int64_t frow = rq.row_base;  // the request's single computed row
+
+  // ---- query rows of the 8 heads ----
+  {
+    constexpr int CH_N = DN / 8, CH_R = DR / 8, CH = CH_N + CH_R;
+    for (int idx = tid; idx < NH * CH; idx += THREADS) {
+      const int h = idx / CH, c = idx - h * CH;
+      const uint16_t* src = a.q;
+      int bytes = 0;
+      if (h < nh) {
+        src = a.q + (frow * a.H + a.global_heads[hbase + h]) * C::DK + c * 8;
+        bytes = 16;
+      }
+      const uint32_t dst = (c < CH_N) ? smem_u32(Qs + h * C::QS + c * 8)
+                                      : smem_u32(Qro + h * DR + (c - CH_N) * 8);
+      cp_async16(dst, src, bytes);
+    }
+    cp_async_commit();
+  }
+  auto load_keys = [&](int k0, int stage) {
+    constexpr int CH = C::DK / 8;
+    uint16_t* dstb = Ks + stage * (TK * C::KS);
+    for (int idx = tid; idx < TK * CH; idx += THREADS) {
+      const int r = idx / CH, c = idx - r * CH;
+      const int key = k0 + r;
+      const bool ok = key < ch.k1;
+      const uint16_t* src = ok ? sg.latent + int64_t(key - sg.delta) * C::DK + c * 8 : sg.latent;
+      cp_async16(smem_u32(dstb + r * C::KS + c * 8), src, ok ? 16 : 0);
+    }
+  };
+  load_keys(ch.k0, 0);
+  cp_async_commit();
+  cp_async_wait<1>();
+  __syncthreads();
+  // rotate q_rope by -delta (hi + lo bf16 parts)
+  {
+    const float* cs = a.rope_cs + int64_t(ch.seg) * DR;
+    for (int idx = tid; idx < NH * (DR / 2); idx += THREADS) {
+      const int h = idx / (DR / 2), j = idx - h * (DR / 2);
+      const float c = cs[2 * j], s = cs[2 * j + 1];
+      const uint32_t xy = *reinterpret_cast<const uint32_t*>(Qro + h * DR + 2 * j);
+      const float x = __uint_as_float(xy << 16), y = __uint_as_float(xy & 0xffff0000u);
+      const float xr = fmaf(x, c, y * s);
+      const float yr = fmaf(-x, s, y * c);
+      const uint32_t hi = pack_bf16x2(xr, yr);
+      const float xh = __uint_as_float(hi << 16), yh = __uint_as_float(hi & 0xffff0000u);
+      *reinterpret_cast<uint32_t*>(Qs + h * C::QS + DN + 2 * j) = hi;
+      *reinterpret_cast<uint32_t*>(Qs + h * C::QS + DN + DR + 2 * j) = pack_bf16x2(xr - xh, yr - yh);
+    }
+  }
+  __syncthreads();
+  // Q^T as mma B fragments (k = dims, n = heads), kept in registers
+  uint32_t qb[C::KSTEPS][2];
+  {
+    const uint32_t base = smem_u32(Qs + (lane & 7) * C::QS + 8 * (lane >> 3));
+#pragma unroll
+    for (int kk = 0; kk < C::KSTEPS / 2; ++kk) {
+      uint32_t r[4];
+      ldsm_x4(r, base + kk * 64);
+      qb[2 * kk][0] = r[0];
+      qb[2 * kk][1] = r[1];
+      qb[2 * kk + 1][0] = r[2];
+      qb[2 * kk + 1][1] = r[3];
+    }
+  }
+
+  float o[C::MT][4];
+#pragma unroll
+  for (int i = 0; i < C::MT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  float mrun[2] = {-INFINITY, -INFINITY};  // heads 2*t4, 2*t4+1
+  float lrun[2] = {0.f, 0.f};              // this warp's share of the sum
+  const float sl2 = a.scale_log2;
+  int stage = 0;
+  for (int k0 = ch.k0; k0 < ch.k1; k0 += TK) {
+    const bool more = k0 + TK < ch.k1;
+    if (more) load_keys(k0 + TK, stage ^ 1);
+    cp_async_commit();
+    cp_async_wait<1>();
+    __syncthreads();
+    const uint16_t* Kt = Ks + stage * (TK * C::KS);
+    // S^T: 16 keys of this warp x 8 heads
+    float s[4] = {0.f, 0.f, 0.f, 0.f};
+    const uint32_t ka = smem_u32(Kt + (warp * 16 + (lane & 15)) * C::KS + 8 * (lane >> 4));
+#pragma unroll
+    for (int kk = 0; kk < DN / 16; ++kk) {
+      uint32_t af[4];
+      ldsm_x4(af, ka + kk * 32);
+      mma16816(s, af, qb[kk][0], qb[kk][1]);
+    }
+#pragma unroll
+    for (int kk = 0; kk < DR / 16; ++kk) {
+      uint32_t af[4];
+      ldsm_x4(af, ka + (DN + kk * 16) * 2);
+      mma16816(s, af, qb[DN / 16 + kk][0], qb[DN / 16 + kk][1]);
+      mma16816(s, af, qb[DN / 16 + DR / 16 + kk][0], qb[DN / 16 + DR / 16 + kk][1]);
+    }
+    const int key0 = k0 + warp * 16 + g;
+    const bool v0 = key0 < ch.k1, v1 = key0 + 8 < ch.k1;
+    s[0] = v0 ? s[0] * sl2 : -INFINITY;
+    s[1] = v0 ? s[1] * sl2 : -INFINITY;
+    s[2] = v1 ? s[2] * sl2 : -INFINITY;
+    s[3] = v1 ? s[3] * sl2 : -INFINITY;
+    float mx0 = fmaxf(s[0], s[2]), mx1 = fmaxf(s[1], s[3]);
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+    }
+    if (g == 0) {
+      red_m[warp * NH + 2 * t4] = mx0;
+      red_m[warp * NH + 2 * t4 + 1] = mx1;
+    }
+    __syncthreads();
+    float alpha[2], base[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      float tm = red_m[2 * t4 + e];
+#pragma unroll
+      for (int w = 1; w < 4; ++w) tm = fmaxf(tm, red_m[w * NH + 2 * t4 + e]);
+      const float mn = fmaxf(mrun[e], tm);
+      if (mn == -INFINITY) {
+        alpha[e] = 1.f;
+        base[e] = 0.f;
+      } else {
+        alpha[e] = fast_exp2(mrun[e] - mn);
+        base[e] = mn;
+      }
+      mrun[e] = mn;
+    }
+    const float p0 = fast_exp2(s[0] - base[0]), p1 = fast_exp2(s[1] - base[1]);
+    const float p2 = fast_exp2(s[2] - base[0]), p3 = fast_exp2(s[3] - base[1]);
+    const int kl = warp * 16 + g;
+    Ps[(2 * t4) * C::PS + kl] = f32_to_bf16(p0);
+    Ps[(2 * t4 + 1) * C::PS + kl] = f32_to_bf16(p1);
+    Ps[(2 * t4) * C::PS + kl + 8] = f32_to_bf16(p2);
+    Ps[(2 * t4 + 1) * C::PS + kl + 8] = f32_to_bf16(p3);
+    float ls0 = p0 + p2, ls1 = p1 + p3;
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      ls0 += __shfl_xor_sync(0xffffffffu, ls0, off);
+      ls1 += __shfl_xor_sync(0xffffffffu, ls1, off);
+    }
+    lrun[0] = lrun[0] * alpha[0] + ls0;
+    lrun[1] = lrun[1] * alpha[1] + ls1;
+#pragma unroll
+    for (int i = 0; i < C::MT; ++i) {
+      o[i][0] *= alpha[0];
+      o[i][1] *= alpha[1];
+      o[i][2] *= alpha[0];
+      o[i][3] *= alpha[1];
+    }
+    __syncthreads();
+    // O^T[dims, heads] += V^T[dims, keys] P^T[keys, heads]
+    uint32_t pb[4][2];
+    {
+      const uint32_t pbase = smem_u32(Ps + (lane & 7) * C::PS + 8 * (lane >> 3));
+      uint32_t r[4];
+      ldsm_x4(r, pbase);
+      pb[0][0] = r[0]; pb[0][1] = r[1]; pb[1][0] = r[2]; pb[1][1] = r[3];
+      ldsm_x4(r, pbase + 64);
+      pb[2][0] = r[0]; pb[2][1] = r[1]; pb[3][0] = r[2]; pb[3][1] = r[3];
+    }
+    const uint32_t va = smem_u32(Kt + ((lane & 7) + 8 * (lane >> 4)) * C::KS + warp * C::DVW +
+                                 8 * ((lane >> 3) & 1));
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+#pragma unroll
+      for (int mt = 0; mt < C::MT; ++mt) {
+        uint32_t af[4];
+        ldsm_x4_t(af, va + (ks * 16 * C::KS + mt * 16) * 2);
+        mma16816(o[mt], af, pb[ks][0], pb[ks][1]);
+      }
+    }
+    __syncthreads();
+    stage ^= 1;
+  }
+  cp_async_wait<0>();
+
+  // ---- chunk partial: normalise by the sum over the 4 warps ----
+  if (g == 0) {
+    red_l[warp * NH + 2 * t4] = lrun[0];
+    red_l[warp * NH + 2 * t4 + 1] = lrun[1];
+  }
+  __syncthreads();
+  float lt[2];
+#pragma unroll
+  for (int e = 0; e < 2; ++e)
+    lt[e] = red_l[2 * t4 + e] + red_l[NH + 2 * t4 + e] + red_l[2 * NH + 2 * t4 + e] +
+            red_l[3 * NH + 2 * t4 + e];
+  float* wo = a.ws_o + int64_t(ch.part) * NH * DN;
+#pragma unroll
+  for (int mt = 0; mt < C::MT; ++mt) {
+    const int d0 = warp * C::DVW + mt * 16 + g;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int h = 2 * t4 + e;
+      const float inv = 1.f / lt[e];
+      wo[h * DN + d0] = o[mt][e] * inv;
+      wo[h * DN + d0 + 8] = o[mt][2 + e] * inv;
+    }
+  }
+  if (warp == 0 && g == 0) {
+    a.ws_lse[int64_t(ch.part) * NH + 2 * t4] = mrun[0] * 0.6931471805599453f + logf(lt[0]);
+    a.ws_lse[int64_t(ch.part) * NH + 2 * t4 + 1] = mrun[1] * 0.6931471805599453f + logf(lt[1]);
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) flag[0] = (atomicAdd(a.ws_ticket + ch.mgroup, 1) == ch.nparts - 1);
+  __syncthreads();
+  if (!flag[0]) return;
+  __threadfence();
+
+  // ---- last CTA of the request: log-sum-exp merge of all partials ----
+  for (int h = 0; h < nh; ++h) {
+    float m = -INFINITY;
+    for (int j = 0; j < ch.nparts; ++j)
+      m = fmaxf(m, __ldcg(a.ws_lse + int64_t(ch.part_first + j) * NH + h));
+    float ssum = 0.f;
+    for (int j = 0; j < ch.nparts; ++j)
+      ssum += __expf(__ldcg(a.ws_lse + int64_t(ch.part_first + j) * NH + h) - m);
+    const int head = a.global_heads[hbase + h];
+    uint16_t* dst = a.out + (frow * a.H + head) * DN;
+    for (int d = tid; d < DN; d += THREADS) {
+      float acc = 0.f;
+      for (int j = 0; j < ch.nparts; ++j) {
+        const int64_t pj = ch.part_first + j;
+        const float w = __expf(__ldcg(a.ws_lse + pj * NH + h) - m);
+        acc += w * __ldcg(a.ws_o + (pj * NH + h) * DN + d);
+      }
+      dst[d] = f32_to_bf16(acc / ssum);
+    }
+    if (tid == 0) a.lse[frow * a.H + head] = m + logf(ssum);
+  }
+}
+
+template <int DN, int DR>
+cudaError_t launch_t(const KernelArgs& a, cudaStream_t s) {
+  using C = SCfg<DN, DR>;
+  auto k = split_decode_kernel<DN, DR>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(C::SMEM));
+  if (e != cudaSuccess) return e;
+  k<<<a.num_chunks, THREADS, C::SMEM, s>>>(a);
+  return cudaGetLastError();
+}
+
+// Stand-alone merge: one warp per (row, head) pair.
+__global__ void lse_merge_kernel(const float* __restrict__ o_parts,
+                                 const float* __restrict__ lse_parts, int P, int64_t pairs,
+                                 int d_v, uint16_t* __restrict__ out, float* __restrict__ lse_out) {
+  const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (warp >= pairs) return;
+  float m = -INFINITY;
+  for (int j = lane; j < P; j += 32) m = fmaxf(m, lse_parts[int64_t(j) * pairs + warp]);
+#pragma unroll
+  for (int off = 16; off; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  uint16_t* dst = out + warp * d_v;
+  if (m == -INFINITY) {
+    for (int d = lane; d < d_v; d += 32) dst[d] = 0;
+    if (lane == 0) lse_out[warp] = -INFINITY;
+    return;
+  }
+  float ssum = 0.f;
+  for (int j = lane; j < P; j += 32) ssum += __expf(lse_parts[int64_t(j) * pairs + warp] - m);
+#pragma unroll
+  for (int off = 16; off; off >>= 1) ssum += __shfl_xor_sync(0xffffffffu, ssum, off);
+  const float inv = 1.f / ssum;
+  for (int d = lane; d < d_v; d += 32) {
+    float acc = 0.f;
+    for (int j = 0; j < P; ++j) {
+      const float l = lse_parts[int64_t(j) * pairs + warp];
+      if (l == -INFINITY) continue;
+      acc += __expf(l - m) * o_parts[(int64_t(j) * pairs + warp) * d_v + d];
+    }
+    dst[d] = f32_to_bf16(acc * inv);
+  }
+  if (lane == 0) lse_out[warp] = m + logf(ssum);
+}
+
+}  // namespace
+
+cudaError_t launch_split_decode(const rk_seg_attn_plan_s& plan, const KernelArgs& a,
+                                cudaStream_t s) {
+  if (plan.d_nope == 512 && plan.d_rope == 64) return launch_t<512, 64>(a, s);
+  if (plan.d_nope == 128 && plan.d_rope == 32) return launch_t<128, 32>(a, s);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_lse_merge(const float* o_parts, const float* lse_parts, int32_t P,
+                             int64_t rows, int32_t H, int32_t d_v, uint16_t* out,
+                             float* lse_out, cudaStream_t s) {
+  const int64_t pairs = rows * H;
+  const int64_t blocks = (pairs * 32 + 255) / 256;
+  if (blocks > INT32_MAX) return cudaErrorInvalidValue;
+  lse_merge_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(o_parts, lse_parts, P, pairs,
+                                                                 d_v, out, lse_out);
+  return cudaGetLastError();
+}
+
+}  // namespace rk

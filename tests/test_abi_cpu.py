@@ -1,0 +1,144 @@
+"""C-ABI checks that need no GPU: the library loads, exports every symbol the
+header declares, rejects bad descriptors before touching the device, and its
+host plan counts exactly the attended pairs the oracle's visibility rule
+gives."""
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle as O
+from position_independent_kv_gb300 import binding as B
+from position_independent_kv_gb300 import build as BUILD
+from position_independent_kv_gb300.protected import build_bitmap
+from position_independent_kv_gb300.workloads import make_geometry
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    BUILD.build()
+
+
+def _declared():
+    names = set()
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            txt = open(os.path.join(ROOT, "include", f)).read()
+            txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+            names |= set(re.findall(r"\b(rk_\w+)\s*\(", txt))
+    return names
+
+
+def test_exports_every_declared_symbol():
+    L = B.lib()
+    declared = _declared()
+    assert declared >= set(B.EXPORTS)
+    for name in declared:
+        assert hasattr(L, name), name
+
+
+def test_status_strings():
+    for code in range(12):
+        assert B.status_string(code)
+    assert B.status_string(0) == "ok"
+    assert B.status_string(999) == "unknown status"
+
+
+def _fake_addr(i, s):
+    return 0x10000000 + i * 0x1000000
+
+
+def _host_plan(name, **over):
+    wl = make_geometry(name, 0)
+    bm, _ = build_bitmap(wl)
+    from position_independent_kv_gb300.workloads import segments_for_abi
+    flat, begins = segments_for_abi(wl)
+    segs = [(_fake_addr(i, s), s[1], s[2], s[3]) for i, s in enumerate(flat)]
+    kw = dict(segments=segs, seg_begin=begins, q_row_begin=[r.q_row_begin for r in wl.requests],
+              num_heads=wl.H, d_nope=wl.d_nope, d_rope=wl.d_rope, rope_base=wl.rope_base,
+              softmax_scale=wl.scale, head_role=wl.head_role, sink=wl.sink, window=wl.window,
+              bitmap=bm, flags=B.RK_PLAN_HOST_ONLY)
+    kw.update(over)
+    return wl, B.SegAttnPlan(**kw)
+
+
+def _expect(status, **over):
+    with pytest.raises(B.RkError) as ei:
+        _host_plan("tiny", **over)
+    assert ei.value.status == status, str(ei.value)
+
+
+def test_plan_errors():
+    wl, plan = _host_plan("tiny")
+    segs = plan._keep[0]
+    _expect(2, num_heads=12)                  # not a multiple of 8
+    _expect(5, d_nope=256)                    # dims not compiled
+    _expect(2, rope_base=1.0)
+    _expect(2, softmax_scale=0.0)
+    _expect(2, window=-1)
+    _expect(2, flags=B.RK_PLAN_HOST_ONLY | 64)
+    _expect(2, q_row_begin=[576])             # beyond T
+    _expect(2, head_role=np.array([0, 0, 0, 0, 0, 0, 0, 2], np.uint8))
+    _expect(2, seg_begin=[0, 0])              # empty request
+    # overlap: second segment starts inside the first
+    bad = [segs[0], (segs[1][0], 256, 200, False), segs[2]]
+    _expect(3, segments=bad)
+    # gap: second segment leaves rows 256..299 uncovered
+    bad = [segs[0], (segs[1][0], 256, 300, False), (segs[2][0], 64, 556, True)]
+    _expect(4, segments=bad)
+    # misaligned latent pointer
+    bad = [(segs[0][0] + 8, 256, 0, False), segs[1], segs[2]]
+    _expect(10, segments=bad)
+    bad = [(0, 256, 0, False), segs[1], segs[2]]
+    _expect(1, segments=bad)
+    bad = [segs[0], (segs[1][0], 0, 256, False), segs[2]]
+    _expect(2, segments=bad)
+
+
+def test_host_only_plan_refuses_forward():
+    _, plan = _host_plan("tiny")
+    with pytest.raises(B.RkError) as ei:
+        plan.forward(0x1000, 0x2000, 0x3000, stream=0)
+    assert ei.value.status == 9
+
+
+def test_lse_merge_argument_errors():
+    L = B.lib()
+    assert L.rk_lse_merge(None, None, 1, 1, 1, 1, None, None, None) == 1
+    assert L.rk_lse_merge(16, 32, 0, 1, 1, 1, 64, 128, None) == 2
+    assert L.rk_lse_merge(16, 32, 1, 1, 1, 4096, 64, 128, None) == 2
+    assert L.rk_lse_merge(18, 32, 1, 1, 1, 8, 64, 128, None) == 10
+
+
+@pytest.mark.parametrize("name", ["tiny", "flash_mini", "varlen_mini", "ctx128k_mini",
+                                  "decode_mini", "tiny_wide", "flash", "decode"])
+def test_plan_counts_attended_pairs(name):
+    """The plan's pair accounting equals the oracle's visibility rule summed
+    over the computed rows (Global heads) and the protected computed rows
+    (Local heads)."""
+    wl, plan = _host_plan(name)
+    info = plan.info
+    _, rows = build_bitmap(wl)
+    HG = int(wl.head_role.sum())
+    HL = wl.H - HG
+    pg = pl = nprot = 0
+    for req, prot in zip(wl.requests, rows):
+        p = np.arange(req.q_row_begin, req.T)
+        pg += HG * int((p + 1).sum())
+        sel = p[prot[req.q_row_begin:]] if len(p) else p
+        nprot += len(sel)
+        if len(sel) < 5000:
+            pl += HL * sum(len(O.visible_keys(int(x), False, wl.sink, wl.window)) for x in sel)
+        else:
+            lo = np.maximum(0, sel - wl.window)
+            cnt = np.where(lo <= wl.sink, sel + 1, np.minimum(wl.sink, sel + 1) + sel - lo + 1)
+            pl += HL * int(cnt.sum())
+    assert info["rows"] == wl.rows
+    assert info["pairs_global"] == pg
+    assert info["pairs_local"] == pl
+    assert info["protected_local_rows"] == nprot
+    assert info["performed_pairs"] >= pg + pl
+    assert info["num_global_heads"] == HG and info["num_local_heads"] == HL
