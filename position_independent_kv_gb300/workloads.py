@@ -162,6 +162,10 @@ SPECS: dict[str, Spec] = {
                          seg_lengths=[130] * 5, n_new=203),
     "decode_mini": Spec("decode_mini", 64, 512, 64, 4, 256, ProtectRule(none=True),
                         decode_requests=5, decode_len_range=(300, 1500), decode_seg_range=(2, 6)),
+    # a 16K-row version of the long-context workload for profiling captures
+    # (inputs larger than L2, a few GB on the device)
+    "ctx16k": Spec("ctx16k", 128, 512, 64, 4, 256, ProtectRule(boundary=128, budget=0.25),
+                   seg_lengths=[2048] * 6, n_new=4096),
     "tiny_wide": Spec("tiny_wide", 8, 128, 32, 4, 10000, ProtectRule(boundary=16),
                       seg_lengths=[256, 256], n_new=64, shuffle=False),
 }
