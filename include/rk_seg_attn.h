@@ -201,6 +201,27 @@ rk_status_t rk_lse_merge(const float* o_parts, const float* lse_parts, int32_t P
                          int64_t rows, int32_t H, int32_t d_v, void* out, float* lse_out,
                          void* stream);
 
+/* Size of the device array that rk_seg_attn_forward_noalloc uses as scratch. */
+#define RK_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/* rk_seg_attn_forward for callers that cannot allocate device memory when
+ * they issue the forward (engines that reserve all memory up front, code
+ * that cannot reach an allocator).  The paper has no counterpart: this is a
+ * memory-management variant of rk_seg_attn_forward, with the same
+ * arguments minus the workspace and the same results.  The scratch that
+ * rk_seg_attn_forward takes as `workspace` lives instead in one file-scope
+ * device array of RK_NOALLOC_SCRATCH_BYTES bytes, which every GPU that loads
+ * the library holds until the process exits.  The call allocates nothing.
+ * All calls on a device share that array and it keeps the previous call's
+ * contents (each call clears what must start at zero); calls whose kernels
+ * overlap on the GPU race on it, so order them on one stream.  The first
+ * call on a device looks up the array's address with that device current;
+ * make that first call before any stream capture.
+ * Errors: as rk_seg_attn_forward, plus RK_ERR_CAPACITY (before any launch)
+ * when rk_seg_attn_workspace_bytes(plan) > RK_NOALLOC_SCRATCH_BYTES. */
+rk_status_t rk_seg_attn_forward_noalloc(rk_seg_attn_plan_t plan, const void* q, void* out,
+                                        float* lse, void* stream);
+
 /* Synchronise `stream`, return and clear the plan's device status word
  * (RK_OK, or RK_ERR_DEVICE_TIMEOUT if a bounded wait expired). */
 rk_status_t rk_seg_attn_last_device_status(rk_seg_attn_plan_t plan, void* stream);

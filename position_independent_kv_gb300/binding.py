@@ -20,7 +20,8 @@ RK_PLAN_LEGACY_MMA = 2
 
 EXPORTS = ["rk_seg_attn_plan", "rk_seg_attn_plan_destroy", "rk_seg_attn_plan_info",
            "rk_seg_attn_workspace_bytes", "rk_seg_attn_forward", "rk_lse_merge",
-           "rk_seg_attn_last_device_status", "rk_status_string"]
+           "rk_seg_attn_last_device_status", "rk_status_string",
+           "rk_seg_attn_forward_noalloc"]
 
 STATUS = {0: "RK_OK", 1: "RK_ERR_NULL", 2: "RK_ERR_INVALID_ARG", 3: "RK_ERR_SEGMENT_OVERLAP",
           4: "RK_ERR_SEGMENT_GAP", 5: "RK_ERR_UNSUPPORTED_DIMS", 6: "RK_ERR_CAPACITY",
@@ -86,6 +87,9 @@ def lib() -> C.CDLL:
         L.rk_seg_attn_forward.argtypes = [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
                                           C.c_void_p, C.c_size_t, C.c_void_p]
         L.rk_seg_attn_forward.restype = C.c_int
+        L.rk_seg_attn_forward_noalloc.argtypes = [C.c_void_p, C.c_void_p, C.c_void_p,
+                                                  C.c_void_p, C.c_void_p]
+        L.rk_seg_attn_forward_noalloc.restype = C.c_int
         L.rk_lse_merge.argtypes = [C.c_void_p, C.c_void_p, C.c_int32, C.c_int64, C.c_int32,
                                    C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p]
         L.rk_lse_merge.restype = C.c_int
@@ -189,6 +193,14 @@ class SegAttnPlan:
         st = lib().rk_seg_attn_forward(self._h, _ptr(q), _ptr(out), _ptr(lse), _ptr(workspace),
                                        ws_bytes, _stream(stream))
         _check(st, "rk_seg_attn_forward")
+
+    def forward_noalloc(self, q, out, lse, stream=None):
+        """rk_seg_attn_forward_noalloc: same results as forward, with the
+        scratch in the library's static device array instead of a caller
+        workspace (for callers that cannot allocate at call time)."""
+        st = lib().rk_seg_attn_forward_noalloc(self._h, _ptr(q), _ptr(out), _ptr(lse),
+                                               _stream(stream))
+        _check(st, "rk_seg_attn_forward_noalloc")
 
     def device_status(self, stream=None) -> int:
         return int(lib().rk_seg_attn_last_device_status(self._h, _stream(stream)))

@@ -20,7 +20,7 @@ BUILD = os.path.join(ROOT, "_build")
 LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "librk_seg_attn.so")
 
-SOURCES = ["plan.cpp", "dense_mma.cu", "split_decode.cu", "dense_tc.cu"]
+SOURCES = ["plan.cpp", "dense_mma.cu", "split_decode.cu", "dense_tc.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
