@@ -46,11 +46,19 @@ def peaks():
     return dict(FALLBACK), "fallback"
 
 
-def kernel_source_hash() -> str:
+KERNEL_SOURCES = {"mma_sync": ["dense_mma.cu", "common.cuh"],
+                  "tcgen05": ["dense_tc.cu", "tc_ptx.cuh", "common.cuh"]}
+
+
+def kernel_source_hash(kernel: str) -> str:
+    """Hash of the source files of one kernel (traffic records go stale when
+    these change)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "position_independent_kv_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        h.update(open(os.path.join(csrc, f), "rb").read())
+    for f in KERNEL_SOURCES[kernel]:
+        fp = os.path.join(csrc, f)
+        if os.path.exists(fp):
+            h.update(open(fp, "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -63,7 +71,7 @@ def recorded_traffic(kernel: str, workload: str):
     try:
         d = json.load(open(p))
         e = d.get(f"{kernel}:{workload}")
-        if e and e.get("source_hash") == kernel_source_hash():
+        if e and e.get("source_hash") == kernel_source_hash(kernel):
             return e.get("dram_bytes_per_launch")
     except Exception:
         return None
