@@ -21,6 +21,9 @@ LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "librk_seg_attn.so")
 
 SOURCES = ["plan.cpp", "dense_mma.cu", "split_decode.cu", "dense_tc.cu", "noalloc.cu"]
+# test-only library: single-CTA checks of the tensor-path building blocks
+SELFTEST_SOURCES = ["tc_selftest.cu"]
+SELFTEST_LIB = os.path.join(LIBDIR, "librk_tc_selftest.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -46,27 +49,33 @@ def _compile(src: str, extra: list[str]) -> str:
 
 
 def build(verbose: bool = False, extra: list[str] | None = None, force: bool = False) -> str:
+    lib = _build_lib(SOURCES, LIB, verbose, extra, force)
+    _build_lib(SELFTEST_SOURCES, SELFTEST_LIB, verbose, extra, force)
+    return lib
+
+
+def _build_lib(sources, target, verbose, extra, force) -> str:
     os.makedirs(BUILD, exist_ok=True)
     os.makedirs(LIBDIR, exist_ok=True)
-    srcs = [s for s in SOURCES if os.path.exists(os.path.join(CSRC, s))]
+    srcs = [s for s in sources if os.path.exists(os.path.join(CSRC, s))]
     deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + \
         [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE)] + [os.path.abspath(__file__)]
-    if not force and os.path.exists(LIB):
+    if not force and os.path.exists(target):
         newest = max(os.path.getmtime(d) for d in deps)
-        if os.path.getmtime(LIB) >= newest:
-            return LIB
+        if os.path.getmtime(target) >= newest:
+            return target
     extra = list(extra or [])
     with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
         objs = list(ex.map(lambda s: _compile(s, extra), srcs))
-    tmp = LIB + ".tmp"
+    tmp = target + ".tmp"
     cmd = [nvcc()] + ARCH + ["-shared", "-cudart", "shared", "-o", tmp] + objs
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, target)
     if verbose:
-        print("built", LIB)
-    return LIB
+        print("built", target)
+    return target
 
 
 if __name__ == "__main__":

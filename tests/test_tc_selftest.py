@@ -1,0 +1,48 @@
+"""Tensor-path building blocks on the GPU: tcgen05.mma with 128-byte
+swizzled shared-memory descriptors (K-major and MN-major B), A from tensor
+memory, and TMA tiled loads, each checked against a float64 matmul."""
+import ctypes
+
+import pytest
+import torch
+
+from position_independent_kv_gb300 import build as BUILD
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def selftest_lib():
+    assert torch.cuda.is_available()
+    BUILD.build()
+    L = ctypes.CDLL(BUILD.SELFTEST_LIB)
+    L.rk_tc_selftest.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                 ctypes.c_void_p, ctypes.c_void_p]
+    L.rk_tc_selftest.restype = ctypes.c_int
+    return L
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2, 3],
+                         ids=["ss_kmajor", "ss_b_mnmajor", "ts_b_mnmajor", "tma_ss_kmajor"])
+def test_tcgen05_building_blocks(selftest_lib, mode):
+    g = torch.Generator(device="cuda").manual_seed(100 + mode)
+    A = torch.randn(128, 64, device="cuda", generator=g).to(torch.bfloat16)
+    if mode in (1, 2):
+        B = torch.randn(64, 64, device="cuda", generator=g).to(torch.bfloat16)
+        ref = A.double().cpu() @ B.double().cpu()
+    else:
+        B = torch.randn(128, 64, device="cuda", generator=g).to(torch.bfloat16)
+        ref = A.double().cpu() @ B.double().cpu().T
+    D = torch.full(tuple(ref.shape), float("nan"), dtype=torch.float32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = selftest_lib.rk_tc_selftest(mode, A.data_ptr(), B.data_ptr(), D.data_ptr(),
+                                     status.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert rc == 0
+    assert int(status.item()) == 0, "a bounded wait expired"
+    got = D.double().cpu()
+    err = (got - ref).abs()
+    assert torch.isfinite(got).all(), "accumulator not fully written"
+    assert float(err.max()) <= 1e-3 * max(1.0, float(ref.abs().max())), (
+        f"mode {mode}: max err {float(err.max())}, first row got {got[0, :6].tolist()} "
+        f"want {ref[0, :6].tolist()}")
