@@ -67,26 +67,7 @@ extern "C" rk_status_t rk_seg_attn_forward_noalloc(rk_seg_attn_plan_t p, const v
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
   rk::KernelArgs a{};
-  a.q = static_cast<const uint16_t*>(q);
-  a.out = static_cast<uint16_t*>(out);
-  a.lse = lse;
-  a.segs = p->d_segs;
-  a.reqs = p->d_reqs;
-  a.rope_cs = p->d_rope_cs;
-  a.tiles = p->d_tiles;
-  a.num_tiles = static_cast<int32_t>(p->tiles.size());
-  a.local_rows = p->d_local_rows;
-  a.global_heads = p->d_global_heads;
-  a.local_heads = p->d_local_heads;
-  a.num_global = static_cast<int32_t>(p->global_heads.size());
-  a.num_local = static_cast<int32_t>(p->local_heads.size());
-  a.H = p->H;
-  a.sink = p->sink;
-  a.window = p->window;
-  a.scale_log2 = p->softmax_scale * 1.4426950408889634f;
-  a.chunks = p->d_chunks;
-  a.num_chunks = static_cast<int32_t>(p->chunks.size());
-  a.status = p->d_status;
+  rk::fill_args(*p, a, q, out, lse);
   if (p->num_parts) {
     void* base = nullptr;
     rk_status_t st = scratch_address(cur, &base);
@@ -101,7 +82,5 @@ extern "C" rk_status_t rk_seg_attn_forward_noalloc(rk_seg_attn_plan_t p, const v
     if (cudaMemsetAsync(a.ws_ticket, 0, p->num_mgroups * sizeof(int32_t), s) != cudaSuccess)
       return RK_ERR_CUDA;
   }
-  if (a.num_chunks && rk::launch_split_decode(*p, a, s) != cudaSuccess) return RK_ERR_CUDA;
-  if (a.num_tiles && rk::launch_dense_mma(*p, a, s) != cudaSuccess) return RK_ERR_CUDA;
-  return RK_OK;
+  return rk::launch_forward(*p, a, q, s) == cudaSuccess ? RK_OK : RK_ERR_CUDA;
 }

@@ -14,17 +14,21 @@
 #include <numeric>
 
 #include "rk_internal.h"
+#include "tmap.h"
 
 using rk::DenseTile;
 using rk::DevReq;
 using rk::DevSeg;
 using rk::SplitChunk;
+using rk::TcTile;
 
 namespace {
 
 constexpr int kMmaTileM = 64;     // query pairs per mma.sync tile
 constexpr int kMmaTileN = 32;     // keys per mma.sync key tile
 constexpr int kSplitHeads = 8;    // Global heads per split chunk
+constexpr int kTcM = 128;         // query pairs per tcgen05 tile
+constexpr int kTcN = 128;         // keys per tcgen05 key tile
 
 bool dims_supported(int d_nope, int d_rope) {
   return (d_nope == 512 && d_rope == 64) || (d_nope == 128 && d_rope == 32);
@@ -53,6 +57,9 @@ void free_device(rk_seg_attn_plan_s* p) {
   cudaFree(p->d_global_heads);
   cudaFree(p->d_local_heads);
   cudaFree(p->d_chunks);
+  cudaFree(p->d_tc_tiles);
+  cudaFree(p->d_segmaps);
+  cudaFree(p->d_head_role);
   cudaFree(p->d_status);
   p->d_segs = nullptr;
   p->d_reqs = nullptr;
@@ -61,6 +68,9 @@ void free_device(rk_seg_attn_plan_s* p) {
   p->d_local_rows = nullptr;
   p->d_global_heads = p->d_local_heads = nullptr;
   p->d_chunks = nullptr;
+  p->d_tc_tiles = nullptr;
+  p->d_segmaps = nullptr;
+  p->d_head_role = nullptr;
   p->d_status = nullptr;
 }
 
@@ -141,6 +151,16 @@ static rk_status_t build_plan(const rk_seg_attn_desc_t* d, rk_seg_attn_plan_s* p
   p->host_only = (d->flags & RK_PLAN_HOST_ONLY) != 0;
   p->kernel = 0;
   p->tile_m = kMmaTileM;
+  {
+    int hg = 0;
+    for (int h = 0; h < d->num_heads; ++h) hg += d->head_role[h] ? 1 : 0;
+    const bool hg_ok = hg == 0 || (kTcM % hg == 0 && (kTcM / hg) % 8 == 0);
+    const bool h_ok = d->num_heads == 64 || d->num_heads == 128;
+    if (!(d->flags & RK_PLAN_LEGACY_MMA) && d->d_nope == 512 && d->d_rope == 64 && hg_ok && h_ok) {
+      p->kernel = 1;
+      p->tile_m = kTcM;
+    }
+  }
 
   // segments, sorted by offset inside each request; contiguity check
   std::vector<int64_t> T(R), word_off(R + 1, 0);
@@ -183,6 +203,7 @@ static rk_status_t build_plan(const rk_seg_attn_desc_t* d, rk_seg_attn_plan_s* p
 
   // heads
   for (int h = 0; h < H; ++h) (d->head_role[h] ? p->global_heads : p->local_heads).push_back(h);
+  p->head_role.assign(d->head_role, d->head_role + H);
   const int HG = static_cast<int>(p->global_heads.size());
   const int HL = static_cast<int>(p->local_heads.size());
 
@@ -212,9 +233,11 @@ static rk_status_t build_plan(const rk_seg_attn_desc_t* d, rk_seg_attn_plan_s* p
     info.latent_bytes += p->segs[i].n * int64_t(d->d_nope + d->d_rope) * 2;
 
   const int TM = p->tile_m;
-  const int TN = kMmaTileN;
+  const int TN = p->kernel == 1 ? kTcN : kMmaTileN;
+  const bool tc = p->kernel == 1;
   const int64_t sink = d->sink, window = d->window;
   std::vector<std::pair<int64_t, DenseTile>> tiles;  // (cost, tile)
+  std::vector<std::pair<int64_t, TcTile>> tc_list;   // (cost, tile)
   int64_t mgroups = 0, parts = 0;
   const int groups = (HG + kSplitHeads - 1) / kSplitHeads;
   for (int r = 0; r < R; ++r) {
@@ -274,6 +297,25 @@ static rk_status_t build_plan(const rk_seg_attn_desc_t* d, rk_seg_attn_plan_s* p
         }
         ++mgroups;
       }
+    } else if (HG && tc) {
+      const int rows_per = kTcM / HG;
+      for (int64_t q0 = qb; q0 < Tr; q0 += rows_per) {
+        TcTile t{};
+        t.req = r;
+        t.kind = 0;
+        t.p0 = static_cast<int32_t>(q0);
+        t.p1 = static_cast<int32_t>(std::min<int64_t>(rows_per, Tr - q0));
+        t.key_hi = t.p0 + t.p1;
+        DenseTile shape{};
+        shape.key_hi = t.key_hi;
+        int64_t kt = 0;
+        for (int j = 0; j < rq.seg_count; ++j) {
+          const DevSeg& s = p->segs[rq.seg_first + j];
+          kt += key_tiles_in_segment(shape, s.delta, s.n, TN);
+        }
+        info.performed_pairs += kt * TN * TM;
+        tc_list.push_back({kt, t});
+      }
     } else if (HG) {
       const int rows_per = std::max(1, TM / HG);
       for (int64_t q0 = qb; q0 < Tr; q0 += rows_per) {
@@ -295,7 +337,44 @@ static rk_status_t build_plan(const rk_seg_attn_desc_t* d, rk_seg_attn_plan_s* p
       }
     }
     // Local heads on protected rows
-    if (HL && nprot) {
+    if (HL && nprot && tc) {
+      const int rows_per = kTcM / H;  // 1 or 2 rows of every head per tile
+      int64_t i = 0;
+      while (i < nprot) {
+        const int64_t pa = p->local_rows[lr_first + i];
+        int64_t pb = -1;
+        if (rows_per == 2 && i + 1 < nprot &&
+            p->local_rows[lr_first + i + 1] - pa <= window / 2 + 1)
+          pb = p->local_rows[lr_first + i + 1];
+        TcTile t{};
+        t.req = r;
+        t.kind = 1;
+        t.p0 = static_cast<int32_t>(pa);
+        t.p1 = static_cast<int32_t>(pb);
+        const int64_t plast = pb >= 0 ? pb : pa;
+        t.key_hi = static_cast<int32_t>(plast + 1);
+        const int64_t wl = std::max<int64_t>(0, pa - window);
+        if (wl <= sink) {
+          t.win_lo = 0;
+          t.sink_hi = 0;
+        } else {
+          t.win_lo = static_cast<int32_t>(wl);
+          t.sink_hi = static_cast<int32_t>(sink);
+        }
+        DenseTile shape{};
+        shape.key_hi = t.key_hi;
+        shape.win_lo = t.win_lo;
+        shape.sink_hi = t.sink_hi;
+        int64_t kt = 0;
+        for (int j = 0; j < rq.seg_count; ++j) {
+          const DevSeg& s = p->segs[rq.seg_first + j];
+          kt += key_tiles_in_segment(shape, s.delta, s.n, TN);
+        }
+        info.performed_pairs += kt * TN * TM;
+        tc_list.push_back({kt, t});
+        i += pb >= 0 ? 2 : 1;
+      }
+    } else if (HL && nprot) {
       const int64_t npairs = nprot * HL;
       const int64_t pair_base = static_cast<int64_t>(lr_first) * HL;
       int64_t i = 0;
@@ -343,7 +422,11 @@ static rk_status_t build_plan(const rk_seg_attn_desc_t* d, rk_seg_attn_plan_s* p
                    [](const auto& a, const auto& b) { return a.first > b.first; });
   p->tiles.reserve(tiles.size());
   for (auto& t : tiles) p->tiles.push_back(t.second);
-  info.dense_tiles = static_cast<int64_t>(p->tiles.size());
+  std::stable_sort(tc_list.begin(), tc_list.end(),
+                   [](const auto& a, const auto& b) { return a.first > b.first; });
+  for (auto& t : tc_list) p->tc_tiles.push_back(t.second);
+  if (p->tc_tiles.size() > (INT32_MAX / 4)) return RK_ERR_CAPACITY;
+  info.dense_tiles = static_cast<int64_t>(p->tiles.size() + p->tc_tiles.size());
   info.split_chunks = static_cast<int64_t>(p->chunks.size());
   p->num_parts = parts;
   p->num_mgroups = mgroups;
@@ -382,6 +465,20 @@ extern "C" rk_status_t rk_seg_attn_plan(const rk_seg_attn_desc_t* desc, void* st
     if (st == RK_OK) st = upload(p->global_heads, &p->d_global_heads, s);
     if (st == RK_OK) st = upload(p->local_heads, &p->d_local_heads, s);
     if (st == RK_OK) st = upload(p->chunks, &p->d_chunks, s);
+    if (st == RK_OK) st = upload(p->tc_tiles, &p->d_tc_tiles, s);
+    if (st == RK_OK) st = upload(p->head_role, &p->d_head_role, s);
+    if (st == RK_OK && p->kernel == 1) {
+      // one TMA map per segment latent: [n rows, 576 bf16], boxes of 64 x 128
+      p->segmaps.resize(p->segs.size());
+      for (size_t i = 0; i < p->segs.size() && st == RK_OK; ++i) {
+        const uint64_t dims[2] = {576, static_cast<uint64_t>(p->segs[i].n)};
+        const uint64_t strides[1] = {576 * 2};
+        const uint32_t box[2] = {64, 128};
+        if (!rk::make_tmap_bf16(&p->segmaps[i], p->segs[i].latent, 2, dims, strides, box))
+          st = RK_ERR_CUDA;
+      }
+      if (st == RK_OK) st = upload(p->segmaps, &p->d_segmaps, s);
+    }
     if (st == RK_OK) {
       if (cudaMalloc(reinterpret_cast<void**>(&p->d_status), sizeof(int32_t)) != cudaSuccess)
         st = RK_ERR_CUDA;
@@ -438,28 +535,8 @@ extern "C" rk_status_t rk_seg_attn_forward(rk_seg_attn_plan_t p, const void* q, 
   if (cudaGetDevice(&cur) != cudaSuccess) return RK_ERR_CUDA;
   if (cur != p->device) return RK_ERR_PLAN_MISMATCH;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-
   rk::KernelArgs a{};
-  a.q = static_cast<const uint16_t*>(q);
-  a.out = static_cast<uint16_t*>(out);
-  a.lse = lse;
-  a.segs = p->d_segs;
-  a.reqs = p->d_reqs;
-  a.rope_cs = p->d_rope_cs;
-  a.tiles = p->d_tiles;
-  a.num_tiles = static_cast<int32_t>(p->tiles.size());
-  a.local_rows = p->d_local_rows;
-  a.global_heads = p->d_global_heads;
-  a.local_heads = p->d_local_heads;
-  a.num_global = static_cast<int32_t>(p->global_heads.size());
-  a.num_local = static_cast<int32_t>(p->local_heads.size());
-  a.H = p->H;
-  a.sink = p->sink;
-  a.window = p->window;
-  a.scale_log2 = p->softmax_scale * 1.4426950408889634f;
-  a.chunks = p->d_chunks;
-  a.num_chunks = static_cast<int32_t>(p->chunks.size());
-  a.status = p->d_status;
+  rk::fill_args(*p, a, q, out, lse);
   if (p->num_parts) {
     char* w = static_cast<char*>(workspace);
     a.ws_o = reinterpret_cast<float*>(w);
@@ -471,14 +548,49 @@ extern "C" rk_status_t rk_seg_attn_forward(rk_seg_attn_plan_t p, const void* q, 
     if (cudaMemsetAsync(a.ws_ticket, 0, p->num_mgroups * sizeof(int32_t), s) != cudaSuccess)
       return RK_ERR_CUDA;
   }
-  if (a.num_chunks) {
-    if (rk::launch_split_decode(*p, a, s) != cudaSuccess) return RK_ERR_CUDA;
-  }
-  if (a.num_tiles) {
-    if (rk::launch_dense_mma(*p, a, s) != cudaSuccess) return RK_ERR_CUDA;
-  }
-  return RK_OK;
+  return rk::launch_forward(*p, a, q, s) == cudaSuccess ? RK_OK : RK_ERR_CUDA;
 }
+
+namespace rk {
+
+void fill_args(const rk_seg_attn_plan_s& p, KernelArgs& a, const void* q, void* out, float* lse) {
+  a.q = static_cast<const uint16_t*>(q);
+  a.out = static_cast<uint16_t*>(out);
+  a.lse = lse;
+  a.segs = p.d_segs;
+  a.reqs = p.d_reqs;
+  a.rope_cs = p.d_rope_cs;
+  a.tiles = p.d_tiles;
+  a.num_tiles = static_cast<int32_t>(p.tiles.size());
+  a.local_rows = p.d_local_rows;
+  a.global_heads = p.d_global_heads;
+  a.local_heads = p.d_local_heads;
+  a.num_global = static_cast<int32_t>(p.global_heads.size());
+  a.num_local = static_cast<int32_t>(p.local_heads.size());
+  a.H = p.H;
+  a.sink = p.sink;
+  a.window = p.window;
+  a.scale_log2 = p.softmax_scale * 1.4426950408889634f;
+  a.chunks = p.d_chunks;
+  a.num_chunks = static_cast<int32_t>(p.chunks.size());
+  a.status = p.d_status;
+  a.tc_tiles = p.d_tc_tiles;
+  a.num_tc_tiles = static_cast<int32_t>(p.tc_tiles.size());
+  a.rows_per_gtile = p.global_heads.empty() ? 0 : kTcM / static_cast<int>(p.global_heads.size());
+  a.segmaps = p.d_segmaps;
+  a.head_role = p.d_head_role;
+}
+
+cudaError_t launch_forward(const rk_seg_attn_plan_s& p, const KernelArgs& a, const void* q,
+                           cudaStream_t s) {
+  cudaError_t e = cudaSuccess;
+  if (a.num_chunks) e = launch_split_decode(p, a, s);
+  if (e == cudaSuccess && a.num_tiles) e = launch_dense_mma(p, a, s);
+  if (e == cudaSuccess && a.num_tc_tiles) e = launch_dense_tc(p, a, q, s);
+  return e;
+}
+
+}  // namespace rk
 
 extern "C" rk_status_t rk_lse_merge(const float* o_parts, const float* lse_parts, int32_t P,
                                     int64_t rows, int32_t H, int32_t d_v, void* out,

@@ -1,6 +1,7 @@
 // Internal types shared by the host plan and the CUDA kernels.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -60,6 +61,23 @@ struct SplitChunk {
   int32_t pad[3];
 };
 
+// A tile of the tcgen05 kernel: 128 query pairs.  kind 0: rows
+// [p0, p0 + p1) x every Global head (128 / HG rows per tile, head-major).
+// kind 1: protected rows p0 and p1 (p1 < 0: none) x every head (128 / H rows
+// per tile, row-major); only the Local heads are stored.  Keys visited:
+// [0, sink_hi) u [win_lo, key_hi).  Each tile runs on two CTAs, one per half
+// of d_v.
+struct TcTile {
+  int32_t req;
+  int32_t kind;
+  int32_t p0;
+  int32_t p1;
+  int32_t key_hi;
+  int32_t win_lo;
+  int32_t sink_hi;
+  int32_t pad;
+};
+
 struct KernelArgs {
   const uint16_t* q;
   uint16_t* out;
@@ -82,6 +100,11 @@ struct KernelArgs {
   float* ws_lse;              // [parts][8]
   int32_t* ws_ticket;         // [mgroups]
   int32_t* status;            // device status word
+  const TcTile* tc_tiles;
+  int32_t num_tc_tiles;
+  int32_t rows_per_gtile;     // 128 / HG
+  const CUtensorMap* segmaps; // per segment: latent [n, 576], box 64 x 128
+  const uint8_t* head_role;   // [H]
 };
 
 }  // namespace rk
@@ -103,6 +126,9 @@ struct rk_seg_attn_plan_s {
   std::vector<int32_t> local_rows;
   std::vector<int32_t> global_heads, local_heads;
   std::vector<rk::SplitChunk> chunks;
+  std::vector<rk::TcTile> tc_tiles;
+  std::vector<CUtensorMap> segmaps;
+  std::vector<uint8_t> head_role;
   int64_t num_parts = 0;
   int64_t num_mgroups = 0;
   // device copies
@@ -114,6 +140,9 @@ struct rk_seg_attn_plan_s {
   int32_t* d_global_heads = nullptr;
   int32_t* d_local_heads = nullptr;
   rk::SplitChunk* d_chunks = nullptr;
+  rk::TcTile* d_tc_tiles = nullptr;
+  CUtensorMap* d_segmaps = nullptr;
+  uint8_t* d_head_role = nullptr;
   int32_t* d_status = nullptr;
   size_t workspace_bytes = 0;
 };
@@ -124,6 +153,14 @@ cudaError_t launch_dense_mma(const rk_seg_attn_plan_s& plan, const KernelArgs& a
                              cudaStream_t stream);
 cudaError_t launch_split_decode(const rk_seg_attn_plan_s& plan, const KernelArgs& a,
                                 cudaStream_t stream);
+cudaError_t launch_dense_tc(const rk_seg_attn_plan_s& plan, const KernelArgs& a,
+                            const void* q, cudaStream_t stream);
+// Fill the kernel arguments shared by every launch of a forward.
+void fill_args(const rk_seg_attn_plan_s& plan, KernelArgs& a, const void* q, void* out,
+               float* lse);
+// Launch every kernel of a forward (split chunks, then prefill tiles).
+cudaError_t launch_forward(const rk_seg_attn_plan_s& plan, const KernelArgs& a, const void* q,
+                           cudaStream_t stream);
 cudaError_t launch_lse_merge(const float* o_parts, const float* lse_parts, int32_t P,
                              int64_t rows, int32_t H, int32_t d_v, uint16_t* out,
                              float* lse_out, cudaStream_t stream);
