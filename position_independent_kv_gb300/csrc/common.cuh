@@ -28,9 +28,10 @@ __device__ __forceinline__ uint16_t f32_to_bf16(float x) {
 }
 
 // 2^x with the hardware approximation (flush-to-zero); exp2(-inf) = 0.
+// Not volatile: the compiler may schedule it like any arithmetic.
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
-  asm volatile("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
 

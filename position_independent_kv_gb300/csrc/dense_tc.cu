@@ -3,28 +3,36 @@
 // One tile = 128 query pairs (Global: 128/HG consecutive rows x the HG
 // Global heads; Local: one or two protected rows x every head, only the
 // Local heads stored) over the tile's key range.  Two CTAs run each tile,
-// one per half of d_v (256 output columns each), because the fp32 output of
-// 128 pairs x 512 columns alone would fill tensor memory.
+// one per half of d_v (256 output columns each): the fp32 output of 128
+// pairs x 512 columns alone would fill tensor memory.
 //
-// Per CTA (256 threads, warp-specialised):
-//   warp 0  TMA producer: the 8 nope chunks of Q once (128 rows x 64 dims,
-//           128-byte swizzle), then the latent stream through a 4-slot ring
-//           of 16 KB chunks (128 keys x 64 dims): for key tile j the 9 chunks
-//           of the score contraction, then (one tile later) the 4 chunks of
-//           this CTA's d_v half again for P.V.
-//   warp 1  MMA issuer: S_j = Q K^T (M=128, N=128, K = 512 + 64 hi + 64 lo)
-//           into one of two TMEM score buffers, P.V (A = P from TMEM, B =
-//           the V chunk in MN-major form) into the 256 fp32 output columns.
-//   warps 2-3  query rotation: per segment, q_rope' = R(-delta) q_rope (fp32
-//           from the fp64-derived table) written as bf16 hi + lo chunks
-//           (RedKnot-MLA paper, RoPE-orthogonality paragraph).
-//   warps 4-7  online softmax, one thread per query pair (TMEM lane): masks
-//           (Global k <= p; Local sink u [p - w, p], RedKnot blog "Insight
-//           1"), running max in the log2 domain with a lazy rescale of the
-//           output when the max grows by more than 2^8, P (bf16) written
-//           over the score buffer, and the epilogue (normalise, bf16 store,
-//           LSE).  The running state carries across segments: each segment
-//           boundary is a log-sum-exp merge point.
+// Data movement is organised around large TMA transactions: on this part a
+// TMA load's throughput grows with its size, so Q arrives as one 128 KB box
+// and each key tile of the canonical latent as three 48 KB boxes (3 chunks of
+// 128 keys x 64 dims each, "chunk-major" so every chunk is a 128-row,
+// 128-byte-swizzled MMA operand), plus two 32 KB boxes with this CTA's half
+// of the V columns for P.V, through a 2 x 48 KB ring.
+//
+// Tensor memory (512 columns): O (256, fp32) | S (128, fp32) | P (64, bf16
+// pairs) | rotated q_rope hi (32) | lo (32).
+//
+// Roles (192 threads):
+//   warp 0     TMA producer.
+//   warp 1     MMA issuer: S_j = Q K^T (A = Q nope chunks from shared memory;
+//              for the rope chunk A = q_rope' hi and lo from TMEM), then P.V
+//              for the previous tile (A = P from TMEM, B = V in MN-major
+//              form, N = 128 columns per instruction: an MMA costs about the
+//              same time for N = 64 and N = 128) into the output columns.
+//   warps 2-5  one thread per query pair (its TMEM lane): loads S, writes the
+//              rotated q_rope of the next segment into TMEM when the key
+//              walk crosses a segment boundary (RedKnot-MLA paper,
+//              RoPE-orthogonality paragraph: the query turns by -delta_i),
+//              releases S, applies the masks (Global k <= p; Local sink u
+//              [p - w, p], RedKnot blog "Insight 1"), keeps the running max
+//              in the log2 domain with a lazy rescale of O when it grows by
+//              more than 2^8, writes P, and in the end normalises and stores
+//              O and the LSE.  The running state carries across segments:
+//              each segment boundary is a log-sum-exp merge point.
 // Every wait is bounded in time; on expiry the CTA records
 // RK_ERR_DEVICE_TIMEOUT, every role stops, the producer waits (bounded) for
 // its copies in flight and TMEM is released only after the MMA pipe drains.
@@ -38,31 +46,19 @@ namespace {
 constexpr int TM = 128;
 constexpr int TNK = 128;
 constexpr uint32_t CHUNK = 16384;
-constexpr int RING = 4;
-constexpr int THREADS = 256;
+constexpr int RING = 2;
+constexpr uint32_t SLOT = 3 * CHUNK;
+constexpr int THREADS = 192;
 constexpr uint64_t WAIT_NS = 2000000000ull;
 
 constexpr uint32_t OFF_Q = 0;
-constexpr uint32_t OFF_HI = 8 * CHUNK;
-constexpr uint32_t OFF_LO = 9 * CHUNK;
-constexpr uint32_t OFF_RING = 10 * CHUNK;
-constexpr uint32_t OFF_BAR = OFF_RING + RING * CHUNK;
-enum {
-  B_FULL = 0,
-  B_EMPTY = RING,
-  B_QFULL = 2 * RING,
-  B_SFULL = 2 * RING + 1,   // 2
-  B_PREADY = 2 * RING + 3,  // 2
-  B_ODONE = 2 * RING + 5,
-  B_RREADY,
-  B_RFREE,
-  B_FINAL,
-  NBAR
-};
+constexpr uint32_t OFF_RING = 8 * CHUNK;
+constexpr uint32_t OFF_BAR = OFF_RING + RING * SLOT;
+enum { B_FULL = 0, B_EMPTY = RING, B_QFULL = 2 * RING, B_SFULL, B_SFREE, B_PREADY, B_ODONE, B_FINAL, NBAR };
 constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
 constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;
 
-constexpr uint32_t T_O = 0, T_S0 = 256, T_S1 = 384;
+constexpr uint32_t T_O = 0, T_S = 256, T_P = 384, T_RH = 448, T_RL = 480;
 
 struct Ctx {
   uint64_t* bar;
@@ -138,9 +134,51 @@ __device__ __forceinline__ RowInfo row_info(const KernelArgs& a, const TcTile& t
   return r;
 }
 
+// q_rope' = R(-delta) q_rope of one row as bf16 hi and lo parts, written to
+// this thread's TMEM lane (columns T_RH.., T_RL..; pair j in column j).  The
+// row's q_rope (`src`, 64 bf16) is re-read from global memory each time; an
+// unused pair (src == nullptr) writes zeros.
+__device__ __forceinline__ void write_rope(uint32_t lane_taddr, const uint16_t* src,
+                                           const float* cs) {
+  uint32_t raw[32];
+  if (src) {
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const uint4 v = __ldg(s4 + u);
+      raw[4 * u] = v.x;
+      raw[4 * u + 1] = v.y;
+      raw[4 * u + 2] = v.z;
+      raw[4 * u + 3] = v.w;
+    }
+  } else {
+#pragma unroll
+    for (int u = 0; u < 32; ++u) raw[u] = 0;
+  }
+  uint32_t hi[32];
+#pragma unroll
+  for (int jj = 0; jj < 32; ++jj) {
+    const float x = __uint_as_float(raw[jj] << 16), y = __uint_as_float(raw[jj] & 0xffff0000u);
+    const float co = __ldg(cs + 2 * jj), si = __ldg(cs + 2 * jj + 1);
+    const float xr = fmaf(x, co, y * si), yr = fmaf(-x, si, y * co);
+    hi[jj] = pack_bf16x2(xr, yr);
+    raw[jj] = pack_bf16x2(xr - __uint_as_float(hi[jj] << 16),
+                          yr - __uint_as_float(hi[jj] & 0xffff0000u));
+  }
+  tc::tmem_st32(lane_taddr + T_RH, hi);
+  tc::tmem_st32(lane_taddr + T_RL, raw);
+  tc::tmem_wait_st();
+}
+
+struct QMaps {
+  CUtensorMap g5;   // Global, one Global head per group: (64, rows, groups, 8 chunks, in-group)
+  CUtensorMap g3;   // Global, any roles: (576, H, rows), box (64, 1, R)
+  CUtensorMap l4;   // Local, H = 128: (64, H, 8 chunks, rows), box (64, 128, 8, 1)
+  CUtensorMap l3;   // Local, any H: (576, H, rows), box (64, H, 1)
+};
+
 __global__ void __launch_bounds__(THREADS, 1)
-    dense_tc_kernel(const KernelArgs a, const __grid_constant__ CUtensorMap tmQg,
-                    const __grid_constant__ CUtensorMap tmQl) {
+    dense_tc_kernel(const KernelArgs a, const __grid_constant__ QMaps qm) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
@@ -163,12 +201,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     tc::mbar_init(&bar[B_QFULL], 1);
     tc::mbar_init(&bar[B_SFULL], 1);
-    tc::mbar_init(&bar[B_SFULL + 1], 1);
+    tc::mbar_init(&bar[B_SFREE], 128);
     tc::mbar_init(&bar[B_PREADY], 128);
-    tc::mbar_init(&bar[B_PREADY + 1], 128);
     tc::mbar_init(&bar[B_ODONE], 1);
-    tc::mbar_init(&bar[B_RREADY], 2);
-    tc::mbar_init(&bar[B_RFREE], 1);
     tc::mbar_init(&bar[B_FINAL], 1);
     misc[1] = 0;
     tc::fence_barrier_init();
@@ -185,36 +220,43 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer --
     if (lane == 0) {
-      tc::prefetch_tmap(&tmQg);
-      tc::prefetch_tmap(&tmQl);
       tc::mbar_arrive_expect_tx(&bar[B_QFULL], 8 * CHUNK);
-      for (int ch = 0; ch < 8; ++ch) {
-        const uint32_t dst = smem_u32(sm + OFF_Q + ch * CHUNK);
-        if (t.kind == 0) {
-          const int R = a.rows_per_gtile;
-          const int64_t fr = rq.row_base + (t.p0 - rq.q_row_begin);
-          for (int hi = 0; hi < a.num_global; ++hi)
-            tc::tma_load_3d(dst + hi * R * 128, &tmQg, &bar[B_QFULL], 64 * ch,
-                            a.global_heads[hi], static_cast<int32_t>(fr));
+      const uint32_t qdst = smem_u32(sm + OFF_Q);
+      if (t.kind == 0) {
+        const int64_t fr = rq.row_base + (t.p0 - rq.q_row_begin);
+        if (a.g_ingroup >= 0) {
+          tc::tma_load_5d(qdst, &qm.g5, &bar[B_QFULL], 0, static_cast<int32_t>(fr), 0, 0,
+                          a.g_ingroup);
         } else {
-          const int rows_per = TM / a.H;
+          const int R = a.rows_per_gtile;
+          for (int ch = 0; ch < 8; ++ch)
+            for (int hi = 0; hi < a.num_global; ++hi)
+              tc::tma_load_3d(qdst + ch * CHUNK + hi * R * 128, &qm.g3, &bar[B_QFULL], 64 * ch,
+                              a.global_heads[hi], static_cast<int32_t>(fr));
+        }
+      } else if (a.H == TM) {
+        const int64_t fr = rq.row_base + (t.p0 - rq.q_row_begin);
+        tc::tma_load_4d(qdst, &qm.l4, &bar[B_QFULL], 0, 0, 0, static_cast<int32_t>(fr));
+      } else {
+        const int rows_per = TM / a.H;
+        for (int ch = 0; ch < 8; ++ch)
           for (int ri = 0; ri < rows_per; ++ri) {
             const int pr = (ri == 0 || t.p1 < 0) ? t.p0 : t.p1;
             const int64_t fr = rq.row_base + (pr - rq.q_row_begin);
-            tc::tma_load_3d(dst + ri * a.H * 128, &tmQl, &bar[B_QFULL], 64 * ch, 0,
+            tc::tma_load_3d(qdst + ch * CHUNK + ri * a.H * 128, &qm.l3, &bar[B_QFULL], 64 * ch, 0,
                             static_cast<int32_t>(fr));
           }
-        }
       }
       uint32_t cnt = 0;
       bool ok = true;
-      auto load = [&](const KeyTile& kt, int ch) {
+      auto load = [&](const KeyTile& kt, int map, int z, uint32_t bytes) {
         const int slot = cnt % RING;
         const uint32_t ph = (cnt / RING) & 1;
         if (!wait_bar(c, B_EMPTY + slot, ph ^ 1)) return false;
-        tc::mbar_arrive_expect_tx(&bar[B_FULL + slot], CHUNK);
-        tc::tma_load_2d(smem_u32(sm + OFF_RING + slot * CHUNK), a.segmaps + rq.seg_first + kt.j,
-                        &bar[B_FULL + slot], 64 * ch, kt.k0 - segs[kt.j].delta);
+        tc::mbar_arrive_expect_tx(&bar[B_FULL + slot], bytes);
+        tc::tma_load_3d(smem_u32(sm + OFF_RING + slot * SLOT),
+                        a.segmaps + 2 * (rq.seg_first + kt.j) + map, &bar[B_FULL + slot], 0,
+                        kt.k0 - segs[kt.j].delta, z);
         ++cnt;
         return true;
       };
@@ -223,9 +265,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       bool has_prev = false;
       while (ok && (have || has_prev)) {
         if (have)
-          for (int ch = 0; ch < 9 && ok; ++ch) ok = load(cur, ch);
+          for (int b = 0; b < 3 && ok; ++b) ok = load(cur, 0, 3 * b, 3 * CHUNK);
         if (has_prev && ok)
-          for (int v = 0; v < 4 && ok; ++v) ok = load(prev, 4 * half + v);
+          for (int vb = 0; vb < 2 && ok; ++vb) ok = load(prev, 1, 4 * half + 2 * vb, 2 * CHUNK);
         prev = cur;
         has_prev = have;
         if (have) have = next_key_tile<TNK>(cur, segs, nseg, 0, r0hi, r1lo, r1hi);
@@ -241,65 +283,61 @@ __global__ void __launch_bounds__(THREADS, 1)
       bool ok = wait_bar(c, B_QFULL, 0);
       tc::tc_fence_after();
       const uint32_t idS = tc::idesc_bf16(128, 128, false, false);
-      const uint32_t idPV = tc::idesc_bf16(128, 64, false, true);
-      const uint32_t qa = smem_u32(sm + OFF_Q), ha = smem_u32(sm + OFF_HI),
-                     la = smem_u32(sm + OFF_LO), ra = smem_u32(sm + OFF_RING);
+      const uint32_t idPV = tc::idesc_bf16(128, 128, false, true);
+      const uint32_t qa = smem_u32(sm + OFF_Q), ra = smem_u32(sm + OFF_RING);
       uint32_t cnt = 0;
-      int j = 0, jprev = -1, cur_seg = -1, sidx = -1;
+      int j = 0, jprev = -1;
       KeyTile cur{0, 0, 0, -1};
       bool have = next_key_tile<TNK>(cur, segs, nseg, 0, r0hi, r1lo, r1hi);
       bool has_prev = false;
       while (ok && (have || has_prev)) {
         if (have) {
-          const uint32_t Sb = tbase + ((j & 1) ? T_S1 : T_S0);
-          if (cur.j != cur_seg) {
-            ++sidx;
-            ok = wait_bar(c, B_RREADY, sidx & 1);
-            tc::tc_fence_after();
-            cur_seg = cur.j;
-          }
-          for (int ch = 0; ch < 9 && ok; ++ch) {
+          ok = wait_bar(c, B_SFREE, j & 1);
+          if (!ok) break;
+          tc::tc_fence_after();
+          for (int b = 0; b < 3 && ok; ++b) {
             const int slot = cnt % RING;
             ok = wait_bar(c, B_FULL + slot, (cnt / RING) & 1);
             if (!ok) break;
             tc::tc_fence_after();
-            const uint32_t kb = ra + slot * CHUNK;
+            const uint32_t base = ra + slot * SLOT;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const uint64_t bd = tc::sdesc_sw128(kb + 32 * k, 16, 1024);
-              if (ch < 8) {
-                tc::mma_ss(Sb, tc::sdesc_sw128(qa + ch * CHUNK + 32 * k, 16, 1024), bd, idS,
-                           (ch | k) != 0);
-              } else {
-                tc::mma_ss(Sb, tc::sdesc_sw128(ha + 32 * k, 16, 1024), bd, idS, 1);
-                tc::mma_ss(Sb, tc::sdesc_sw128(la + 32 * k, 16, 1024), bd, idS, 1);
+            for (int ch = 0; ch < 3; ++ch) {
+              const int cc = 3 * b + ch;
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const uint64_t bd = tc::sdesc_sw128(base + ch * CHUNK + 32 * k, 16, 1024);
+                if (cc < 8) {
+                  tc::mma_ss(tbase + T_S, tc::sdesc_sw128(qa + cc * CHUNK + 32 * k, 16, 1024), bd,
+                             idS, (cc | k) != 0);
+                } else {
+                  tc::mma_ts(tbase + T_S, tbase + T_RH + 8 * k, bd, idS, 1);
+                  tc::mma_ts(tbase + T_S, tbase + T_RL + 8 * k, bd, idS, 1);
+                }
               }
             }
             tc::mma_commit(&bar[B_EMPTY + slot]);
             ++cnt;
           }
           if (!ok) break;
-          tc::mma_commit(&bar[B_SFULL + (j & 1)]);
-          KeyTile nx = cur;
-          const bool hn = next_key_tile<TNK>(nx, segs, nseg, 0, r0hi, r1lo, r1hi);
-          if (!hn || nx.j != cur.j) tc::mma_commit(&bar[B_RFREE]);
+          tc::mma_commit(&bar[B_SFULL]);
         }
         if (has_prev) {
-          const int pb = jprev & 1;
-          const uint32_t Pb = tbase + (pb ? T_S1 : T_S0);
-          ok = wait_bar(c, B_PREADY + pb, (jprev >> 1) & 1);
+          ok = wait_bar(c, B_PREADY, jprev & 1);
           if (!ok) break;
           tc::tc_fence_after();
-          for (int v = 0; v < 4 && ok; ++v) {
+          for (int vb = 0; vb < 2 && ok; ++vb) {
             const int slot = cnt % RING;
             ok = wait_bar(c, B_FULL + slot, (cnt / RING) & 1);
             if (!ok) break;
             tc::tc_fence_after();
-            const uint32_t vb = ra + slot * CHUNK;
+            const uint32_t base = ra + slot * SLOT;
+            // B = V[16 keys x 128 dims]: two 64-dim chunks 16 KB apart (LBO)
 #pragma unroll
             for (int k = 0; k < 8; ++k)
-              tc::mma_ts(tbase + T_O + 64 * v, Pb + 8 * k, tc::sdesc_sw128(vb + 2048 * k, 1024, 1024),
-                         idPV, (jprev > 0 || k > 0) ? 1u : 0u);
+              tc::mma_ts(tbase + T_O + 128 * vb, tbase + T_P + 8 * k,
+                         tc::sdesc_sw128(base + 2048 * k, CHUNK, 1024), idPV,
+                         (jprev > 0 || k > 0) ? 1u : 0u);
             tc::mma_commit(&bar[B_EMPTY + slot]);
             ++cnt;
           }
@@ -315,96 +353,67 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       tc::mma_commit(&bar[B_FINAL]);
     }
-  } else if (warp == 2 || warp == 3) {
-    // -------------------------------------------------- query rotation ----
-    // warp 2 rotates rows 0..63, warp 3 rows 64..127
-    const int mbase = (warp - 2) * 64;
-    uint32_t raw[2][32];
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const RowInfo ri = row_info(a, t, rq, mbase + lane + 32 * i);
-      if (ri.p >= 0) {
-        const uint4* src = reinterpret_cast<const uint4*>(a.q + (ri.frow * a.H + ri.head) * 576 + 512);
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const uint4 v = src[u];
-          raw[i][4 * u] = v.x;
-          raw[i][4 * u + 1] = v.y;
-          raw[i][4 * u + 2] = v.z;
-          raw[i][4 * u + 3] = v.w;
-        }
-      } else {
-#pragma unroll
-        for (int u = 0; u < 32; ++u) raw[i][u] = 0;
-      }
-    }
-    int cur_seg = -1, sidx = -1;
-    bool ok = true;
-    KeyTile kt{0, 0, 0, -1};
-    while (ok && next_key_tile<TNK>(kt, segs, nseg, 0, r0hi, r1lo, r1hi)) {
-      if (kt.j == cur_seg) continue;
-      ++sidx;
-      if (sidx > 0) ok = __all_sync(0xffffffffu, wait_bar(c, B_RFREE, (sidx - 1) & 1));
-      if (!ok) break;
-      const float* cs = a.rope_cs + static_cast<int64_t>(rq.seg_first + kt.j) * 64;
-#pragma unroll
-      for (int jj = 0; jj < 32; ++jj) {
-        const float co = __ldg(cs + 2 * jj), si = __ldg(cs + 2 * jj + 1);
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          const uint32_t m = mbase + lane + 32 * i;
-          const float x = __uint_as_float(raw[i][jj] << 16);
-          const float y = __uint_as_float(raw[i][jj] & 0xffff0000u);
-          const float xr = fmaf(x, co, y * si);
-          const float yr = fmaf(-x, si, y * co);
-          const uint32_t h2 = pack_bf16x2(xr, yr);
-          const float xh = __uint_as_float(h2 << 16), yh = __uint_as_float(h2 & 0xffff0000u);
-          const uint32_t off = tc::sw128_offset(m, 2 * jj);
-          *reinterpret_cast<uint32_t*>(sm + OFF_HI + off) = h2;
-          *reinterpret_cast<uint32_t*>(sm + OFF_LO + off) = pack_bf16x2(xr - xh, yr - yh);
-        }
-      }
-      tc::fence_proxy_async();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&bar[B_RREADY]);
-      cur_seg = kt.j;
-    }
-  } else if (warp >= 4) {
-    // --------------------------------------------------- online softmax ---
+  } else {
+    // ---------------------------------- softmax, rotation and epilogue ---
     const int quarter = warp & 3;
     const int m = quarter * 32 + lane;
     const RowInfo ri = row_info(a, t, rq, m);
-    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t lt = tbase + (static_cast<uint32_t>(quarter * 32) << 16);
     const float sl2 = a.scale_log2;
     const int sink = a.sink, window = a.window;
+    const uint16_t* qrope = ri.p >= 0 ? a.q + (ri.frow * a.H + ri.head) * 576 + 512 : nullptr;
+    KeyTile kt{0, 0, 0, -1};
+    bool have = next_key_tile<TNK>(kt, segs, nseg, 0, r0hi, r1lo, r1hi);
+    // q_rope' of the first segment, then release the (empty) S buffer
+    write_rope(lt, qrope, a.rope_cs + static_cast<int64_t>(rq.seg_first + kt.j) * 64);
+    tc::tc_fence_before();
+    tc::mbar_arrive(&bar[B_SFREE]);
     float m_run = -INFINITY, l_run = 0.f;
     int j = 0;
     bool ok = true;
-    KeyTile kt{0, 0, 0, -1};
-    while (ok && next_key_tile<TNK>(kt, segs, nseg, 0, r0hi, r1lo, r1hi)) {
-      const int b = j & 1;
-      const uint32_t Sb = tbase + lane_off + (b ? T_S1 : T_S0);
-      ok = __all_sync(0xffffffffu, wait_bar(c, B_SFULL + b, (j >> 1) & 1));
+    while (ok && have) {
+      KeyTile nx = kt;
+      const bool have_next = next_key_tile<TNK>(nx, segs, nseg, 0, r0hi, r1lo, r1hi);
+      ok = __all_sync(0xffffffffu, wait_bar(c, B_SFULL, j & 1));
       if (!ok) break;
       tc::tc_fence_after();
+      // S_j is complete, so no score MMA still reads the rotated q_rope
+      if (have_next && nx.j != kt.j)
+        write_rope(lt, qrope, a.rope_cs + static_cast<int64_t>(rq.seg_first + nx.j) * 64);
       uint32_t s[4][32];
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) tc::tmem_ld32(Sb + 32 * q4, s[q4]);
+      for (int q4 = 0; q4 < 4; ++q4) tc::tmem_ld32(lt + T_S + 32 * q4, s[q4]);
       tc::tmem_wait_ld();
-      float mx = -INFINITY;
+      tc::tc_fence_before();
+      tc::mbar_arrive(&bar[B_SFREE]);
+
+      // scores are scaled inside the exponent: x = s * scale * log2(e)
       const int p = ri.p;
+      // every key of the tile visible for this row?  (then no masks)
+      const bool full = kt.k1 - kt.k0 == TNK && kt.k0 + TNK - 1 <= p &&
+                        (ri.glob || kt.k0 >= p - window || kt.k0 + TNK <= sink);
+      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      if (__all_sync(0xffffffffu, full)) {
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
+        for (int q4 = 0; q4 < 4; ++q4)
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int key = kt.k0 + 32 * q4 + i;
-          bool vis = key < kt.k1 && key <= p;
-          if (!ri.glob) vis = vis && (key < sink || key >= p - window);
-          const float x = vis ? __uint_as_float(s[q4][i]) * sl2 : -INFINITY;
-          s[q4][i] = __float_as_uint(x);
-          mx = fmaxf(mx, x);
+          for (int i = 0; i < 32; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], __uint_as_float(s[q4][i]));
+      } else {
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int key = kt.k0 + 32 * q4 + i;
+            bool vis = key < kt.k1 && key <= p;
+            if (!ri.glob) vis = vis && (key < sink || key >= p - window);
+            const float x = vis ? __uint_as_float(s[q4][i]) : -INFINITY;
+            s[q4][i] = __float_as_uint(x);
+            mx4[i & 3] = fmaxf(mx4[i & 3], x);
+          }
         }
       }
+      const float mxs = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+      const float mx = mxs * sl2;  // sl2 > 0, so the max commutes with the scale
       bool need = false;
       float alpha = 1.f;
       if (mx > m_run + 8.f) {
@@ -414,44 +423,45 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         m_run = mx;
       }
-      const float base = (m_run == -INFINITY) ? 0.f : m_run;
-      float ls = 0.f;
+      const float nb = (m_run == -INFINITY) ? 0.f : -m_run;
+      float ls4[4] = {0.f, 0.f, 0.f, 0.f};
       // P in place: pair i of column block q4 goes to word 16 * q4 + i, i.e.
       // s[q4 >> 1][16 * (q4 & 1) + i]; every word is read before it is written
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float p0 = fast_exp2(__uint_as_float(s[q4][2 * i]) - base);
-          const float p1 = fast_exp2(__uint_as_float(s[q4][2 * i + 1]) - base);
-          ls += p0 + p1;
+          const float p0 = fast_exp2(fmaf(__uint_as_float(s[q4][2 * i]), sl2, nb));
+          const float p1 = fast_exp2(fmaf(__uint_as_float(s[q4][2 * i + 1]), sl2, nb));
+          ls4[i & 3] += p0 + p1;
           s[q4 >> 1][16 * (q4 & 1) + i] = pack_bf16x2(p0, p1);
         }
       }
+      const float ls = (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
       l_run = l_run * alpha + ls;
-      tc::tmem_st32(Sb, s[0]);
-      tc::tmem_st32(Sb + 32, s[1]);
-      tc::tmem_wait_st();
+      // the previous P.V must be done before P and O are touched
+      if (j >= 1) ok = __all_sync(0xffffffffu, wait_bar(c, B_ODONE, (j - 1) & 1));
+      if (!ok) break;
+      tc::tc_fence_after();
+      tc::tmem_st32(lt + T_P, s[0]);
+      tc::tmem_st32(lt + T_P + 32, s[1]);
       if (__any_sync(0xffffffffu, need)) {
-        if (j >= 1) ok = __all_sync(0xffffffffu, wait_bar(c, B_ODONE, (j - 1) & 1));
-        if (ok) {
-          tc::tc_fence_after();
-          const uint32_t Ob = tbase + lane_off + T_O;
 #pragma unroll 1
-          for (int q8 = 0; q8 < 8; ++q8) {
-            uint32_t o[32];
-            tc::tmem_ld32(Ob + 32 * q8, o);
-            tc::tmem_wait_ld();
+        for (int q8 = 0; q8 < 8; ++q8) {
+          uint32_t o[32];
+          tc::tmem_ld32(lt + T_O + 32 * q8, o);
+          tc::tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tc::tmem_st32(Ob + 32 * q8, o);
-          }
-          tc::tmem_wait_st();
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tc::tmem_st32(lt + T_O + 32 * q8, o);
         }
       }
+      tc::tmem_wait_st();
       tc::tc_fence_before();
-      tc::mbar_arrive(&bar[B_PREADY + b]);
+      tc::mbar_arrive(&bar[B_PREADY]);
       ++j;
+      kt = nx;
+      have = have_next;
     }
     // ---- epilogue ----
     if (ok) ok = __all_sync(0xffffffffu, wait_bar(c, B_FINAL, 0));
@@ -460,11 +470,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       const bool st = ri.store && l_run > 0.f;
       const float inv = st ? 1.f / l_run : 0.f;
       uint16_t* dst = st ? a.out + (ri.frow * a.H + ri.head) * 512 + 256 * half : nullptr;
-      const uint32_t Ob = tbase + lane_off + T_O;
 #pragma unroll 1
       for (int q8 = 0; q8 < 8; ++q8) {
         uint32_t o[32];
-        tc::tmem_ld32(Ob + 32 * q8, o);
+        tc::tmem_ld32(lt + T_O + 32 * q8, o);
         tc::tmem_wait_ld();
         if (st) {
           uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * q8);
@@ -497,18 +506,35 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 cudaError_t launch_dense_tc(const rk_seg_attn_plan_s& p, const KernelArgs& a, const void* q,
                             cudaStream_t s) {
-  CUtensorMap tg{}, tl{};
-  const uint64_t dims[3] = {576, static_cast<uint64_t>(p.H), static_cast<uint64_t>(p.info.rows)};
-  const uint64_t strides[2] = {1152, static_cast<uint64_t>(p.H) * 1152};
-  const uint32_t boxg[3] = {64, 1, static_cast<uint32_t>(a.rows_per_gtile > 0 ? a.rows_per_gtile : 8)};
-  const uint32_t boxl[3] = {64, static_cast<uint32_t>(p.H), 1};
-  if (!make_tmap_bf16(&tg, q, 3, dims, strides, boxg)) return cudaErrorInvalidValue;
-  if (!make_tmap_bf16(&tl, q, 3, dims, strides, boxl)) return cudaErrorInvalidValue;
+  QMaps qm{};
+  const uint64_t H = static_cast<uint64_t>(p.H), rows = static_cast<uint64_t>(p.info.rows);
+  const uint32_t R = static_cast<uint32_t>(a.rows_per_gtile > 0 ? a.rows_per_gtile : 8);
+  if (a.g_ingroup >= 0) {  // Global, one Global head per group of 8: the whole tile in one box
+    const uint64_t G = H / 8;
+    const uint64_t dims[5] = {64, rows, G, 8, 8};
+    const uint64_t strides[4] = {H * 1152, 8 * 1152, 128, 1152};
+    const uint32_t box[5] = {64, R, static_cast<uint32_t>(G), 8, 1};
+    if (!make_tmap_bf16(&qm.g5, q, 5, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[3] = {576, H, rows};
+    const uint64_t strides[2] = {1152, H * 1152};
+    const uint32_t boxg[3] = {64, 1, R};
+    const uint32_t boxl[3] = {64, static_cast<uint32_t>(H), 1};
+    if (!make_tmap_bf16(&qm.g3, q, 3, dims, strides, boxg)) return cudaErrorInvalidValue;
+    if (!make_tmap_bf16(&qm.l3, q, 3, dims, strides, boxl)) return cudaErrorInvalidValue;
+  }
+  if (H == TM) {
+    const uint64_t dims[4] = {64, H, 8, rows};
+    const uint64_t strides[3] = {1152, 128, H * 1152};
+    const uint32_t box[4] = {64, static_cast<uint32_t>(H), 8, 1};
+    if (!make_tmap_bf16(&qm.l4, q, 4, dims, strides, box)) return cudaErrorInvalidValue;
+  }
   cudaError_t e = cudaFuncSetAttribute(dense_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(SMEM_BYTES));
   if (e != cudaSuccess) return e;
   const int64_t grid = 2 * static_cast<int64_t>(a.num_tc_tiles);
-  dense_tc_kernel<<<static_cast<unsigned>(grid), THREADS, SMEM_BYTES, s>>>(a, tg, tl);
+  dense_tc_kernel<<<static_cast<unsigned>(grid), THREADS, SMEM_BYTES, s>>>(a, qm);
   return cudaGetLastError();
 }
 

@@ -204,6 +204,13 @@ static rk_status_t build_plan(const rk_seg_attn_desc_t* d, rk_seg_attn_plan_s* p
   // heads
   for (int h = 0; h < H; ++h) (d->head_role[h] ? p->global_heads : p->local_heads).push_back(h);
   p->head_role.assign(d->head_role, d->head_role + H);
+  if (static_cast<int>(p->global_heads.size()) == H / 8) {
+    const int c0 = p->global_heads.empty() ? -1 : p->global_heads[0];
+    bool pat = c0 >= 0 && c0 < 8;
+    for (size_t g = 0; g < p->global_heads.size() && pat; ++g)
+      pat = p->global_heads[g] == static_cast<int>(8 * g) + c0;
+    p->g_ingroup = pat ? c0 : -1;
+  }
   const int HG = static_cast<int>(p->global_heads.size());
   const int HL = static_cast<int>(p->local_heads.size());
 
@@ -468,13 +475,17 @@ extern "C" rk_status_t rk_seg_attn_plan(const rk_seg_attn_desc_t* desc, void* st
     if (st == RK_OK) st = upload(p->tc_tiles, &p->d_tc_tiles, s);
     if (st == RK_OK) st = upload(p->head_role, &p->d_head_role, s);
     if (st == RK_OK && p->kernel == 1) {
-      // one TMA map per segment latent: [n rows, 576 bf16], boxes of 64 x 128
-      p->segmaps.resize(p->segs.size());
+      // two TMA maps per segment latent, viewing a row as 9 chunks of 64
+      // bf16: (64, n, 9) so that a box lands chunk-major in shared memory;
+      // boxes of 3 chunks (scores) and 2 chunks (V columns) x 128 rows
+      p->segmaps.resize(2 * p->segs.size());
       for (size_t i = 0; i < p->segs.size() && st == RK_OK; ++i) {
-        const uint64_t dims[2] = {576, static_cast<uint64_t>(p->segs[i].n)};
-        const uint64_t strides[1] = {576 * 2};
-        const uint32_t box[2] = {64, 128};
-        if (!rk::make_tmap_bf16(&p->segmaps[i], p->segs[i].latent, 2, dims, strides, box))
+        const uint64_t dims[3] = {64, static_cast<uint64_t>(p->segs[i].n), 9};
+        const uint64_t strides[2] = {576 * 2, 128};
+        const uint32_t box3[3] = {64, 128, 3};
+        const uint32_t box2[3] = {64, 128, 2};
+        if (!rk::make_tmap_bf16(&p->segmaps[2 * i], p->segs[i].latent, 3, dims, strides, box3) ||
+            !rk::make_tmap_bf16(&p->segmaps[2 * i + 1], p->segs[i].latent, 3, dims, strides, box2))
           st = RK_ERR_CUDA;
       }
       if (st == RK_OK) st = upload(p->segmaps, &p->d_segmaps, s);
@@ -579,6 +590,7 @@ void fill_args(const rk_seg_attn_plan_s& p, KernelArgs& a, const void* q, void* 
   a.rows_per_gtile = p.global_heads.empty() ? 0 : kTcM / static_cast<int>(p.global_heads.size());
   a.segmaps = p.d_segmaps;
   a.head_role = p.d_head_role;
+  a.g_ingroup = p.g_ingroup;
 }
 
 cudaError_t launch_forward(const rk_seg_attn_plan_s& p, const KernelArgs& a, const void* q,

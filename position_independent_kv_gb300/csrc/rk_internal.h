@@ -103,8 +103,9 @@ struct KernelArgs {
   const TcTile* tc_tiles;
   int32_t num_tc_tiles;
   int32_t rows_per_gtile;     // 128 / HG
-  const CUtensorMap* segmaps; // per segment: latent [n, 576], box 64 x 128
+  const CUtensorMap* segmaps; // 2 per segment: latent viewed (64, n, 9 chunks), boxes of 3 / 2 chunks x 128 rows
   const uint8_t* head_role;   // [H]
+  int32_t g_ingroup;          // Global heads are 8g + g_ingroup for every group g, or -1
 };
 
 }  // namespace rk
@@ -117,6 +118,7 @@ struct rk_seg_attn_plan_s {
   float softmax_scale = 0.f;
   int kernel = 0;          // 0 mma.sync tiles, 1 tcgen05 tiles
   int tile_m = 64;         // query pairs per dense tile
+  int g_ingroup = -1;      // Global heads are exactly 8g + g_ingroup, else -1
   rk_plan_info_t info{};
   // host copies
   std::vector<rk::DevSeg> segs;

@@ -115,8 +115,150 @@ __global__ void __launch_bounds__(128, 1)
   if (warp == 0) tc::tmem_dealloc(tbase, 256);
 }
 
+// Streaming probe: each CTA pulls `chunks` boxes of 64 bf16 x box_rows rows
+// of a [rows, 576] bf16 tensor through a ring of `slots` shared-memory
+// buffers; one thread issues the TMA loads, another releases each buffer as
+// soon as it lands.  Measures how much data a ring depth keeps in flight.
+__global__ void __launch_bounds__(64, 1)
+    tma_stream_probe_kernel(const __grid_constant__ CUtensorMap tm, int rows, int box_rows,
+                            int box_chunks, int slots, int chunks, int32_t* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  const uint32_t box_bytes = 128u * box_rows * box_chunks;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + slots * box_bytes);
+  uint64_t* empty = full + slots;
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    for (int i = 0; i < slots; ++i) {
+      tc::mbar_init(&full[i], 1);
+      tc::mbar_init(&empty[i], 1);
+    }
+    tc::fence_barrier_init();
+  }
+  __syncthreads();
+  const int span = rows - box_rows;
+  if (tid == 0) {
+    for (int c = 0; c < chunks; ++c) {
+      const int slot = c % slots;
+      const uint32_t ph = (c / slots) & 1;
+      if (!tc::mbar_wait(&empty[slot], ph ^ 1, status, kWaitNs)) return;
+      tc::mbar_arrive_expect_tx(&full[slot], box_bytes);
+      const int t = blockIdx.x * chunks + c;
+      const int y = static_cast<int>((static_cast<int64_t>(t / 9) * box_rows) % span);
+      if (box_chunks == 1)
+        tc::tma_load_2d(smem_u32(sm + slot * box_bytes), &tm, &full[slot], 64 * (t % 9), y);
+      else
+        tc::tma_load_3d(smem_u32(sm + slot * box_bytes), &tm, &full[slot], 0, y,
+                        (t % (10 - box_chunks)));
+    }
+    for (int c = chunks > slots ? chunks - slots : 0; c < chunks; ++c)
+      tc::mbar_wait(&full[c % slots], (c / slots) & 1, status, kWaitNs);
+  } else if (tid == 32) {
+    for (int c = 0; c < chunks; ++c) {
+      const int slot = c % slots;
+      if (!tc::mbar_wait(&full[slot], (c / slots) & 1, status, kWaitNs)) return;
+      tc::mbar_arrive(&empty[slot]);
+    }
+  }
+}
+
+// MMA rate probe: one CTA issues `iters` MMAs of one shape back to back on
+// resident operands and reports the elapsed nanoseconds from the first issue
+// to the completion of the last (mode 0: SS, M=128 N=128 K=16, both K-major;
+// mode 1: TS, M=128 N=64, A from TMEM, B MN-major; mode 2: SS M=128 N=256).
+__global__ void __launch_bounds__(128, 1)
+    tc_rate_kernel(int mode, int iters, unsigned long long* ns, int32_t* status) {
+  extern __shared__ uint8_t dyn[];
+  uint8_t* sA = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  uint8_t* sB = sA + 16384;
+  __shared__ __align__(8) uint64_t bar_mma;
+  __shared__ uint32_t tmem_base;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  for (int i = tid; i < 16384 / 4; i += 128) reinterpret_cast<uint32_t*>(sA)[i] = 0x3f803f80u;
+  for (int i = tid; i < 32768 / 4; i += 128) reinterpret_cast<uint32_t*>(sB)[i] = 0x3f803f80u;
+  tc::fence_proxy_async();
+  if (warp == 0) {
+    tc::tmem_alloc(&tmem_base, 512);
+    tc::tmem_relinquish();
+  }
+  if (tid == 0) {
+    tc::mbar_init(&bar_mma, 1);
+    tc::fence_barrier_init();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tbase = tmem_base;
+  if (tid == 0) {
+    const int N = mode == 1 ? 64 : (mode == 2 ? 256 : 128);
+    const uint32_t idesc = tc::idesc_bf16(128, N, false, mode == 1);
+    const uint64_t ad = tc::sdesc_sw128(smem_u32(sA), 16, 1024);
+    const uint64_t bd = mode == 1 ? tc::sdesc_sw128(smem_u32(sB), 1024, 1024)
+                                  : tc::sdesc_sw128(smem_u32(sB), 16, 1024);
+    const uint64_t t0 = tc::global_ns();
+    for (int i = 0; i < iters; ++i) {
+      if (mode == 1)
+        tc::mma_ts(tbase, tbase + 256, bd, idesc, i > 0);
+      else
+        tc::mma_ss(tbase, ad, bd, idesc, i > 0);
+    }
+    tc::mma_commit(&bar_mma);
+    tc::mbar_wait(&bar_mma, 0, status, kWaitNs);
+    ns[0] = tc::global_ns() - t0;
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tbase, 512);
+}
+
 }  // namespace
 }  // namespace rk
+
+extern "C" int rk_tc_mma_rate(int mode, int iters, unsigned long long* ns, int32_t* status,
+                              void* stream) {
+  if (mode < 0 || mode > 2 || iters < 1) return -1;
+  const int smem = 16384 + 32768 + 1024;
+  cudaError_t e = cudaFuncSetAttribute(rk::tc_rate_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return static_cast<int>(e);
+  rk::tc_rate_kernel<<<1, 128, smem, static_cast<cudaStream_t>(stream)>>>(mode, iters, ns, status);
+  return static_cast<int>(cudaGetLastError());
+}
+
+// TMA streaming probe (see above).  lat: device bf16 [rows, 576].  Returns 0
+// or -1 (bad arguments / tensor map) or the launch error.
+extern "C" int rk_tma_stream_probe(const void* lat, int rows, int box_rows, int box_chunks,
+                                   int slots, int chunks, int ctas, int32_t* status,
+                                   void* stream) {
+  if (box_rows < 8 || box_rows > 256 || slots < 1 || slots > 13 || rows <= box_rows) return -1;
+  if (box_chunks < 1 || box_chunks > 9) return -1;
+  const int64_t bb = static_cast<int64_t>(128) * box_rows * box_chunks;
+  if (slots * bb > 200 * 1024) return -1;
+  CUtensorMap tm{};
+  if (box_chunks == 1) {
+    const uint64_t dims[2] = {576, static_cast<uint64_t>(rows)};
+    const uint64_t strides[1] = {1152};
+    const uint32_t box[2] = {64, static_cast<uint32_t>(box_rows)};
+    if (!rk::make_tmap_bf16(&tm, lat, 2, dims, strides, box)) return -1;
+  } else {
+    // the row viewed as 9 chunks of 64: dims (64, rows, 9), the box lands
+    // chunk-major in shared memory
+    const uint64_t dims[3] = {64, static_cast<uint64_t>(rows), 9};
+    const uint64_t strides[2] = {1152, 128};
+    const uint32_t box[3] = {64, static_cast<uint32_t>(box_rows), static_cast<uint32_t>(box_chunks)};
+    if (!rk::make_tmap_bf16(&tm, lat, 3, dims, strides, box)) return -2;
+  }
+  const size_t smem = static_cast<size_t>(slots * bb) + 2 * 13 * 8 + 1024;
+  cudaError_t e = cudaFuncSetAttribute(rk::tma_stream_probe_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return static_cast<int>(e);
+  rk::tma_stream_probe_kernel<<<ctas, 64, smem, static_cast<cudaStream_t>(stream)>>>(
+      tm, rows, box_rows, box_chunks, slots, chunks, status);
+  return static_cast<int>(cudaGetLastError());
+}
 
 // mode: see the file comment.  A, B: device bf16 row-major; D: device fp32
 // [128, N] (N = 128 for modes 0 and 3, 64 for modes 1 and 2); status: device
