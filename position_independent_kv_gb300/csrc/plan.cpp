@@ -59,8 +59,14 @@ void free_device(rk_seg_attn_plan_s* p) {
   cudaFree(p->d_chunks);
   cudaFree(p->d_tc_tiles);
   cudaFree(p->d_segmaps);
+  cudaFree(p->d_decmaps);
   cudaFree(p->d_head_role);
   cudaFree(p->d_status);
+  if (p->side) cudaStreamDestroy(p->side);
+  if (p->ev_fork) cudaEventDestroy(p->ev_fork);
+  if (p->ev_join) cudaEventDestroy(p->ev_join);
+  p->side = nullptr;
+  p->ev_fork = p->ev_join = nullptr;
   p->d_segs = nullptr;
   p->d_reqs = nullptr;
   p->d_rope_cs = nullptr;
@@ -70,6 +76,7 @@ void free_device(rk_seg_attn_plan_s* p) {
   p->d_chunks = nullptr;
   p->d_tc_tiles = nullptr;
   p->d_segmaps = nullptr;
+  p->d_decmaps = nullptr;
   p->d_head_role = nullptr;
   p->d_status = nullptr;
 }
@@ -490,10 +497,29 @@ extern "C" rk_status_t rk_seg_attn_plan(const rk_seg_attn_desc_t* desc, void* st
       }
       if (st == RK_OK) st = upload(p->segmaps, &p->d_segmaps, s);
     }
+    if (st == RK_OK && !p->chunks.empty() && p->d_nope == 512 && p->d_rope == 64 &&
+        !(desc->flags & RK_PLAN_LEGACY_MMA)) {
+      // split-over-segments chunks stream 32-row boxes of whole latent rows
+      p->decmaps.resize(p->segs.size());
+      for (size_t i = 0; i < p->segs.size() && st == RK_OK; ++i) {
+        const uint64_t dims[3] = {64, static_cast<uint64_t>(p->segs[i].n), 9};
+        const uint64_t strides[2] = {576 * 2, 128};
+        const uint32_t box[3] = {64, 32, 9};
+        if (!rk::make_tmap_bf16(&p->decmaps[i], p->segs[i].latent, 3, dims, strides, box))
+          st = RK_ERR_CUDA;
+      }
+      if (st == RK_OK) st = upload(p->decmaps, &p->d_decmaps, s);
+    }
     if (st == RK_OK) {
       if (cudaMalloc(reinterpret_cast<void**>(&p->d_status), sizeof(int32_t)) != cudaSuccess)
         st = RK_ERR_CUDA;
       else if (cudaMemsetAsync(p->d_status, 0, sizeof(int32_t), s) != cudaSuccess)
+        st = RK_ERR_CUDA;
+    }
+    if (st == RK_OK && !p->chunks.empty() && (!p->tiles.empty() || !p->tc_tiles.empty())) {
+      if (cudaStreamCreateWithFlags(&p->side, cudaStreamNonBlocking) != cudaSuccess ||
+          cudaEventCreateWithFlags(&p->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
+          cudaEventCreateWithFlags(&p->ev_join, cudaEventDisableTiming) != cudaSuccess)
         st = RK_ERR_CUDA;
     }
     // host vectors are pageable: make the uploads complete before returning
@@ -591,14 +617,28 @@ void fill_args(const rk_seg_attn_plan_s& p, KernelArgs& a, const void* q, void* 
   a.segmaps = p.d_segmaps;
   a.head_role = p.d_head_role;
   a.g_ingroup = p.g_ingroup;
+  a.decmaps = p.d_decmaps;
 }
 
 cudaError_t launch_forward(const rk_seg_attn_plan_s& p, const KernelArgs& a, const void* q,
                            cudaStream_t s) {
   cudaError_t e = cudaSuccess;
-  if (a.num_chunks) e = launch_split_decode(p, a, s);
-  if (e == cudaSuccess && a.num_tiles) e = launch_dense_mma(p, a, s);
-  if (e == cudaSuccess && a.num_tc_tiles) e = launch_dense_tc(p, a, q, s);
+  // prefill tiles overlap the split chunks on the plan's side stream
+  cudaStream_t ts = s;
+  if (p.side && a.num_chunks && (a.num_tiles || a.num_tc_tiles)) {
+    e = cudaEventRecord(p.ev_fork, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(p.side, p.ev_fork, 0);
+    if (e != cudaSuccess) return e;
+    ts = p.side;
+  }
+  if (a.num_tiles) e = launch_dense_mma(p, a, ts);
+  if (e == cudaSuccess && a.num_tc_tiles) e = launch_dense_tc(p, a, q, ts);
+  if (e == cudaSuccess && a.num_chunks) e = launch_split_decode(p, a, s);
+  if (ts != s) {
+    const cudaError_t e1 = cudaEventRecord(p.ev_join, ts);
+    const cudaError_t e2 = e1 == cudaSuccess ? cudaStreamWaitEvent(s, p.ev_join, 0) : e1;
+    if (e == cudaSuccess) e = e2;
+  }
   return e;
 }
 

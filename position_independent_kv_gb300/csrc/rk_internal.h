@@ -106,6 +106,7 @@ struct KernelArgs {
   const CUtensorMap* segmaps; // 2 per segment: latent viewed (64, n, 9 chunks), boxes of 3 / 2 chunks x 128 rows
   const uint8_t* head_role;   // [H]
   int32_t g_ingroup;          // Global heads are 8g + g_ingroup for every group g, or -1
+  const CUtensorMap* decmaps; // per segment: latent viewed (64, n, 9 chunks), box 32 rows x 9 chunks
 };
 
 }  // namespace rk
@@ -130,6 +131,7 @@ struct rk_seg_attn_plan_s {
   std::vector<rk::SplitChunk> chunks;
   std::vector<rk::TcTile> tc_tiles;
   std::vector<CUtensorMap> segmaps;
+  std::vector<CUtensorMap> decmaps;
   std::vector<uint8_t> head_role;
   int64_t num_parts = 0;
   int64_t num_mgroups = 0;
@@ -144,9 +146,14 @@ struct rk_seg_attn_plan_s {
   rk::SplitChunk* d_chunks = nullptr;
   rk::TcTile* d_tc_tiles = nullptr;
   CUtensorMap* d_segmaps = nullptr;
+  CUtensorMap* d_decmaps = nullptr;
   uint8_t* d_head_role = nullptr;
   int32_t* d_status = nullptr;
   size_t workspace_bytes = 0;
+  // when a forward has both split chunks and prefill tiles, the tiles run on
+  // this plan-owned stream, forked from and joined back to the caller's
+  cudaStream_t side = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
 };
 
 namespace rk {

@@ -16,6 +16,7 @@
 // latent; the tensor path only keeps arithmetic off the critical path.
 
 #include "common.cuh"
+#include "tc_ptx.cuh"
 
 namespace rk {
 namespace {
@@ -295,6 +296,324 @@ __global__ void __launch_bounds__(THREADS, 1) split_decode_kernel(const KernelAr
   }
 }
 
+
+// ---------------------------------------------------------------------------
+// d = (512, 64) version fed by TMA: each stage is one 3-D box of 32 keys x 9
+// chunks of 64 dims (36 KB of whole 1152-byte latent rows, laid out
+// chunk-major with the 128-byte swizzle), four stages deep; fragment
+// addresses apply the same XOR swizzle, so the ldmatrix reads are
+// conflict-free.  The scores of the 32 keys are split over the four warps
+// (two key halves x two halves of d_k); all four warps take 128 output rows
+// each of P.V.
+constexpr int DT_TK = 32;
+constexpr int DT_ST = 4;
+constexpr uint32_t DT_CH = DT_TK * 128;        // one 64-dim chunk of a stage
+constexpr uint32_t DT_STAGE = 9 * DT_CH;       // 36,864 B
+constexpr uint64_t DT_WAIT_NS = 2000000000ull;
+constexpr int DT_QS = 512 + 128 + 8;
+constexpr int DT_PS = DT_TK + 8;
+constexpr size_t DT_SMEM = 1024 + DT_ST * DT_STAGE + NH * DT_QS * 2 + NH * 64 * 2 + NH * DT_PS * 2 +
+                           (2 + 4) * NH * 4 + 16 + DT_ST * 8 + 2 * 32 * 4 * 4;
+
+__global__ void __launch_bounds__(THREADS, 1) split_decode_tma_kernel(const KernelArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  uint8_t* Kst = sm;
+  uint16_t* Qs = reinterpret_cast<uint16_t*>(sm + DT_ST * DT_STAGE);
+  uint16_t* Qro = Qs + NH * DT_QS;
+  uint16_t* Ps = Qro + NH * 64;
+  float* red_m = reinterpret_cast<float*>(Ps + NH * DT_PS);
+  float* red_l = red_m + 2 * NH;
+  int* flag = reinterpret_cast<int*>(red_l + 4 * NH);
+  uint64_t* full = reinterpret_cast<uint64_t*>(flag + 4);
+  float* part = reinterpret_cast<float*>(full + DT_ST);  // [2 key halves][32 lanes][4]
+
+  const SplitChunk ch = a.chunks[blockIdx.x];
+  const DevReq rq = a.reqs[ch.req];
+  const DevSeg sg = a.segs[ch.seg];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t4 = lane & 3;
+  const int hbase = ch.group * NH;
+  const int nh = min(NH, a.num_global - hbase);
+  const int64_t frow = rq.row_base;
+  const int ntiles = (ch.k1 - ch.k0 + DT_TK - 1) / DT_TK;
+  const CUtensorMap* map = a.decmaps + ch.seg;
+
+  if (tid == 0) {
+    for (int s = 0; s < DT_ST; ++s) tc::mbar_init(&full[s], 1);
+    tc::fence_barrier_init();
+  }
+  __syncthreads();
+  if (tid == 0) {
+    tc::prefetch_tmap(map);
+    for (int s = 0; s < DT_ST && s < ntiles; ++s) {
+      tc::mbar_arrive_expect_tx(&full[s], DT_STAGE);
+      tc::tma_load_3d(smem_u32(Kst + s * DT_STAGE), map, &full[s], 0,
+                      ch.k0 - sg.delta + s * DT_TK, 0);
+    }
+  }
+  // ---- query rows of the 8 heads ----
+  {
+    constexpr int CH_N = 512 / 8, CH = CH_N + 8;
+    for (int idx = tid; idx < NH * CH; idx += THREADS) {
+      const int h = idx / CH, c = idx - h * CH;
+      const uint16_t* src = a.q;
+      int bytes = 0;
+      if (h < nh) {
+        src = a.q + (frow * a.H + a.global_heads[hbase + h]) * 576 + c * 8;
+        bytes = 16;
+      }
+      const uint32_t dst = (c < CH_N) ? smem_u32(Qs + h * DT_QS + c * 8)
+                                      : smem_u32(Qro + h * 64 + (c - CH_N) * 8);
+      cp_async16(dst, src, bytes);
+    }
+    cp_async_commit();
+    cp_async_wait<0>();
+  }
+  __syncthreads();
+  {
+    const float* cs = a.rope_cs + int64_t(ch.seg) * 64;
+    for (int idx = tid; idx < NH * 32; idx += THREADS) {
+      const int h = idx >> 5, j = idx & 31;
+      const float c = cs[2 * j], s = cs[2 * j + 1];
+      const uint32_t xy = *reinterpret_cast<const uint32_t*>(Qro + h * 64 + 2 * j);
+      const float x = __uint_as_float(xy << 16), y = __uint_as_float(xy & 0xffff0000u);
+      const float xr = fmaf(x, c, y * s), yr = fmaf(-x, s, y * c);
+      const uint32_t hi = pack_bf16x2(xr, yr);
+      const float xh = __uint_as_float(hi << 16), yh = __uint_as_float(hi & 0xffff0000u);
+      *reinterpret_cast<uint32_t*>(Qs + h * DT_QS + 512 + 2 * j) = hi;
+      *reinterpret_cast<uint32_t*>(Qs + h * DT_QS + 576 + 2 * j) = pack_bf16x2(xr - xh, yr - yh);
+    }
+  }
+  __syncthreads();
+  uint32_t qb[40][2];
+  {
+    const uint32_t base = smem_u32(Qs + (lane & 7) * DT_QS + 8 * (lane >> 3));
+#pragma unroll
+    for (int kk = 0; kk < 20; ++kk) {
+      uint32_t r[4];
+      ldsm_x4(r, base + kk * 64);
+      qb[2 * kk][0] = r[0];
+      qb[2 * kk][1] = r[1];
+      qb[2 * kk + 1][0] = r[2];
+      qb[2 * kk + 1][1] = r[3];
+    }
+  }
+
+  float o[8][4];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  float mrun[2] = {-INFINITY, -INFINITY};
+  float lrun[2] = {0.f, 0.f};
+  const float sl2 = a.scale_log2;
+  bool ok = true;
+  int i = 0;
+  for (; i < ntiles; ++i) {
+    const int s = i % DT_ST;
+    const bool got = tc::mbar_wait(&full[s], (i / DT_ST) & 1, a.status, DT_WAIT_NS);
+    ok = __syncthreads_and(got) != 0;
+    if (!ok) break;
+    const uint32_t st = smem_u32(Kst + s * DT_STAGE);
+    const int k0 = ch.k0 + i * DT_TK;
+    // scores: warp w takes keys 16 * (w >> 1).. over half of the 40 k-steps
+    // (w even: nope 0..19; w odd: nope 20..31 + rope hi and lo), on two
+    // interleaved accumulators; the halves are added through shared memory
+    float sc[4] = {0.f, 0.f, 0.f, 0.f};
+    {
+      float sd[4] = {0.f, 0.f, 0.f, 0.f};
+      const int kq = warp >> 1, dh = warp & 1;
+      const int r = kq * 16 + (lane & 15);
+      const uint32_t rb = st + r * 128;
+      const uint32_t rs = r & 7, hl = lane >> 4;
+      // byte address of this lane's 16-byte row segment for k-step kk
+      auto kaddr = [&](int kk) -> uint32_t {
+        const uint32_t unit = ((static_cast<uint32_t>(kk) & 3u) << 1) | hl;
+        return rb + static_cast<uint32_t>(kk >> 2) * DT_CH + ((unit ^ rs) << 4);
+      };
+      if (dh == 0) {
+#pragma unroll
+        for (int kk = 0; kk < 20; kk += 2) {
+          uint32_t a0[4], a1[4];
+          ldsm_x4(a0, kaddr(kk));
+          ldsm_x4(a1, kaddr(kk + 1));
+          mma16816(sc, a0, qb[kk][0], qb[kk][1]);
+          mma16816(sd, a1, qb[kk + 1][0], qb[kk + 1][1]);
+        }
+      } else {
+#pragma unroll
+        for (int kk = 20; kk < 32; kk += 2) {
+          uint32_t a0[4], a1[4];
+          ldsm_x4(a0, kaddr(kk));
+          ldsm_x4(a1, kaddr(kk + 1));
+          mma16816(sc, a0, qb[kk][0], qb[kk][1]);
+          mma16816(sd, a1, qb[kk + 1][0], qb[kk + 1][1]);
+        }
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          uint32_t af[4];
+          ldsm_x4(af, kaddr(32 + kk));
+          mma16816(sc, af, qb[32 + kk][0], qb[32 + kk][1]);
+          mma16816(sd, af, qb[36 + kk][0], qb[36 + kk][1]);
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sc[e] += sd[e];
+      if (dh == 1) *reinterpret_cast<float4*>(part + (kq * 32 + lane) * 4) =
+          make_float4(sc[0], sc[1], sc[2], sc[3]);
+    }
+    __syncthreads();
+    if ((warp & 1) == 0) {
+      const int kq = warp >> 1;
+      const float4 pt = *reinterpret_cast<const float4*>(part + (kq * 32 + lane) * 4);
+      sc[0] += pt.x;
+      sc[1] += pt.y;
+      sc[2] += pt.z;
+      sc[3] += pt.w;
+      const int key0 = k0 + kq * 16 + g;
+      const bool v0 = key0 < ch.k1, v1 = key0 + 8 < ch.k1;
+      sc[0] = v0 ? sc[0] * sl2 : -INFINITY;
+      sc[1] = v0 ? sc[1] * sl2 : -INFINITY;
+      sc[2] = v1 ? sc[2] * sl2 : -INFINITY;
+      sc[3] = v1 ? sc[3] * sl2 : -INFINITY;
+      float mx0 = fmaxf(sc[0], sc[2]), mx1 = fmaxf(sc[1], sc[3]);
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+      }
+      if (g == 0) {
+        red_m[kq * NH + 2 * t4] = mx0;
+        red_m[kq * NH + 2 * t4 + 1] = mx1;
+      }
+    }
+    __syncthreads();
+    float alpha[2], base[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const float tm = fmaxf(red_m[2 * t4 + e], red_m[NH + 2 * t4 + e]);
+      const float mn = fmaxf(mrun[e], tm);
+      if (mn == -INFINITY) {
+        alpha[e] = 1.f;
+        base[e] = 0.f;
+      } else {
+        alpha[e] = fast_exp2(mrun[e] - mn);
+        base[e] = mn;
+      }
+      mrun[e] = mn;
+    }
+    if ((warp & 1) == 0) {
+      const float p0 = fast_exp2(sc[0] - base[0]), p1 = fast_exp2(sc[1] - base[1]);
+      const float p2 = fast_exp2(sc[2] - base[0]), p3 = fast_exp2(sc[3] - base[1]);
+      const int kl = (warp >> 1) * 16 + g;
+      Ps[(2 * t4) * DT_PS + kl] = f32_to_bf16(p0);
+      Ps[(2 * t4 + 1) * DT_PS + kl] = f32_to_bf16(p1);
+      Ps[(2 * t4) * DT_PS + kl + 8] = f32_to_bf16(p2);
+      Ps[(2 * t4 + 1) * DT_PS + kl + 8] = f32_to_bf16(p3);
+      float ls0 = p0 + p2, ls1 = p1 + p3;
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        ls0 += __shfl_xor_sync(0xffffffffu, ls0, off);
+        ls1 += __shfl_xor_sync(0xffffffffu, ls1, off);
+      }
+      lrun[0] = lrun[0] * alpha[0] + ls0;
+      lrun[1] = lrun[1] * alpha[1] + ls1;
+    }
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      o[mt][0] *= alpha[0];
+      o[mt][1] *= alpha[1];
+      o[mt][2] *= alpha[0];
+      o[mt][3] *= alpha[1];
+    }
+    __syncthreads();
+    // O^T[dims, heads] += V^T[dims, keys] P^T[keys, heads]; warp w: dims 128w..
+    uint32_t pb[2][2];
+    {
+      uint32_t r[4];
+      ldsm_x4(r, smem_u32(Ps + (lane & 7) * DT_PS + 8 * (lane >> 3)));
+      pb[0][0] = r[0]; pb[0][1] = r[1]; pb[1][0] = r[2]; pb[1][1] = r[3];
+    }
+#pragma unroll
+    for (int ks = 0; ks < 2; ++ks) {
+      const int key = 16 * ks + (lane & 7) + 8 * (lane >> 4);
+      const uint32_t kb = st + key * 128;
+      const uint32_t ks7 = key & 7;
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        const int dim = 128 * warp + 16 * mt + 8 * ((lane >> 3) & 1);
+        uint32_t af[4];
+        ldsm_x4_t(af, kb + (dim >> 6) * DT_CH + ((((dim & 63) >> 3) ^ ks7) << 4));
+        mma16816(o[mt], af, pb[ks][0], pb[ks][1]);
+      }
+    }
+    __syncthreads();
+    if (tid == 0 && i + DT_ST < ntiles) {
+      tc::mbar_arrive_expect_tx(&full[s], DT_STAGE);
+      tc::tma_load_3d(st, map, &full[s], 0, ch.k0 - sg.delta + (i + DT_ST) * DT_TK, 0);
+    }
+  }
+  if (!ok) {
+    // drain the copies still in flight before the CTA exits
+    if (tid == 0)
+      for (int k = i; k < ntiles && k < i + DT_ST; ++k)
+        tc::mbar_wait(&full[k % DT_ST], (k / DT_ST) & 1, a.status, DT_WAIT_NS);
+    return;
+  }
+
+  // ---- chunk partial ----
+  if ((warp & 1) == 0 && g == 0) {
+    red_l[(warp >> 1) * NH + 2 * t4] = lrun[0];
+    red_l[(warp >> 1) * NH + 2 * t4 + 1] = lrun[1];
+  }
+  __syncthreads();
+  float lt[2];
+#pragma unroll
+  for (int e = 0; e < 2; ++e) lt[e] = red_l[2 * t4 + e] + red_l[NH + 2 * t4 + e];
+  float* wo = a.ws_o + int64_t(ch.part) * NH * 512;
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt) {
+    const int d0 = 128 * warp + mt * 16 + g;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int h = 2 * t4 + e;
+      const float inv = 1.f / lt[e];
+      wo[h * 512 + d0] = o[mt][e] * inv;
+      wo[h * 512 + d0 + 8] = o[mt][2 + e] * inv;
+    }
+  }
+  if (warp == 0 && g == 0) {
+    a.ws_lse[int64_t(ch.part) * NH + 2 * t4] = mrun[0] * 0.6931471805599453f + logf(lt[0]);
+    a.ws_lse[int64_t(ch.part) * NH + 2 * t4 + 1] = mrun[1] * 0.6931471805599453f + logf(lt[1]);
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) flag[0] = (atomicAdd(a.ws_ticket + ch.mgroup, 1) == ch.nparts - 1);
+  __syncthreads();
+  if (!flag[0]) return;
+  __threadfence();
+  for (int h = 0; h < nh; ++h) {
+    float m = -INFINITY;
+    for (int j = 0; j < ch.nparts; ++j)
+      m = fmaxf(m, __ldcg(a.ws_lse + int64_t(ch.part_first + j) * NH + h));
+    float ssum = 0.f;
+    for (int j = 0; j < ch.nparts; ++j)
+      ssum += __expf(__ldcg(a.ws_lse + int64_t(ch.part_first + j) * NH + h) - m);
+    const int head = a.global_heads[hbase + h];
+    uint16_t* dst = a.out + (frow * a.H + head) * 512;
+    for (int d = tid; d < 512; d += THREADS) {
+      float acc = 0.f;
+      for (int j = 0; j < ch.nparts; ++j) {
+        const int64_t pj = ch.part_first + j;
+        const float w = __expf(__ldcg(a.ws_lse + pj * NH + h) - m);
+        acc += w * __ldcg(a.ws_o + (pj * NH + h) * 512 + d);
+      }
+      dst[d] = f32_to_bf16(acc / ssum);
+    }
+    if (tid == 0) a.lse[frow * a.H + head] = m + logf(ssum);
+  }
+}
+
 template <int DN, int DR>
 cudaError_t launch_t(const KernelArgs& a, cudaStream_t s) {
   using C = SCfg<DN, DR>;
@@ -344,6 +663,14 @@ __global__ void lse_merge_kernel(const float* __restrict__ o_parts,
 
 cudaError_t launch_split_decode(const rk_seg_attn_plan_s& plan, const KernelArgs& a,
                                 cudaStream_t s) {
+  if (plan.d_nope == 512 && plan.d_rope == 64 && a.decmaps) {
+    cudaError_t e = cudaFuncSetAttribute(split_decode_tma_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(DT_SMEM));
+    if (e != cudaSuccess) return e;
+    split_decode_tma_kernel<<<a.num_chunks, THREADS, DT_SMEM, s>>>(a);
+    return cudaGetLastError();
+  }
   if (plan.d_nope == 512 && plan.d_rope == 64) return launch_t<512, 64>(a, s);
   if (plan.d_nope == 128 && plan.d_rope == 32) return launch_t<128, 32>(a, s);
   return cudaErrorInvalidValue;
