@@ -8,10 +8,12 @@
 //
 // Data movement is organised around large TMA transactions: on this part a
 // TMA load's throughput grows with its size, so Q arrives as one 128 KB box
-// and each key tile of the canonical latent as three 48 KB boxes (3 chunks of
+// and each key tile of the canonical latent as four 32 KB boxes (2 chunks of
 // 128 keys x 64 dims each, "chunk-major" so every chunk is a 128-row,
-// 128-byte-swizzled MMA operand), plus two 32 KB boxes with this CTA's half
-// of the V columns for P.V, through a 2 x 48 KB ring.
+// 128-byte-swizzled MMA operand) and one 16 KB box for the rope chunk, plus
+// two 32 KB boxes with this CTA's half of the V columns for P.V, through a
+// 3 x 32 KB ring (a slot is held while its MMAs run, so more, smaller slots
+// keep more bytes in flight).
 //
 // Tensor memory (512 columns): O (256, fp32) | S (128, fp32) | P (64, bf16
 // pairs) | rotated q_rope hi (32) | lo (32).
@@ -46,8 +48,8 @@ namespace {
 constexpr int TM = 128;
 constexpr int TNK = 128;
 constexpr uint32_t CHUNK = 16384;
-constexpr int RING = 2;
-constexpr uint32_t SLOT = 3 * CHUNK;
+constexpr int RING = 3;
+constexpr uint32_t SLOT = 2 * CHUNK;
 constexpr int THREADS = 192;
 constexpr uint64_t WAIT_NS = 2000000000ull;
 
@@ -264,10 +266,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       bool have = next_key_tile<TNK>(cur, segs, nseg, 0, r0hi, r1lo, r1hi);
       bool has_prev = false;
       while (ok && (have || has_prev)) {
-        if (have)
-          for (int b = 0; b < 3 && ok; ++b) ok = load(cur, 0, 3 * b, 3 * CHUNK);
+        if (have) {
+          for (int b = 0; b < 4 && ok; ++b) ok = load(cur, 0, 2 * b, 2 * CHUNK);
+          if (ok) ok = load(cur, 1, 8, CHUNK);
+        }
         if (has_prev && ok)
-          for (int vb = 0; vb < 2 && ok; ++vb) ok = load(prev, 1, 4 * half + 2 * vb, 2 * CHUNK);
+          for (int vb = 0; vb < 2 && ok; ++vb) ok = load(prev, 0, 4 * half + 2 * vb, 2 * CHUNK);
         prev = cur;
         has_prev = have;
         if (have) have = next_key_tile<TNK>(cur, segs, nseg, 0, r0hi, r1lo, r1hi);
@@ -295,25 +299,28 @@ __global__ void __launch_bounds__(THREADS, 1)
           ok = wait_bar(c, B_SFREE, j & 1);
           if (!ok) break;
           tc::tc_fence_after();
-          for (int b = 0; b < 3 && ok; ++b) {
+          for (int b = 0; b < 5 && ok; ++b) {
             const int slot = cnt % RING;
             ok = wait_bar(c, B_FULL + slot, (cnt / RING) & 1);
             if (!ok) break;
             tc::tc_fence_after();
             const uint32_t base = ra + slot * SLOT;
+            if (b < 4) {
 #pragma unroll
-            for (int ch = 0; ch < 3; ++ch) {
-              const int cc = 3 * b + ch;
+              for (int ch = 0; ch < 2; ++ch) {
+                const int cc = 2 * b + ch;
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                  tc::mma_ss(tbase + T_S, tc::sdesc_sw128(qa + cc * CHUNK + 32 * k, 16, 1024),
+                             tc::sdesc_sw128(base + ch * CHUNK + 32 * k, 16, 1024), idS,
+                             (cc | k) != 0);
+              }
+            } else {
 #pragma unroll
               for (int k = 0; k < 4; ++k) {
-                const uint64_t bd = tc::sdesc_sw128(base + ch * CHUNK + 32 * k, 16, 1024);
-                if (cc < 8) {
-                  tc::mma_ss(tbase + T_S, tc::sdesc_sw128(qa + cc * CHUNK + 32 * k, 16, 1024), bd,
-                             idS, (cc | k) != 0);
-                } else {
-                  tc::mma_ts(tbase + T_S, tbase + T_RH + 8 * k, bd, idS, 1);
-                  tc::mma_ts(tbase + T_S, tbase + T_RL + 8 * k, bd, idS, 1);
-                }
+                const uint64_t bd = tc::sdesc_sw128(base + 32 * k, 16, 1024);
+                tc::mma_ts(tbase + T_S, tbase + T_RH + 8 * k, bd, idS, 1);
+                tc::mma_ts(tbase + T_S, tbase + T_RL + 8 * k, bd, idS, 1);
               }
             }
             tc::mma_commit(&bar[B_EMPTY + slot]);

@@ -484,15 +484,15 @@ extern "C" rk_status_t rk_seg_attn_plan(const rk_seg_attn_desc_t* desc, void* st
     if (st == RK_OK && p->kernel == 1) {
       // two TMA maps per segment latent, viewing a row as 9 chunks of 64
       // bf16: (64, n, 9) so that a box lands chunk-major in shared memory;
-      // boxes of 3 chunks (scores) and 2 chunks (V columns) x 128 rows
+      // boxes of 2 chunks and of 1 chunk x 128 rows
       p->segmaps.resize(2 * p->segs.size());
       for (size_t i = 0; i < p->segs.size() && st == RK_OK; ++i) {
         const uint64_t dims[3] = {64, static_cast<uint64_t>(p->segs[i].n), 9};
         const uint64_t strides[2] = {576 * 2, 128};
-        const uint32_t box3[3] = {64, 128, 3};
         const uint32_t box2[3] = {64, 128, 2};
-        if (!rk::make_tmap_bf16(&p->segmaps[2 * i], p->segs[i].latent, 3, dims, strides, box3) ||
-            !rk::make_tmap_bf16(&p->segmaps[2 * i + 1], p->segs[i].latent, 3, dims, strides, box2))
+        const uint32_t box1[3] = {64, 128, 1};
+        if (!rk::make_tmap_bf16(&p->segmaps[2 * i], p->segs[i].latent, 3, dims, strides, box2) ||
+            !rk::make_tmap_bf16(&p->segmaps[2 * i + 1], p->segs[i].latent, 3, dims, strides, box1))
           st = RK_ERR_CUDA;
       }
       if (st == RK_OK) st = upload(p->segmaps, &p->d_segmaps, s);

@@ -103,7 +103,7 @@ struct KernelArgs {
   const TcTile* tc_tiles;
   int32_t num_tc_tiles;
   int32_t rows_per_gtile;     // 128 / HG
-  const CUtensorMap* segmaps; // 2 per segment: latent viewed (64, n, 9 chunks), boxes of 3 / 2 chunks x 128 rows
+  const CUtensorMap* segmaps; // 2 per segment: latent viewed (64, n, 9 chunks), boxes of 2 / 1 chunks x 128 rows
   const uint8_t* head_role;   // [H]
   int32_t g_ingroup;          // Global heads are 8g + g_ingroup for every group g, or -1
   const CUtensorMap* decmaps; // per segment: latent viewed (64, n, 9 chunks), box 32 rows x 9 chunks
