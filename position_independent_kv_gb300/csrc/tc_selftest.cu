@@ -213,8 +213,100 @@ __global__ void __launch_bounds__(128, 1)
   if (warp == 0) tc::tmem_dealloc(tbase, 512);
 }
 
+// CTA-pair check: a cluster of two CTAs computes D[256 x N] = A[256 x 64] *
+// B[N x 64]^T with one tcgen05.mma.cta_group::2 per K step issued by CTA 0.
+// CTA r holds rows 128r.. of A and columns (N/2)r.. of B (both K-major,
+// 128-byte swizzled) and receives rows 128r.. of D in its tensor memory.
+// Mode 0: N = 128 (S-shaped).  Mode 1: N = 256, B stored MN-major (K rows x
+// N/2 columns per CTA, P.V-shaped).  256 columns are allocated per CTA, so
+// even two separate allocations would fit in tensor memory.
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(128, 1)
+    tc_2sm_selftest_kernel(int mode, const uint16_t* __restrict__ A,
+                           const uint16_t* __restrict__ B, float* __restrict__ D,
+                           int32_t* status, uint32_t* tmem_addr_out) {
+  __shared__ __align__(1024) uint8_t sA[16384];
+  __shared__ __align__(1024) uint8_t sB[16384];
+  __shared__ __align__(8) uint64_t bar_mma;
+  __shared__ uint32_t tmem_base;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t rank = tc::cluster_ctarank();
+  const int N = mode == 1 ? 256 : 128;
+  const int NH2 = N / 2;
+  if (warp == 0) {
+    tc::tmem_alloc_2sm(&tmem_base, 256);
+    tc::tmem_relinquish_2sm();
+  }
+  if (tid == 0) {
+    tc::mbar_init(&bar_mma, 1);
+    tc::fence_barrier_init();
+  }
+  // this CTA's operands
+  for (int i = tid; i < 128 * 64; i += 128) {
+    const int r = i >> 6, c = i & 63;
+    *reinterpret_cast<uint16_t*>(sA + tc::sw128_offset(r, c)) = A[(128 * rank + r) * 64 + c];
+  }
+  if (mode == 0) {
+    for (int i = tid; i < NH2 * 64; i += 128) {
+      const int r = i >> 6, c = i & 63;  // row = n within this CTA's half, col = k
+      *reinterpret_cast<uint16_t*>(sB + tc::sw128_offset(r, c)) = B[(NH2 * rank + r) * 64 + c];
+    }
+  } else {
+    // MN-major: K rows (64) x this CTA's 128 N columns as two 64-column blocks 8 KB apart
+    for (int i = tid; i < 64 * NH2; i += 128) {
+      const int k = i / NH2, n = i - k * NH2;
+      const int blk = n >> 6, nn = n & 63;
+      *reinterpret_cast<uint16_t*>(sB + blk * 8192 + tc::sw128_offset(k, nn)) =
+          B[(NH2 * rank + n) * 64 + k];
+    }
+  }
+  tc::fence_proxy_async();
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::cluster_sync();
+  tc::tc_fence_after();
+  const uint32_t tbase = tmem_base;
+  if (tid == 0) tmem_addr_out[rank] = tbase;
+  if (rank == 0 && tid == 0) {
+    const uint32_t idesc = tc::idesc_bf16(256, N, false, mode == 1);
+    for (int k = 0; k < 4; ++k) {
+      const uint64_t ad = tc::sdesc_sw128(smem_u32(sA) + 32 * k, 16, 1024);
+      const uint64_t bd = mode == 0 ? tc::sdesc_sw128(smem_u32(sB) + 32 * k, 16, 1024)
+                                    : tc::sdesc_sw128(smem_u32(sB) + 2048 * k, 8192, 1024);
+      tc::mma_ss_2sm(tbase, ad, bd, idesc, k > 0);
+    }
+    tc::mma_commit_2sm(&bar_mma, 0x3);
+  }
+  const bool ok = tc::mbar_wait(&bar_mma, 0, status, kWaitNs);
+  tc::tc_fence_after();
+  if (ok) {
+    for (int c = 0; c < N / 32; ++c) {
+      uint32_t r[32];
+      tc::tmem_ld32(tbase + (static_cast<uint32_t>(32 * warp) << 16) + 32 * c, r);
+      tc::tmem_wait_ld();
+      float* dst = D + (128 * rank + 32 * warp + lane) * N + 32 * c;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) dst[i] = __uint_as_float(r[i]);
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::cluster_sync();
+  if (warp == 0) tc::tmem_dealloc_2sm(tbase, 256);
+}
+
 }  // namespace
 }  // namespace rk
+
+// CTA-pair check (see above).  A: bf16 [256, 64]; B: bf16 [N, 64]; D: fp32
+// [256, N]; tmem_addr_out: uint32 [2].
+extern "C" int rk_tc_2sm_selftest(int mode, const void* A, const void* B, float* D,
+                                  int32_t* status, uint32_t* tmem_addr_out, void* stream) {
+  if (mode < 0 || mode > 1) return -1;
+  rk::tc_2sm_selftest_kernel<<<2, 128, 0, static_cast<cudaStream_t>(stream)>>>(
+      mode, static_cast<const uint16_t*>(A), static_cast<const uint16_t*>(B), D, status,
+      tmem_addr_out);
+  return static_cast<int>(cudaGetLastError());
+}
 
 extern "C" int rk_tc_mma_rate(int mode, int iters, unsigned long long* ns, int32_t* status,
                               void* stream) {

@@ -46,3 +46,34 @@ def test_tcgen05_building_blocks(selftest_lib, mode):
     assert float(err.max()) <= 1e-3 * max(1.0, float(ref.abs().max())), (
         f"mode {mode}: max err {float(err.max())}, first row got {got[0, :6].tolist()} "
         f"want {ref[0, :6].tolist()}")
+
+
+@pytest.mark.parametrize("mode", [0, 1], ids=["pair_n128_kmajor", "pair_n256_mnmajor"])
+def test_tcgen05_cta_pair(selftest_lib, mode):
+    """tcgen05.mma.cta_group::2 over a cluster of two CTAs: A and D rows
+    split between the CTAs, B split along N, one issuing thread, completion
+    multicast to both CTAs."""
+    L = selftest_lib
+    L.rk_tc_2sm_selftest.argtypes = [ctypes.c_int] + [ctypes.c_void_p] * 6
+    L.rk_tc_2sm_selftest.restype = ctypes.c_int
+    N = 256 if mode == 1 else 128
+    g = torch.Generator(device="cuda").manual_seed(200 + mode)
+    A = torch.randn(256, 64, device="cuda", generator=g).to(torch.bfloat16)
+    B = torch.randn(N, 64, device="cuda", generator=g).to(torch.bfloat16)
+    D = torch.full((256, N), float("nan"), dtype=torch.float32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    taddr = torch.full((2,), 0xFFFFFFFF, dtype=torch.int64, device="cuda").to(torch.int32)
+    rc = L.rk_tc_2sm_selftest(mode, A.data_ptr(), B.data_ptr(), D.data_ptr(), status.data_ptr(),
+                              taddr.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert rc == 0
+    assert int(status.item()) == 0, "a bounded wait expired"
+    t = taddr.cpu().tolist()
+    assert t[0] == t[1], f"the pair got different TMEM addresses {t}"
+    ref = A.double().cpu() @ B.double().cpu().T
+    got = D.double().cpu()
+    assert torch.isfinite(got).all(), "accumulator not fully written"
+    err = (got - ref).abs()
+    assert float(err.max()) <= 1e-3 * max(1.0, float(ref.abs().max())), (
+        f"mode {mode}: max err {float(err.max())}; row 0 {got[0, :4].tolist()} vs "
+        f"{ref[0, :4].tolist()}; row 128 {got[128, :4].tolist()} vs {ref[128, :4].tolist()}")
