@@ -46,8 +46,10 @@ def peaks():
     return dict(FALLBACK), "fallback"
 
 
+PLAN_FLAGS = {"auto": 0, "single": 4, "legacy": 2}
 KERNEL_SOURCES = {"mma_sync": ["dense_mma.cu", "common.cuh"],
-                  "tcgen05": ["dense_tc.cu", "tc_ptx.cuh", "common.cuh"]}
+                  "tcgen05": ["dense_tc.cu", "tc_ptx.cuh", "common.cuh"],
+                  "tcgen05_pair": ["dense_tc2.cu", "tc_ptx.cuh", "common.cuh"]}
 
 
 def kernel_source_hash(kernel: str) -> str:
@@ -212,7 +214,8 @@ def bench_prefill(args, ws, local, pk):
     wl = make_workload(args.workload, seed=0, device=dev)
     bm, _ = build_bitmap(wl)
     stream = torch.cuda.current_stream(dev)
-    plan = B.SegAttnPlan.from_workload(wl, bitmap=bm, stream=stream)
+    plan = B.SegAttnPlan.from_workload(wl, bitmap=bm, stream=stream,
+                                       flags=PLAN_FLAGS[args.kernel])
     info = plan.info
     ws_buf = None
     if plan.workspace_bytes:
@@ -397,7 +400,7 @@ def run_ours(args):
     line = None
     if rank == 0:
         info = res["info"]
-        kernel = "tcgen05" if info["kernel"] == 1 else "mma_sync"
+        kernel = {0: "mma_sync", 1: "tcgen05", 2: "tcgen05_pair"}[info["kernel"]]
         peak = pk["bf16_tflops"]
         line = {
             "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": ws,
@@ -482,6 +485,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--kernel", default="auto", choices=list(PLAN_FLAGS),
+                    help="prefill tile kernel: auto (CTA pairs where eligible), single "
+                         "(one tile per CTA), legacy (mma.sync)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")

@@ -17,6 +17,7 @@ from .build import LIB
 RK_SEG_NEW = 1
 RK_PLAN_HOST_ONLY = 1
 RK_PLAN_LEGACY_MMA = 2
+RK_PLAN_SINGLE_CTA = 4
 
 EXPORTS = ["rk_seg_attn_plan", "rk_seg_attn_plan_destroy", "rk_seg_attn_plan_info",
            "rk_seg_attn_workspace_bytes", "rk_seg_attn_forward", "rk_lse_merge",

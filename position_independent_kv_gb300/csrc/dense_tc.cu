@@ -257,7 +257,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!wait_bar(c, B_EMPTY + slot, ph ^ 1)) return false;
         tc::mbar_arrive_expect_tx(&bar[B_FULL + slot], bytes);
         tc::tma_load_3d(smem_u32(sm + OFF_RING + slot * SLOT),
-                        a.segmaps + 2 * (rq.seg_first + kt.j) + map, &bar[B_FULL + slot], 0,
+                        a.segmaps + 4 * (rq.seg_first + kt.j) + map, &bar[B_FULL + slot], 0,
                         kt.k0 - segs[kt.j].delta, z);
         ++cnt;
         return true;

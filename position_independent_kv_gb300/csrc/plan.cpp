@@ -20,6 +20,7 @@ using rk::DenseTile;
 using rk::DevReq;
 using rk::DevSeg;
 using rk::SplitChunk;
+using rk::TcPair;
 using rk::TcTile;
 
 namespace {
@@ -58,6 +59,7 @@ void free_device(rk_seg_attn_plan_s* p) {
   cudaFree(p->d_local_heads);
   cudaFree(p->d_chunks);
   cudaFree(p->d_tc_tiles);
+  cudaFree(p->d_tc_pairs);
   cudaFree(p->d_segmaps);
   cudaFree(p->d_decmaps);
   cudaFree(p->d_head_role);
@@ -75,6 +77,7 @@ void free_device(rk_seg_attn_plan_s* p) {
   p->d_global_heads = p->d_local_heads = nullptr;
   p->d_chunks = nullptr;
   p->d_tc_tiles = nullptr;
+  p->d_tc_pairs = nullptr;
   p->d_segmaps = nullptr;
   p->d_decmaps = nullptr;
   p->d_head_role = nullptr;
@@ -132,7 +135,8 @@ static rk_status_t build_plan(const rk_seg_attn_desc_t* d, rk_seg_attn_plan_s* p
   if (!(d->rope_base > 1.0) || !std::isfinite(d->rope_base)) return RK_ERR_INVALID_ARG;
   if (!(d->softmax_scale > 0.f) || !std::isfinite(d->softmax_scale)) return RK_ERR_INVALID_ARG;
   if (d->sink < 0 || d->window < 0) return RK_ERR_INVALID_ARG;
-  if (d->flags & ~(RK_PLAN_HOST_ONLY | RK_PLAN_LEGACY_MMA)) return RK_ERR_INVALID_ARG;
+  if (d->flags & ~(RK_PLAN_HOST_ONLY | RK_PLAN_LEGACY_MMA | RK_PLAN_SINGLE_CTA))
+    return RK_ERR_INVALID_ARG;
   if (d->seg_begin[0] != 0) return RK_ERR_INVALID_ARG;
   for (int r = 0; r < R; ++r)
     if (d->seg_begin[r + 1] <= d->seg_begin[r]) return RK_ERR_INVALID_ARG;
@@ -164,7 +168,7 @@ static rk_status_t build_plan(const rk_seg_attn_desc_t* d, rk_seg_attn_plan_s* p
     const bool hg_ok = hg == 0 || (kTcM % hg == 0 && (kTcM / hg) % 8 == 0);
     const bool h_ok = d->num_heads == 64 || d->num_heads == 128;
     if (!(d->flags & RK_PLAN_LEGACY_MMA) && d->d_nope == 512 && d->d_rope == 64 && hg_ok && h_ok) {
-      p->kernel = 1;
+      p->kernel = (d->flags & RK_PLAN_SINGLE_CTA) ? 1 : 2;
       p->tile_m = kTcM;
     }
   }
@@ -247,8 +251,8 @@ static rk_status_t build_plan(const rk_seg_attn_desc_t* d, rk_seg_attn_plan_s* p
     info.latent_bytes += p->segs[i].n * int64_t(d->d_nope + d->d_rope) * 2;
 
   const int TM = p->tile_m;
-  const int TN = p->kernel == 1 ? kTcN : kMmaTileN;
-  const bool tc = p->kernel == 1;
+  const bool tc = p->kernel >= 1;
+  const int TN = tc ? kTcN : kMmaTileN;
   const int64_t sink = d->sink, window = d->window;
   std::vector<std::pair<int64_t, DenseTile>> tiles;  // (cost, tile)
   std::vector<std::pair<int64_t, TcTile>> tc_list;   // (cost, tile)
@@ -327,7 +331,6 @@ static rk_status_t build_plan(const rk_seg_attn_desc_t* d, rk_seg_attn_plan_s* p
           const DevSeg& s = p->segs[rq.seg_first + j];
           kt += key_tiles_in_segment(shape, s.delta, s.n, TN);
         }
-        info.performed_pairs += kt * TN * TM;
         tc_list.push_back({kt, t});
       }
     } else if (HG) {
@@ -384,7 +387,6 @@ static rk_status_t build_plan(const rk_seg_attn_desc_t* d, rk_seg_attn_plan_s* p
           const DevSeg& s = p->segs[rq.seg_first + j];
           kt += key_tiles_in_segment(shape, s.delta, s.n, TN);
         }
-        info.performed_pairs += kt * TN * TM;
         tc_list.push_back({kt, t});
         i += pb >= 0 ? 2 : 1;
       }
@@ -436,11 +438,77 @@ static rk_status_t build_plan(const rk_seg_attn_desc_t* d, rk_seg_attn_plan_s* p
                    [](const auto& a, const auto& b) { return a.first > b.first; });
   p->tiles.reserve(tiles.size());
   for (auto& t : tiles) p->tiles.push_back(t.second);
-  std::stable_sort(tc_list.begin(), tc_list.end(),
-                   [](const auto& a, const auto& b) { return a.first > b.first; });
-  for (auto& t : tc_list) p->tc_tiles.push_back(t.second);
-  if (p->tc_tiles.size() > (INT32_MAX / 4)) return RK_ERR_CAPACITY;
-  info.dense_tiles = static_cast<int64_t>(p->tiles.size() + p->tc_tiles.size());
+  info.dense_tiles = static_cast<int64_t>(p->tiles.size() + tc_list.size());
+  if (p->kernel == 2) {
+    // Pair neighbouring tiles of one request and kind (adjacent Global row
+    // blocks, consecutive protected rows) when the union of their key
+    // ranges costs at most 1/8 more key tiles than the two ranges apart;
+    // a tile left alone gets a partner without work.
+    auto req_tiles = [&](int r, int64_t sink_hi, int64_t win_lo, int64_t key_hi) {
+      DenseTile shape{};
+      shape.key_hi = static_cast<int32_t>(key_hi);
+      shape.win_lo = static_cast<int32_t>(win_lo);
+      shape.sink_hi = static_cast<int32_t>(sink_hi);
+      int64_t kt = 0;
+      const DevReq& rq = p->reqs[r];
+      for (int j = 0; j < rq.seg_count; ++j) {
+        const DevSeg& s = p->segs[rq.seg_first + j];
+        kt += key_tiles_in_segment(shape, s.delta, s.n, TN);
+      }
+      return kt;
+    };
+    std::vector<std::pair<int64_t, TcPair>> pairs;
+    size_t i = 0;
+    while (i < tc_list.size()) {
+      const TcTile& A = tc_list[i].second;
+      TcPair pr{};
+      pr.t[0] = A;
+      pr.key_hi = A.key_hi;
+      pr.win_lo = A.win_lo;
+      pr.sink_hi = A.sink_hi;
+      int64_t cost = tc_list[i].first;
+      bool paired = false;
+      if (i + 1 < tc_list.size()) {
+        const TcTile& B = tc_list[i + 1].second;
+        if (B.req == A.req && B.kind == A.kind) {
+          int64_t sh = std::max(A.sink_hi, B.sink_hi);
+          int64_t wl = std::min(A.win_lo, B.win_lo);
+          const int64_t kh = std::max(A.key_hi, B.key_hi);
+          if (sh >= wl) sh = wl = 0;
+          const int64_t u = req_tiles(A.req, sh, wl, kh);
+          const int64_t apart = tc_list[i].first + tc_list[i + 1].first;
+          if (2 * u <= apart + apart / 8) {
+            pr.t[1] = B;
+            pr.key_hi = static_cast<int32_t>(kh);
+            pr.win_lo = static_cast<int32_t>(wl);
+            pr.sink_hi = static_cast<int32_t>(sh);
+            cost = u;
+            paired = true;
+          }
+        }
+      }
+      if (!paired) {
+        pr.t[1] = A;
+        pr.t[1].pad |= 1;
+      }
+      // both CTAs of a real pair do attention work; a partner without work does not count
+      info.performed_pairs += (paired ? 2 : 1) * cost * TN * TM;
+      pairs.push_back({cost, pr});
+      i += paired ? 2 : 1;
+    }
+    std::stable_sort(pairs.begin(), pairs.end(),
+                     [](const auto& a, const auto& b) { return a.first > b.first; });
+    for (auto& pr : pairs) p->tc_pairs.push_back(pr.second);
+    if (p->tc_pairs.size() > (INT32_MAX / 8)) return RK_ERR_CAPACITY;
+  } else {
+    std::stable_sort(tc_list.begin(), tc_list.end(),
+                     [](const auto& a, const auto& b) { return a.first > b.first; });
+    for (auto& t : tc_list) {
+      info.performed_pairs += t.first * TN * TM;
+      p->tc_tiles.push_back(t.second);
+    }
+    if (p->tc_tiles.size() > (INT32_MAX / 4)) return RK_ERR_CAPACITY;
+  }
   info.split_chunks = static_cast<int64_t>(p->chunks.size());
   p->num_parts = parts;
   p->num_mgroups = mgroups;
@@ -480,20 +548,22 @@ extern "C" rk_status_t rk_seg_attn_plan(const rk_seg_attn_desc_t* desc, void* st
     if (st == RK_OK) st = upload(p->local_heads, &p->d_local_heads, s);
     if (st == RK_OK) st = upload(p->chunks, &p->d_chunks, s);
     if (st == RK_OK) st = upload(p->tc_tiles, &p->d_tc_tiles, s);
+    if (st == RK_OK) st = upload(p->tc_pairs, &p->d_tc_pairs, s);
     if (st == RK_OK) st = upload(p->head_role, &p->d_head_role, s);
-    if (st == RK_OK && p->kernel == 1) {
-      // two TMA maps per segment latent, viewing a row as 9 chunks of 64
+    if (st == RK_OK && p->kernel >= 1) {
+      // four TMA maps per segment latent, viewing a row as 9 chunks of 64
       // bf16: (64, n, 9) so that a box lands chunk-major in shared memory;
-      // boxes of 2 chunks and of 1 chunk x 128 rows
-      p->segmaps.resize(2 * p->segs.size());
+      // boxes of 128 rows x 2 chunks and x 1 chunk, of 64 rows x 4 chunks
+      // and x 1 chunk
+      p->segmaps.resize(4 * p->segs.size());
       for (size_t i = 0; i < p->segs.size() && st == RK_OK; ++i) {
         const uint64_t dims[3] = {64, static_cast<uint64_t>(p->segs[i].n), 9};
         const uint64_t strides[2] = {576 * 2, 128};
-        const uint32_t box2[3] = {64, 128, 2};
-        const uint32_t box1[3] = {64, 128, 1};
-        if (!rk::make_tmap_bf16(&p->segmaps[2 * i], p->segs[i].latent, 3, dims, strides, box2) ||
-            !rk::make_tmap_bf16(&p->segmaps[2 * i + 1], p->segs[i].latent, 3, dims, strides, box1))
-          st = RK_ERR_CUDA;
+        const uint32_t boxes[4][3] = {{64, 128, 2}, {64, 128, 1}, {64, 64, 4}, {64, 64, 1}};
+        for (int b = 0; b < 4 && st == RK_OK; ++b)
+          if (!rk::make_tmap_bf16(&p->segmaps[4 * i + b], p->segs[i].latent, 3, dims, strides,
+                                  boxes[b]))
+            st = RK_ERR_CUDA;
       }
       if (st == RK_OK) st = upload(p->segmaps, &p->d_segmaps, s);
     }
@@ -516,7 +586,8 @@ extern "C" rk_status_t rk_seg_attn_plan(const rk_seg_attn_desc_t* desc, void* st
       else if (cudaMemsetAsync(p->d_status, 0, sizeof(int32_t), s) != cudaSuccess)
         st = RK_ERR_CUDA;
     }
-    if (st == RK_OK && !p->chunks.empty() && (!p->tiles.empty() || !p->tc_tiles.empty())) {
+    if (st == RK_OK && !p->chunks.empty() &&
+        (!p->tiles.empty() || !p->tc_tiles.empty() || !p->tc_pairs.empty())) {
       if (cudaStreamCreateWithFlags(&p->side, cudaStreamNonBlocking) != cudaSuccess ||
           cudaEventCreateWithFlags(&p->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
           cudaEventCreateWithFlags(&p->ev_join, cudaEventDisableTiming) != cudaSuccess)
@@ -618,6 +689,8 @@ void fill_args(const rk_seg_attn_plan_s& p, KernelArgs& a, const void* q, void* 
   a.head_role = p.d_head_role;
   a.g_ingroup = p.g_ingroup;
   a.decmaps = p.d_decmaps;
+  a.tc_pairs = p.d_tc_pairs;
+  a.num_tc_pairs = static_cast<int32_t>(p.tc_pairs.size());
 }
 
 cudaError_t launch_forward(const rk_seg_attn_plan_s& p, const KernelArgs& a, const void* q,
@@ -625,7 +698,7 @@ cudaError_t launch_forward(const rk_seg_attn_plan_s& p, const KernelArgs& a, con
   cudaError_t e = cudaSuccess;
   // prefill tiles overlap the split chunks on the plan's side stream
   cudaStream_t ts = s;
-  if (p.side && a.num_chunks && (a.num_tiles || a.num_tc_tiles)) {
+  if (p.side && a.num_chunks && (a.num_tiles || a.num_tc_tiles || a.num_tc_pairs)) {
     e = cudaEventRecord(p.ev_fork, s);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(p.side, p.ev_fork, 0);
     if (e != cudaSuccess) return e;
@@ -633,6 +706,7 @@ cudaError_t launch_forward(const rk_seg_attn_plan_s& p, const KernelArgs& a, con
   }
   if (a.num_tiles) e = launch_dense_mma(p, a, ts);
   if (e == cudaSuccess && a.num_tc_tiles) e = launch_dense_tc(p, a, q, ts);
+  if (e == cudaSuccess && a.num_tc_pairs) e = launch_dense_tc2(p, a, q, ts);
   if (e == cudaSuccess && a.num_chunks) e = launch_split_decode(p, a, s);
   if (ts != s) {
     const cudaError_t e1 = cudaEventRecord(p.ev_join, ts);

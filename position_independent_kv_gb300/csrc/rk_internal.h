@@ -78,6 +78,19 @@ struct TcTile {
   int32_t pad;
 };
 
+// Two tcgen05 tiles of one request run as a CTA pair (cta_group::2) over
+// the union of their key ranges, [0, sink_hi) u [win_lo, key_hi) with
+// sink_hi <= win_lo.  t[1].pad bit 0 marks a partner without work (its CTA
+// computes on a copy of t[0] and stores nothing).  Each pair runs on four
+// CTAs: two per half of d_v.
+struct TcPair {
+  TcTile t[2];
+  int32_t key_hi;
+  int32_t win_lo;
+  int32_t sink_hi;
+  int32_t pad;
+};
+
 struct KernelArgs {
   const uint16_t* q;
   uint16_t* out;
@@ -103,10 +116,13 @@ struct KernelArgs {
   const TcTile* tc_tiles;
   int32_t num_tc_tiles;
   int32_t rows_per_gtile;     // 128 / HG
-  const CUtensorMap* segmaps; // 2 per segment: latent viewed (64, n, 9 chunks), boxes of 2 / 1 chunks x 128 rows
+  const CUtensorMap* segmaps; // 4 per segment: latent viewed (64, n, 9 chunks); boxes of
+                              // 128 rows x 2 / 1 chunks and of 64 rows x 4 / 1 chunks
   const uint8_t* head_role;   // [H]
   int32_t g_ingroup;          // Global heads are 8g + g_ingroup for every group g, or -1
   const CUtensorMap* decmaps; // per segment: latent viewed (64, n, 9 chunks), box 32 rows x 9 chunks
+  const TcPair* tc_pairs;
+  int32_t num_tc_pairs;
 };
 
 }  // namespace rk
@@ -117,7 +133,7 @@ struct rk_seg_attn_plan_s {
   int32_t H = 0, d_nope = 0, d_rope = 0;
   int32_t sink = 0, window = 0;
   float softmax_scale = 0.f;
-  int kernel = 0;          // 0 mma.sync tiles, 1 tcgen05 tiles
+  int kernel = 0;          // 0 mma.sync tiles, 1 tcgen05 tiles, 2 tcgen05 CTA-pair tiles
   int tile_m = 64;         // query pairs per dense tile
   int g_ingroup = -1;      // Global heads are exactly 8g + g_ingroup, else -1
   rk_plan_info_t info{};
@@ -130,6 +146,7 @@ struct rk_seg_attn_plan_s {
   std::vector<int32_t> global_heads, local_heads;
   std::vector<rk::SplitChunk> chunks;
   std::vector<rk::TcTile> tc_tiles;
+  std::vector<rk::TcPair> tc_pairs;
   std::vector<CUtensorMap> segmaps;
   std::vector<CUtensorMap> decmaps;
   std::vector<uint8_t> head_role;
@@ -145,6 +162,7 @@ struct rk_seg_attn_plan_s {
   int32_t* d_local_heads = nullptr;
   rk::SplitChunk* d_chunks = nullptr;
   rk::TcTile* d_tc_tiles = nullptr;
+  rk::TcPair* d_tc_pairs = nullptr;
   CUtensorMap* d_segmaps = nullptr;
   CUtensorMap* d_decmaps = nullptr;
   uint8_t* d_head_role = nullptr;
@@ -164,6 +182,8 @@ cudaError_t launch_split_decode(const rk_seg_attn_plan_s& plan, const KernelArgs
                                 cudaStream_t stream);
 cudaError_t launch_dense_tc(const rk_seg_attn_plan_s& plan, const KernelArgs& a,
                             const void* q, cudaStream_t stream);
+cudaError_t launch_dense_tc2(const rk_seg_attn_plan_s& plan, const KernelArgs& a,
+                             const void* q, cudaStream_t stream);
 // Fill the kernel arguments shared by every launch of a forward.
 void fill_args(const rk_seg_attn_plan_s& plan, KernelArgs& a, const void* q, void* out,
                float* lse);

@@ -142,3 +142,21 @@ def test_plan_counts_attended_pairs(name):
     assert info["protected_local_rows"] == nprot
     assert info["performed_pairs"] >= pg + pl
     assert info["num_global_heads"] == HG and info["num_local_heads"] == HL
+
+
+@pytest.mark.parametrize("name", ["flash_mini", "varlen_mini", "ctx128k_mini", "flash", "ctx16k",
+                                  "ctx128k"])
+def test_pair_plan_work_bounds(name):
+    """For d = (512, 64) the default plan pairs tcgen05 tiles on CTA pairs
+    (kernel 2); RK_PLAN_SINGLE_CTA keeps one tile per CTA pair of d_v halves
+    (kernel 1).  Pairing walks the union of two tiles' key ranges: the
+    pairing rule bounds the extra key tiles by 1/8, and a merged range can
+    also save a key tile where a tile's sink and window ranges split one
+    128-key block.  Either way every attended pair is still covered."""
+    _, pp = _host_plan(name)
+    _, ps = _host_plan(name, flags=B.RK_PLAN_HOST_ONLY | B.RK_PLAN_SINGLE_CTA)
+    a, b = pp.info, ps.info
+    assert a["kernel"] == 2 and b["kernel"] == 1
+    assert a["dense_tiles"] == b["dense_tiles"]
+    assert a["performed_pairs"] <= b["performed_pairs"] * 9 // 8
+    assert a["performed_pairs"] >= a["pairs_global"] + a["pairs_local"]
