@@ -46,10 +46,11 @@ def peaks():
     return dict(FALLBACK), "fallback"
 
 
-PLAN_FLAGS = {"auto": 0, "single": 4, "legacy": 2}
+PLAN_FLAGS = {"auto": 0, "pair": 8, "single": 4, "legacy": 2}
 KERNEL_SOURCES = {"mma_sync": ["dense_mma.cu", "common.cuh"],
                   "tcgen05": ["dense_tc.cu", "tc_ptx.cuh", "common.cuh"],
-                  "tcgen05_pair": ["dense_tc2.cu", "tc_ptx.cuh", "common.cuh"]}
+                  "tcgen05_pair": ["dense_tc2.cu", "tc_tile.cuh", "tc_ptx.cuh", "common.cuh"],
+                  "tcgen05_quad": ["dense_tc4.cu", "tc_tile.cuh", "tc_ptx.cuh", "common.cuh"]}
 
 
 def kernel_source_hash(kernel: str) -> str:
@@ -400,7 +401,7 @@ def run_ours(args):
     line = None
     if rank == 0:
         info = res["info"]
-        kernel = {0: "mma_sync", 1: "tcgen05", 2: "tcgen05_pair"}[info["kernel"]]
+        kernel = {0: "mma_sync", 1: "tcgen05", 2: "tcgen05_pair", 3: "tcgen05_quad"}[info["kernel"]]
         peak = pk["bf16_tflops"]
         line = {
             "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": ws,
@@ -486,8 +487,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--kernel", default="auto", choices=list(PLAN_FLAGS),
-                    help="prefill tile kernel: auto (CTA pairs where eligible), single "
-                         "(one tile per CTA), legacy (mma.sync)")
+                    help="prefill tile kernel: auto (4-CTA clusters where eligible), pair "
+                         "(tile pairs per half of d_v), single (one tile per two CTAs), "
+                         "legacy (mma.sync)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")

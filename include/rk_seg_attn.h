@@ -73,8 +73,12 @@ typedef enum {
                                    device memory, forward refuses the plan */
 #define RK_PLAN_LEGACY_MMA 2u   /* run the prefill tiles on the mma.sync
                                    kernel instead of the tcgen05 kernel */
-#define RK_PLAN_SINGLE_CTA 4u   /* run each tcgen05 tile on its own CTAs
-                                   instead of pairing tiles on CTA pairs */
+#define RK_PLAN_SINGLE_CTA 4u   /* run each tcgen05 tile on its own two CTAs
+                                   (one per half of d_v) */
+#define RK_PLAN_CTA_PAIR 8u     /* run pairs of tcgen05 tiles on CTA pairs,
+                                   one pair per half of d_v, instead of
+                                   4-CTA clusters (scores on one CTA pair,
+                                   outputs on the other) */
 
 /* One document segment of a request.
  * latent  device pointer, bf16 [n, d_k] row-major (row stride d_k elements),
@@ -143,7 +147,8 @@ typedef struct {
   int64_t performed_pairs;   /* M_tile x N_tile summed over issued key tiles */
   int64_t latent_bytes;      /* bytes of every segment latent */
   int32_t kernel;            /* 0 = mma.sync tiles, 1 = tcgen05 tiles,
-                                2 = tcgen05 tiles paired on CTA pairs */
+                                2 = tcgen05 tiles paired on CTA pairs,
+                                3 = tcgen05 tile pairs on 4-CTA clusters */
   int32_t reserved;
 } rk_plan_info_t;
 

@@ -18,6 +18,7 @@ RK_SEG_NEW = 1
 RK_PLAN_HOST_ONLY = 1
 RK_PLAN_LEGACY_MMA = 2
 RK_PLAN_SINGLE_CTA = 4
+RK_PLAN_CTA_PAIR = 8
 
 EXPORTS = ["rk_seg_attn_plan", "rk_seg_attn_plan_destroy", "rk_seg_attn_plan_info",
            "rk_seg_attn_workspace_bytes", "rk_seg_attn_forward", "rk_lse_merge",

@@ -39,19 +39,16 @@
 // RK_ERR_DEVICE_TIMEOUT, every role stops, the producer waits (bounded) for
 // its copies in flight and TMEM is released only after the MMA pipe drains.
 
-#include "tc_ptx.cuh"
-#include "tmap.h"
+#include "tc_tile.cuh"
 
 namespace rk {
 namespace {
 
-constexpr int TM = 128;
 constexpr int TNK = 128;
 constexpr uint32_t CHUNK = 16384;
 constexpr int RING = 3;
 constexpr uint32_t SLOT = 2 * CHUNK;
 constexpr int THREADS = 192;
-constexpr uint64_t WAIT_NS = 2000000000ull;
 
 constexpr uint32_t OFF_Q = 0;
 constexpr uint32_t OFF_RING = 8 * CHUNK;
@@ -62,125 +59,13 @@ constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;
 
 constexpr uint32_t T_O = 0, T_S = 256, T_P = 384, T_RH = 448, T_RL = 480;
 
-struct Ctx {
-  uint64_t* bar;
-  volatile uint32_t* abort;
-  int32_t* status;
-};
+using tt::Ctx;
+using tt::drain_bar;
+using tt::wait_bar;
 
-// Bounded wait; also gives up as soon as another role of this CTA, or any
-// CTA of the launch, has recorded an error.
-__device__ __forceinline__ bool wait_bar(const Ctx& c, int i, uint32_t parity) {
-  uint64_t* b = c.bar + i;
-  uint32_t it = 0;
-  uint64_t t0 = 0;
-  while (!tc::mbar_try_wait(b, parity)) {
-    if ((++it & 63u) == 0) {
-      if (*c.abort || *reinterpret_cast<volatile int32_t*>(c.status)) {
-        *c.abort = 1;
-        return false;
-      }
-      const uint64_t now = tc::global_ns();
-      if (t0 == 0) {
-        t0 = now;
-      } else if (now - t0 > WAIT_NS) {
-        *c.abort = 1;
-        atomicCAS(c.status, 0, static_cast<int32_t>(RK_ERR_DEVICE_TIMEOUT));
-        return false;
-      }
-    }
-  }
-  return true;
-}
-
-// Bounded wait that ignores the abort flag (used to drain copies in flight).
-__device__ __forceinline__ void drain_bar(const Ctx& c, int i, uint32_t parity) {
-  uint64_t* b = c.bar + i;
-  const uint64_t t0 = tc::global_ns();
-  while (!tc::mbar_try_wait(b, parity)) {
-    if (tc::global_ns() - t0 > WAIT_NS) {
-      atomicCAS(c.status, 0, static_cast<int32_t>(RK_ERR_DEVICE_TIMEOUT));
-      return;
-    }
-  }
-}
-
-struct RowInfo {
-  int p;       // absolute row, -1 if the pair is unused
-  int head;
-  bool glob;   // Global visibility rule
-  bool store;  // written by the epilogue
-  int64_t frow;
-};
-
-__device__ __forceinline__ RowInfo row_info(const KernelArgs& a, const TcTile& t,
-                                            const DevReq& rq, int m) {
-  RowInfo r;
-  if (t.kind == 0) {
-    const int R = a.rows_per_gtile;
-    const int hi = m / R, ri = m - hi * R;
-    const bool v = ri < t.p1 && hi < a.num_global;
-    r.p = v ? t.p0 + ri : -1;
-    r.head = v ? a.global_heads[hi] : 0;
-    r.glob = true;
-    r.store = v;
-  } else {
-    const int ri = m / a.H, h = m - ri * a.H;
-    const int pr = (ri == 0) ? t.p0 : t.p1;
-    r.p = pr;
-    r.head = h;
-    r.glob = false;
-    r.store = pr >= 0 && a.head_role[h] == 0;
-  }
-  r.frow = r.p >= 0 ? rq.row_base + (r.p - rq.q_row_begin) : -1;
-  return r;
-}
-
-// q_rope' = R(-delta) q_rope of one row as bf16 hi and lo parts, written to
-// this thread's TMEM lane (columns T_RH.., T_RL..; pair j in column j).  The
-// row's q_rope (`src`, 64 bf16) is re-read from global memory each time; an
-// unused pair (src == nullptr) writes zeros.
-__device__ __forceinline__ void write_rope(uint32_t lane_taddr, const uint16_t* src,
-                                           const float* cs) {
-  uint32_t raw[32];
-  if (src) {
-    const uint4* s4 = reinterpret_cast<const uint4*>(src);
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const uint4 v = __ldg(s4 + u);
-      raw[4 * u] = v.x;
-      raw[4 * u + 1] = v.y;
-      raw[4 * u + 2] = v.z;
-      raw[4 * u + 3] = v.w;
-    }
-  } else {
-#pragma unroll
-    for (int u = 0; u < 32; ++u) raw[u] = 0;
-  }
-  uint32_t hi[32];
-#pragma unroll
-  for (int jj = 0; jj < 32; ++jj) {
-    const float x = __uint_as_float(raw[jj] << 16), y = __uint_as_float(raw[jj] & 0xffff0000u);
-    const float co = __ldg(cs + 2 * jj), si = __ldg(cs + 2 * jj + 1);
-    const float xr = fmaf(x, co, y * si), yr = fmaf(-x, si, y * co);
-    hi[jj] = pack_bf16x2(xr, yr);
-    raw[jj] = pack_bf16x2(xr - __uint_as_float(hi[jj] << 16),
-                          yr - __uint_as_float(hi[jj] & 0xffff0000u));
-  }
-  tc::tmem_st32(lane_taddr + T_RH, hi);
-  tc::tmem_st32(lane_taddr + T_RL, raw);
-  tc::tmem_wait_st();
-}
-
-struct QMaps {
-  CUtensorMap g5;   // Global, one Global head per group: (64, rows, groups, 8 chunks, in-group)
-  CUtensorMap g3;   // Global, any roles: (576, H, rows), box (64, 1, R)
-  CUtensorMap l4;   // Local, H = 128: (64, H, 8 chunks, rows), box (64, 128, 8, 1)
-  CUtensorMap l3;   // Local, any H: (576, H, rows), box (64, H, 1)
-};
 
 __global__ void __launch_bounds__(THREADS, 1)
-    dense_tc_kernel(const KernelArgs a, const __grid_constant__ QMaps qm) {
+    dense_tc_kernel(const KernelArgs a, const __grid_constant__ tt::QMaps qm) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
@@ -223,32 +108,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ------------------------------------------------------ TMA producer --
     if (lane == 0) {
       tc::mbar_arrive_expect_tx(&bar[B_QFULL], 8 * CHUNK);
-      const uint32_t qdst = smem_u32(sm + OFF_Q);
-      if (t.kind == 0) {
-        const int64_t fr = rq.row_base + (t.p0 - rq.q_row_begin);
-        if (a.g_ingroup >= 0) {
-          tc::tma_load_5d(qdst, &qm.g5, &bar[B_QFULL], 0, static_cast<int32_t>(fr), 0, 0,
-                          a.g_ingroup);
-        } else {
-          const int R = a.rows_per_gtile;
-          for (int ch = 0; ch < 8; ++ch)
-            for (int hi = 0; hi < a.num_global; ++hi)
-              tc::tma_load_3d(qdst + ch * CHUNK + hi * R * 128, &qm.g3, &bar[B_QFULL], 64 * ch,
-                              a.global_heads[hi], static_cast<int32_t>(fr));
-        }
-      } else if (a.H == TM) {
-        const int64_t fr = rq.row_base + (t.p0 - rq.q_row_begin);
-        tc::tma_load_4d(qdst, &qm.l4, &bar[B_QFULL], 0, 0, 0, static_cast<int32_t>(fr));
-      } else {
-        const int rows_per = TM / a.H;
-        for (int ch = 0; ch < 8; ++ch)
-          for (int ri = 0; ri < rows_per; ++ri) {
-            const int pr = (ri == 0 || t.p1 < 0) ? t.p0 : t.p1;
-            const int64_t fr = rq.row_base + (pr - rq.q_row_begin);
-            tc::tma_load_3d(qdst + ch * CHUNK + ri * a.H * 128, &qm.l3, &bar[B_QFULL], 64 * ch, 0,
-                            static_cast<int32_t>(fr));
-          }
-      }
+      tt::load_q_tile<false>(a, qm, t, rq, smem_u32(sm + OFF_Q), smem_u32(&bar[B_QFULL]));
       uint32_t cnt = 0;
       bool ok = true;
       auto load = [&](const KeyTile& kt, int map, int z, uint32_t bytes) {
@@ -257,7 +117,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!wait_bar(c, B_EMPTY + slot, ph ^ 1)) return false;
         tc::mbar_arrive_expect_tx(&bar[B_FULL + slot], bytes);
         tc::tma_load_3d(smem_u32(sm + OFF_RING + slot * SLOT),
-                        a.segmaps + 4 * (rq.seg_first + kt.j) + map, &bar[B_FULL + slot], 0,
+                        a.segmaps + kSegMaps * (rq.seg_first + kt.j) + map, &bar[B_FULL + slot], 0,
                         kt.k0 - segs[kt.j].delta, z);
         ++cnt;
         return true;
@@ -364,7 +224,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ---------------------------------- softmax, rotation and epilogue ---
     const int quarter = warp & 3;
     const int m = quarter * 32 + lane;
-    const RowInfo ri = row_info(a, t, rq, m);
+    const tt::RowInfo ri = tt::row_info(a, t, rq, m);
     const uint32_t lt = tbase + (static_cast<uint32_t>(quarter * 32) << 16);
     const float sl2 = a.scale_log2;
     const int sink = a.sink, window = a.window;
@@ -372,7 +232,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     KeyTile kt{0, 0, 0, -1};
     bool have = next_key_tile<TNK>(kt, segs, nseg, 0, r0hi, r1lo, r1hi);
     // q_rope' of the first segment, then release the (empty) S buffer
-    write_rope(lt, qrope, a.rope_cs + static_cast<int64_t>(rq.seg_first + kt.j) * 64);
+    tt::write_rope(lt, T_RH, T_RL, qrope, a.rope_cs + static_cast<int64_t>(rq.seg_first + kt.j) * 64);
     tc::tc_fence_before();
     tc::mbar_arrive(&bar[B_SFREE]);
     float m_run = -INFINITY, l_run = 0.f;
@@ -386,7 +246,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc::tc_fence_after();
       // S_j is complete, so no score MMA still reads the rotated q_rope
       if (have_next && nx.j != kt.j)
-        write_rope(lt, qrope, a.rope_cs + static_cast<int64_t>(rq.seg_first + nx.j) * 64);
+        tt::write_rope(lt, T_RH, T_RL, qrope, a.rope_cs + static_cast<int64_t>(rq.seg_first + nx.j) * 64);
       uint32_t s[4][32];
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) tc::tmem_ld32(lt + T_S + 32 * q4, s[q4]);
@@ -513,31 +373,10 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 cudaError_t launch_dense_tc(const rk_seg_attn_plan_s& p, const KernelArgs& a, const void* q,
                             cudaStream_t s) {
-  QMaps qm{};
-  const uint64_t H = static_cast<uint64_t>(p.H), rows = static_cast<uint64_t>(p.info.rows);
-  const uint32_t R = static_cast<uint32_t>(a.rows_per_gtile > 0 ? a.rows_per_gtile : 8);
-  if (a.g_ingroup >= 0) {  // Global, one Global head per group of 8: the whole tile in one box
-    const uint64_t G = H / 8;
-    const uint64_t dims[5] = {64, rows, G, 8, 8};
-    const uint64_t strides[4] = {H * 1152, 8 * 1152, 128, 1152};
-    const uint32_t box[5] = {64, R, static_cast<uint32_t>(G), 8, 1};
-    if (!make_tmap_bf16(&qm.g5, q, 5, dims, strides, box)) return cudaErrorInvalidValue;
-  }
-  {
-    const uint64_t dims[3] = {576, H, rows};
-    const uint64_t strides[2] = {1152, H * 1152};
-    const uint32_t boxg[3] = {64, 1, R};
-    const uint32_t boxl[3] = {64, static_cast<uint32_t>(H), 1};
-    if (!make_tmap_bf16(&qm.g3, q, 3, dims, strides, boxg)) return cudaErrorInvalidValue;
-    if (!make_tmap_bf16(&qm.l3, q, 3, dims, strides, boxl)) return cudaErrorInvalidValue;
-  }
-  if (H == TM) {
-    const uint64_t dims[4] = {64, H, 8, rows};
-    const uint64_t strides[3] = {1152, 128, H * 1152};
-    const uint32_t box[4] = {64, static_cast<uint32_t>(H), 8, 1};
-    if (!make_tmap_bf16(&qm.l4, q, 4, dims, strides, box)) return cudaErrorInvalidValue;
-  }
-  cudaError_t e = cudaFuncSetAttribute(dense_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  tt::QMaps qm;
+  cudaError_t e = tt::make_qmaps(p, a, q, qm);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(dense_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(SMEM_BYTES));
   if (e != cudaSuccess) return e;
   const int64_t grid = 2 * static_cast<int64_t>(a.num_tc_tiles);

@@ -1,0 +1,575 @@
+// Prefill-style tiles on 4-CTA clusters: the scores of two tiles on one CTA
+// pair, their outputs on another (tcgen05 cta_group::2 + TMEM + TMA).
+//
+// Tensor memory cannot hold a tile's fp32 output over all of d_v (128 x 512
+// columns) next to its scores, so a tile handled by one CTA pair per half
+// of d_v computes S = Q K^T twice.  Here the work is split by role instead:
+//
+//   ranks 0, 1  "S pair": rank r holds tile r's queries, the nope part in
+//               tensor memory (256 columns, A operand of the score MMAs) and
+//               the rotated rope part in shared memory, and computes
+//               S_j = Q K_j^T for both tiles with M = 256 MMAs (N = 128
+//               keys: rank r streams keys 64r..64r+63 of every key tile, 72 KB
+//               through a ring of five 24 KB slots) into one of two S
+//               buffers, runs the online softmax of its 128 lanes, stages
+//               P_j (bf16, 32 KB) and a per-lane record (rescale factor,
+//               running sum) in its shared memory and copies them in one bulk
+//               copy into the shared memory of rank r + 2.
+//   ranks 2, 3  "O pair": rank 2 + r holds tile r's fp32 output for all 512
+//               columns in tensor memory and computes O += P_j V_j with
+//               M = 256, N = 256 MMAs (A = P_j from shared memory; rank 2 + r
+//               streams the V column chunks 2r, 2r+1, 4+2r, 5+2r of every key
+//               tile, 64 KB through four 32 KB slots), rescales O when the
+//               record says so, and stores the normalised output.
+//
+// Each latent byte is read once per cluster, every MMA does useful work, and
+// the score and output MMAs of a key tile run on different SMs at the same
+// time.  The method is the one of the other prefill kernels: the query
+// rotates by -delta at each segment of the key walk and the running max /
+// sum / output carry across segments as a log-sum-exp merge (RedKnot-MLA
+// paper, RoPE-orthogonality paragraph); Global rows see k <= p and Local
+// rows sink u [p - w, p] (RedKnot blog, "Insight 1").  Every wait is bounded
+// in time; on expiry the CTA records RK_ERR_DEVICE_TIMEOUT, every CTA of the
+// launch stops, leaders wait (bounded) for their copies in flight, and
+// tensor memory is released after each pair's MMA pipe has drained.
+
+#include "tc_tile.cuh"
+
+namespace rk {
+namespace {
+
+using tt::Ctx;
+using tt::drain_bar;
+using tt::wait_bar;
+
+constexpr int TNK = 128;                   // keys per key tile
+constexpr uint32_t CHUNK = 16384;          // 128 rows x 64 bf16
+constexpr uint32_t HCHUNK = 8192;          // 64 rows x 64 bf16
+constexpr int THREADS = 192;
+
+// S pair: rotated q_rope hi and lo (K-major operands), a staging buffer for
+// P and the records, the key ring
+constexpr uint32_t OFF_ROPE = 0;
+constexpr uint32_t PBUF = 2 * CHUNK;       // 128 lanes x 128 keys bf16, two 64-key chunks
+constexpr uint32_t RBUF = 128 * 8;         // (alpha, l) per lane, after P
+constexpr uint32_t PREC_BYTES = PBUF + RBUF;
+constexpr uint32_t PSTRIDE = PBUF + 2048;  // 1024-aligned buffers
+constexpr uint32_t OFF_STG = 2 * CHUNK;
+constexpr int KRING = 2;
+constexpr uint32_t KSLOT = 9 * HCHUNK;     // 64 keys x 9 chunks: one box per key tile
+constexpr uint32_t OFF_KRING = OFF_STG + PSTRIDE;
+// O pair: two P + record buffers, the V ring (128 keys x 4 chunks per slot)
+constexpr uint32_t OFF_P = 0;
+constexpr int VRING = 2;
+constexpr uint32_t VSLOT = 4 * CHUNK;
+constexpr uint32_t OFF_VRING = OFF_P + 2 * PSTRIDE;
+constexpr uint32_t OFF_BAR = OFF_KRING + KRING * KSLOT;
+static_assert(OFF_KRING % 1024 == 0 && OFF_VRING % 1024 == 0, "operand alignment");
+static_assert(OFF_VRING + VRING * VSLOT <= OFF_BAR, "O-pair layout");
+enum {
+  B_KFULL = 0,
+  B_KEMPTY = B_KFULL + KRING,
+  B_SFULL = B_KEMPTY + KRING,  // 2: S buffer j & 1 written
+  B_SFREE = B_SFULL + 2,  // 2: S buffer read by both S CTAs' softmax lanes
+  B_ROPE = B_SFREE + 2,   // rotated q_rope of the next segment written (the first
+                          // event also publishes the queries in tensor memory)
+  B_SFINAL,
+  B_PEMPTY,             // 2 (S CTAs): P buffer consumed by the output MMAs
+  B_VFULL = B_PEMPTY + 2,
+  B_VEMPTY = B_VFULL + VRING,
+  B_PFULL = B_VEMPTY + VRING,  // 2 (O CTAs): P and records copied in
+  B_PREADY = B_PFULL + 2,      // 2: O rescaled where needed, P buffer ready for the MMAs
+  B_ODONE = B_PREADY + 2,
+  B_OFINAL,
+  NBAR
+};
+constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
+constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;
+static_assert(SMEM_BYTES <= 232448, "shared memory");
+
+// tensor memory: S pair | O pair
+constexpr uint32_t T_Q = 0, T_S = 256;
+constexpr uint32_t T_O = 0;
+
+// segment maps (kSegMaps per segment)
+constexpr int MAP_K9 = 4;    // 64 rows x 9 chunks
+constexpr int MAP_V4 = 5;    // 128 rows x 4 chunks
+
+__global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
+    dense_tc4_kernel(const KernelArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
+  uint32_t* misc = reinterpret_cast<uint32_t*>(sm + OFF_MISC);
+  const Ctx c{bar, reinterpret_cast<volatile uint32_t*>(misc + 1), a.status};
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t crank = tc::cluster_ctarank();
+  const bool spair = crank < 2;
+  const uint32_t r = crank & 1;      // tile of the pair
+  const TcPair& P = a.tc_pairs[blockIdx.x >> 2];
+  const TcTile t = P.t[r];
+  const DevReq rq = a.reqs[t.req];
+  const DevSeg* segs = a.segs + rq.seg_first;
+  const int nseg = rq.seg_count;
+  const int r0hi = P.sink_hi, r1lo = P.win_lo, r1hi = P.key_hi;
+  auto cbar = [&](int i, uint32_t rank) { return tc::mapa_shared(smem_u32(&bar[i]), rank); };
+
+  if (tid == 0) {
+    for (int i = 0; i < KRING; ++i) {
+      tc::mbar_init(&bar[B_KFULL + i], 1);
+      tc::mbar_init(&bar[B_KEMPTY + i], 1);
+    }
+    for (int i = 0; i < VRING; ++i) {
+      tc::mbar_init(&bar[B_VFULL + i], 1);
+      tc::mbar_init(&bar[B_VEMPTY + i], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(&bar[B_SFULL + b], 1);
+      tc::mbar_init(&bar[B_SFREE + b], 2 * 128);
+      tc::mbar_init(&bar[B_PEMPTY + b], 1);
+      tc::mbar_init(&bar[B_PFULL + b], 1);
+      tc::mbar_init(&bar[B_PREADY + b], 2 * 128);
+    }
+    tc::mbar_init(&bar[B_ROPE], 2 * 128);
+    tc::mbar_init(&bar[B_SFINAL], 1);
+    tc::mbar_init(&bar[B_ODONE], 1);
+    tc::mbar_init(&bar[B_OFINAL], 1);
+    misc[1] = 0;
+    if (!spair)  // each P buffer expects one bulk copy per use; armed one use ahead
+      for (int b = 0; b < 2; ++b) tc::mbar_arrive_expect_tx(&bar[B_PFULL + b], PREC_BYTES);
+    tc::fence_barrier_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc_2sm(misc, 512);
+    tc::tmem_relinquish_2sm();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::cluster_sync();  // every barrier of the cluster is initialised before any remote use
+  tc::tc_fence_after();
+  const uint32_t tbase = misc[0];
+
+  if (spair) {
+    if (warp == 0) {
+      // ------------------------------------------- S pair: TMA producer --
+      if (lane == 0) {
+        uint32_t cnt = 0;
+        bool ok = true;
+        KeyTile cur{0, 0, 0, -1};
+        bool have = next_key_tile<TNK>(cur, segs, nseg, 0, r0hi, r1lo, r1hi);
+        while (ok && have) {
+          const int slot = cnt % KRING;
+          ok = wait_bar(c, B_KEMPTY + slot, ((cnt / KRING) & 1) ^ 1);
+          if (!ok) break;
+          // the leader's barrier counts both CTAs' boxes
+          if (r == 0) tc::mbar_arrive_expect_tx(&bar[B_KFULL + slot], 2 * KSLOT);
+          tc::tma_load_3d_2sm(smem_u32(sm + OFF_KRING + slot * KSLOT),
+                              a.segmaps + kSegMaps * (rq.seg_first + cur.j) + MAP_K9,
+                              cbar(B_KFULL + slot, 0), 0,
+                              cur.k0 - segs[cur.j].delta + 64 * static_cast<int>(r), 0);
+          ++cnt;
+          have = next_key_tile<TNK>(cur, segs, nseg, 0, r0hi, r1lo, r1hi);
+        }
+        // the pair's copies in flight land before either CTA may exit
+        if (r == 0)
+          for (uint32_t k = (cnt > KRING ? cnt - KRING : 0); k < cnt; ++k)
+            drain_bar(c, B_KFULL + k % KRING, (k / KRING) & 1);
+      }
+    } else if (warp == 1) {
+      // ------------------------------ S pair: MMA issuer (rank 0 only) --
+      if (lane == 0 && r == 0) {
+        const uint32_t idS = tc::idesc_bf16(256, 128, false, false);
+        const uint32_t ropa = smem_u32(sm + OFF_ROPE), ka = smem_u32(sm + OFF_KRING);
+        uint32_t rope_ev = 0;
+        // the first event also publishes the queries in tensor memory
+        bool ok = wait_bar<true>(c, B_ROPE, rope_ev++ & 1);
+        uint32_t cnt = 0;
+        int j = 0, prev_seg = -1;
+        KeyTile cur{0, 0, 0, -1};
+        bool have = next_key_tile<TNK>(cur, segs, nseg, 0, r0hi, r1lo, r1hi);
+        while (ok && have) {
+          const int b = j & 1;
+          ok = wait_bar<true>(c, B_SFREE + b, ((j >> 1) & 1) ^ 1);
+          if (ok && prev_seg >= 0 && cur.j != prev_seg)
+            ok = wait_bar<true>(c, B_ROPE, rope_ev++ & 1);
+          if (!ok) break;
+          tc::tc_fence_after();
+          const uint32_t ts = tbase + T_S + 128 * b;
+          const int slot = cnt % KRING;
+          ok = wait_bar(c, B_KFULL + slot, (cnt / KRING) & 1);
+          if (!ok) break;
+          tc::tc_fence_after();
+          const uint32_t base = ka + slot * KSLOT;
+          // B = K[64 keys of each CTA x 16 dims]: nope chunks 0..7, then the rope chunk
+#pragma unroll
+          for (int cc = 0; cc < 8; ++cc)
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              tc::mma_ts_2sm(ts, tbase + T_Q + 8 * (4 * cc + k),
+                             tc::sdesc_sw128(base + cc * HCHUNK + 32 * k, 16, 1024), idS,
+                             (cc | k) != 0);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint64_t bd = tc::sdesc_sw128(base + 8 * HCHUNK + 32 * k, 16, 1024);
+            tc::mma_ss_2sm(ts, tc::sdesc_sw128(ropa + 32 * k, 16, 1024), bd, idS, 1);
+            tc::mma_ss_2sm(ts, tc::sdesc_sw128(ropa + CHUNK + 32 * k, 16, 1024), bd, idS, 1);
+          }
+          tc::mma_commit_2sm(&bar[B_KEMPTY + slot], 0x3);
+          ++cnt;
+          tc::mma_commit_2sm(&bar[B_SFULL + b], 0x3);
+          prev_seg = cur.j;
+          ++j;
+          have = next_key_tile<TNK>(cur, segs, nseg, 0, r0hi, r1lo, r1hi);
+        }
+        tc::mma_commit_2sm(&bar[B_SFINAL], 0x3);
+      }
+    } else {
+      // ------------------- S pair: queries, rotation and online softmax ---
+      const int quarter = warp & 3;
+      const int m = quarter * 32 + lane;
+      const bool issuer = tid == 64;  // issues the bulk copies of P
+      const tt::RowInfo ri = tt::row_info(a, t, rq, m);
+      const uint32_t lt = tbase + (static_cast<uint32_t>(quarter * 32) << 16);
+      const float sl2 = a.scale_log2;
+      const int sink = a.sink, window = a.window;
+      const uint16_t* qrow = ri.p >= 0 ? a.q + (ri.frow * a.H + ri.head) * 576 : nullptr;
+      const uint32_t orank = crank + 2;
+      const uint32_t sw = static_cast<uint32_t>(m & 7);
+      // this lane's nope queries -> tensor memory (32-bit column c = dims 2c, 2c + 1)
+#pragma unroll 1
+      for (int i = 0; i < 8; ++i) {
+        uint32_t w[32];
+        if (qrow) {
+          const uint4* s4 = reinterpret_cast<const uint4*>(qrow) + 8 * i;
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const uint4 v = __ldg(s4 + u);
+            w[4 * u] = v.x;
+            w[4 * u + 1] = v.y;
+            w[4 * u + 2] = v.z;
+            w[4 * u + 3] = v.w;
+          }
+        } else {
+#pragma unroll
+          for (int u = 0; u < 32; ++u) w[u] = 0;
+        }
+        tc::tmem_st32(lt + T_Q + 32 * i, w);
+      }
+      tc::tmem_wait_st();
+      // q_rope' = R(-delta) q_rope as bf16 hi and lo rows of two K-major
+      // 128-byte-swizzled operands (RedKnot-MLA paper, RoPE-orthogonality
+      // paragraph)
+      auto put_rope = [&](int seg) {
+        const float* cs = a.rope_cs + static_cast<int64_t>(rq.seg_first + seg) * 64;
+        uint32_t raw[32];
+        if (qrow) {
+          const uint4* s4 = reinterpret_cast<const uint4*>(qrow + 512);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const uint4 v = __ldg(s4 + u);
+            raw[4 * u] = v.x;
+            raw[4 * u + 1] = v.y;
+            raw[4 * u + 2] = v.z;
+            raw[4 * u + 3] = v.w;
+          }
+        } else {
+#pragma unroll
+          for (int u = 0; u < 32; ++u) raw[u] = 0;
+        }
+        uint32_t hi[32];
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
+          const float x = __uint_as_float(raw[jj] << 16), y = __uint_as_float(raw[jj] & 0xffff0000u);
+          const float co = __ldg(cs + 2 * jj), si = __ldg(cs + 2 * jj + 1);
+          const float xr = fmaf(x, co, y * si), yr = fmaf(-x, si, y * co);
+          hi[jj] = pack_bf16x2(xr, yr);
+          raw[jj] = pack_bf16x2(xr - __uint_as_float(hi[jj] << 16),
+                                yr - __uint_as_float(hi[jj] & 0xffff0000u));
+        }
+        uint8_t* rrow = sm + OFF_ROPE + m * 128;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          *reinterpret_cast<uint4*>(rrow + ((u ^ sw) << 4)) =
+              make_uint4(hi[4 * u], hi[4 * u + 1], hi[4 * u + 2], hi[4 * u + 3]);
+          *reinterpret_cast<uint4*>(rrow + CHUNK + ((u ^ sw) << 4)) =
+              make_uint4(raw[4 * u], raw[4 * u + 1], raw[4 * u + 2], raw[4 * u + 3]);
+        }
+        tc::fence_proxy_async();
+      };
+      KeyTile kt{0, 0, 0, -1};
+      bool have = next_key_tile<TNK>(kt, segs, nseg, 0, r0hi, r1lo, r1hi);
+      put_rope(kt.j);
+      tc::tc_fence_before();
+      tc::mbar_arrive_cluster(cbar(B_ROPE, 0));
+      float m_run = -INFINITY, l_run = 0.f;
+      int j = 0;
+      bool ok = true;
+      // Every wait below is bounded; a failed wait skips the work but the
+      // lane still reaches the per-tile vote, so the four warps leave the
+      // loop together and no lane is left at a named barrier.
+      while (ok && have) {
+        const int b = j & 1;
+        KeyTile nx = kt;
+        const bool have_next = next_key_tile<TNK>(nx, segs, nseg, 0, r0hi, r1lo, r1hi);
+        bool okw = __all_sync(0xffffffffu, wait_bar(c, B_SFULL + b, (j >> 1) & 1));
+        uint32_t s[4][32];
+        float alpha = 1.f;
+        if (okw) {
+          tc::tc_fence_after();
+          // S_j is complete, so no score MMA still reads the rotated q_rope
+          if (have_next && nx.j != kt.j) {
+            put_rope(nx.j);
+            tc::mbar_arrive_cluster(cbar(B_ROPE, 0));
+          }
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) tc::tmem_ld32(lt + T_S + 128 * b + 32 * q4, s[q4]);
+          tc::tmem_wait_ld();
+          tc::tc_fence_before();
+          tc::mbar_arrive_cluster(cbar(B_SFREE + b, 0));
+
+          // scores are scaled inside the exponent: x = s * scale * log2(e)
+          const int p = ri.p;
+          const bool full = kt.k1 - kt.k0 == TNK && kt.k0 + TNK - 1 <= p &&
+                            (ri.glob || kt.k0 >= p - window || kt.k0 + TNK <= sink);
+          float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+          if (__all_sync(0xffffffffu, full)) {
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4)
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                mx4[i & 3] = fmaxf(mx4[i & 3], __uint_as_float(s[q4][i]));
+          } else {
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                const int key = kt.k0 + 32 * q4 + i;
+                bool vis = key < kt.k1 && key <= p;
+                if (!ri.glob) vis = vis && (key < sink || key >= p - window);
+                const float x = vis ? __uint_as_float(s[q4][i]) : -INFINITY;
+                s[q4][i] = __float_as_uint(x);
+                mx4[i & 3] = fmaxf(mx4[i & 3], x);
+              }
+            }
+          }
+          const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * sl2;
+          if (mx > m_run + 8.f) {  // lazy rescale: only when the max grows by more than 2^8
+            if (m_run != -INFINITY) alpha = fast_exp2(m_run - mx);
+            m_run = mx;
+          }
+          const float nb = (m_run == -INFINITY) ? 0.f : -m_run;
+          float ls4[4] = {0.f, 0.f, 0.f, 0.f};
+          // P in place: keys 2w, 2w + 1 in word w = 16 q4 + i of s[q4 >> 1]
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float p0 = fast_exp2(fmaf(__uint_as_float(s[q4][2 * i]), sl2, nb));
+              const float p1 = fast_exp2(fmaf(__uint_as_float(s[q4][2 * i + 1]), sl2, nb));
+              ls4[i & 3] += p0 + p1;
+              s[q4 >> 1][16 * (q4 & 1) + i] = pack_bf16x2(p0, p1);
+            }
+          }
+          l_run = l_run * alpha + ((ls4[0] + ls4[1]) + (ls4[2] + ls4[3]));
+          // the O pair's P buffer b is free once the output MMAs of tile
+          // j - 2 are done; the staging buffer once the copy of tile j - 1
+          // has read it
+          okw = __all_sync(0xffffffffu, wait_bar(c, B_PEMPTY + b, ((j >> 1) & 1) ^ 1));
+          if (okw && issuer) tc::bulk_wait_read<0>();  // the staging buffer is free
+        }
+        ok = tc::named_and(1, 128, okw);
+        if (!ok) break;
+        uint8_t* stg = sm + OFF_STG;
+        // lane m's 128 keys: two 64-key chunks of 8 16-byte units, 128-byte swizzle
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            *reinterpret_cast<uint4*>(stg + h * CHUNK + m * 128 + ((u ^ sw) << 4)) =
+                make_uint4(s[h][4 * u], s[h][4 * u + 1], s[h][4 * u + 2], s[h][4 * u + 3]);
+        *reinterpret_cast<float2*>(stg + PBUF + m * 8) = make_float2(alpha, l_run);
+        tc::fence_proxy_async();
+        tc::named_sync(1, 128);
+        if (issuer) {
+          tc::bulk_copy_to_cluster(tc::mapa_shared(smem_u32(sm + OFF_P + b * PSTRIDE), orank),
+                                   smem_u32(stg), PREC_BYTES, cbar(B_PFULL + b, orank));
+          tc::bulk_commit_group();
+        }
+        ++j;
+        kt = nx;
+        have = have_next;
+      }
+      // every output MMA has consumed its P before the cluster may exit
+      for (int jj = j - 1; ok && jj >= 0 && jj >= j - 2; --jj)
+        ok = __all_sync(0xffffffffu, wait_bar(c, B_PEMPTY + (jj & 1), (jj >> 1) & 1));
+      if (issuer) tc::bulk_wait_read<0>();
+      if (ok && ri.store && l_run > 0.f)
+        a.lse[ri.frow * a.H + ri.head] = m_run * 0.6931471805599453f + logf(l_run);
+    }
+  } else {
+    if (warp == 0) {
+      // ------------------------------------------- O pair: TMA producer --
+      if (lane == 0) {
+        uint32_t cnt = 0;
+        bool ok = true;
+        KeyTile cur{0, 0, 0, -1};
+        bool have = next_key_tile<TNK>(cur, segs, nseg, 0, r0hi, r1lo, r1hi);
+        while (ok && have) {
+          const int slot = cnt % VRING;
+          ok = wait_bar(c, B_VEMPTY + slot, ((cnt / VRING) & 1) ^ 1);
+          if (!ok) break;
+          if (r == 0) tc::mbar_arrive_expect_tx(&bar[B_VFULL + slot], 2 * VSLOT);
+          // value columns 256 r .. 256 r + 255 (chunks 4 r .. 4 r + 3)
+          tc::tma_load_3d_2sm(smem_u32(sm + OFF_VRING + slot * VSLOT),
+                              a.segmaps + kSegMaps * (rq.seg_first + cur.j) + MAP_V4,
+                              cbar(B_VFULL + slot, 2), 0, cur.k0 - segs[cur.j].delta,
+                              4 * static_cast<int>(r));
+          ++cnt;
+          have = next_key_tile<TNK>(cur, segs, nseg, 0, r0hi, r1lo, r1hi);
+        }
+        if (r == 0)
+          for (uint32_t k = (cnt > VRING ? cnt - VRING : 0); k < cnt; ++k)
+            drain_bar(c, B_VFULL + k % VRING, (k / VRING) & 1);
+      }
+    } else if (warp == 1) {
+      // ------------------------------ O pair: MMA issuer (rank 2 only) --
+      if (lane == 0 && r == 0) {
+        const uint32_t idPV = tc::idesc_bf16(256, 256, false, true);
+        const uint32_t pa = smem_u32(sm + OFF_P), va = smem_u32(sm + OFF_VRING);
+        uint32_t cnt = 0;
+        int j = 0;
+        bool ok = true;
+        KeyTile cur{0, 0, 0, -1};
+        bool have = next_key_tile<TNK>(cur, segs, nseg, 0, r0hi, r1lo, r1hi);
+        while (ok && have) {
+          const int b = j & 1;
+          ok = wait_bar<true>(c, B_PREADY + b, (j >> 1) & 1);
+          if (!ok) break;
+          tc::tc_fence_after();
+          const int slot = cnt % VRING;
+          ok = wait_bar(c, B_VFULL + slot, (cnt / VRING) & 1);
+          if (!ok) break;
+          tc::tc_fence_after();
+          const uint32_t base = va + slot * VSLOT;
+          // A = P[128 lanes of each CTA x 16 keys]; B = V[16 keys x 256
+          // columns]: 128 from each CTA, two 64-column chunks 16 KB apart.
+          // Output columns 256 v + 128 h + i hold value column
+          // 256 h + 128 v + i (h: the CTA that supplied them).
+#pragma unroll
+          for (int v = 0; v < 2; ++v)
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              tc::mma_ss_2sm(tbase + T_O + 256 * v,
+                             tc::sdesc_sw128(pa + b * PSTRIDE + (k >> 2) * CHUNK + 32 * (k & 3), 16, 1024),
+                             tc::sdesc_sw128(base + 2 * CHUNK * v + 2048 * k, CHUNK, 1024), idPV,
+                             (j > 0 || k > 0) ? 1u : 0u);
+          tc::mma_commit_2sm(&bar[B_VEMPTY + slot], 0xC);
+          ++cnt;
+          tc::mma_commit_2sm(&bar[B_ODONE], 0xC);
+          tc::mma_commit_2sm(&bar[B_PEMPTY + b], 0x3);
+          ++j;
+          have = next_key_tile<TNK>(cur, segs, nseg, 0, r0hi, r1lo, r1hi);
+        }
+        tc::mma_commit_2sm(&bar[B_OFINAL], 0xC);
+      }
+    } else {
+      // ------------------------------- O pair: rescale and epilogue ------
+      const int quarter = warp & 3;
+      const int m = quarter * 32 + lane;
+      const tt::RowInfo ri = tt::row_info(a, t, rq, m);
+      const uint32_t lt = tbase + (static_cast<uint32_t>(quarter * 32) << 16);
+
+      float l_fin = 0.f;
+      int j = 0;
+      bool ok = true;
+      KeyTile kt{0, 0, 0, -1};
+      bool have = next_key_tile<TNK>(kt, segs, nseg, 0, r0hi, r1lo, r1hi);
+      while (ok && have) {
+        const int b = j & 1;
+        ok = __all_sync(0xffffffffu, wait_bar<true>(c, B_PFULL + b, (j >> 1) & 1));
+        if (!ok) break;
+        const volatile float* rp =
+            reinterpret_cast<const volatile float*>(sm + OFF_P + b * PSTRIDE + PBUF + m * 8);
+        const float alpha = rp[0];
+        l_fin = rp[1];
+        // arm buffer b for tile j + 2 (its copy starts after the MMAs of tile j)
+        if (m == 0) tc::mbar_arrive_expect_tx(&bar[B_PFULL + b], PREC_BYTES);
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+          // the output MMAs of tile j - 1 finish before O is rescaled
+          if (j >= 1) ok = __all_sync(0xffffffffu, wait_bar(c, B_ODONE, (j - 1) & 1));
+          if (!ok) break;
+          tc::tc_fence_after();
+#pragma unroll 1
+          for (int q8 = 0; q8 < 16; ++q8) {
+            uint32_t o[32];
+            tc::tmem_ld32(lt + T_O + 32 * q8, o);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tc::tmem_st32(lt + T_O + 32 * q8, o);
+          }
+          tc::tmem_wait_st();
+        }
+        tc::tc_fence_before();
+        tc::mbar_arrive_cluster(cbar(B_PREADY + b, 2));
+        ++j;
+        have = next_key_tile<TNK>(kt, segs, nseg, 0, r0hi, r1lo, r1hi);
+      }
+      if (ok) ok = __all_sync(0xffffffffu, wait_bar(c, B_OFINAL, 0));
+      tc::tc_fence_after();
+      if (ok) {
+        const bool st = ri.store && l_fin > 0.f;
+        const float inv = st ? 1.f / l_fin : 0.f;
+        uint16_t* dst = st ? a.out + (ri.frow * a.H + ri.head) * 512 : nullptr;
+#pragma unroll 1
+        for (int q8 = 0; q8 < 16; ++q8) {
+          uint32_t o[32];
+          tc::tmem_ld32(lt + T_O + 32 * q8, o);
+          tc::tmem_wait_ld();
+          if (st) {
+            const int c0 = 32 * q8;
+            const int col = 256 * ((c0 >> 7) & 1) + 128 * (c0 >> 8) + (c0 & 127);
+            uint4* d4 = reinterpret_cast<uint4*>(dst + col);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              uint4 w;
+              w.x = pack_bf16x2(__uint_as_float(o[8 * u + 0]) * inv, __uint_as_float(o[8 * u + 1]) * inv);
+              w.y = pack_bf16x2(__uint_as_float(o[8 * u + 2]) * inv, __uint_as_float(o[8 * u + 3]) * inv);
+              w.z = pack_bf16x2(__uint_as_float(o[8 * u + 4]) * inv, __uint_as_float(o[8 * u + 5]) * inv);
+              w.w = pack_bf16x2(__uint_as_float(o[8 * u + 6]) * inv, __uint_as_float(o[8 * u + 7]) * inv);
+              d4[u] = w;
+            }
+          }
+        }
+      }
+    }
+  }
+
+  // ------------------------------------------------------------ teardown --
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) drain_bar(c, spair ? B_SFINAL : B_OFINAL, 0);  // the pair's MMA pipe is empty
+  __syncthreads();
+  tc::cluster_sync();  // no CTA leaves while another may still use its memory
+  if (warp == 1) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc_2sm(tbase, 512);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_dense_tc4(const rk_seg_attn_plan_s& p, const KernelArgs& a, const void* q,
+                             cudaStream_t s) {
+  (void)p;
+  (void)q;
+  cudaError_t e = cudaFuncSetAttribute(dense_tc4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(SMEM_BYTES));
+  if (e != cudaSuccess) return e;
+  const int64_t grid = 4 * static_cast<int64_t>(a.num_tc_pairs);
+  dense_tc4_kernel<<<static_cast<unsigned>(grid), THREADS, SMEM_BYTES, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace rk

@@ -135,7 +135,7 @@ static rk_status_t build_plan(const rk_seg_attn_desc_t* d, rk_seg_attn_plan_s* p
   if (!(d->rope_base > 1.0) || !std::isfinite(d->rope_base)) return RK_ERR_INVALID_ARG;
   if (!(d->softmax_scale > 0.f) || !std::isfinite(d->softmax_scale)) return RK_ERR_INVALID_ARG;
   if (d->sink < 0 || d->window < 0) return RK_ERR_INVALID_ARG;
-  if (d->flags & ~(RK_PLAN_HOST_ONLY | RK_PLAN_LEGACY_MMA | RK_PLAN_SINGLE_CTA))
+  if (d->flags & ~(RK_PLAN_HOST_ONLY | RK_PLAN_LEGACY_MMA | RK_PLAN_SINGLE_CTA | RK_PLAN_CTA_PAIR))
     return RK_ERR_INVALID_ARG;
   if (d->seg_begin[0] != 0) return RK_ERR_INVALID_ARG;
   for (int r = 0; r < R; ++r)
@@ -168,7 +168,7 @@ static rk_status_t build_plan(const rk_seg_attn_desc_t* d, rk_seg_attn_plan_s* p
     const bool hg_ok = hg == 0 || (kTcM % hg == 0 && (kTcM / hg) % 8 == 0);
     const bool h_ok = d->num_heads == 64 || d->num_heads == 128;
     if (!(d->flags & RK_PLAN_LEGACY_MMA) && d->d_nope == 512 && d->d_rope == 64 && hg_ok && h_ok) {
-      p->kernel = (d->flags & RK_PLAN_SINGLE_CTA) ? 1 : 2;
+      p->kernel = (d->flags & RK_PLAN_SINGLE_CTA) ? 1 : (d->flags & RK_PLAN_CTA_PAIR) ? 2 : 3;
       p->tile_m = kTcM;
     }
   }
@@ -439,7 +439,7 @@ static rk_status_t build_plan(const rk_seg_attn_desc_t* d, rk_seg_attn_plan_s* p
   p->tiles.reserve(tiles.size());
   for (auto& t : tiles) p->tiles.push_back(t.second);
   info.dense_tiles = static_cast<int64_t>(p->tiles.size() + tc_list.size());
-  if (p->kernel == 2) {
+  if (p->kernel >= 2) {
     // Pair neighbouring tiles of one request and kind (adjacent Global row
     // blocks, consecutive protected rows) when the union of their key
     // ranges costs at most 1/8 more key tiles than the two ranges apart;
@@ -551,18 +551,17 @@ extern "C" rk_status_t rk_seg_attn_plan(const rk_seg_attn_desc_t* desc, void* st
     if (st == RK_OK) st = upload(p->tc_pairs, &p->d_tc_pairs, s);
     if (st == RK_OK) st = upload(p->head_role, &p->d_head_role, s);
     if (st == RK_OK && p->kernel >= 1) {
-      // four TMA maps per segment latent, viewing a row as 9 chunks of 64
-      // bf16: (64, n, 9) so that a box lands chunk-major in shared memory;
-      // boxes of 128 rows x 2 chunks and x 1 chunk, of 64 rows x 4 chunks
-      // and x 1 chunk
-      p->segmaps.resize(4 * p->segs.size());
+      // TMA maps of each segment latent, viewing a row as 9 chunks of 64
+      // bf16: (64, n, 9) so that a box lands chunk-major in shared memory
+      p->segmaps.resize(rk::kSegMaps * p->segs.size());
       for (size_t i = 0; i < p->segs.size() && st == RK_OK; ++i) {
         const uint64_t dims[3] = {64, static_cast<uint64_t>(p->segs[i].n), 9};
         const uint64_t strides[2] = {576 * 2, 128};
-        const uint32_t boxes[4][3] = {{64, 128, 2}, {64, 128, 1}, {64, 64, 4}, {64, 64, 1}};
-        for (int b = 0; b < 4 && st == RK_OK; ++b)
-          if (!rk::make_tmap_bf16(&p->segmaps[4 * i + b], p->segs[i].latent, 3, dims, strides,
-                                  boxes[b]))
+        const uint32_t boxes[rk::kSegMaps][3] = {
+            {64, 128, 2}, {64, 128, 1}, {64, 64, 4}, {64, 64, 1}, {64, 64, 9}, {64, 128, 4}};
+        for (int b = 0; b < rk::kSegMaps && st == RK_OK; ++b)
+          if (!rk::make_tmap_bf16(&p->segmaps[rk::kSegMaps * i + b], p->segs[i].latent, 3, dims,
+                                  strides, boxes[b]))
             st = RK_ERR_CUDA;
       }
       if (st == RK_OK) st = upload(p->segmaps, &p->d_segmaps, s);
@@ -706,7 +705,8 @@ cudaError_t launch_forward(const rk_seg_attn_plan_s& p, const KernelArgs& a, con
   }
   if (a.num_tiles) e = launch_dense_mma(p, a, ts);
   if (e == cudaSuccess && a.num_tc_tiles) e = launch_dense_tc(p, a, q, ts);
-  if (e == cudaSuccess && a.num_tc_pairs) e = launch_dense_tc2(p, a, q, ts);
+  if (e == cudaSuccess && a.num_tc_pairs)
+    e = p.kernel == 3 ? launch_dense_tc4(p, a, q, ts) : launch_dense_tc2(p, a, q, ts);
   if (e == cudaSuccess && a.num_chunks) e = launch_split_decode(p, a, s);
   if (ts != s) {
     const cudaError_t e1 = cudaEventRecord(p.ev_join, ts);

@@ -11,6 +11,11 @@
 
 namespace rk {
 
+// TMA maps per segment latent (viewed as (64, n, 9 chunks)), by box:
+// 0: 128 rows x 2 chunks, 1: 128 rows x 1 chunk, 2: 64 rows x 4 chunks,
+// 3: 64 rows x 1 chunk, 4: 64 rows x 9 chunks, 5: 128 rows x 4 chunks.
+constexpr int kSegMaps = 6;
+
 // One segment as the kernels see it; segments of a request are stored
 // contiguously, sorted by offset.
 struct DevSeg {
@@ -116,8 +121,7 @@ struct KernelArgs {
   const TcTile* tc_tiles;
   int32_t num_tc_tiles;
   int32_t rows_per_gtile;     // 128 / HG
-  const CUtensorMap* segmaps; // 4 per segment: latent viewed (64, n, 9 chunks); boxes of
-                              // 128 rows x 2 / 1 chunks and of 64 rows x 4 / 1 chunks
+  const CUtensorMap* segmaps; // kSegMaps per segment
   const uint8_t* head_role;   // [H]
   int32_t g_ingroup;          // Global heads are 8g + g_ingroup for every group g, or -1
   const CUtensorMap* decmaps; // per segment: latent viewed (64, n, 9 chunks), box 32 rows x 9 chunks
@@ -133,7 +137,7 @@ struct rk_seg_attn_plan_s {
   int32_t H = 0, d_nope = 0, d_rope = 0;
   int32_t sink = 0, window = 0;
   float softmax_scale = 0.f;
-  int kernel = 0;          // 0 mma.sync tiles, 1 tcgen05 tiles, 2 tcgen05 CTA-pair tiles
+  int kernel = 0;          // 0 mma.sync, 1 tcgen05 tiles, 2 CTA-pair tiles, 3 4-CTA tiles
   int tile_m = 64;         // query pairs per dense tile
   int g_ingroup = -1;      // Global heads are exactly 8g + g_ingroup, else -1
   rk_plan_info_t info{};
@@ -183,6 +187,8 @@ cudaError_t launch_split_decode(const rk_seg_attn_plan_s& plan, const KernelArgs
 cudaError_t launch_dense_tc(const rk_seg_attn_plan_s& plan, const KernelArgs& a,
                             const void* q, cudaStream_t stream);
 cudaError_t launch_dense_tc2(const rk_seg_attn_plan_s& plan, const KernelArgs& a,
+                             const void* q, cudaStream_t stream);
+cudaError_t launch_dense_tc4(const rk_seg_attn_plan_s& plan, const KernelArgs& a,
                              const void* q, cudaStream_t stream);
 // Fill the kernel arguments shared by every launch of a forward.
 void fill_args(const rk_seg_attn_plan_s& plan, KernelArgs& a, const void* q, void* out,

@@ -1,0 +1,218 @@
+// Pieces shared by the tcgen05 prefill-tile kernels: bounded mbarrier waits,
+// the (row, head) of a tile lane, the rotated q_rope written to tensor
+// memory, and the TMA maps and loads of a tile's queries.
+#pragma once
+
+#include "tc_ptx.cuh"
+#include "tmap.h"
+
+namespace rk {
+namespace tt {
+
+constexpr uint64_t WAIT_NS = 2000000000ull;  // bound of every wait: 2 s
+
+struct Ctx {
+  uint64_t* bar;              // this CTA's barrier array
+  volatile uint32_t* abort;   // set by any role of this CTA that gives up
+  int32_t* status;            // the launch's device status word
+};
+
+// Bounded wait for the phase with `parity` of barrier i; also gives up as
+// soon as another role of this CTA, or any CTA of the launch, has recorded
+// an error.  On expiry records RK_ERR_DEVICE_TIMEOUT.
+// CLUSTER: acquire at cluster scope (the phase is completed by arrivals
+// from other CTAs that publish shared-memory data).
+template <bool CLUSTER = false>
+__device__ __forceinline__ bool wait_bar(const Ctx& c, int i, uint32_t parity) {
+  uint64_t* b = c.bar + i;
+  uint32_t it = 0;
+  uint64_t t0 = 0;
+  while (!(CLUSTER ? tc::mbar_try_wait_cluster(b, parity) : tc::mbar_try_wait(b, parity))) {
+    if ((++it & 63u) == 0) {
+      if (*c.abort || *reinterpret_cast<volatile int32_t*>(c.status)) {
+        *c.abort = 1;
+        return false;
+      }
+      const uint64_t now = tc::global_ns();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > WAIT_NS) {
+        *c.abort = 1;
+        atomicCAS(c.status, 0, static_cast<int32_t>(RK_ERR_DEVICE_TIMEOUT));
+        return false;
+      }
+    }
+  }
+  return true;
+}
+
+// Bounded wait that ignores the abort flag (drains work in flight).
+__device__ __forceinline__ void drain_bar(const Ctx& c, int i, uint32_t parity) {
+  uint64_t* b = c.bar + i;
+  const uint64_t t0 = tc::global_ns();
+  while (!tc::mbar_try_wait(b, parity)) {
+    if (tc::global_ns() - t0 > WAIT_NS) {
+      atomicCAS(c.status, 0, static_cast<int32_t>(RK_ERR_DEVICE_TIMEOUT));
+      return;
+    }
+  }
+}
+
+struct RowInfo {
+  int p;       // absolute row, -1 if the lane is unused
+  int head;
+  bool glob;   // Global visibility rule (k <= p), else Local (sink u [p - w, p])
+  bool store;  // written by the epilogue
+  int64_t frow;
+};
+
+// The query pair of TMEM lane m of tile t.  kind 0: row t.p0 + m % R of
+// Global head m / R (R = 128 / HG).  kind 1: row t.p0 (m < H) or t.p1 of
+// head m % H, stored only for Local heads.  Bit 0 of t.pad marks a tile
+// without work (every lane unused).
+__device__ __forceinline__ RowInfo row_info(const KernelArgs& a, const TcTile& t,
+                                            const DevReq& rq, int m) {
+  RowInfo r;
+  const bool idle = (t.pad & 1) != 0;
+  if (t.kind == 0) {
+    const int R = a.rows_per_gtile;
+    const int hi = m / R, ri = m - hi * R;
+    const bool v = !idle && ri < t.p1 && hi < a.num_global;
+    r.p = v ? t.p0 + ri : -1;
+    r.head = v ? a.global_heads[hi] : 0;
+    r.glob = true;
+    r.store = v;
+  } else {
+    const int ri = m / a.H, h = m - ri * a.H;
+    const int pr = idle ? -1 : ((ri == 0) ? t.p0 : t.p1);
+    r.p = pr;
+    r.head = h;
+    r.glob = false;
+    r.store = pr >= 0 && a.head_role[h] == 0;
+  }
+  r.frow = r.p >= 0 ? rq.row_base + (r.p - rq.q_row_begin) : -1;
+  return r;
+}
+
+// q_rope' = R(-delta) q_rope of one row (RedKnot-MLA paper, RoPE-orthogonality
+// paragraph: the query turns by -delta_i instead of rewriting the cache) as
+// bf16 hi and lo parts, written to this thread's TMEM lane at columns rh..
+// and rl.. (rotation pair j in column j).  The row's q_rope (`src`, 64 bf16)
+// is re-read from global memory each time; an unused lane (src == nullptr)
+// writes zeros.
+__device__ __forceinline__ void write_rope(uint32_t lane_taddr, uint32_t rh, uint32_t rl,
+                                           const uint16_t* src, const float* cs) {
+  uint32_t raw[32];
+  if (src) {
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const uint4 v = __ldg(s4 + u);
+      raw[4 * u] = v.x;
+      raw[4 * u + 1] = v.y;
+      raw[4 * u + 2] = v.z;
+      raw[4 * u + 3] = v.w;
+    }
+  } else {
+#pragma unroll
+    for (int u = 0; u < 32; ++u) raw[u] = 0;
+  }
+  uint32_t hi[32];
+#pragma unroll
+  for (int jj = 0; jj < 32; ++jj) {
+    const float x = __uint_as_float(raw[jj] << 16), y = __uint_as_float(raw[jj] & 0xffff0000u);
+    const float co = __ldg(cs + 2 * jj), si = __ldg(cs + 2 * jj + 1);
+    const float xr = fmaf(x, co, y * si), yr = fmaf(-x, si, y * co);
+    hi[jj] = pack_bf16x2(xr, yr);
+    raw[jj] = pack_bf16x2(xr - __uint_as_float(hi[jj] << 16),
+                          yr - __uint_as_float(hi[jj] & 0xffff0000u));
+  }
+  tc::tmem_st32(lane_taddr + rh, hi);
+  tc::tmem_st32(lane_taddr + rl, raw);
+  tc::tmem_wait_st();
+}
+
+// TMA views of q (bf16 [rows, H, 576]) for loading a tile's nope part
+// chunk-major into shared memory (8 chunks of 128 lanes x 64 dims, 128-byte
+// swizzled).
+struct QMaps {
+  CUtensorMap g5;   // Global, one Global head per group: (64, rows, groups, 8 chunks, in-group)
+  CUtensorMap g3;   // Global, any roles: (576, H, rows), box (64, 1, R)
+  CUtensorMap l4;   // Local, H = 128: (64, H, 8 chunks, rows), box (64, 128, 8, 1)
+  CUtensorMap l3;   // Local, any H: (576, H, rows), box (64, H, 1)
+};
+
+inline cudaError_t make_qmaps(const rk_seg_attn_plan_s& p, const KernelArgs& a, const void* q,
+                              QMaps& qm) {
+  qm = QMaps{};
+  const uint64_t H = static_cast<uint64_t>(p.H), rows = static_cast<uint64_t>(p.info.rows);
+  const uint32_t R = static_cast<uint32_t>(a.rows_per_gtile > 0 ? a.rows_per_gtile : 8);
+  if (a.g_ingroup >= 0) {  // the whole Global tile in one box
+    const uint64_t G = H / 8;
+    const uint64_t dims[5] = {64, rows, G, 8, 8};
+    const uint64_t strides[4] = {H * 1152, 8 * 1152, 128, 1152};
+    const uint32_t box[5] = {64, R, static_cast<uint32_t>(G), 8, 1};
+    if (!make_tmap_bf16(&qm.g5, q, 5, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[3] = {576, H, rows};
+    const uint64_t strides[2] = {1152, H * 1152};
+    const uint32_t boxg[3] = {64, 1, R};
+    const uint32_t boxl[3] = {64, static_cast<uint32_t>(H), 1};
+    if (!make_tmap_bf16(&qm.g3, q, 3, dims, strides, boxg)) return cudaErrorInvalidValue;
+    if (!make_tmap_bf16(&qm.l3, q, 3, dims, strides, boxl)) return cudaErrorInvalidValue;
+  }
+  if (H == 128) {
+    const uint64_t dims[4] = {64, H, 8, rows};
+    const uint64_t strides[3] = {1152, 128, H * 1152};
+    const uint32_t box[4] = {64, static_cast<uint32_t>(H), 8, 1};
+    if (!make_tmap_bf16(&qm.l4, q, 4, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  return cudaSuccess;
+}
+
+// Issue the TMA loads of tile t's queries (128 KB) into `qdst`.  PAIR: the
+// copies complete on the barrier at cluster address `bar` (cta_group::2
+// form, the barrier may be the peer's); otherwise on this CTA's barrier at
+// shared address `bar`.
+template <bool PAIR>
+__device__ __forceinline__ void load_q_tile(const KernelArgs& a, const QMaps& qm, const TcTile& t,
+                                            const DevReq& rq, uint32_t qdst, uint32_t bar) {
+  auto ld3 = [&](uint32_t dst, const CUtensorMap* m, int32_t x, int32_t y, int32_t z) {
+    if (PAIR)
+      tc::tma_load_3d_2sm(dst, m, bar, x, y, z);
+    else
+      tc::tma_load_3d_u32(dst, m, bar, x, y, z);
+  };
+  if (t.kind == 0) {
+    const int32_t fr = static_cast<int32_t>(rq.row_base + (t.p0 - rq.q_row_begin));
+    if (a.g_ingroup >= 0) {
+      if (PAIR)
+        tc::tma_load_5d_2sm(qdst, &qm.g5, bar, 0, fr, 0, 0, a.g_ingroup);
+      else
+        tc::tma_load_5d_u32(qdst, &qm.g5, bar, 0, fr, 0, 0, a.g_ingroup);
+    } else {
+      const int R = a.rows_per_gtile;
+      for (int ch = 0; ch < 8; ++ch)
+        for (int hi = 0; hi < a.num_global; ++hi)
+          ld3(qdst + ch * 16384 + hi * R * 128, &qm.g3, 64 * ch, a.global_heads[hi], fr);
+    }
+  } else if (a.H == 128) {
+    const int32_t fr = static_cast<int32_t>(rq.row_base + (t.p0 - rq.q_row_begin));
+    if (PAIR)
+      tc::tma_load_4d_2sm(qdst, &qm.l4, bar, 0, 0, 0, fr);
+    else
+      tc::tma_load_4d_u32(qdst, &qm.l4, bar, 0, 0, 0, fr);
+  } else {
+    const int rows_per = 128 / a.H;
+    for (int ch = 0; ch < 8; ++ch)
+      for (int ri = 0; ri < rows_per; ++ri) {
+        const int pr = (ri == 0 || t.p1 < 0) ? t.p0 : t.p1;
+        const int32_t fr = static_cast<int32_t>(rq.row_base + (pr - rq.q_row_begin));
+        ld3(qdst + ch * 16384 + ri * a.H * 128, &qm.l3, 64 * ch, 0, fr);
+      }
+  }
+}
+
+}  // namespace tt
+}  // namespace rk

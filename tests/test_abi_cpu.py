@@ -147,16 +147,18 @@ def test_plan_counts_attended_pairs(name):
 @pytest.mark.parametrize("name", ["flash_mini", "varlen_mini", "ctx128k_mini", "flash", "ctx16k",
                                   "ctx128k"])
 def test_pair_plan_work_bounds(name):
-    """For d = (512, 64) the default plan pairs tcgen05 tiles on CTA pairs
-    (kernel 2); RK_PLAN_SINGLE_CTA keeps one tile per CTA pair of d_v halves
-    (kernel 1).  Pairing walks the union of two tiles' key ranges: the
+    """For d = (512, 64) the default plan pairs tcgen05 tiles on 4-CTA
+    clusters (kernel 3), RK_PLAN_CTA_PAIR on CTA pairs (kernel 2), and
+    RK_PLAN_SINGLE_CTA keeps one tile per two CTAs (kernel 1).  Pairing walks the union of two tiles' key ranges: the
     pairing rule bounds the extra key tiles by 1/8, and a merged range can
     also save a key tile where a tile's sink and window ranges split one
     128-key block.  Either way every attended pair is still covered."""
     _, pp = _host_plan(name)
+    _, p2 = _host_plan(name, flags=B.RK_PLAN_HOST_ONLY | B.RK_PLAN_CTA_PAIR)
     _, ps = _host_plan(name, flags=B.RK_PLAN_HOST_ONLY | B.RK_PLAN_SINGLE_CTA)
     a, b = pp.info, ps.info
-    assert a["kernel"] == 2 and b["kernel"] == 1
+    assert a["kernel"] == 3 and p2.info["kernel"] == 2 and b["kernel"] == 1
+    assert p2.info["performed_pairs"] == a["performed_pairs"]
     assert a["dense_tiles"] == b["dense_tiles"]
     assert a["performed_pairs"] <= b["performed_pairs"] * 9 // 8
     assert a["performed_pairs"] >= a["pairs_global"] + a["pairs_local"]

@@ -17,7 +17,8 @@ from position_independent_kv_gb300.workloads import SPECS, make_workload
 pytestmark = pytest.mark.gpu
 
 MINI = ["tiny", "tiny_wide", "flash_mini", "varlen_mini", "ctx128k_mini", "decode_mini"]
-KERNELS = {"default": 0, "single_cta": B.RK_PLAN_SINGLE_CTA, "legacy": B.RK_PLAN_LEGACY_MMA}
+KERNELS = {"default": 0, "cta_pair": B.RK_PLAN_CTA_PAIR, "single_cta": B.RK_PLAN_SINGLE_CTA,
+           "legacy": B.RK_PLAN_LEGACY_MMA}
 
 
 @pytest.fixture(scope="module", autouse=True)
