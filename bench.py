@@ -32,9 +32,38 @@ sys.path.insert(0, ROOT)
 METRIC = ("seg-relocated MLA attention TFLOP/s & % bf16 peak (1×GB300); "
           "decode HBM GB/s")
 WORKLOAD = "ctx128k"
-WORKLOAD_DESC = ("128K long context: 48 x 2048-row latents (shuffled) + 32768 new rows, "
-                 "H=128 (112 Local/16 Global), d_nope=512, d_rope=64, sink=4, w=256, "
-                 "protected budget 25%, bf16 N(0,1)/sqrt(576), seed 0")
+
+
+def workload_desc(name: str) -> str:
+    """One-line description of a named synthetic workload."""
+    from position_independent_kv_gb300.workloads import SPECS
+    sp = SPECS[name]
+    hg = sp.H // 8
+    if sp.decode_requests:
+        lo, hi = sp.decode_len_range
+        s0, s1 = sp.decode_seg_range
+        seg = (f"{sp.decode_requests} requests x 1 row, {s0}-{s1} segments, {lo}-{hi} keys")
+    elif sp.seg_lengths:
+        seg = (f"{len(sp.seg_lengths)} x {sp.seg_lengths[0]}-row latents"
+               f"{' (shuffled)' if sp.shuffle else ''} + {sp.n_new} new rows")
+    else:
+        lo, hi = sp.seg_len_range
+        seg = f"{sp.n_segments} latents of {lo}-{hi} rows (shuffled) + {sp.n_new} new rows"
+    r = sp.rule
+    if r.none:
+        prot = "no protected rows"
+    elif r.budget:
+        prot = f"protected budget {int(round(100 * r.budget))}% (boundary {r.boundary} first)"
+    elif r.p_random:
+        prot = f"protected: boundary {r.boundary} + {int(round(100 * r.p_random))}% random"
+    else:
+        prot = f"protected: query rows + boundary {r.boundary}"
+    out = f", {int(round(100 * sp.outlier_frac))}% outlier rows x8" if sp.outlier_frac else ""
+    return (f"{name}: {seg}, H={sp.H} ({sp.H - hg} Local/{hg} Global), d_nope={sp.d_nope}, "
+            f"d_rope={sp.d_rope}, sink={sp.sink}, w={sp.window}, {prot}, "
+            f"bf16 N(0,1)/sqrt({sp.d_nope + sp.d_rope}){out}, seed 0")
+
+
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -292,6 +321,8 @@ def bench_prefill(args, ws, local, pk):
         del h_q, h_out, h_lse, h_lat
     plan.close()
     res["wl"] = wl
+    res["q_bytes"] = wl.q.numel() * wl.q.element_size()
+    res["o_bytes"] = wl.out_init.numel() * wl.out_init.element_size()
     return res
 
 
@@ -408,9 +439,10 @@ def run_ours(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": WORKLOAD_DESC, "name": args.workload,
+            "config": {"workload": workload_desc(args.workload), "name": args.workload,
                        "parallelism": f"replicas{ws}",
-                       "l2": "inputs larger than L2 (Q 19.3 GB + O 17.2 GB per step), no flush",
+                       "l2": (f"inputs larger than L2 (Q {res['q_bytes'] / 1e9:.1f} GB + "
+                              f"O {res['o_bytes'] / 1e9:.1f} GB per step), no flush"),
                        "kernel": kernel, "dense_tiles": info["dense_tiles"],
                        "pairs_global": info["pairs_global"], "pairs_local": info["pairs_local"],
                        "performed_pairs": info["performed_pairs"]},
@@ -471,7 +503,7 @@ def run_reference(args):
             "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "impl": "reference",
-            "config": {"workload": WORKLOAD_DESC, "name": args.workload},
+            "config": {"workload": workload_desc(args.workload), "name": args.workload},
             "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": last["cores"],
                              "kind": "oracle", "sample": last["sample"]},
             "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
