@@ -294,6 +294,117 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(128, 1)
   if (warp == 0) tc::tmem_dealloc_2sm(tbase, 256);
 }
 
+
+// Pair streaming probe: clusters of two CTAs pull `n` boxes each of a
+// [rows, 576] bf16 tensor (viewed (64, rows, 9), box 64 x box_rows x
+// box_chunks) through `slots` buffers.  mode 0: each CTA loads into its own
+// buffer on its own barrier and releases it on arrival; mode 1: both CTAs'
+// boxes complete on rank 0's barrier (cta_group::2 form) and rank 0 releases
+// the slot in both CTAs; mode 2: each CTA loads on its own barrier, rank 1
+// forwards its arrival to rank 0 with a remote arrive, and rank 0 releases
+// the slot in both CTAs.  Every wait is bounded.
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64, 1)
+    tma_pair_probe_kernel(const __grid_constant__ CUtensorMap tm, int rows, int box_rows,
+                          int box_chunks, int slots, int n, int mode, int32_t* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  const uint32_t bb = 128u * box_rows * box_chunks;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + slots * bb);
+  uint64_t* empty = full + slots;
+  uint64_t* peer = empty + slots;
+  const int tid = threadIdx.x;
+  const uint32_t rank = tc::cluster_ctarank();
+  if (tid == 0) {
+    for (int i = 0; i < slots; ++i) {
+      tc::mbar_init(&full[i], 1);
+      tc::mbar_init(&empty[i], 1);
+      tc::mbar_init(&peer[i], 1);
+    }
+    tc::fence_barrier_init();
+  }
+  __syncthreads();
+  tc::cluster_sync();
+  const int span = rows - box_rows;
+  if (tid == 0) {
+    for (int c = 0; c < n; ++c) {
+      const int slot = c % slots;
+      if (!tc::mbar_wait(&empty[slot], ((c / slots) & 1) ^ 1, status, kWaitNs)) break;
+      const int y = (c * box_rows + 64 * static_cast<int>(rank)) % span;
+      if (mode == 1) {
+        if (rank == 0) tc::mbar_arrive_expect_tx(&full[slot], 2 * bb);
+        tc::tma_load_3d_2sm(smem_u32(sm + slot * bb), &tm,
+                            tc::mapa_shared(smem_u32(&full[slot]), 0), 0, y, 0);
+      } else {
+        tc::mbar_arrive_expect_tx(&full[slot], bb);
+        tc::tma_load_3d(smem_u32(sm + slot * bb), &tm, &full[slot], 0, y, 0);
+      }
+    }
+    // copies in flight land before the CTA exits
+    for (int c = n > slots ? n - slots : 0; c < n && (mode != 1 || rank == 0); ++c)
+      tc::mbar_wait(&full[c % slots], (c / slots) & 1, status, kWaitNs);
+  } else if (tid == 32) {
+    for (int c = 0; c < n; ++c) {
+      const int slot = c % slots;
+      const uint32_t ph = (c / slots) & 1;
+      if (mode == 0) {
+        if (!tc::mbar_wait(&full[slot], ph, status, kWaitNs)) break;
+        tc::mbar_arrive(&empty[slot]);
+      } else if (rank == 1) {
+        if (mode == 2) {
+          if (!tc::mbar_wait(&full[slot], ph, status, kWaitNs)) break;
+          tc::mbar_arrive_cluster(tc::mapa_shared(smem_u32(&peer[slot]), 0));
+        }
+      } else {
+        if (!tc::mbar_wait(&full[slot], ph, status, kWaitNs)) break;
+        if (mode == 2 && !tc::mbar_wait(&peer[slot], ph, status, kWaitNs)) break;
+        tc::mbar_arrive(&empty[slot]);
+        tc::mbar_arrive_cluster(tc::mapa_shared(smem_u32(&empty[slot]), 1));
+      }
+    }
+  }
+  __syncthreads();
+  tc::cluster_sync();
+}
+
+// Remote-arrive ping-pong between the two CTAs of a cluster: `n` round trips
+// of one arrive each way (release or relaxed at cluster scope); rank 0 of
+// cluster 0 reports the elapsed nanoseconds.
+__global__ void __cluster_dims__(2, 1, 1)
+    remote_arrive_probe_kernel(int n, int relaxed, int32_t* status, unsigned long long* ns) {
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t rank = tc::cluster_ctarank();
+  if (threadIdx.x == 0) {
+    tc::mbar_init(&bar, 1);
+    tc::fence_barrier_init();
+  }
+  __syncthreads();
+  tc::cluster_sync();
+  const uint32_t other = tc::mapa_shared(smem_u32(&bar), rank ^ 1);
+  auto arrive = [&]() {
+    if (relaxed)
+      asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(other)
+                   : "memory");
+    else
+      tc::mbar_arrive_cluster(other);
+  };
+  const uint64_t t0 = tc::global_ns();
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < n; ++i) {
+      if (rank == 0) {
+        arrive();
+        if (!tc::mbar_wait(&bar, i & 1, status, kWaitNs)) break;
+      } else {
+        if (!tc::mbar_wait(&bar, i & 1, status, kWaitNs)) break;
+        arrive();
+      }
+    }
+  }
+  __syncthreads();
+  tc::cluster_sync();
+  if (threadIdx.x == 0 && rank == 0 && blockIdx.x == 0) ns[0] = tc::global_ns() - t0;
+}
+
 }  // namespace
 }  // namespace rk
 
@@ -368,5 +479,41 @@ extern "C" int rk_tc_selftest(int mode, const void* A, const void* B, float* D, 
   }
   rk::tc_selftest_kernel<<<1, 128, 0, static_cast<cudaStream_t>(stream)>>>(
       mode, static_cast<const uint16_t*>(A), static_cast<const uint16_t*>(B), D, status, ta, tb);
+  return static_cast<int>(cudaGetLastError());
+}
+
+// Pair streaming probe (see above): ctas (even) CTAs in clusters of two.
+// lat: device bf16 [rows, 576].  Returns 0, -1 (bad arguments or tensor map)
+// or the launch error.
+extern "C" int rk_tma_pair_probe(const void* lat, int rows, int box_rows, int box_chunks,
+                                 int slots, int n, int mode, int ctas, int32_t* status,
+                                 void* stream) {
+  if (box_rows < 8 || box_rows > 256 || box_chunks < 1 || box_chunks > 9 || slots < 1 ||
+      slots > 8 || rows <= box_rows + 64 || n < 1 || mode < 0 || mode > 2 || ctas < 2 ||
+      (ctas & 1))
+    return -1;
+  const int64_t bb = static_cast<int64_t>(128) * box_rows * box_chunks;
+  if (slots * bb > 200 * 1024) return -1;
+  CUtensorMap tm{};
+  const uint64_t dims[3] = {64, static_cast<uint64_t>(rows), 9};
+  const uint64_t strides[2] = {1152, 128};
+  const uint32_t box[3] = {64, static_cast<uint32_t>(box_rows), static_cast<uint32_t>(box_chunks)};
+  if (!rk::make_tmap_bf16(&tm, lat, 3, dims, strides, box)) return -1;
+  const size_t smem = static_cast<size_t>(slots * bb) + 3 * 8 * 8 + 1024;
+  cudaError_t e = cudaFuncSetAttribute(rk::tma_pair_probe_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return static_cast<int>(e);
+  rk::tma_pair_probe_kernel<<<ctas, 64, smem, static_cast<cudaStream_t>(stream)>>>(
+      tm, rows, box_rows, box_chunks, slots, n, mode, status);
+  return static_cast<int>(cudaGetLastError());
+}
+
+// Remote-arrive ping-pong (see above) on `ctas` (even) CTAs.
+extern "C" int rk_remote_arrive_probe(int n, int relaxed, int ctas, int32_t* status,
+                                      unsigned long long* ns, void* stream) {
+  if (n < 1 || ctas < 2 || (ctas & 1)) return -1;
+  rk::remote_arrive_probe_kernel<<<ctas, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      n, relaxed, status, ns);
   return static_cast<int>(cudaGetLastError());
 }

@@ -77,3 +77,57 @@ def test_tcgen05_cta_pair(selftest_lib, mode):
     assert float(err.max()) <= 1e-3 * max(1.0, float(ref.abs().max())), (
         f"mode {mode}: max err {float(err.max())}; row 0 {got[0, :4].tolist()} vs "
         f"{ref[0, :4].tolist()}; row 128 {got[128, :4].tolist()} vs {ref[128, :4].tolist()}")
+
+
+def test_data_movement_probes(selftest_lib):
+    """Hardware probes behind the prefill kernels' data movement (run with -s
+    to see the tables): TMA streaming throughput over all SMs by box shape for
+    per-CTA loads, CTA-pair loads completing on the leader's barrier, and
+    per-CTA loads whose arrival is forwarded to the leader; then the round trip
+    of remote mbarrier arrives between the CTAs of a pair.  Asserts only that
+    every probe runs to completion without an expired wait."""
+    L = selftest_lib
+    L.rk_tma_stream_probe.argtypes = [ctypes.c_void_p] + [ctypes.c_int] * 6 + [ctypes.c_void_p] * 2
+    L.rk_tma_stream_probe.restype = ctypes.c_int
+    L.rk_tma_pair_probe.argtypes = [ctypes.c_void_p] + [ctypes.c_int] * 7 + [ctypes.c_void_p] * 2
+    L.rk_tma_pair_probe.restype = ctypes.c_int
+    L.rk_remote_arrive_probe.argtypes = [ctypes.c_int] * 3 + [ctypes.c_void_p] * 3
+    L.rk_remote_arrive_probe.restype = ctypes.c_int
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    ctas = sms - (sms & 1)
+    rows = 131072
+    g = torch.Generator(device="cuda").manual_seed(7)
+    lat = torch.randn(rows, 576, device="cuda", generator=g).to(torch.bfloat16)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    clk = 2.07e9  # the part's maximum SM clock, for B/clk/SM
+    print(f"\nTMA streaming, {ctas} CTAs, [{rows}, 576] bf16, box 64 dims x rows x chunks")
+    print("box           bytes  slots  per-CTA  pair  forwarded   (B/clk/SM)")
+    for br, bc, slots in [(64, 3, 5), (128, 2, 4), (64, 4, 3), (64, 9, 2), (128, 4, 3)]:
+        bb = 128 * br * bc
+        n = max(16, int(24e6 // bb))
+        res = []
+        for mode in (0, 1, 2):
+            best = None
+            for _ in range(2):
+                e0, e1 = torch.cuda.Event(True), torch.cuda.Event(True)
+                e0.record()
+                rc = L.rk_tma_pair_probe(lat.data_ptr(), rows, br, bc, slots, n, mode, ctas,
+                                         status.data_ptr(), stream)
+                e1.record()
+                torch.cuda.synchronize()
+                assert rc == 0
+                ms = e0.elapsed_time(e1)
+                best = ms if best is None else min(best, ms)
+            assert int(status.item()) == 0, "a bounded wait expired"
+            res.append(ctas * n * bb / (best * 1e-3) / ctas / clk)
+        print(f"{br:3d} x {bc}     {bb // 1024:3d} KB  {slots:4d}  {res[0]:7.1f} {res[1]:5.1f} {res[2]:8.1f}")
+    ns = torch.zeros(1, dtype=torch.int64, device="cuda")
+    for relaxed in (0, 1):
+        n = 20000
+        assert L.rk_remote_arrive_probe(n, relaxed, ctas, status.data_ptr(), ns.data_ptr(),
+                                        stream) == 0
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0, "a bounded wait expired"
+        print(f"remote mbarrier arrive round trip ({'relaxed' if relaxed else 'release'}): "
+              f"{int(ns.item()) / n:.1f} ns")
