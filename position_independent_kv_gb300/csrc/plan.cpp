@@ -433,6 +433,10 @@ static rk_status_t build_plan(const rk_seg_attn_desc_t* d, rk_seg_attn_plan_s* p
   if (static_cast<int64_t>(p->local_rows.size()) * std::max(HL, 1) > INT32_MAX)
     return RK_ERR_CAPACITY;
   if (tiles.size() > INT32_MAX / 2 || p->chunks.size() > INT32_MAX / 2) return RK_ERR_CAPACITY;
+  // longest chunks first (each chunk carries its own partial slot)
+  std::stable_sort(p->chunks.begin(), p->chunks.end(), [](const SplitChunk& a, const SplitChunk& b) {
+    return a.k1 - a.k0 > b.k1 - b.k0;
+  });
   // longest first
   std::stable_sort(tiles.begin(), tiles.end(),
                    [](const auto& a, const auto& b) { return a.first > b.first; });

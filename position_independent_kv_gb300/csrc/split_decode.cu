@@ -300,34 +300,47 @@ __global__ void __launch_bounds__(THREADS, 1) split_decode_kernel(const KernelAr
 // ---------------------------------------------------------------------------
 // d = (512, 64) version fed by TMA: each stage is one 3-D box of 32 keys x 9
 // chunks of 64 dims (36 KB of whole 1152-byte latent rows, laid out
-// chunk-major with the 128-byte swizzle), four stages deep; fragment
+// chunk-major with the 128-byte swizzle), two stages deep with two CTAs per
+// SM (the two CTAs' compute overlaps each other's copy latency); fragment
 // addresses apply the same XOR swizzle, so the ldmatrix reads are
 // conflict-free.  The scores of the 32 keys are split over the four warps
 // (two key halves x two halves of d_k); all four warps take 128 output rows
 // each of P.V.
 constexpr int DT_TK = 32;
-constexpr int DT_ST = 4;
+constexpr int DT_ST = 2;                       // stages per CTA
+constexpr int DT_CTAS = 2;                     // CTAs per SM
 constexpr uint32_t DT_CH = DT_TK * 128;        // one 64-dim chunk of a stage
 constexpr uint32_t DT_STAGE = 9 * DT_CH;       // 36,864 B
 constexpr uint64_t DT_WAIT_NS = 2000000000ull;
 constexpr int DT_QS = 512 + 128 + 8;
 constexpr int DT_PS = DT_TK + 8;
-constexpr size_t DT_SMEM = 1024 + DT_ST * DT_STAGE + NH * DT_QS * 2 + NH * 64 * 2 + NH * DT_PS * 2 +
-                           (2 + 4) * NH * 4 + 16 + DT_ST * 8 + 2 * 32 * 4 * 4;
+// shared-memory layout (byte offsets from the 1024-aligned base)
+constexpr size_t DT_OFF_Q = size_t(DT_ST) * DT_STAGE;
+constexpr size_t DT_OFF_QRO = DT_OFF_Q + size_t(NH) * DT_QS * 2;
+constexpr size_t DT_OFF_P = DT_OFF_QRO + size_t(NH) * 64 * 2;
+constexpr size_t DT_OFF_RED = DT_OFF_P + size_t(NH) * DT_PS * 2;       // red_m [2][NH], red_l [4][NH]
+constexpr size_t DT_OFF_FLAG = DT_OFF_RED + size_t(6) * NH * 4;
+constexpr size_t DT_OFF_BAR = (DT_OFF_FLAG + 16 + 7) & ~size_t(7);
+constexpr size_t DT_OFF_PART = (DT_OFF_BAR + size_t(DT_ST) * 8 + 15) & ~size_t(15);  // float4
+constexpr size_t DT_SMEM = 1024 + DT_OFF_PART + 2 * 32 * 4 * 4;
+static_assert(DT_OFF_Q % 16 == 0 && DT_OFF_QRO % 16 == 0 && DT_OFF_P % 16 == 0,
+              "cp.async / ldmatrix targets are 16-byte aligned");
+static_assert(DT_OFF_PART % 16 == 0 && DT_OFF_BAR % 8 == 0, "float4 and mbarrier alignment");
+static_assert(DT_CTAS * (DT_SMEM + 1024) <= 228 * 1024, "two CTAs per SM");
 
-__global__ void __launch_bounds__(THREADS, 1) split_decode_tma_kernel(const KernelArgs a) {
+__global__ void __launch_bounds__(THREADS, DT_CTAS) split_decode_tma_kernel(const KernelArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
   uint8_t* Kst = sm;
-  uint16_t* Qs = reinterpret_cast<uint16_t*>(sm + DT_ST * DT_STAGE);
-  uint16_t* Qro = Qs + NH * DT_QS;
-  uint16_t* Ps = Qro + NH * 64;
-  float* red_m = reinterpret_cast<float*>(Ps + NH * DT_PS);
+  uint16_t* Qs = reinterpret_cast<uint16_t*>(sm + DT_OFF_Q);
+  uint16_t* Qro = reinterpret_cast<uint16_t*>(sm + DT_OFF_QRO);
+  uint16_t* Ps = reinterpret_cast<uint16_t*>(sm + DT_OFF_P);
+  float* red_m = reinterpret_cast<float*>(sm + DT_OFF_RED);
   float* red_l = red_m + 2 * NH;
-  int* flag = reinterpret_cast<int*>(red_l + 4 * NH);
-  uint64_t* full = reinterpret_cast<uint64_t*>(flag + 4);
-  float* part = reinterpret_cast<float*>(full + DT_ST);  // [2 key halves][32 lanes][4]
+  int* flag = reinterpret_cast<int*>(sm + DT_OFF_FLAG);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + DT_OFF_BAR);
+  float* part = reinterpret_cast<float*>(sm + DT_OFF_PART);  // [2 key halves][32 lanes][4]
 
   const SplitChunk ch = a.chunks[blockIdx.x];
   const DevReq rq = a.reqs[ch.req];
