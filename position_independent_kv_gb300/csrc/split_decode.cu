@@ -300,15 +300,15 @@ __global__ void __launch_bounds__(THREADS, 1) split_decode_kernel(const KernelAr
 // ---------------------------------------------------------------------------
 // d = (512, 64) version fed by TMA: each stage is one 3-D box of 32 keys x 9
 // chunks of 64 dims (36 KB of whole 1152-byte latent rows, laid out
-// chunk-major with the 128-byte swizzle), two stages deep with two CTAs per
-// SM (the two CTAs' compute overlaps each other's copy latency); fragment
-// addresses apply the same XOR swizzle, so the ldmatrix reads are
-// conflict-free.  The scores of the 32 keys are split over the four warps
-// (two key halves x two halves of d_k); all four warps take 128 output rows
-// each of P.V.
+// chunk-major with the 128-byte swizzle), five stages deep, so that four
+// stages (144 KB) stay in flight while one is computed; fragment addresses
+// apply the same XOR swizzle, so the ldmatrix reads are conflict-free.  Eight
+// warps: the scores of the 32 keys are split over two key halves x four
+// quarters of d_k (each warp holds only its quarter of Q^T in registers),
+// and each warp takes 64 output rows of P.V.
 constexpr int DT_TK = 32;
-constexpr int DT_ST = 2;                       // stages per CTA
-constexpr int DT_CTAS = 2;                     // CTAs per SM
+constexpr int DT_ST = 5;                       // stages per CTA
+constexpr int DT_THREADS = 256;
 constexpr uint32_t DT_CH = DT_TK * 128;        // one 64-dim chunk of a stage
 constexpr uint32_t DT_STAGE = 9 * DT_CH;       // 36,864 B
 constexpr uint64_t DT_WAIT_NS = 2000000000ull;
@@ -318,17 +318,18 @@ constexpr int DT_PS = DT_TK + 8;
 constexpr size_t DT_OFF_Q = size_t(DT_ST) * DT_STAGE;
 constexpr size_t DT_OFF_QRO = DT_OFF_Q + size_t(NH) * DT_QS * 2;
 constexpr size_t DT_OFF_P = DT_OFF_QRO + size_t(NH) * 64 * 2;
-constexpr size_t DT_OFF_RED = DT_OFF_P + size_t(NH) * DT_PS * 2;       // red_m [2][NH], red_l [4][NH]
-constexpr size_t DT_OFF_FLAG = DT_OFF_RED + size_t(6) * NH * 4;
+constexpr size_t DT_OFF_RED = DT_OFF_P + size_t(NH) * DT_PS * 2;       // red_m [2][NH], red_l [2][NH]
+constexpr size_t DT_OFF_FLAG = DT_OFF_RED + size_t(4) * NH * 4;
 constexpr size_t DT_OFF_BAR = (DT_OFF_FLAG + 16 + 7) & ~size_t(7);
-constexpr size_t DT_OFF_PART = (DT_OFF_BAR + size_t(DT_ST) * 8 + 15) & ~size_t(15);  // float4
-constexpr size_t DT_SMEM = 1024 + DT_OFF_PART + 2 * 32 * 4 * 4;
+constexpr size_t DT_OFF_PART = (DT_OFF_BAR + size_t(DT_ST) * 8 + 15) & ~size_t(15);
+constexpr size_t DT_PART_BYTES = size_t(2) * 3 * 32 * 16;  // [key half][d_k quarter 1..3][lane] float4
+constexpr size_t DT_SMEM = 1024 + DT_OFF_PART + DT_PART_BYTES;
 static_assert(DT_OFF_Q % 16 == 0 && DT_OFF_QRO % 16 == 0 && DT_OFF_P % 16 == 0,
               "cp.async / ldmatrix targets are 16-byte aligned");
 static_assert(DT_OFF_PART % 16 == 0 && DT_OFF_BAR % 8 == 0, "float4 and mbarrier alignment");
-static_assert(DT_CTAS * (DT_SMEM + 1024) <= 228 * 1024, "two CTAs per SM");
+static_assert(DT_SMEM <= 227 * 1024, "shared memory");
 
-__global__ void __launch_bounds__(THREADS, DT_CTAS) split_decode_tma_kernel(const KernelArgs a) {
+__global__ void __launch_bounds__(DT_THREADS, 1) split_decode_tma_kernel(const KernelArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
@@ -340,13 +341,14 @@ __global__ void __launch_bounds__(THREADS, DT_CTAS) split_decode_tma_kernel(cons
   float* red_l = red_m + 2 * NH;
   int* flag = reinterpret_cast<int*>(sm + DT_OFF_FLAG);
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + DT_OFF_BAR);
-  float* part = reinterpret_cast<float*>(sm + DT_OFF_PART);  // [2 key halves][32 lanes][4]
+  float* part = reinterpret_cast<float*>(sm + DT_OFF_PART);
 
   const SplitChunk ch = a.chunks[blockIdx.x];
   const DevReq rq = a.reqs[ch.req];
   const DevSeg sg = a.segs[ch.seg];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t4 = lane & 3;
+  const int kq = warp >> 2, dq = warp & 3;  // key half, quarter of d_k
   const int hbase = ch.group * NH;
   const int nh = min(NH, a.num_global - hbase);
   const int64_t frow = rq.row_base;
@@ -369,7 +371,7 @@ __global__ void __launch_bounds__(THREADS, DT_CTAS) split_decode_tma_kernel(cons
   // ---- query rows of the 8 heads ----
   {
     constexpr int CH_N = 512 / 8, CH = CH_N + 8;
-    for (int idx = tid; idx < NH * CH; idx += THREADS) {
+    for (int idx = tid; idx < NH * CH; idx += DT_THREADS) {
       const int h = idx / CH, c = idx - h * CH;
       const uint16_t* src = a.q;
       int bytes = 0;
@@ -387,7 +389,7 @@ __global__ void __launch_bounds__(THREADS, DT_CTAS) split_decode_tma_kernel(cons
   __syncthreads();
   {
     const float* cs = a.rope_cs + int64_t(ch.seg) * 64;
-    for (int idx = tid; idx < NH * 32; idx += THREADS) {
+    for (int idx = tid; idx < NH * 32; idx += DT_THREADS) {
       const int h = idx >> 5, j = idx & 31;
       const float c = cs[2 * j], s = cs[2 * j + 1];
       const uint32_t xy = *reinterpret_cast<const uint32_t*>(Qro + h * 64 + 2 * j);
@@ -400,23 +402,25 @@ __global__ void __launch_bounds__(THREADS, DT_CTAS) split_decode_tma_kernel(cons
     }
   }
   __syncthreads();
-  uint32_t qb[40][2];
+  // this warp's 10 k-steps of Q^T (k-steps 10 dq .. 10 dq + 9 of the 40:
+  // nope 0..31, rope hi 32..35, rope lo 36..39) as mma B fragments
+  uint32_t qb[10][2];
   {
     const uint32_t base = smem_u32(Qs + (lane & 7) * DT_QS + 8 * (lane >> 3));
 #pragma unroll
-    for (int kk = 0; kk < 20; ++kk) {
+    for (int i = 0; i < 5; ++i) {
       uint32_t r[4];
-      ldsm_x4(r, base + kk * 64);
-      qb[2 * kk][0] = r[0];
-      qb[2 * kk][1] = r[1];
-      qb[2 * kk + 1][0] = r[2];
-      qb[2 * kk + 1][1] = r[3];
+      ldsm_x4(r, base + (5 * dq + i) * 64);
+      qb[2 * i][0] = r[0];
+      qb[2 * i][1] = r[1];
+      qb[2 * i + 1][0] = r[2];
+      qb[2 * i + 1][1] = r[3];
     }
   }
 
-  float o[8][4];
+  float o[4][4];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  for (int i = 0; i < 4; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
   float mrun[2] = {-INFINITY, -INFINITY};
   float lrun[2] = {0.f, 0.f};
   const float sl2 = a.scale_log2;
@@ -429,13 +433,11 @@ __global__ void __launch_bounds__(THREADS, DT_CTAS) split_decode_tma_kernel(cons
     if (!ok) break;
     const uint32_t st = smem_u32(Kst + s * DT_STAGE);
     const int k0 = ch.k0 + i * DT_TK;
-    // scores: warp w takes keys 16 * (w >> 1).. over half of the 40 k-steps
-    // (w even: nope 0..19; w odd: nope 20..31 + rope hi and lo), on two
-    // interleaved accumulators; the halves are added through shared memory
+    // scores: warp (kq, dq) takes keys 16 kq.. over k-steps 10 dq.. on two
+    // interleaved accumulators; the quarters are added through shared memory
     float sc[4] = {0.f, 0.f, 0.f, 0.f};
     {
       float sd[4] = {0.f, 0.f, 0.f, 0.f};
-      const int kq = warp >> 1, dh = warp & 1;
       const int r = kq * 16 + (lane & 15);
       const uint32_t rb = st + r * 128;
       const uint32_t rs = r & 7, hl = lane >> 4;
@@ -444,45 +446,48 @@ __global__ void __launch_bounds__(THREADS, DT_CTAS) split_decode_tma_kernel(cons
         const uint32_t unit = ((static_cast<uint32_t>(kk) & 3u) << 1) | hl;
         return rb + static_cast<uint32_t>(kk >> 2) * DT_CH + ((unit ^ rs) << 4);
       };
-      if (dh == 0) {
+      if (dq < 3) {
 #pragma unroll
-        for (int kk = 0; kk < 20; kk += 2) {
+        for (int j = 0; j < 10; j += 2) {
           uint32_t a0[4], a1[4];
-          ldsm_x4(a0, kaddr(kk));
-          ldsm_x4(a1, kaddr(kk + 1));
-          mma16816(sc, a0, qb[kk][0], qb[kk][1]);
-          mma16816(sd, a1, qb[kk + 1][0], qb[kk + 1][1]);
+          ldsm_x4(a0, kaddr(10 * dq + j));
+          ldsm_x4(a1, kaddr(10 * dq + j + 1));
+          mma16816(sc, a0, qb[j][0], qb[j][1]);
+          mma16816(sd, a1, qb[j + 1][0], qb[j + 1][1]);
         }
       } else {
-#pragma unroll
-        for (int kk = 20; kk < 32; kk += 2) {
+        {
           uint32_t a0[4], a1[4];
-          ldsm_x4(a0, kaddr(kk));
-          ldsm_x4(a1, kaddr(kk + 1));
-          mma16816(sc, a0, qb[kk][0], qb[kk][1]);
-          mma16816(sd, a1, qb[kk + 1][0], qb[kk + 1][1]);
+          ldsm_x4(a0, kaddr(30));
+          ldsm_x4(a1, kaddr(31));
+          mma16816(sc, a0, qb[0][0], qb[0][1]);
+          mma16816(sd, a1, qb[1][0], qb[1][1]);
         }
+        // the rope chunk meets q_rope' hi (k-steps 32..35) and lo (36..39)
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           uint32_t af[4];
           ldsm_x4(af, kaddr(32 + kk));
-          mma16816(sc, af, qb[32 + kk][0], qb[32 + kk][1]);
-          mma16816(sd, af, qb[36 + kk][0], qb[36 + kk][1]);
+          mma16816(sc, af, qb[2 + kk][0], qb[2 + kk][1]);
+          mma16816(sd, af, qb[6 + kk][0], qb[6 + kk][1]);
         }
       }
 #pragma unroll
       for (int e = 0; e < 4; ++e) sc[e] += sd[e];
-      if (dh == 1) *reinterpret_cast<float4*>(part + (kq * 32 + lane) * 4) =
-          make_float4(sc[0], sc[1], sc[2], sc[3]);
+      if (dq > 0)
+        *reinterpret_cast<float4*>(part + ((kq * 3 + dq - 1) * 32 + lane) * 4) =
+            make_float4(sc[0], sc[1], sc[2], sc[3]);
     }
     __syncthreads();
-    if ((warp & 1) == 0) {
-      const int kq = warp >> 1;
-      const float4 pt = *reinterpret_cast<const float4*>(part + (kq * 32 + lane) * 4);
-      sc[0] += pt.x;
-      sc[1] += pt.y;
-      sc[2] += pt.z;
-      sc[3] += pt.w;
+    if (dq == 0) {
+#pragma unroll
+      for (int q = 0; q < 3; ++q) {
+        const float4 pt = *reinterpret_cast<const float4*>(part + ((kq * 3 + q) * 32 + lane) * 4);
+        sc[0] += pt.x;
+        sc[1] += pt.y;
+        sc[2] += pt.z;
+        sc[3] += pt.w;
+      }
       const int key0 = k0 + kq * 16 + g;
       const bool v0 = key0 < ch.k1, v1 = key0 + 8 < ch.k1;
       sc[0] = v0 ? sc[0] * sl2 : -INFINITY;
@@ -515,10 +520,10 @@ __global__ void __launch_bounds__(THREADS, DT_CTAS) split_decode_tma_kernel(cons
       }
       mrun[e] = mn;
     }
-    if ((warp & 1) == 0) {
+    if (dq == 0) {
       const float p0 = fast_exp2(sc[0] - base[0]), p1 = fast_exp2(sc[1] - base[1]);
       const float p2 = fast_exp2(sc[2] - base[0]), p3 = fast_exp2(sc[3] - base[1]);
-      const int kl = (warp >> 1) * 16 + g;
+      const int kl = kq * 16 + g;
       Ps[(2 * t4) * DT_PS + kl] = f32_to_bf16(p0);
       Ps[(2 * t4 + 1) * DT_PS + kl] = f32_to_bf16(p1);
       Ps[(2 * t4) * DT_PS + kl + 8] = f32_to_bf16(p2);
@@ -533,14 +538,14 @@ __global__ void __launch_bounds__(THREADS, DT_CTAS) split_decode_tma_kernel(cons
       lrun[1] = lrun[1] * alpha[1] + ls1;
     }
 #pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
+    for (int mt = 0; mt < 4; ++mt) {
       o[mt][0] *= alpha[0];
       o[mt][1] *= alpha[1];
       o[mt][2] *= alpha[0];
       o[mt][3] *= alpha[1];
     }
     __syncthreads();
-    // O^T[dims, heads] += V^T[dims, keys] P^T[keys, heads]; warp w: dims 128w..
+    // O^T[dims, heads] += V^T[dims, keys] P^T[keys, heads]; warp w: dims 64w..
     uint32_t pb[2][2];
     {
       uint32_t r[4];
@@ -553,8 +558,8 @@ __global__ void __launch_bounds__(THREADS, DT_CTAS) split_decode_tma_kernel(cons
       const uint32_t kb = st + key * 128;
       const uint32_t ks7 = key & 7;
 #pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        const int dim = 128 * warp + 16 * mt + 8 * ((lane >> 3) & 1);
+      for (int mt = 0; mt < 4; ++mt) {
+        const int dim = 64 * warp + 16 * mt + 8 * ((lane >> 3) & 1);
         uint32_t af[4];
         ldsm_x4_t(af, kb + (dim >> 6) * DT_CH + ((((dim & 63) >> 3) ^ ks7) << 4));
         mma16816(o[mt], af, pb[ks][0], pb[ks][1]);
@@ -575,9 +580,9 @@ __global__ void __launch_bounds__(THREADS, DT_CTAS) split_decode_tma_kernel(cons
   }
 
   // ---- chunk partial ----
-  if ((warp & 1) == 0 && g == 0) {
-    red_l[(warp >> 1) * NH + 2 * t4] = lrun[0];
-    red_l[(warp >> 1) * NH + 2 * t4 + 1] = lrun[1];
+  if (dq == 0 && g == 0) {
+    red_l[kq * NH + 2 * t4] = lrun[0];
+    red_l[kq * NH + 2 * t4 + 1] = lrun[1];
   }
   __syncthreads();
   float lt[2];
@@ -585,8 +590,8 @@ __global__ void __launch_bounds__(THREADS, DT_CTAS) split_decode_tma_kernel(cons
   for (int e = 0; e < 2; ++e) lt[e] = red_l[2 * t4 + e] + red_l[NH + 2 * t4 + e];
   float* wo = a.ws_o + int64_t(ch.part) * NH * 512;
 #pragma unroll
-  for (int mt = 0; mt < 8; ++mt) {
-    const int d0 = 128 * warp + mt * 16 + g;
+  for (int mt = 0; mt < 4; ++mt) {
+    const int d0 = 64 * warp + mt * 16 + g;
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       const int h = 2 * t4 + e;
@@ -614,7 +619,7 @@ __global__ void __launch_bounds__(THREADS, DT_CTAS) split_decode_tma_kernel(cons
       ssum += __expf(__ldcg(a.ws_lse + int64_t(ch.part_first + j) * NH + h) - m);
     const int head = a.global_heads[hbase + h];
     uint16_t* dst = a.out + (frow * a.H + head) * 512;
-    for (int d = tid; d < 512; d += THREADS) {
+    for (int d = tid; d < 512; d += DT_THREADS) {
       float acc = 0.f;
       for (int j = 0; j < ch.nparts; ++j) {
         const int64_t pj = ch.part_first + j;
@@ -681,7 +686,7 @@ cudaError_t launch_split_decode(const rk_seg_attn_plan_s& plan, const KernelArgs
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(DT_SMEM));
     if (e != cudaSuccess) return e;
-    split_decode_tma_kernel<<<a.num_chunks, THREADS, DT_SMEM, s>>>(a);
+    split_decode_tma_kernel<<<a.num_chunks, DT_THREADS, DT_SMEM, s>>>(a);
     return cudaGetLastError();
   }
   if (plan.d_nope == 512 && plan.d_rope == 64) return launch_t<512, 64>(a, s);
