@@ -196,6 +196,29 @@ rk_status_t rk_seg_attn_forward(rk_seg_attn_plan_t plan, const void* q, void* ou
                                 float* lse, void* workspace, size_t workspace_bytes,
                                 void* stream);
 
+/* The same forward with q, out and lse starting and ending in host memory:
+ * the copies to and from the device run inside the call, overlapped with
+ * the kernels.  The computed rows are taken in eight consecutive ranges;
+ * a range is copied in on a plan-owned stream, its tiles run on `stream` as
+ * soon as it (and every earlier range) is on the device, and it is copied
+ * back on a second plan-owned stream once the tiles that write it are done.
+ * (The pages have no counterpart; this is how a host-resident query batch
+ * meets the device-resident document latents.)
+ * q_host, out_host, lse_host  host arrays of the shapes of q, out, lse
+ *            below; out_host and lse_host are in/out exactly like out and
+ *            lse.  Page-locked memory lets the copies overlap; pageable
+ *            memory is accepted and is copied synchronously.
+ * q, out, lse device arrays of the full sizes (as for rk_seg_attn_forward);
+ *            the call overwrites them with the host contents first.
+ * workspace  as for rk_seg_attn_forward.
+ * Asynchronous on `stream`: work queued on `stream` before the call runs
+ * first, and `stream` continues only after out_host and lse_host hold the
+ * results.  Calls on one plan must not overlap (they share its copy streams
+ * and events).  Errors: as rk_seg_attn_forward. */
+rk_status_t rk_seg_attn_forward_host(rk_seg_attn_plan_t plan, const void* q_host, void* out_host,
+                                     float* lse_host, void* q, void* out, float* lse,
+                                     void* workspace, size_t workspace_bytes, void* stream);
+
 /* Stand-alone segment LSE merge (paper, RoPE-orthogonality paragraph).
  * o_parts    device fp32 [P, rows, H, d_v]   partial outputs (normalised)
  * lse_parts  device fp32 [P, rows, H]        partial LSEs; -inf = empty part

@@ -23,7 +23,7 @@ RK_PLAN_CTA_PAIR = 8
 EXPORTS = ["rk_seg_attn_plan", "rk_seg_attn_plan_destroy", "rk_seg_attn_plan_info",
            "rk_seg_attn_workspace_bytes", "rk_seg_attn_forward", "rk_lse_merge",
            "rk_seg_attn_last_device_status", "rk_status_string",
-           "rk_seg_attn_forward_noalloc"]
+           "rk_seg_attn_forward_noalloc", "rk_seg_attn_forward_host"]
 
 STATUS = {0: "RK_OK", 1: "RK_ERR_NULL", 2: "RK_ERR_INVALID_ARG", 3: "RK_ERR_SEGMENT_OVERLAP",
           4: "RK_ERR_SEGMENT_GAP", 5: "RK_ERR_UNSUPPORTED_DIMS", 6: "RK_ERR_CAPACITY",
@@ -89,6 +89,8 @@ def lib() -> C.CDLL:
         L.rk_seg_attn_forward.argtypes = [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
                                           C.c_void_p, C.c_size_t, C.c_void_p]
         L.rk_seg_attn_forward.restype = C.c_int
+        L.rk_seg_attn_forward_host.argtypes = [C.c_void_p] * 8 + [C.c_size_t, C.c_void_p]
+        L.rk_seg_attn_forward_host.restype = C.c_int
         L.rk_seg_attn_forward_noalloc.argtypes = [C.c_void_p, C.c_void_p, C.c_void_p,
                                                   C.c_void_p, C.c_void_p]
         L.rk_seg_attn_forward_noalloc.restype = C.c_int
@@ -195,6 +197,16 @@ class SegAttnPlan:
         st = lib().rk_seg_attn_forward(self._h, _ptr(q), _ptr(out), _ptr(lse), _ptr(workspace),
                                        ws_bytes, _stream(stream))
         _check(st, "rk_seg_attn_forward")
+
+    def forward_host(self, q_host, out_host, lse_host, q, out, lse, workspace=None, stream=None):
+        """rk_seg_attn_forward_host: q_host/out_host/lse_host are host tensors
+        (pinned for overlap); q/out/lse are device tensors of the same shapes
+        that the call fills from the host first."""
+        ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+        st = lib().rk_seg_attn_forward_host(self._h, _ptr(q_host), _ptr(out_host), _ptr(lse_host),
+                                            _ptr(q), _ptr(out), _ptr(lse), _ptr(workspace),
+                                            ws_bytes, _stream(stream))
+        _check(st, "rk_seg_attn_forward_host")
 
     def forward_noalloc(self, q, out, lse, stream=None):
         """rk_seg_attn_forward_noalloc: same results as forward, with the

@@ -60,6 +60,7 @@ void free_device(rk_seg_attn_plan_s* p) {
   cudaFree(p->d_chunks);
   cudaFree(p->d_tc_tiles);
   cudaFree(p->d_tc_pairs);
+  cudaFree(p->d_tc_pairs_chunked);
   cudaFree(p->d_segmaps);
   cudaFree(p->d_decmaps);
   cudaFree(p->d_head_role);
@@ -69,6 +70,18 @@ void free_device(rk_seg_attn_plan_s* p) {
   if (p->ev_join) cudaEventDestroy(p->ev_join);
   p->side = nullptr;
   p->ev_fork = p->ev_join = nullptr;
+  if (p->copy_in) cudaStreamDestroy(p->copy_in);
+  if (p->copy_out) cudaStreamDestroy(p->copy_out);
+  for (cudaEvent_t* e : {&p->ev_start, &p->ev_split, &p->ev_done})
+    if (*e) cudaEventDestroy(*e);
+  for (int c = 0; c < rk_seg_attn_plan_s::kHostChunks; ++c) {
+    if (p->ev_in[c]) cudaEventDestroy(p->ev_in[c]);
+    if (p->ev_k[c]) cudaEventDestroy(p->ev_k[c]);
+    p->ev_in[c] = p->ev_k[c] = nullptr;
+  }
+  p->copy_in = p->copy_out = nullptr;
+  p->ev_start = p->ev_split = p->ev_done = nullptr;
+  p->d_tc_pairs_chunked = nullptr;
   p->d_segs = nullptr;
   p->d_reqs = nullptr;
   p->d_rope_cs = nullptr;
@@ -503,6 +516,30 @@ static rk_status_t build_plan(const rk_seg_attn_desc_t* d, rk_seg_attn_plan_s* p
     std::stable_sort(pairs.begin(), pairs.end(),
                      [](const auto& a, const auto& b) { return a.first > b.first; });
     for (auto& pr : pairs) p->tc_pairs.push_back(pr.second);
+    // the same pairs grouped by the row range of their last computed row
+    // (a pair spans at most a few hundred rows, so with ranges of >= 1024
+    // rows it touches only its own range and the one before)
+    constexpr int NC = rk_seg_attn_plan_s::kHostChunks;
+    p->chunk_rows = std::max<int64_t>(1024, (((rows_total + NC - 1) / NC) + 255) / 256 * 256);
+    auto last_row = [&](const TcPair& pr) {
+      int64_t last = -1;
+      for (int k = 0; k < 2; ++k) {
+        const TcTile& t = pr.t[k];
+        if (t.pad & 1) continue;
+        const DevReq& rq = p->reqs[t.req];
+        const int64_t pl = t.kind == 0 ? int64_t(t.p0) + t.p1 - 1 : std::max<int64_t>(t.p0, t.p1);
+        last = std::max(last, rq.row_base + (pl - rq.q_row_begin));
+      }
+      return last;
+    };
+    std::vector<std::vector<TcPair>> byc(NC);
+    for (const TcPair& pr : p->tc_pairs)
+      byc[std::min<int64_t>(NC - 1, last_row(pr) / p->chunk_rows)].push_back(pr);
+    p->chunk_pair_begin[0] = 0;
+    for (int c = 0; c < NC; ++c) {
+      for (const TcPair& pr : byc[c]) p->tc_pairs_chunked.push_back(pr);
+      p->chunk_pair_begin[c + 1] = static_cast<int32_t>(p->tc_pairs_chunked.size());
+    }
     if (p->tc_pairs.size() > (INT32_MAX / 8)) return RK_ERR_CAPACITY;
   } else {
     std::stable_sort(tc_list.begin(), tc_list.end(),
@@ -553,6 +590,7 @@ extern "C" rk_status_t rk_seg_attn_plan(const rk_seg_attn_desc_t* desc, void* st
     if (st == RK_OK) st = upload(p->chunks, &p->d_chunks, s);
     if (st == RK_OK) st = upload(p->tc_tiles, &p->d_tc_tiles, s);
     if (st == RK_OK) st = upload(p->tc_pairs, &p->d_tc_pairs, s);
+    if (st == RK_OK) st = upload(p->tc_pairs_chunked, &p->d_tc_pairs_chunked, s);
     if (st == RK_OK) st = upload(p->head_role, &p->d_head_role, s);
     if (st == RK_OK && p->kernel >= 1) {
       // TMA maps of each segment latent, viewing a row as 9 chunks of 64
@@ -596,6 +634,16 @@ extern "C" rk_status_t rk_seg_attn_plan(const rk_seg_attn_desc_t* desc, void* st
           cudaEventCreateWithFlags(&p->ev_join, cudaEventDisableTiming) != cudaSuccess)
         st = RK_ERR_CUDA;
     }
+    if (st == RK_OK) {
+      bool okc = cudaStreamCreateWithFlags(&p->copy_in, cudaStreamNonBlocking) == cudaSuccess &&
+                 cudaStreamCreateWithFlags(&p->copy_out, cudaStreamNonBlocking) == cudaSuccess;
+      for (cudaEvent_t* e : {&p->ev_start, &p->ev_split, &p->ev_done})
+        okc = okc && cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess;
+      for (int c = 0; c < rk_seg_attn_plan_s::kHostChunks && okc; ++c)
+        okc = cudaEventCreateWithFlags(&p->ev_in[c], cudaEventDisableTiming) == cudaSuccess &&
+              cudaEventCreateWithFlags(&p->ev_k[c], cudaEventDisableTiming) == cudaSuccess;
+      if (!okc) st = RK_ERR_CUDA;
+    }
     // host vectors are pageable: make the uploads complete before returning
     if (st == RK_OK && cudaStreamSynchronize(s) != cudaSuccess) st = RK_ERR_CUDA;
     if (st != RK_OK) {
@@ -631,9 +679,27 @@ extern "C" size_t rk_seg_attn_workspace_bytes(rk_seg_attn_plan_t p) {
   return p ? p->workspace_bytes : 0;
 }
 
-extern "C" rk_status_t rk_seg_attn_forward(rk_seg_attn_plan_t p, const void* q, void* out,
-                                           float* lse, void* workspace, size_t ws_bytes,
-                                           void* stream) {
+namespace {
+
+// Point the split-decode arguments at the caller's workspace and clear the
+// merge tickets on stream s.
+rk_status_t bind_workspace(const rk_seg_attn_plan_s& p, rk::KernelArgs& a, void* workspace,
+                           cudaStream_t s) {
+  if (!p.num_parts) return RK_OK;
+  char* w = static_cast<char*>(workspace);
+  a.ws_o = reinterpret_cast<float*>(w);
+  size_t off = static_cast<size_t>(p.num_parts) * kSplitHeads * p.d_nope * sizeof(float);
+  a.ws_lse = reinterpret_cast<float*>(w + off);
+  off += static_cast<size_t>(p.num_parts) * kSplitHeads * sizeof(float);
+  off = (off + 255) & ~size_t(255);
+  a.ws_ticket = reinterpret_cast<int32_t*>(w + off);
+  return cudaMemsetAsync(a.ws_ticket, 0, p.num_mgroups * sizeof(int32_t), s) == cudaSuccess
+             ? RK_OK
+             : RK_ERR_CUDA;
+}
+
+rk_status_t check_forward_args(const rk_seg_attn_plan_s* p, const void* q, const void* out,
+                               const float* lse, const void* workspace, size_t ws_bytes) {
   if (!p || !q || !out || !lse) return RK_ERR_NULL;
   if (p->host_only) return RK_ERR_PLAN_MISMATCH;
   auto mis = [](const void* x) { return (reinterpret_cast<uintptr_t>(x) & 15) != 0; };
@@ -645,21 +711,115 @@ extern "C" rk_status_t rk_seg_attn_forward(rk_seg_attn_plan_t p, const void* q, 
   int cur = -1;
   if (cudaGetDevice(&cur) != cudaSuccess) return RK_ERR_CUDA;
   if (cur != p->device) return RK_ERR_PLAN_MISMATCH;
+  return RK_OK;
+}
+
+}  // namespace
+
+extern "C" rk_status_t rk_seg_attn_forward(rk_seg_attn_plan_t p, const void* q, void* out,
+                                           float* lse, void* workspace, size_t ws_bytes,
+                                           void* stream) {
+  rk_status_t st = check_forward_args(p, q, out, lse, workspace, ws_bytes);
+  if (st != RK_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   rk::KernelArgs a{};
   rk::fill_args(*p, a, q, out, lse);
-  if (p->num_parts) {
-    char* w = static_cast<char*>(workspace);
-    a.ws_o = reinterpret_cast<float*>(w);
-    size_t off = static_cast<size_t>(p->num_parts) * kSplitHeads * p->d_nope * sizeof(float);
-    a.ws_lse = reinterpret_cast<float*>(w + off);
-    off += static_cast<size_t>(p->num_parts) * kSplitHeads * sizeof(float);
-    off = (off + 255) & ~size_t(255);
-    a.ws_ticket = reinterpret_cast<int32_t*>(w + off);
-    if (cudaMemsetAsync(a.ws_ticket, 0, p->num_mgroups * sizeof(int32_t), s) != cudaSuccess)
-      return RK_ERR_CUDA;
-  }
+  st = bind_workspace(*p, a, workspace, s);
+  if (st != RK_OK) return st;
   return rk::launch_forward(*p, a, q, s) == cudaSuccess ? RK_OK : RK_ERR_CUDA;
+}
+
+extern "C" rk_status_t rk_seg_attn_forward_host(rk_seg_attn_plan_t p, const void* q_host,
+                                                void* out_host, float* lse_host, void* q,
+                                                void* out, float* lse, void* workspace,
+                                                size_t ws_bytes, void* stream) {
+  if (!q_host || !out_host || !lse_host) return RK_ERR_NULL;
+  rk_status_t st = check_forward_args(p, q, out, lse, workspace, ws_bytes);
+  if (st != RK_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  constexpr int NC = rk_seg_attn_plan_s::kHostChunks;
+  const int64_t rows = p->info.rows, H = p->H;
+  const size_t qrow = static_cast<size_t>(H) * (p->d_nope + p->d_rope) * 2;
+  const size_t orow = static_cast<size_t>(H) * p->d_nope * 2, lrow = static_cast<size_t>(H) * 4;
+  const int64_t CR = p->chunk_rows > 0 ? p->chunk_rows : rows;
+  auto range = [&](int c, int64_t& r0, int64_t& r1) {
+    r0 = std::min<int64_t>(rows, c * CR);
+    r1 = c == NC - 1 ? rows : std::min<int64_t>(rows, (c + 1) * CR);
+  };
+  auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+  const char* qh = static_cast<const char*>(q_host);
+  char* oh = static_cast<char*>(out_host);
+  char* lh = reinterpret_cast<char*>(lse_host);
+  char* qd = static_cast<char*>(q);
+  char* od = static_cast<char*>(out);
+  char* ld = reinterpret_cast<char*>(lse);
+  // the copies start after the caller's earlier work on s
+  bool good = ok(cudaEventRecord(p->ev_start, s)) &&
+              ok(cudaStreamWaitEvent(p->copy_in, p->ev_start, 0)) &&
+              ok(cudaStreamWaitEvent(p->copy_out, p->ev_start, 0));
+  for (int c = 0; c < NC && good; ++c) {
+    int64_t r0, r1;
+    range(c, r0, r1);
+    if (r1 > r0) {
+      const int64_t n = r1 - r0;
+      good = ok(cudaMemcpyAsync(qd + r0 * qrow, qh + r0 * qrow, n * qrow, cudaMemcpyHostToDevice,
+                                p->copy_in)) &&
+             ok(cudaMemcpyAsync(od + r0 * orow, oh + r0 * orow, n * orow, cudaMemcpyHostToDevice,
+                                p->copy_in)) &&
+             ok(cudaMemcpyAsync(ld + r0 * lrow, lh + r0 * lrow, n * lrow, cudaMemcpyHostToDevice,
+                                p->copy_in));
+    }
+    good = good && ok(cudaEventRecord(p->ev_in[c], p->copy_in));
+  }
+  rk::KernelArgs a{};
+  rk::fill_args(*p, a, q, out, lse);
+  if (good) good = bind_workspace(*p, a, workspace, s) == RK_OK;
+  const bool pipelined = !p->tc_pairs_chunked.empty() && a.num_tiles == 0 && a.num_tc_tiles == 0;
+  if (pipelined) {
+    // the tile pairs of row range c run once rows 0 .. c are on the device
+    for (int c = 0; c < NC && good; ++c) {
+      good = ok(cudaStreamWaitEvent(s, p->ev_in[c], 0));
+      const int32_t b = p->chunk_pair_begin[c], e = p->chunk_pair_begin[c + 1];
+      if (good && e > b) {
+        rk::KernelArgs ac = a;
+        ac.tc_pairs = p->d_tc_pairs_chunked + b;
+        ac.num_tc_pairs = e - b;
+        ac.num_chunks = 0;
+        good = ok(p->kernel == 3 ? rk::launch_dense_tc4(*p, ac, q, s)
+                                 : rk::launch_dense_tc2(*p, ac, q, s));
+      }
+      good = good && ok(cudaEventRecord(p->ev_k[c], s));
+    }
+    if (good && a.num_chunks) {
+      rk::KernelArgs ac = a;
+      ac.num_tc_pairs = 0;
+      good = ok(rk::launch_split_decode(*p, ac, s));
+    }
+  } else {
+    good = good && ok(cudaStreamWaitEvent(s, p->ev_in[NC - 1], 0)) &&
+           ok(rk::launch_forward(*p, a, q, s));
+    for (int c = 0; c < NC && good; ++c) good = ok(cudaEventRecord(p->ev_k[c], s));
+  }
+  good = good && ok(cudaEventRecord(p->ev_split, s));
+  // range c is final once the kernels of ranges c and c + 1 (and any split
+  // chunks) are done
+  for (int c = 0; c < NC && good; ++c) {
+    int64_t r0, r1;
+    range(c, r0, r1);
+    good = ok(cudaStreamWaitEvent(p->copy_out, p->ev_k[std::min(c + 1, NC - 1)], 0));
+    if (good && a.num_chunks) good = ok(cudaStreamWaitEvent(p->copy_out, p->ev_split, 0));
+    if (good && r1 > r0) {
+      const int64_t n = r1 - r0;
+      good = ok(cudaMemcpyAsync(oh + r0 * orow, od + r0 * orow, n * orow, cudaMemcpyDeviceToHost,
+                                p->copy_out)) &&
+             ok(cudaMemcpyAsync(lh + r0 * lrow, ld + r0 * lrow, n * lrow, cudaMemcpyDeviceToHost,
+                                p->copy_out));
+    }
+  }
+  // the caller's stream resumes when everything is back on the host
+  good = good && ok(cudaEventRecord(p->ev_done, p->copy_out)) &&
+         ok(cudaStreamWaitEvent(s, p->ev_done, 0));
+  return good ? RK_OK : RK_ERR_CUDA;
 }
 
 namespace rk {

@@ -176,6 +176,18 @@ struct rk_seg_attn_plan_s {
   // this plan-owned stream, forked from and joined back to the caller's
   cudaStream_t side = nullptr;
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+  // forward from host buffers: the computed rows in kHostChunks ranges of
+  // chunk_rows rows, the tile pairs grouped by the range of their last row
+  // (each group longest first), and the streams and events that overlap the
+  // copies of one range with the kernels of another
+  static constexpr int kHostChunks = 8;
+  int64_t chunk_rows = 0;
+  std::vector<rk::TcPair> tc_pairs_chunked;
+  int32_t chunk_pair_begin[kHostChunks + 1] = {};
+  rk::TcPair* d_tc_pairs_chunked = nullptr;
+  cudaStream_t copy_in = nullptr, copy_out = nullptr;
+  cudaEvent_t ev_start = nullptr, ev_split = nullptr, ev_done = nullptr;
+  cudaEvent_t ev_in[kHostChunks] = {}, ev_k[kHostChunks] = {};
 };
 
 namespace rk {

@@ -103,6 +103,12 @@ def test_host_only_plan_refuses_forward():
     with pytest.raises(B.RkError) as ei:
         plan.forward(0x1000, 0x2000, 0x3000, stream=0)
     assert ei.value.status == 9
+    with pytest.raises(B.RkError) as ei:
+        plan.forward_host(0x4000, 0x5000, 0x6000, 0x1000, 0x2000, 0x3000, stream=0)
+    assert ei.value.status == 9
+    with pytest.raises(B.RkError) as ei:  # a missing host array is reported first
+        plan.forward_host(0, 0x5000, 0x6000, 0x1000, 0x2000, 0x3000, stream=0)
+    assert ei.value.status == 1
 
 
 def test_lse_merge_argument_errors():
