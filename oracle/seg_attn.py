@@ -215,8 +215,10 @@ def attend_partial(qh: np.ndarray, K: np.ndarray, V: np.ndarray, scale: float):
 
 
 def build_protected(T: int, segs, boundary: int, p_random: float, budget: float,
-                    none: bool, u: np.ndarray, perm: np.ndarray) -> np.ndarray:
-    """segs: list of (n, delta, is_new).  Returns bool [T]."""
+                    none: bool, u: np.ndarray, perm: np.ndarray, dirty=None) -> np.ndarray:
+    """segs: list of (n, delta, is_new).  dirty: optional bool [T] of rows
+    whose cached values are stale (the paper's D); they are protected on top
+    of the rule and do not count toward the budget.  Returns bool [T]."""
     prot = [False] * T
     cached = [False] * T
     bnd = [False] * T
@@ -252,6 +254,10 @@ def build_protected(T: int, segs, boundary: int, p_random: float, budget: float,
             for p in range(T):
                 if bnd[p]:
                     prot[p] = True
+    if dirty is not None:
+        for p in range(T):
+            if dirty[p]:
+                prot[p] = True
     return np.array(prot, dtype=bool)
 
 

@@ -75,3 +75,19 @@ def test_decode_geometry():
         for d, n in spans:
             assert d == pos and n >= 1
             pos += n
+
+
+def test_dirty_rows_protected_outside_the_budget():
+    """The paper's D (dirty rows) joins the protected union; the budget fill
+    (boundary first, then the permutation) is the same with or without it."""
+    wl = make_geometry("varlen_mini", 0)
+    r = wl.rule
+    req = wl.requests[0]
+    segs = [(s.n, s.delta, s.is_new) for s in req.segments]
+    base = O.build_protected(req.T, segs, r.boundary, r.p_random, r.budget, r.none,
+                             req.u, req.perm)
+    rng = np.random.default_rng(3)
+    dirty = rng.random(req.T) < 0.05
+    got = O.build_protected(req.T, segs, r.boundary, r.p_random, r.budget, r.none,
+                            req.u, req.perm, dirty=dirty)
+    assert np.array_equal(got, base | dirty)
