@@ -360,6 +360,44 @@ def bench_decode(args, local):
     return dict(ms=ms, bytes=byt, gbs=byt / (ms * 1e-3) / 1e9, ok=ok, info=info)
 
 
+def bench_protected_builder(name: str, local: int) -> dict:
+    """rk_protected_build on a workload's geometry (device time per build,
+    CUDA events, median of 20 after 3 warm-ups)."""
+    import torch
+    from position_independent_kv_gb300 import binding as B
+    from position_independent_kv_gb300.workloads import make_geometry
+    dev = torch.device("cuda", local)
+    wl = make_geometry(name, 0)
+    segs, begins = [], [0]
+    for r in wl.requests:
+        segs += [(s.n, s.delta, s.is_new) for s in r.segments]
+        begins.append(len(segs))
+    rows = sum(r.T for r in wl.requests)
+    u = torch.from_numpy(np.concatenate([r.u for r in wl.requests]).astype(np.float64)).to(dev)
+    sc = torch.empty(rows, dtype=torch.float32, device=dev).uniform_()
+    bitmap = torch.empty(sum((r.T + 31) // 32 for r in wl.requests), dtype=torch.int32, device=dev)
+    ws = torch.empty(B.protected_workspace_bytes(len(wl.requests), len(segs)), dtype=torch.uint8,
+                     device=dev)
+    ru = wl.rule
+    args = (segs, begins, ru.boundary, ru.p_random, int(round(100 * ru.budget)), ru.none, u, sc,
+            None, bitmap, ws)
+    for _ in range(3):
+        B.protected_build(*args)
+    torch.cuda.synchronize(dev)
+    times = []
+    for _ in range(20):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        B.protected_build(*args)
+        b.record()
+        torch.cuda.synchronize(dev)
+        times.append(a.elapsed_time(b))
+    ms = statistics.median(times)
+    return {"workload": name, "rows": rows, "requests": len(wl.requests), "ms": round(ms, 4),
+            "rows_per_s": rows / (ms * 1e-3)}
+
+
 def cpu_baseline(wl, budget_s: float = 20.0):
     """The fp64 oracle on a bounded, stratified sample of the workload's rows
     (host cores; relocation of all keys included in the time)."""
@@ -427,6 +465,9 @@ def run_ours(args):
     dec = None
     if not args.no_decode:
         dec = bench_decode(args, local)
+    prot = None
+    if not args.no_builder and rank == 0:
+        prot = [bench_protected_builder(n, local) for n in ("ctx128k", "decode")]
     line = None
     if rank == 0:
         info = res["info"]
@@ -458,6 +499,8 @@ def run_ours(args):
         }
         if e2e:
             line["e2e"] = e2e
+        if prot:
+            line["protected_builder"] = prot
         if dec:
             line["decode"] = {"workload": "64 requests x 1 row, 4-32 segments, 8K-64K keys, "
                                           "H=64 (56/8), split over segments + fused LSE merge",
@@ -522,6 +565,8 @@ def main():
                          "legacy (mma.sync)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-builder", action="store_true",
+                    help="skip the timing of the on-device protected-row builder")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     args = ap.parse_args()

@@ -75,6 +75,9 @@ typedef enum {
                                    kernel instead of the tcgen05 kernel */
 #define RK_PLAN_SINGLE_CTA 4u   /* run each tcgen05 tile on its own two CTAs
                                    (one per half of d_v) */
+#define RK_PLAN_DEVICE_BITMAP 16u /* protected_bitmap is a device pointer
+                                   (e.g. written by rk_protected_build); the
+                                   plan copies it to the host */
 #define RK_PLAN_CTA_PAIR 8u     /* run pairs of tcgen05 tiles on CTA pairs,
                                    one pair per half of d_v, instead of
                                    4-CTA clusters (scores on one CTA pair,
@@ -259,6 +262,52 @@ rk_status_t rk_seg_attn_last_device_status(rk_seg_attn_plan_t plan, void* stream
 
 /* Static description of a status code (never NULL). */
 const char* rk_status_string(rk_status_t status);
+
+/* ---- protected-row set on the device ---------------------------------- */
+
+/* Rule flag: no boundary, Bernoulli or budget rows (only new and dirty rows). */
+#define RK_PROT_NONE 1u
+
+/* Device scratch (bytes) rk_protected_build needs for num_requests requests
+ * with num_segments segments in total (0 for invalid counts). */
+size_t rk_protected_workspace_bytes(int32_t num_requests, int32_t num_segments);
+
+/* Build the protected-row bitmap of every request on the device (paper,
+ * protected-set paragraph: the union of query rows, new rows, dirty rows,
+ * the first and last rows of every relocated segment and Indexer-selected
+ * rows, grown by a fixed controller to a 10 / 20 / 25 % budget).  Per
+ * request (segments in the layout of rk_seg_attn_desc_t; the latent
+ * pointers are ignored):
+ *   - rows of RK_SEG_NEW segments and rows whose `dirty` bit is set are
+ *     protected;
+ *   - unless RK_PROT_NONE: the first and last `boundary` rows of every
+ *     cached segment are protected, and then
+ *       p_random > 0:   every cached row with u[row] < p_random (compared in
+ *                       double precision);
+ *       budget_pct > 0: until ceil(budget_pct * C / 100) of the C cached rows
+ *                       are protected (boundary rows first, all of them kept
+ *                       if they alone exceed it), the non-boundary cached rows
+ *                       with the highest score, ties to the lower row (the
+ *                       score vector stands in for the Indexer; finite values;
+ *                       -0 ranks as +0).
+ * u, score   device arrays, the requests' rows concatenated (T_r entries per
+ *            request); u may be NULL unless p_random > 0, score unless
+ *            budget_pct > 0.
+ * dirty      device uint32 words in the bitmap layout below, or NULL.
+ * bitmap     device uint32 out: per request ceil(T_r / 32) words, requests
+ *            concatenated; bit p % 32 of word p / 32 set when row p is
+ *            protected (LSB first).  Usable as rk_seg_attn_desc_t's bitmap
+ *            with RK_PLAN_DEVICE_BITMAP.
+ * workspace  device scratch of rk_protected_workspace_bytes bytes, 16-byte
+ *            aligned; overwritten.
+ * Asynchronous on `stream`.  Errors: RK_ERR_NULL, RK_ERR_INVALID_ARG,
+ * RK_ERR_SEGMENT_OVERLAP, RK_ERR_SEGMENT_GAP, RK_ERR_CAPACITY,
+ * RK_ERR_WORKSPACE, RK_ERR_ALIGNMENT, RK_ERR_CUDA. */
+rk_status_t rk_protected_build(int32_t num_requests, const int32_t* seg_begin,
+                               const rk_segment_t* segs, int32_t boundary, double p_random,
+                               int32_t budget_pct, uint32_t rule_flags, const double* u,
+                               const float* score, const uint32_t* dirty, uint32_t* bitmap,
+                               void* workspace, size_t workspace_bytes, void* stream);
 
 #ifdef __cplusplus
 }

@@ -19,11 +19,14 @@ RK_PLAN_HOST_ONLY = 1
 RK_PLAN_LEGACY_MMA = 2
 RK_PLAN_SINGLE_CTA = 4
 RK_PLAN_CTA_PAIR = 8
+RK_PLAN_DEVICE_BITMAP = 16
+RK_PROT_NONE = 1
 
 EXPORTS = ["rk_seg_attn_plan", "rk_seg_attn_plan_destroy", "rk_seg_attn_plan_info",
            "rk_seg_attn_workspace_bytes", "rk_seg_attn_forward", "rk_lse_merge",
            "rk_seg_attn_last_device_status", "rk_status_string",
-           "rk_seg_attn_forward_noalloc", "rk_seg_attn_forward_host"]
+           "rk_seg_attn_forward_noalloc", "rk_seg_attn_forward_host",
+           "rk_protected_workspace_bytes", "rk_protected_build"]
 
 STATUS = {0: "RK_OK", 1: "RK_ERR_NULL", 2: "RK_ERR_INVALID_ARG", 3: "RK_ERR_SEGMENT_OVERLAP",
           4: "RK_ERR_SEGMENT_GAP", 5: "RK_ERR_UNSUPPORTED_DIMS", 6: "RK_ERR_CAPACITY",
@@ -89,6 +92,13 @@ def lib() -> C.CDLL:
         L.rk_seg_attn_forward.argtypes = [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
                                           C.c_void_p, C.c_size_t, C.c_void_p]
         L.rk_seg_attn_forward.restype = C.c_int
+        L.rk_protected_workspace_bytes.argtypes = [C.c_int32, C.c_int32]
+        L.rk_protected_workspace_bytes.restype = C.c_size_t
+        L.rk_protected_build.argtypes = [C.c_int32, C.POINTER(C.c_int32), C.POINTER(RkSegment),
+                                         C.c_int32, C.c_double, C.c_int32, C.c_uint32,
+                                         C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
+                                         C.c_void_p, C.c_size_t, C.c_void_p]
+        L.rk_protected_build.restype = C.c_int
         L.rk_seg_attn_forward_host.argtypes = [C.c_void_p] * 8 + [C.c_size_t, C.c_void_p]
         L.rk_seg_attn_forward_host.restype = C.c_int
         L.rk_seg_attn_forward_noalloc.argtypes = [C.c_void_p, C.c_void_p, C.c_void_p,
@@ -147,7 +157,9 @@ class SegAttnPlan:
         sb = np.ascontiguousarray(seg_begin, dtype=np.int32)
         qb = np.ascontiguousarray(q_row_begin, dtype=np.int64)
         role = np.ascontiguousarray(head_role, dtype=np.uint8)
-        bm = None if bitmap is None else np.ascontiguousarray(bitmap, dtype=np.uint32)
+        device_bitmap = bool(flags & RK_PLAN_DEVICE_BITMAP)
+        bm = (None if bitmap is None or device_bitmap
+              else np.ascontiguousarray(bitmap, dtype=np.uint32))
         desc = RkDesc()
         desc.num_requests = R
         desc.seg_begin = sb.ctypes.data_as(C.POINTER(C.c_int32))
@@ -161,8 +173,11 @@ class SegAttnPlan:
         desc.head_role = role.ctypes.data_as(C.POINTER(C.c_uint8))
         desc.sink = int(sink)
         desc.window = int(window)
-        desc.protected_bitmap = (bm.ctypes.data_as(C.POINTER(C.c_uint32)) if bm is not None
-                                 else C.POINTER(C.c_uint32)())
+        if device_bitmap and bitmap is not None:
+            desc.protected_bitmap = C.cast(C.c_void_p(_ptr(bitmap)), C.POINTER(C.c_uint32))
+        else:
+            desc.protected_bitmap = (bm.ctypes.data_as(C.POINTER(C.c_uint32)) if bm is not None
+                                     else C.POINTER(C.c_uint32)())
         desc.flags = int(flags)
         host_only = bool(flags & RK_PLAN_HOST_ONLY)
         handle = C.c_void_p()
@@ -237,6 +252,28 @@ def lse_merge(o_parts, lse_parts, out, lse_out, stream=None):
     st = lib().rk_lse_merge(_ptr(o_parts), _ptr(lse_parts), P, rows, H, d_v, _ptr(out),
                             _ptr(lse_out), _stream(stream))
     _check(st, "rk_lse_merge")
+
+
+def protected_build(segments, seg_begin, boundary, p_random, budget_pct, none, u, score, dirty,
+                    bitmap, workspace, stream=None):
+    """rk_protected_build.  segments: (n, delta, is_new) per segment, requests
+    concatenated with prefix offsets seg_begin; u (float64), score (float32),
+    dirty and bitmap (uint32 words): device tensors or None; workspace: a
+    device tensor of at least protected_workspace_bytes(...) bytes."""
+    segs = (RkSegment * max(1, len(segments)))()
+    for i, (n, delta, is_new) in enumerate(segments):
+        segs[i] = RkSegment(0, int(n), int(delta), RK_SEG_NEW if is_new else 0, 0)
+    sb = np.ascontiguousarray(seg_begin, dtype=np.int32)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().rk_protected_build(len(seg_begin) - 1, sb.ctypes.data_as(C.POINTER(C.c_int32)),
+                                  segs, int(boundary), float(p_random), int(budget_pct),
+                                  RK_PROT_NONE if none else 0, _ptr(u), _ptr(score), _ptr(dirty),
+                                  _ptr(bitmap), _ptr(workspace), ws_bytes, _stream(stream))
+    _check(st, "rk_protected_build")
+
+
+def protected_workspace_bytes(num_requests: int, num_segments: int) -> int:
+    return int(lib().rk_protected_workspace_bytes(int(num_requests), int(num_segments)))
 
 
 def status_string(st: int) -> str:

@@ -148,8 +148,10 @@ static rk_status_t build_plan(const rk_seg_attn_desc_t* d, rk_seg_attn_plan_s* p
   if (!(d->rope_base > 1.0) || !std::isfinite(d->rope_base)) return RK_ERR_INVALID_ARG;
   if (!(d->softmax_scale > 0.f) || !std::isfinite(d->softmax_scale)) return RK_ERR_INVALID_ARG;
   if (d->sink < 0 || d->window < 0) return RK_ERR_INVALID_ARG;
-  if (d->flags & ~(RK_PLAN_HOST_ONLY | RK_PLAN_LEGACY_MMA | RK_PLAN_SINGLE_CTA | RK_PLAN_CTA_PAIR))
+  if (d->flags & ~(RK_PLAN_HOST_ONLY | RK_PLAN_LEGACY_MMA | RK_PLAN_SINGLE_CTA | RK_PLAN_CTA_PAIR |
+                   RK_PLAN_DEVICE_BITMAP))
     return RK_ERR_INVALID_ARG;
+  if ((d->flags & RK_PLAN_DEVICE_BITMAP) && (d->flags & RK_PLAN_HOST_ONLY)) return RK_ERR_INVALID_ARG;
   if (d->seg_begin[0] != 0) return RK_ERR_INVALID_ARG;
   for (int r = 0; r < R; ++r)
     if (d->seg_begin[r + 1] <= d->seg_begin[r]) return RK_ERR_INVALID_ARG;
@@ -224,6 +226,16 @@ static rk_status_t build_plan(const rk_seg_attn_desc_t* d, rk_seg_attn_plan_s* p
     word_off[r + 1] = word_off[r] + (pos + 31) / 32;
   }
   if (rows_total * H > (int64_t(1) << 40)) return RK_ERR_CAPACITY;
+  // a device bitmap is brought to the host once the geometry is validated
+  std::vector<uint32_t> host_bits;
+  const uint32_t* bitmap = d->protected_bitmap;
+  if (bitmap && (d->flags & RK_PLAN_DEVICE_BITMAP)) {
+    host_bits.resize(static_cast<size_t>(word_off[R]));
+    if (cudaMemcpy(host_bits.data(), bitmap, host_bits.size() * sizeof(uint32_t),
+                   cudaMemcpyDeviceToHost) != cudaSuccess)
+      return RK_ERR_CUDA;
+    bitmap = host_bits.data();
+  }
 
   // heads
   for (int h = 0; h < H; ++h) (d->head_role[h] ? p->global_heads : p->local_heads).push_back(h);
@@ -276,8 +288,8 @@ static rk_status_t build_plan(const rk_seg_attn_desc_t* d, rk_seg_attn_plan_s* p
     const int64_t qb = rq.q_row_begin, Tr = rq.T;
     // protected computed rows
     std::vector<uint8_t> prot(Tr, 0);
-    if (d->protected_bitmap) {
-      const uint32_t* w = d->protected_bitmap + word_off[r];
+    if (bitmap) {
+      const uint32_t* w = bitmap + word_off[r];
       for (int64_t q = 0; q < Tr; ++q) prot[q] = (w[q >> 5] >> (q & 31)) & 1u;
     }
     for (int j = 0; j < rq.seg_count; ++j) {
