@@ -309,6 +309,51 @@ rk_status_t rk_protected_build(int32_t num_requests, const int32_t* seg_begin,
                                const float* score, const uint32_t* dirty, uint32_t* bitmap,
                                void* workspace, size_t workspace_bytes, void* stream);
 
+/* ---- projected state and layer output ----------------------------------- */
+
+/* Shapes of the projection that follows the attention (paper, first
+ * paragraphs: eqs. 2-4; TP8 fast-path paragraph).  Heads act in their native
+ * output groups of 8 consecutive heads; each group has its own block of the
+ * first output projection W_a. */
+typedef struct {
+  int64_t rows;              /* computed rows (as the attention's out) */
+  int32_t num_heads;         /* H, a multiple of 8, at most 256 */
+  int32_t d_v;               /* per-head output width (512) */
+  int32_t d_g;               /* projected width per group, a multiple of 256 */
+  int32_t d_model;           /* layer output width, a multiple of 256 */
+  const uint8_t* head_role;  /* host [H]: 0 Local, 1 Global */
+} rk_project_desc_t;
+
+/* Projected state and layer output with row-wise replacement of the Local
+ * contribution (paper: sliced W_a projection, Local restoration and row-wise
+ * replacement into a contiguous projected state, W_b once; blog: z = z_off +
+ * z_on, y = W_b z).  For every row t and group g:
+ *   z[t, g] = W_aG(g) O_G[t] + (row t protected ? W_aL(g) O_L[t] : z_off[t, g])
+ *   y[t]    = W_b z[t]
+ * where W_aG(g) / W_aL(g) are the columns of group g's W_a block that belong
+ * to its Global / Local heads.  bf16 operands, fp32 accumulation, bf16
+ * results.  The inverse output rotation is the identity (the values carry
+ * no rotary part).
+ * o         device bf16 [rows, H, d_v]: the attention output (its Local heads
+ *           hold fresh values on the protected rows).
+ * z_off     device bf16 [rows, H / 8, d_g]: the cached projected Local
+ *           contribution of every row.
+ * prot      device uint32 [ceil(rows / 32)]: bit r % 32 of word r / 32 set
+ *           when row r is protected.
+ * w_a       device bf16 [H / 8, d_g, 8 d_v], row-major per group.
+ * w_b       device bf16 [d_model, (H / 8) d_g], row-major.
+ * z         device bf16 [rows, (H / 8) d_g], out (the projected state).
+ * y         device bf16 [rows, d_model], out.
+ * status    device int32, 0 on entry; a bounded device wait that expires
+ *           stores RK_ERR_DEVICE_TIMEOUT.
+ * All device pointers 16-byte aligned (prot and status 4-byte).  Allocates
+ * nothing; asynchronous on `stream`.  Errors: RK_ERR_NULL,
+ * RK_ERR_INVALID_ARG, RK_ERR_UNSUPPORTED_DIMS (d_v != 512), RK_ERR_ALIGNMENT,
+ * RK_ERR_CAPACITY, RK_ERR_CUDA. */
+rk_status_t rk_project_forward(const rk_project_desc_t* desc, const void* o, const void* z_off,
+                               const uint32_t* prot, const void* w_a, const void* w_b, void* z,
+                               void* y, int32_t* status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

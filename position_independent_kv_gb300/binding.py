@@ -26,7 +26,7 @@ EXPORTS = ["rk_seg_attn_plan", "rk_seg_attn_plan_destroy", "rk_seg_attn_plan_inf
            "rk_seg_attn_workspace_bytes", "rk_seg_attn_forward", "rk_lse_merge",
            "rk_seg_attn_last_device_status", "rk_status_string",
            "rk_seg_attn_forward_noalloc", "rk_seg_attn_forward_host",
-           "rk_protected_workspace_bytes", "rk_protected_build"]
+           "rk_protected_workspace_bytes", "rk_protected_build", "rk_project_forward"]
 
 STATUS = {0: "RK_OK", 1: "RK_ERR_NULL", 2: "RK_ERR_INVALID_ARG", 3: "RK_ERR_SEGMENT_OVERLAP",
           4: "RK_ERR_SEGMENT_GAP", 5: "RK_ERR_UNSUPPORTED_DIMS", 6: "RK_ERR_CAPACITY",
@@ -61,6 +61,12 @@ class RkPlanInfo(C.Structure):
         return {k: getattr(self, k) for k, _ in self._fields_ if k != "reserved"}
 
 
+class RkProjectDesc(C.Structure):
+    _fields_ = [("rows", C.c_int64), ("num_heads", C.c_int32), ("d_v", C.c_int32),
+                ("d_g", C.c_int32), ("d_model", C.c_int32),
+                ("head_role", C.POINTER(C.c_uint8))]
+
+
 class RkError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
@@ -92,6 +98,8 @@ def lib() -> C.CDLL:
         L.rk_seg_attn_forward.argtypes = [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
                                           C.c_void_p, C.c_size_t, C.c_void_p]
         L.rk_seg_attn_forward.restype = C.c_int
+        L.rk_project_forward.argtypes = [C.POINTER(RkProjectDesc)] + [C.c_void_p] * 9
+        L.rk_project_forward.restype = C.c_int
         L.rk_protected_workspace_bytes.argtypes = [C.c_int32, C.c_int32]
         L.rk_protected_workspace_bytes.restype = C.c_size_t
         L.rk_protected_build.argtypes = [C.c_int32, C.POINTER(C.c_int32), C.POINTER(RkSegment),
@@ -270,6 +278,22 @@ def protected_build(segments, seg_begin, boundary, p_random, budget_pct, none, u
                                   RK_PROT_NONE if none else 0, _ptr(u), _ptr(score), _ptr(dirty),
                                   _ptr(bitmap), _ptr(workspace), ws_bytes, _stream(stream))
     _check(st, "rk_protected_build")
+
+
+def project_forward(o, z_off, prot, w_a, w_b, z, y, head_role, status, stream=None):
+    """rk_project_forward.  o bf16 [rows, H, d_v]; z_off bf16 [rows, H/8, d_g];
+    prot uint32 words; w_a bf16 [H/8, d_g, 8 d_v]; w_b bf16 [d_model, H/8 d_g];
+    z, y bf16 outputs; status int32 [1] (device)."""
+    rows, H, dv = (int(x) for x in o.shape)
+    d = RkProjectDesc()
+    d.rows, d.num_heads, d.d_v = rows, H, dv
+    d.d_g = int(w_a.shape[1])
+    d.d_model = int(w_b.shape[0])
+    role = np.ascontiguousarray(head_role, dtype=np.uint8)
+    d.head_role = role.ctypes.data_as(C.POINTER(C.c_uint8))
+    st = lib().rk_project_forward(C.byref(d), _ptr(o), _ptr(z_off), _ptr(prot), _ptr(w_a),
+                                  _ptr(w_b), _ptr(z), _ptr(y), _ptr(status), _stream(stream))
+    _check(st, "rk_project_forward")
 
 
 def protected_workspace_bytes(num_requests: int, num_segments: int) -> int:
