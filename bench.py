@@ -398,6 +398,64 @@ def bench_protected_builder(name: str, local: int) -> dict:
             "rows_per_s": rows / (ms * 1e-3)}
 
 
+def bench_projection(local: int, name: str = "ctx128k", dg: int = 1024, dm: int = 4096) -> dict:
+    """rk_project_forward on the workload's rows and protected rows (random
+    bf16 operands of those shapes): device time per call (CUDA events, median
+    of 5 after 3 warm-ups), algorithmic and performed TFLOP/s."""
+    import torch
+    from position_independent_kv_gb300 import binding as B
+    from position_independent_kv_gb300.protected import build_bitmap
+    from position_independent_kv_gb300.workloads import make_geometry
+    dev = torch.device("cuda", local)
+    wl = make_geometry(name, 0)
+    words, rows_prot = build_bitmap(wl)
+    rows = sum(r.T - r.q_row_begin for r in wl.requests)
+    prot = np.concatenate([p[r.q_row_begin:] for r, p in zip(wl.requests, rows_prot)])
+    bits = np.zeros((rows + 31) // 32, np.uint32)
+    idx = np.nonzero(prot)[0]
+    np.bitwise_or.at(bits, idx // 32, (np.uint32(1) << (idx % 32).astype(np.uint32)))
+    H, G = wl.H, wl.H // 8
+    g = torch.Generator(device=dev).manual_seed(0)
+    o = torch.randn(rows, H, 512, device=dev, generator=g).to(torch.bfloat16)
+    z_off = torch.randn(rows, G, dg, device=dev, generator=g).to(torch.bfloat16)
+    w_a = (torch.randn(G, dg, 4096, device=dev, generator=g) / 64.0).to(torch.bfloat16)
+    w_b = (torch.randn(dm, G * dg, device=dev, generator=g) / (G * dg) ** 0.5).to(torch.bfloat16)
+    z = torch.empty(rows, G * dg, dtype=torch.bfloat16, device=dev)
+    y = torch.empty(rows, dm, dtype=torch.bfloat16, device=dev)
+    pw = torch.from_numpy(bits.view(np.int32)).to(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    role = wl.head_role
+    for _ in range(3):
+        B.project_forward(o, z_off, pw, w_a, w_b, z, y, role, status)
+    torch.cuda.synchronize(dev)
+    times = []
+    for _ in range(5):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        B.project_forward(o, z_off, pw, w_a, w_b, z, y, role, status)
+        b.record()
+        torch.cuda.synchronize(dev)
+        times.append(a.elapsed_time(b))
+    ms = statistics.median(times)
+    ngl = int(role.sum())  # Global heads
+    nloc = H - ngl
+    P = int(prot.sum())
+    alg = 2.0 * dg * 512 * (rows * ngl + P * nloc) + 2.0 * rows * G * dg * dm
+    # tiles holding a protected row run the Local part for all their 128 rows
+    tiles_l = len(set((idx // 128).tolist()))
+    perf = 2.0 * dg * 512 * (((rows + 127) // 128) * 128 * ngl + tiles_l * 128 * nloc) + \
+        2.0 * ((rows + 127) // 128) * 128 * G * dg * dm
+    ok = int(status.item()) == 0
+    del o, z_off, w_a, w_b, z, y
+    torch.cuda.empty_cache()
+    return {"workload": f"{name} rows and protected rows, H={H}, d_v=512, d_g={dg}, "
+                        f"d_model={dm}, random bf16 weights",
+            "ms": round(ms, 3), "tflops": round(alg / (ms * 1e-3) / 1e12, 1),
+            "performed_tflops": round(perf / (ms * 1e-3) / 1e12, 1), "status_ok": ok,
+            "protected_rows": P, "rows": rows}
+
+
 def cpu_baseline(wl, budget_s: float = 20.0):
     """The fp64 oracle on a bounded, stratified sample of the workload's rows
     (host cores; relocation of all keys included in the time)."""
@@ -468,6 +526,9 @@ def run_ours(args):
     prot = None
     if not args.no_builder and rank == 0:
         prot = [bench_protected_builder(n, local) for n in ("ctx128k", "decode")]
+    proj = None
+    if not args.no_projection and rank == 0:
+        proj = bench_projection(local)
     line = None
     if rank == 0:
         info = res["info"]
@@ -501,6 +562,9 @@ def run_ours(args):
             line["e2e"] = e2e
         if prot:
             line["protected_builder"] = prot
+        if proj:
+            proj["frac_of_peak"] = round(proj["tflops"] / peak, 4)
+            line["projection"] = proj
         if dec:
             line["decode"] = {"workload": "64 requests x 1 row, 4-32 segments, 8K-64K keys, "
                                           "H=64 (56/8), split over segments + fused LSE merge",
@@ -565,6 +629,8 @@ def main():
                          "legacy (mma.sync)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-projection", action="store_true",
+                    help="skip the timing of the projected-state / W_b step")
     ap.add_argument("--no-builder", action="store_true",
                     help="skip the timing of the on-device protected-row builder")
     ap.add_argument("--no-cpu", action="store_true")
