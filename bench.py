@@ -201,24 +201,25 @@ def barrier(ws):
         dist.barrier()
 
 
-def max_over_ranks(x: float, ws: int) -> float:
+def _reduce(x: float, ws: int, op: str) -> float:
+    """All-reduce one scalar over the ranks (host tensor for gloo, device
+    tensor for nccl)."""
     if ws == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
     return float(t.item())
+
+
+def max_over_ranks(x: float, ws: int) -> float:
+    return _reduce(x, ws, "max")
 
 
 def sum_over_ranks(x: float, ws: int) -> float:
-    if ws == 1:
-        return x
-    import torch
-    import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
-    dist.all_reduce(t, op=dist.ReduceOp.SUM)
-    return float(t.item())
+    return _reduce(x, ws, "sum")
 
 
 def prefill_flops(info, d_nope, d_rope):
