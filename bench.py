@@ -529,7 +529,7 @@ def run_ours(args):
         prot = [bench_protected_builder(n, local) for n in ("ctx128k", "decode")]
     proj = None
     if not args.no_projection and rank == 0:
-        proj = bench_projection(local)
+        proj = bench_projection(local, args.projection_workload)
     line = None
     if rank == 0:
         info = res["info"]
@@ -632,6 +632,8 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-projection", action="store_true",
                     help="skip the timing of the projected-state / W_b step")
+    ap.add_argument("--projection-workload", default="ctx128k",
+                    help="rows and protected rows of this workload feed the projection step")
     ap.add_argument("--no-builder", action="store_true",
                     help="skip the timing of the on-device protected-row builder")
     ap.add_argument("--no-cpu", action="store_true")

@@ -70,6 +70,8 @@ enum {
   B_KFULL = 0,
   B_KEMPTY = B_KFULL + KRING,
   B_SFULL = B_KEMPTY + KRING,  // 2: S buffer j & 1 written
+  // SFREE, ROPE and PREADY take one arrival per lane warp of both CTAs of a
+  // pair, made by lane 0 after the warp has synchronised
   B_SFREE = B_SFULL + 2,  // 2: S buffer read by both S CTAs' softmax lanes
   B_ROPE = B_SFREE + 2,   // rotated q_rope of the next segment written (the first
                           // event also publishes the queries in tensor memory)
@@ -126,12 +128,12 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(&bar[B_SFULL + b], 1);
-      tc::mbar_init(&bar[B_SFREE + b], 2 * 128);
+      tc::mbar_init(&bar[B_SFREE + b], 2 * 4);
       tc::mbar_init(&bar[B_PEMPTY + b], 1);
       tc::mbar_init(&bar[B_PFULL + b], 1);
-      tc::mbar_init(&bar[B_PREADY + b], 2 * 128);
+      tc::mbar_init(&bar[B_PREADY + b], 2 * 4);
     }
-    tc::mbar_init(&bar[B_ROPE], 2 * 128);
+    tc::mbar_init(&bar[B_ROPE], 2 * 4);
     tc::mbar_init(&bar[B_SFINAL], 1);
     tc::mbar_init(&bar[B_ODONE], 1);
     tc::mbar_init(&bar[B_OFINAL], 1);
@@ -301,7 +303,8 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
       bool have = next_key_tile<TNK>(kt, segs, nseg, 0, r0hi, r1lo, r1hi);
       put_rope(kt.j);
       tc::tc_fence_before();
-      tc::mbar_arrive_cluster(cbar(B_ROPE, 0));
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive_cluster(cbar(B_ROPE, 0));
       float m_run = -INFINITY, l_run = 0.f;
       int j = 0;
       bool ok = true;
@@ -320,13 +323,15 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
           // S_j is complete, so no score MMA still reads the rotated q_rope
           if (have_next && nx.j != kt.j) {
             put_rope(nx.j);
-            tc::mbar_arrive_cluster(cbar(B_ROPE, 0));
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive_cluster(cbar(B_ROPE, 0));
           }
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) tc::tmem_ld32(lt + T_S + 128 * b + 32 * q4, s[q4]);
           tc::tmem_wait_ld();
           tc::tc_fence_before();
-          tc::mbar_arrive_cluster(cbar(B_SFREE + b, 0));
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive_cluster(cbar(B_SFREE + b, 0));
 
           // scores are scaled inside the exponent: x = s * scale * log2(e)
           const int p = ri.p;
@@ -512,7 +517,8 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
           tc::tmem_wait_st();
         }
         tc::tc_fence_before();
-        tc::mbar_arrive_cluster(cbar(B_PREADY + b, 2));
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive_cluster(cbar(B_PREADY + b, 2));
         ++j;
         have = next_key_tile<TNK>(kt, segs, nseg, 0, r0hi, r1lo, r1hi);
       }

@@ -81,7 +81,7 @@ __device__ __forceinline__ void chunk_of(const ProjArgs& a, int g, int c, int& a
 }
 
 __global__ void __launch_bounds__(PJ_THREADS, 1)
-    project_kernel(const ProjArgs a, const __grid_constant__ CUtensorMap ma,
+    project_kernel(const __grid_constant__ ProjArgs a, const __grid_constant__ CUtensorMap ma,
                    const __grid_constant__ CUtensorMap mb) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
