@@ -1,7 +1,7 @@
 """CPU fp64 oracle (test infrastructure only; see seg_attn.py)."""
 from .seg_attn import (attend, attend_partial, bitmap_words, brute_force, build_protected,
-                       lse_merge, relocate, rope_theta, rotate, seg_attn_request,
-                       visible_keys)
+                       lse_merge, relocate, restore_output_phase, rope_theta, rotate,
+                       seg_attn_request, visible_keys)
 
 __all__ = ["attend", "attend_partial", "bitmap_words", "brute_force", "build_protected",
-           "lse_merge", "relocate", "rope_theta", "rotate", "seg_attn_request", "visible_keys"]
+           "lse_merge", "relocate", "restore_output_phase", "rope_theta", "rotate", "seg_attn_request", "visible_keys"]

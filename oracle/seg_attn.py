@@ -129,7 +129,8 @@ def attend(qh: np.ndarray, K: np.ndarray, V: np.ndarray, scale: float):
 def seg_attn_request(q: np.ndarray, segments, T: int, q_row_begin: int,
                      head_role, d_nope: int, base: float, scale: float,
                      sink: int, window: int, protected: np.ndarray,
-                     out_init: np.ndarray, lse_init: np.ndarray, rows=None, sampled=False):
+                     out_init: np.ndarray, lse_init: np.ndarray, rows=None, sampled=False,
+                     v_rope: bool = False):
     """One request.
 
     q         fp64 [T - q_row_begin, H, d_k]  (row i = absolute row q_row_begin + i)
@@ -139,11 +140,16 @@ def seg_attn_request(q: np.ndarray, segments, T: int, q_row_begin: int,
     rows      absolute rows to evaluate (default: every computed row)
     sampled   if True, q / out_init / lse_init hold only the evaluated rows,
               in the order of `rows`
+    v_rope    the value carries a rotary part (output-phase restore, see
+              `restore_output_phase`): V is the whole relocated key row, so
+              out_init and the result have d_k columns
 
     Returns (O, lse) for the evaluated rows, already assembled: Global heads
     computed, Local heads computed on protected rows and copied otherwise.
     """
     K, V = relocate([(lat, d) for lat, d, _ in segments], T, d_nope, base)
+    if v_rope:
+        V = K
     prot = np.array(protected, dtype=bool).copy()
     for lat, d, is_new in segments:
         if is_new:
@@ -155,7 +161,7 @@ def seg_attn_request(q: np.ndarray, segments, T: int, q_row_begin: int,
         rows = np.arange(q_row_begin, T)
     rows = np.asarray(rows, dtype=np.int64)
     H = q.shape[1]
-    O = np.empty((len(rows), H, d_nope), dtype=np.float64)
+    O = np.empty((len(rows), H, V.shape[1]), dtype=np.float64)
     L = np.empty((len(rows), H), dtype=np.float64)
     for i, p in enumerate(rows):
         assert q_row_begin <= p < T
@@ -164,12 +170,37 @@ def seg_attn_request(q: np.ndarray, segments, T: int, q_row_begin: int,
         L[i] = lse_init[r]
         if len(gh):
             o, l = attend(q[r, gh], K[:p + 1], V[:p + 1], scale)
+            if v_rope:
+                o = restore_output_phase(o, int(p), d_nope, base)
             O[i, gh], L[i, gh] = o, l
         if len(lh) and prot[p]:
             keys = visible_keys(int(p), False, sink, window)
             o, l = attend(q[r, lh], K[keys], V[keys], scale)
+            if v_rope:
+                o = restore_output_phase(o, int(p), d_nope, base)
             O[i, lh], L[i, lh] = o, l
     return O, L
+
+
+# --------------------------------------------------------------------------
+# Output-phase restore (RedKnot-MLA paper: the head-partition paragraph
+# defines the inverse output RoPE R^-1 applied to the attention output before
+# the sliced W_a; the RoPE-orthogonality paragraph: after attending the
+# canonical latent the runtime "restores the output phase").  Reading: when
+# the value is the packed latent row itself, its rope slice carries the key's
+# absolute phase R(k) once relocated (step 1), so the output's rope slice is
+# sum_k P_k R(k) v_k; the inverse output RoPE at the query's absolute
+# position p turns it by R(-p), leaving sum_k P_k R(k - p) v_k, which depends
+# on relative positions only.
+# --------------------------------------------------------------------------
+
+
+def restore_output_phase(o: np.ndarray, p: int, d_nope: int, base: float) -> np.ndarray:
+    """o [..., d_k] computed against relocated values -> the same with the
+    rope slice turned by R(-p)."""
+    o = np.array(o, dtype=np.float64, copy=True)
+    o[..., d_nope:] = rotate(o[..., d_nope:], -float(p), base)
+    return o
 
 
 # --------------------------------------------------------------------------
@@ -277,7 +308,7 @@ def bitmap_words(prot: np.ndarray) -> np.ndarray:
 
 
 def brute_force(q, segments, T, q_row_begin, head_role, d_nope, base, scale,
-                sink, window, protected, out_init, lse_init):
+                sink, window, protected, out_init, lse_init, v_rope=False):
     """Same contract as seg_attn_request on nested Python lists, every row."""
     d_k = len(q[0][0])
     d_rope = d_k - d_nope
@@ -316,8 +347,15 @@ def brute_force(q, segments, T, q_row_begin, head_role, d_nope, base, scale,
             mx = max(xs)
             es = [math.exp(x - mx) for x in xs]
             den = sum(es)
-            orow.append([sum(es[i] * Kf[k][c] for i, k in enumerate(keys)) / den
-                         for c in range(d_nope)])
+            d_v = d_k if v_rope else d_nope
+            ov = [sum(es[i] * Kf[k][c] for i, k in enumerate(keys)) / den for c in range(d_v)]
+            if v_rope:  # inverse output RoPE at the query's own position
+                for i in range(d_rope // 2):
+                    a = -p * float(base) ** (-2.0 * i / d_rope)
+                    x, y = ov[d_nope + 2 * i], ov[d_nope + 2 * i + 1]
+                    ov[d_nope + 2 * i] = x * math.cos(a) - y * math.sin(a)
+                    ov[d_nope + 2 * i + 1] = x * math.sin(a) + y * math.cos(a)
+            orow.append(ov)
             lrow.append(mx + math.log(den))
         O.append(orow)
         L.append(lrow)
