@@ -23,7 +23,8 @@
  * Conventions shared by every entry point
  * ---------------------------------------
  * bf16     IEEE bfloat16 stored as uint16.
- * d_k      d_nope + d_rope;  d_v = d_nope.
+ * d_k      d_nope + d_rope;  d_v = d_nope (V = c_nope), or d_v = d_k with
+ *          RK_PLAN_V_ROPE (V = the whole latent row, see there).
  * RoPE     interleaved pairs (2j, 2j+1) of the rope slice, theta_j =
  *          rope_base^(-2j/d_rope); R(phi) turns (x, y) into
  *          (x cos - y sin, x sin + y cos) with angle phi * theta_j.
@@ -82,6 +83,26 @@ typedef enum {
                                    one pair per half of d_v, instead of
                                    4-CTA clusters (scores on one CTA pair,
                                    outputs on the other) */
+#define RK_PLAN_V_ROPE 32u      /* the value carries a rotary part: V is the
+                                   whole packed latent row [c_nope | k_rope]
+                                   (d_v = d_k).  Each segment's contribution
+                                   to the output's rope slice is moved to
+                                   absolute positions by R(+delta_i) before
+                                   the merge, and the merged output's rope
+                                   slice is turned by the inverse output RoPE
+                                   R(-p) at the query row's absolute position
+                                   p, so it equals sum_k P_k R(k - p) v_k
+                                   (RedKnot-MLA paper: R^-1 in the
+                                   head-partition paragraph; "restores the
+                                   output phase", RoPE-orthogonality
+                                   paragraph).  Requires (d_nope, d_rope) =
+                                   (448, 64): the fp32 output accumulator of a
+                                   128-row tile fills the 512 columns of
+                                   tensor memory.  Runs on the 4-CTA kernel
+                                   (H = 64 or 128, one Global head per group
+                                   of 8 or none) and the split decode kernel;
+                                   RK_PLAN_LEGACY_MMA, RK_PLAN_SINGLE_CTA and
+                                   RK_PLAN_CTA_PAIR are refused with it. */
 
 /* One document segment of a request.
  * latent  device pointer, bf16 [n, d_k] row-major (row stride d_k elements),
@@ -108,7 +129,7 @@ typedef struct {
  * q_row_begin      [R] first computed row of each request (0 for a prefill
  *                  that recomputes every row; T_r - 1 for a decode step).
  * num_heads        H, a multiple of 8, at most 256.
- * d_nope, d_rope   (512, 64) or (128, 32).
+ * d_nope, d_rope   (512, 64) or (128, 32); (448, 64) with RK_PLAN_V_ROPE.
  * rope_base        theta base (> 1).
  * softmax_scale    s > 0, usually 1/sqrt(d_k).
  * head_role        [H] 0 = Local, 1 = Global.
@@ -152,7 +173,7 @@ typedef struct {
   int32_t kernel;            /* 0 = mma.sync tiles, 1 = tcgen05 tiles,
                                 2 = tcgen05 tiles paired on CTA pairs,
                                 3 = tcgen05 tile pairs on 4-CTA clusters */
-  int32_t reserved;
+  int32_t d_v;               /* output columns: d_nope, or d_k with RK_PLAN_V_ROPE */
 } rk_plan_info_t;
 
 /* Build an immutable, reusable plan for one request bundle geometry
@@ -183,7 +204,7 @@ size_t rk_seg_attn_workspace_bytes(rk_seg_attn_plan_t plan);
  * RoPE-orthogonality and protected-set paragraphs; blog "Insight 1").
  * q          device bf16 [rows, H, d_k], q_rope rotated at the row's absolute
  *            position, 16-byte aligned.
- * out        device bf16 [rows, H, d_nope], in/out.  Global heads: written on
+ * out        device bf16 [rows, H, d_v], in/out.  Global heads: written on
  *            every computed row.  Local heads: written only on protected
  *            rows (bitmap bit set or RK_SEG_NEW row); every other element
  *            keeps its bytes.

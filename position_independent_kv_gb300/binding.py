@@ -20,6 +20,7 @@ RK_PLAN_LEGACY_MMA = 2
 RK_PLAN_SINGLE_CTA = 4
 RK_PLAN_CTA_PAIR = 8
 RK_PLAN_DEVICE_BITMAP = 16
+RK_PLAN_V_ROPE = 32
 RK_PROT_NONE = 1
 
 EXPORTS = ["rk_seg_attn_plan", "rk_seg_attn_plan_destroy", "rk_seg_attn_plan_info",
@@ -55,10 +56,10 @@ class RkPlanInfo(C.Structure):
                 ("dense_tiles", C.c_int64), ("split_chunks", C.c_int64),
                 ("pairs_global", C.c_int64), ("pairs_local", C.c_int64),
                 ("performed_pairs", C.c_int64), ("latent_bytes", C.c_int64),
-                ("kernel", C.c_int32), ("reserved", C.c_int32)]
+                ("kernel", C.c_int32), ("d_v", C.c_int32)]
 
     def as_dict(self) -> dict:
-        return {k: getattr(self, k) for k, _ in self._fields_ if k != "reserved"}
+        return {k: getattr(self, k) for k, _ in self._fields_}
 
 
 class RkProjectDesc(C.Structure):
@@ -199,6 +200,8 @@ class SegAttnPlan:
     def from_workload(cls, wl, bitmap=None, flags=0, stream=None, addresses=None):
         from .workloads import segments_for_abi
         flat, begins = segments_for_abi(wl)
+        if getattr(wl, "v_rope", False):
+            flags |= RK_PLAN_V_ROPE
         if addresses is not None:
             flat = [(addresses(i, s), s[1], s[2], s[3]) for i, s in enumerate(flat)]
         return cls(flat, begins, [r.q_row_begin for r in wl.requests], wl.H, wl.d_nope,

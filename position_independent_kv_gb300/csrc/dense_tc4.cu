@@ -6,21 +6,31 @@
 // of d_v computes S = Q K^T twice.  Here the work is split by role instead:
 //
 //   ranks 0, 1  "S pair": rank r holds tile r's queries, the nope part in
-//               tensor memory (256 columns, A operand of the score MMAs) and
-//               the rotated rope part in shared memory, and computes
+//               tensor memory (32 columns per 64 dims, A operand of the score
+//               MMAs) and the rotated rope part in shared memory, and computes
 //               S_j = Q K_j^T for both tiles with M = 256 MMAs (N = 128
-//               keys: rank r streams keys 64r..64r+63 of every key tile, 72 KB
-//               through a ring of five 24 KB slots) into one of two S
-//               buffers, runs the online softmax of its 128 lanes, stages
-//               P_j (bf16, 32 KB) and a per-lane record (rescale factor,
-//               running sum) in its shared memory and copies them in one bulk
-//               copy into the shared memory of rank r + 2.
+//               keys: rank r streams keys 64r..64r+63 of every key tile as
+//               one box of whole latent rows through a two-slot ring) into
+//               one of two S buffers, runs the online softmax of its 128
+//               lanes, stages P_j (bf16, 32 KB) and a per-lane record
+//               (rescale factor, running sum) in its shared memory and copies
+//               them in one bulk copy into the shared memory of rank r + 2.
 //   ranks 2, 3  "O pair": rank 2 + r holds tile r's fp32 output for all 512
 //               columns in tensor memory and computes O += P_j V_j with
-//               M = 256, N = 256 MMAs (A = P_j from shared memory; rank 2 + r
-//               streams the V column chunks 2r, 2r+1, 4+2r, 5+2r of every key
-//               tile, 64 KB through four 32 KB slots), rescales O when the
-//               record says so, and stores the normalised output.
+//               M = 256, N = 2 x 256 MMAs (A = P_j from shared memory; rank
+//               2 + r streams value chunks 4r..4r+3 of every key tile, 64 KB,
+//               through a two-slot ring), rescales O when the record says
+//               so, and stores the normalised output.
+//
+// Two instantiations: (d_nope, d_rope) = (512, 64) with V = c_nope, and
+// (448, 64) with a value that carries a rotary part (V = the whole 512-wide
+// latent row).  In the second the output's rope columns are kept in the
+// canonical frame of the segment being walked: at a segment switch the O
+// lanes turn them by R(delta_prev - delta_next), and the epilogue turns them
+// by R(delta_last - p), which restores each segment's output phase and
+// applies the inverse output RoPE at the row's position p (RedKnot-MLA
+// paper: R^-1 in the head-partition paragraph, "restores the output phase"
+// in the RoPE-orthogonality paragraph).
 //
 // Each latent byte is read once per cluster, every MMA does useful work, and
 // the score and output MMAs of a key tile run on different SMs at the same
@@ -56,7 +66,7 @@ constexpr uint32_t PREC_BYTES = PBUF + RBUF;
 constexpr uint32_t PSTRIDE = PBUF + 2048;  // 1024-aligned buffers
 constexpr uint32_t OFF_STG = 2 * CHUNK;
 constexpr int KRING = 2;
-constexpr uint32_t KSLOT = 9 * HCHUNK;     // 64 keys x 9 chunks: one box per key tile
+constexpr uint32_t KSLOT = 9 * HCHUNK;     // 64 keys x up to 9 chunks: one box per key tile
 constexpr uint32_t OFF_KRING = OFF_STG + PSTRIDE;
 // O pair: two P + record buffers, the V ring (128 keys x 4 chunks per slot)
 constexpr uint32_t OFF_P = 0;
@@ -94,11 +104,29 @@ constexpr uint32_t T_Q = 0, T_S = 256;
 constexpr uint32_t T_O = 0;
 
 // segment maps (kSegMaps per segment)
-constexpr int MAP_K9 = 4;    // 64 rows x 9 chunks
+constexpr int MAP_K9 = 4;    // 64 rows x all d_k / 64 chunks
 constexpr int MAP_V4 = 5;    // 128 rows x 4 chunks
 
+// Turn the rope pairs held in o[0..31] (32 consecutive output columns: pairs
+// H0 .. H0 + 15 of the rope slice) by the angles whose cos / sin are (c[k],
+// s[k]) for pair k.
+template <int H0>
+__device__ __forceinline__ void turn_pairs(uint32_t (&o)[32], const float (&c)[32],
+                                           const float (&s)[32]) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float x = __uint_as_float(o[2 * i]), y = __uint_as_float(o[2 * i + 1]);
+    o[2 * i] = __float_as_uint(x * c[H0 + i] - y * s[H0 + i]);
+    o[2 * i + 1] = __float_as_uint(fmaf(x, s[H0 + i], y * c[H0 + i]));
+  }
+}
+
+template <int NCH, bool VROPE>
 __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
     dense_tc4_kernel(const KernelArgs a) {
+  constexpr int DK = 64 * (NCH + 1);           // latent row: NCH nope chunks + the rope chunk
+  constexpr uint32_t KBOX = (NCH + 1) * HCHUNK;  // one CTA's key box
+  static_assert(KBOX <= KSLOT, "key slot");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
@@ -165,7 +193,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
           ok = wait_bar(c, B_KEMPTY + slot, ((cnt / KRING) & 1) ^ 1);
           if (!ok) break;
           // the leader's barrier counts both CTAs' boxes
-          if (r == 0) tc::mbar_arrive_expect_tx(&bar[B_KFULL + slot], 2 * KSLOT);
+          if (r == 0) tc::mbar_arrive_expect_tx(&bar[B_KFULL + slot], 2 * KBOX);
           tc::tma_load_3d_2sm(smem_u32(sm + OFF_KRING + slot * KSLOT),
                               a.segmaps + kSegMaps * (rq.seg_first + cur.j) + MAP_K9,
                               cbar(B_KFULL + slot, 0), 0,
@@ -203,9 +231,9 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
           if (!ok) break;
           tc::tc_fence_after();
           const uint32_t base = ka + slot * KSLOT;
-          // B = K[64 keys of each CTA x 16 dims]: nope chunks 0..7, then the rope chunk
+          // B = K[64 keys of each CTA x 16 dims]: the nope chunks, then the rope chunk
 #pragma unroll
-          for (int cc = 0; cc < 8; ++cc)
+          for (int cc = 0; cc < NCH; ++cc)
 #pragma unroll
             for (int k = 0; k < 4; ++k)
               tc::mma_ts_2sm(ts, tbase + T_Q + 8 * (4 * cc + k),
@@ -213,7 +241,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
                              (cc | k) != 0);
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            const uint64_t bd = tc::sdesc_sw128(base + 8 * HCHUNK + 32 * k, 16, 1024);
+            const uint64_t bd = tc::sdesc_sw128(base + NCH * HCHUNK + 32 * k, 16, 1024);
             tc::mma_ss_2sm(ts, tc::sdesc_sw128(ropa + 32 * k, 16, 1024), bd, idS, 1);
             tc::mma_ss_2sm(ts, tc::sdesc_sw128(ropa + CHUNK + 32 * k, 16, 1024), bd, idS, 1);
           }
@@ -235,12 +263,12 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
       const uint32_t lt = tbase + (static_cast<uint32_t>(quarter * 32) << 16);
       const float sl2 = a.scale_log2;
       const int sink = a.sink, window = a.window;
-      const uint16_t* qrow = ri.p >= 0 ? a.q + (ri.frow * a.H + ri.head) * 576 : nullptr;
+      const uint16_t* qrow = ri.p >= 0 ? a.q + (ri.frow * a.H + ri.head) * DK : nullptr;
       const uint32_t orank = crank + 2;
       const uint32_t sw = static_cast<uint32_t>(m & 7);
       // this lane's nope queries -> tensor memory (32-bit column c = dims 2c, 2c + 1)
 #pragma unroll 1
-      for (int i = 0; i < 8; ++i) {
+      for (int i = 0; i < NCH; ++i) {
         uint32_t w[32];
         if (qrow) {
           const uint4* s4 = reinterpret_cast<const uint4*>(qrow) + 8 * i;
@@ -266,7 +294,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
         const float* cs = a.rope_cs + static_cast<int64_t>(rq.seg_first + seg) * 64;
         uint32_t raw[32];
         if (qrow) {
-          const uint4* s4 = reinterpret_cast<const uint4*>(qrow + 512);
+          const uint4* s4 = reinterpret_cast<const uint4*>(qrow + 64 * NCH);
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
             const uint4 v = __ldg(s4 + u);
@@ -490,6 +518,9 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
       bool ok = true;
       KeyTile kt{0, 0, 0, -1};
       bool have = next_key_tile<TNK>(kt, segs, nseg, 0, r0hi, r1lo, r1hi);
+      // rotary value: the segment whose canonical frame the output's rope
+      // columns (448..511, output column = value column there) are in
+      int seg_frame = kt.j;
       while (ok && have) {
         const int b = j & 1;
         ok = __all_sync(0xffffffffu, wait_bar<true>(c, B_PFULL + b, (j >> 1) & 1));
@@ -500,22 +531,44 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
         l_fin = rp[1];
         // arm buffer b for tile j + 2 (its copy starts after the MMAs of tile j)
         if (m == 0) tc::mbar_arrive_expect_tx(&bar[B_PFULL + b], PREC_BYTES);
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
-          // the output MMAs of tile j - 1 finish before O is rescaled
+        const bool scale = __any_sync(0xffffffffu, alpha != 1.f);
+        const bool turn = VROPE && kt.j != seg_frame;
+        if (scale || turn) {
+          // the output MMAs of tile j - 1 finish before O is rescaled / turned
           if (j >= 1) ok = __all_sync(0xffffffffu, wait_bar(c, B_ODONE, (j - 1) & 1));
           if (!ok) break;
           tc::tc_fence_after();
+          // a new segment: R(delta_frame - delta_next) moves the rope columns
+          // into the next segment's canonical frame
+          float tc_[32], ts_[32];
+          if (turn) {
+            const float4* ca = reinterpret_cast<const float4*>(a.rope_cs + int64_t(rq.seg_first + seg_frame) * 64);
+            const float4* cb = reinterpret_cast<const float4*>(a.rope_cs + int64_t(rq.seg_first + kt.j) * 64);
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+              const float4 x = __ldg(ca + u), y = __ldg(cb + u);
+              tc_[2 * u] = fmaf(x.x, y.x, x.y * y.y);
+              ts_[2 * u] = fmaf(x.y, y.x, -x.x * y.y);
+              tc_[2 * u + 1] = fmaf(x.z, y.z, x.w * y.w);
+              ts_[2 * u + 1] = fmaf(x.w, y.z, -x.z * y.w);
+            }
+          }
 #pragma unroll 1
-          for (int q8 = 0; q8 < 16; ++q8) {
+          for (int q8 = scale ? 0 : 14; q8 < 16; ++q8) {
             uint32_t o[32];
             tc::tmem_ld32(lt + T_O + 32 * q8, o);
             tc::tmem_wait_ld();
+            if (scale) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            }
+            if (turn && q8 == 14) turn_pairs<0>(o, tc_, ts_);
+            if (turn && q8 == 15) turn_pairs<16>(o, tc_, ts_);
             tc::tmem_st32(lt + T_O + 32 * q8, o);
           }
           tc::tmem_wait_st();
         }
+        seg_frame = kt.j;
         tc::tc_fence_before();
         __syncwarp();
         if (lane == 0) tc::mbar_arrive_cluster(cbar(B_PREADY + b, 2));
@@ -528,11 +581,33 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
         const bool st = ri.store && l_fin > 0.f;
         const float inv = st ? 1.f / l_fin : 0.f;
         uint16_t* dst = st ? a.out + (ri.frow * a.H + ri.head) * 512 : nullptr;
+        // rotary value: R(delta_frame - p) restores the last segment's output
+        // phase and applies the inverse output RoPE at the row's position p
+        // (cos / sin of p theta from the two-level position table)
+        float ec[32], es[32];
+        if (VROPE && st) {
+          const float4* ca = reinterpret_cast<const float4*>(a.rope_cs + int64_t(rq.seg_first + seg_frame) * 64);
+          const float4* ph = reinterpret_cast<const float4*>(a.pos_cs_hi + int64_t(ri.p >> 8) * 64);
+          const float4* pl = reinterpret_cast<const float4*>(a.pos_cs_lo + int64_t(ri.p & 255) * 64);
+#pragma unroll
+          for (int u = 0; u < 16; ++u) {
+            const float4 x = __ldg(ca + u), h = __ldg(ph + u), l = __ldg(pl + u);
+            // cos / sin of p theta for pairs 2u, 2u + 1
+            const float pc0 = fmaf(h.x, l.x, -h.y * l.y), ps0 = fmaf(h.y, l.x, h.x * l.y);
+            const float pc1 = fmaf(h.z, l.z, -h.w * l.w), ps1 = fmaf(h.w, l.z, h.z * l.w);
+            ec[2 * u] = fmaf(x.x, pc0, x.y * ps0);
+            es[2 * u] = fmaf(x.y, pc0, -x.x * ps0);
+            ec[2 * u + 1] = fmaf(x.z, pc1, x.w * ps1);
+            es[2 * u + 1] = fmaf(x.w, pc1, -x.z * ps1);
+          }
+        }
 #pragma unroll 1
         for (int q8 = 0; q8 < 16; ++q8) {
           uint32_t o[32];
           tc::tmem_ld32(lt + T_O + 32 * q8, o);
           tc::tmem_wait_ld();
+          if (VROPE && st && q8 == 14) turn_pairs<0>(o, ec, es);
+          if (VROPE && st && q8 == 15) turn_pairs<16>(o, ec, es);
           if (st) {
             const int c0 = 32 * q8;
             const int col = 256 * ((c0 >> 7) & 1) + 128 * (c0 >> 8) + (c0 & 127);
@@ -564,18 +639,24 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
   }
 }
 
+template <int NCH, bool VROPE>
+cudaError_t launch_tc4_t(const KernelArgs& a, cudaStream_t s) {
+  auto k = dense_tc4_kernel<NCH, VROPE>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(SMEM_BYTES));
+  if (e != cudaSuccess) return e;
+  const int64_t grid = 4 * static_cast<int64_t>(a.num_tc_pairs);
+  k<<<static_cast<unsigned>(grid), THREADS, SMEM_BYTES, s>>>(a);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_dense_tc4(const rk_seg_attn_plan_s& p, const KernelArgs& a, const void* q,
                              cudaStream_t s) {
-  (void)p;
   (void)q;
-  cudaError_t e = cudaFuncSetAttribute(dense_tc4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(SMEM_BYTES));
-  if (e != cudaSuccess) return e;
-  const int64_t grid = 4 * static_cast<int64_t>(a.num_tc_pairs);
-  dense_tc4_kernel<<<static_cast<unsigned>(grid), THREADS, SMEM_BYTES, s>>>(a);
-  return cudaGetLastError();
+  if (p.v_rope) return launch_tc4_t<7, true>(a, s);
+  return launch_tc4_t<8, false>(a, s);
 }
 
 }  // namespace rk

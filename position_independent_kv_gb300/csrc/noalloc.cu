@@ -74,7 +74,7 @@ extern "C" rk_status_t rk_seg_attn_forward_noalloc(rk_seg_attn_plan_t p, const v
     if (st != RK_OK) return st;
     char* w = static_cast<char*>(base);
     a.ws_o = reinterpret_cast<float*>(w);
-    size_t off = static_cast<size_t>(p->num_parts) * kSplitHeads * p->d_nope * sizeof(float);
+    size_t off = static_cast<size_t>(p->num_parts) * kSplitHeads * p->d_v * sizeof(float);
     a.ws_lse = reinterpret_cast<float*>(w + off);
     off += static_cast<size_t>(p->num_parts) * kSplitHeads * sizeof(float);
     off = (off + 255) & ~size_t(255);

@@ -31,7 +31,8 @@ constexpr int kSplitHeads = 8;    // Global heads per split chunk
 constexpr int kTcM = 128;         // query pairs per tcgen05 tile
 constexpr int kTcN = 128;         // keys per tcgen05 key tile
 
-bool dims_supported(int d_nope, int d_rope) {
+bool dims_supported(int d_nope, int d_rope, bool v_rope) {
+  if (v_rope) return d_nope == 448 && d_rope == 64;
   return (d_nope == 512 && d_rope == 64) || (d_nope == 128 && d_rope == 32);
 }
 
@@ -53,6 +54,8 @@ void free_device(rk_seg_attn_plan_s* p) {
   cudaFree(p->d_segs);
   cudaFree(p->d_reqs);
   cudaFree(p->d_rope_cs);
+  cudaFree(p->d_pos_cs_hi);
+  cudaFree(p->d_pos_cs_lo);
   cudaFree(p->d_tiles);
   cudaFree(p->d_local_rows);
   cudaFree(p->d_global_heads);
@@ -85,6 +88,7 @@ void free_device(rk_seg_attn_plan_s* p) {
   p->d_segs = nullptr;
   p->d_reqs = nullptr;
   p->d_rope_cs = nullptr;
+  p->d_pos_cs_hi = p->d_pos_cs_lo = nullptr;
   p->d_tiles = nullptr;
   p->d_local_rows = nullptr;
   p->d_global_heads = p->d_local_heads = nullptr;
@@ -144,13 +148,16 @@ static rk_status_t build_plan(const rk_seg_attn_desc_t* d, rk_seg_attn_plan_s* p
   const int R = d->num_requests;
   if (R < 1) return RK_ERR_INVALID_ARG;
   if (d->num_heads < 8 || d->num_heads > 256 || d->num_heads % 8) return RK_ERR_INVALID_ARG;
-  if (!dims_supported(d->d_nope, d->d_rope)) return RK_ERR_UNSUPPORTED_DIMS;
+  const bool v_rope = (d->flags & RK_PLAN_V_ROPE) != 0;
+  if (!dims_supported(d->d_nope, d->d_rope, v_rope)) return RK_ERR_UNSUPPORTED_DIMS;
   if (!(d->rope_base > 1.0) || !std::isfinite(d->rope_base)) return RK_ERR_INVALID_ARG;
   if (!(d->softmax_scale > 0.f) || !std::isfinite(d->softmax_scale)) return RK_ERR_INVALID_ARG;
   if (d->sink < 0 || d->window < 0) return RK_ERR_INVALID_ARG;
   if (d->flags & ~(RK_PLAN_HOST_ONLY | RK_PLAN_LEGACY_MMA | RK_PLAN_SINGLE_CTA | RK_PLAN_CTA_PAIR |
-                   RK_PLAN_DEVICE_BITMAP))
+                   RK_PLAN_DEVICE_BITMAP | RK_PLAN_V_ROPE))
     return RK_ERR_INVALID_ARG;
+  if (v_rope && (d->flags & (RK_PLAN_LEGACY_MMA | RK_PLAN_SINGLE_CTA | RK_PLAN_CTA_PAIR)))
+    return RK_ERR_UNSUPPORTED_DIMS;
   if ((d->flags & RK_PLAN_DEVICE_BITMAP) && (d->flags & RK_PLAN_HOST_ONLY)) return RK_ERR_INVALID_ARG;
   if (d->seg_begin[0] != 0) return RK_ERR_INVALID_ARG;
   for (int r = 0; r < R; ++r)
@@ -171,6 +178,8 @@ static rk_status_t build_plan(const rk_seg_attn_desc_t* d, rk_seg_attn_plan_s* p
   p->H = H;
   p->d_nope = d->d_nope;
   p->d_rope = d->d_rope;
+  p->v_rope = v_rope;
+  p->d_v = v_rope ? d->d_nope + d->d_rope : d->d_nope;
   p->sink = d->sink;
   p->window = d->window;
   p->softmax_scale = d->softmax_scale;
@@ -184,6 +193,12 @@ static rk_status_t build_plan(const rk_seg_attn_desc_t* d, rk_seg_attn_plan_s* p
     const bool h_ok = d->num_heads == 64 || d->num_heads == 128;
     if (!(d->flags & RK_PLAN_LEGACY_MMA) && d->d_nope == 512 && d->d_rope == 64 && hg_ok && h_ok) {
       p->kernel = (d->flags & RK_PLAN_SINGLE_CTA) ? 1 : (d->flags & RK_PLAN_CTA_PAIR) ? 2 : 3;
+      p->tile_m = kTcM;
+    }
+    // the rotary value runs on the 4-CTA kernel only
+    if (v_rope) {
+      if (!(hg_ok && h_ok)) return RK_ERR_UNSUPPORTED_DIMS;
+      p->kernel = 3;
       p->tile_m = kTcM;
     }
   }
@@ -261,6 +276,29 @@ static rk_status_t build_plan(const rk_seg_attn_desc_t* d, rk_seg_attn_plan_s* p
       p->rope_cs[(i * half + j) * 2 + 1] = static_cast<float>(std::sin(ang));
     }
   }
+  // inverse output RoPE at any query position p = 256 a + b: cos/sin(256 a
+  // theta_j) and cos/sin(b theta_j), fp64 then fp32; the kernels combine the
+  // two by the angle-addition formulas
+  if (v_rope) {
+    int64_t tmax = 0;
+    for (int r = 0; r < R; ++r) tmax = std::max(tmax, T[r]);
+    const int64_t nhi = tmax / 256 + 1;
+    p->pos_cs_hi.resize(static_cast<size_t>(nhi) * half * 2);
+    p->pos_cs_lo.resize(static_cast<size_t>(256) * half * 2);
+    for (int j = 0; j < half; ++j) {
+      const double theta = std::pow(d->rope_base, -2.0 * j / d->d_rope);
+      for (int64_t a = 0; a < nhi; ++a) {
+        const double ang = static_cast<double>(256 * a) * theta;
+        p->pos_cs_hi[(a * half + j) * 2 + 0] = static_cast<float>(std::cos(ang));
+        p->pos_cs_hi[(a * half + j) * 2 + 1] = static_cast<float>(std::sin(ang));
+      }
+      for (int64_t b = 0; b < 256; ++b) {
+        const double ang = static_cast<double>(b) * theta;
+        p->pos_cs_lo[(b * half + j) * 2 + 0] = static_cast<float>(std::cos(ang));
+        p->pos_cs_lo[(b * half + j) * 2 + 1] = static_cast<float>(std::sin(ang));
+      }
+    }
+  }
 
   // work lists
   rk_plan_info_t& info = p->info;
@@ -272,6 +310,7 @@ static rk_status_t build_plan(const rk_seg_attn_desc_t* d, rk_seg_attn_plan_s* p
   info.num_global_heads = HG;
   info.num_local_heads = HL;
   info.kernel = p->kernel;
+  info.d_v = p->d_v;
   for (int64_t i = 0; i < nseg; ++i)
     info.latent_bytes += p->segs[i].n * int64_t(d->d_nope + d->d_rope) * 2;
 
@@ -566,7 +605,7 @@ static rk_status_t build_plan(const rk_seg_attn_desc_t* d, rk_seg_attn_plan_s* p
   p->num_parts = parts;
   p->num_mgroups = mgroups;
   if (parts) {
-    const size_t dv = d->d_nope;
+    const size_t dv = p->d_v;
     size_t bytes = 0;
     bytes += static_cast<size_t>(parts) * kSplitHeads * dv * sizeof(float);
     bytes += static_cast<size_t>(parts) * kSplitHeads * sizeof(float);
@@ -595,6 +634,8 @@ extern "C" rk_status_t rk_seg_attn_plan(const rk_seg_attn_desc_t* desc, void* st
     if (st == RK_OK) st = upload(p->segs, &p->d_segs, s);
     if (st == RK_OK) st = upload(p->reqs, &p->d_reqs, s);
     if (st == RK_OK) st = upload(p->rope_cs, &p->d_rope_cs, s);
+    if (st == RK_OK) st = upload(p->pos_cs_hi, &p->d_pos_cs_hi, s);
+    if (st == RK_OK) st = upload(p->pos_cs_lo, &p->d_pos_cs_lo, s);
     if (st == RK_OK) st = upload(p->tiles, &p->d_tiles, s);
     if (st == RK_OK) st = upload(p->local_rows, &p->d_local_rows, s);
     if (st == RK_OK) st = upload(p->global_heads, &p->d_global_heads, s);
@@ -605,14 +646,16 @@ extern "C" rk_status_t rk_seg_attn_plan(const rk_seg_attn_desc_t* desc, void* st
     if (st == RK_OK) st = upload(p->tc_pairs_chunked, &p->d_tc_pairs_chunked, s);
     if (st == RK_OK) st = upload(p->head_role, &p->d_head_role, s);
     if (st == RK_OK && p->kernel >= 1) {
-      // TMA maps of each segment latent, viewing a row as 9 chunks of 64
-      // bf16: (64, n, 9) so that a box lands chunk-major in shared memory
+      // TMA maps of each segment latent, viewing a row as d_k / 64 chunks
+      // of 64 bf16: (64, n, d_k / 64) so that a box lands chunk-major in
+      // shared memory; map 4 takes whole rows
       p->segmaps.resize(rk::kSegMaps * p->segs.size());
+      const uint32_t nch = static_cast<uint32_t>((p->d_nope + p->d_rope) / 64);
       for (size_t i = 0; i < p->segs.size() && st == RK_OK; ++i) {
-        const uint64_t dims[3] = {64, static_cast<uint64_t>(p->segs[i].n), 9};
-        const uint64_t strides[2] = {576 * 2, 128};
+        const uint64_t dims[3] = {64, static_cast<uint64_t>(p->segs[i].n), nch};
+        const uint64_t strides[2] = {static_cast<uint64_t>(nch) * 128, 128};
         const uint32_t boxes[rk::kSegMaps][3] = {
-            {64, 128, 2}, {64, 128, 1}, {64, 64, 4}, {64, 64, 1}, {64, 64, 9}, {64, 128, 4}};
+            {64, 128, 2}, {64, 128, 1}, {64, 64, 4}, {64, 64, 1}, {64, 64, nch}, {64, 128, 4}};
         for (int b = 0; b < rk::kSegMaps && st == RK_OK; ++b)
           if (!rk::make_tmap_bf16(&p->segmaps[rk::kSegMaps * i + b], p->segs[i].latent, 3, dims,
                                   strides, boxes[b]))
@@ -700,7 +743,7 @@ rk_status_t bind_workspace(const rk_seg_attn_plan_s& p, rk::KernelArgs& a, void*
   if (!p.num_parts) return RK_OK;
   char* w = static_cast<char*>(workspace);
   a.ws_o = reinterpret_cast<float*>(w);
-  size_t off = static_cast<size_t>(p.num_parts) * kSplitHeads * p.d_nope * sizeof(float);
+  size_t off = static_cast<size_t>(p.num_parts) * kSplitHeads * p.d_v * sizeof(float);
   a.ws_lse = reinterpret_cast<float*>(w + off);
   off += static_cast<size_t>(p.num_parts) * kSplitHeads * sizeof(float);
   off = (off + 255) & ~size_t(255);
@@ -752,7 +795,7 @@ extern "C" rk_status_t rk_seg_attn_forward_host(rk_seg_attn_plan_t p, const void
   constexpr int NC = rk_seg_attn_plan_s::kHostChunks;
   const int64_t rows = p->info.rows, H = p->H;
   const size_t qrow = static_cast<size_t>(H) * (p->d_nope + p->d_rope) * 2;
-  const size_t orow = static_cast<size_t>(H) * p->d_nope * 2, lrow = static_cast<size_t>(H) * 4;
+  const size_t orow = static_cast<size_t>(H) * p->d_v * 2, lrow = static_cast<size_t>(H) * 4;
   const int64_t CR = p->chunk_rows > 0 ? p->chunk_rows : rows;
   auto range = [&](int c, int64_t& r0, int64_t& r1) {
     r0 = std::min<int64_t>(rows, c * CR);
@@ -866,6 +909,10 @@ void fill_args(const rk_seg_attn_plan_s& p, KernelArgs& a, const void* q, void* 
   a.decmaps = p.d_decmaps;
   a.tc_pairs = p.d_tc_pairs;
   a.num_tc_pairs = static_cast<int32_t>(p.tc_pairs.size());
+  a.v_rope = p.v_rope ? 1 : 0;
+  a.d_v = p.d_v;
+  a.pos_cs_hi = p.d_pos_cs_hi;
+  a.pos_cs_lo = p.d_pos_cs_lo;
 }
 
 cudaError_t launch_forward(const rk_seg_attn_plan_s& p, const KernelArgs& a, const void* q,

@@ -127,6 +127,10 @@ struct KernelArgs {
   const CUtensorMap* decmaps; // per segment: latent viewed (64, n, 9 chunks), box 32 rows x 9 chunks
   const TcPair* tc_pairs;
   int32_t num_tc_pairs;
+  int32_t v_rope;             // V is the whole latent row (d_v = d_k), output phase restored
+  int32_t d_v;                // output columns
+  const float* pos_cs_hi;     // [T / 256 + 1][d_rope/2][2] cos, sin of 256 a theta   (v_rope)
+  const float* pos_cs_lo;     // [256][d_rope/2][2] cos, sin of b theta              (v_rope)
 };
 
 }  // namespace rk
@@ -135,6 +139,8 @@ struct rk_seg_attn_plan_s {
   int device = -1;
   bool host_only = false;
   int32_t H = 0, d_nope = 0, d_rope = 0;
+  int32_t d_v = 0;
+  bool v_rope = false;
   int32_t sink = 0, window = 0;
   float softmax_scale = 0.f;
   int kernel = 0;          // 0 mma.sync, 1 tcgen05 tiles, 2 CTA-pair tiles, 3 4-CTA tiles
@@ -145,6 +151,7 @@ struct rk_seg_attn_plan_s {
   std::vector<rk::DevSeg> segs;
   std::vector<rk::DevReq> reqs;
   std::vector<float> rope_cs;
+  std::vector<float> pos_cs_hi, pos_cs_lo;
   std::vector<rk::DenseTile> tiles;
   std::vector<int32_t> local_rows;
   std::vector<int32_t> global_heads, local_heads;
@@ -160,6 +167,8 @@ struct rk_seg_attn_plan_s {
   rk::DevSeg* d_segs = nullptr;
   rk::DevReq* d_reqs = nullptr;
   float* d_rope_cs = nullptr;
+  float* d_pos_cs_hi = nullptr;
+  float* d_pos_cs_lo = nullptr;
   rk::DenseTile* d_tiles = nullptr;
   int32_t* d_local_rows = nullptr;
   int32_t* d_global_heads = nullptr;

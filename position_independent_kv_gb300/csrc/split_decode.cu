@@ -25,13 +25,14 @@ constexpr int THREADS = 128;
 constexpr int TK = 64;        // keys per shared-memory tile (16 per warp)
 constexpr int NH = 8;         // heads per chunk
 
-template <int DN, int DR>
+template <int DN, int DR, bool VROPE>
 struct SCfg {
   static constexpr int DK = DN + DR;
+  static constexpr int DV = VROPE ? DK : DN;  // V = c_nope, or the whole latent row
   static constexpr int QS = DN + 2 * DR + 8;
   static constexpr int KS = DK + 8;
   static constexpr int PS = TK + 8;
-  static constexpr int DVW = DN / 4;       // d_v rows per warp
+  static constexpr int DVW = DV / 4;       // d_v rows per warp
   static constexpr int MT = DVW / 16;      // output m-tiles per warp
   static constexpr int KSTEPS = (DN + 2 * DR) / 16;
   static constexpr size_t Q_BYTES = size_t(NH) * QS * 2;
@@ -41,9 +42,9 @@ struct SCfg {
   static constexpr size_t SMEM = Q_BYTES + QRO_BYTES + 2 * K_BYTES + P_BYTES + 2 * 4 * NH * 4 + 16;
 };
 
-template <int DN, int DR>
+template <int DN, int DR, bool VROPE>
 __global__ void __launch_bounds__(THREADS, 1) split_decode_kernel(const KernelArgs a) {
-  using C = SCfg<DN, DR>;
+  using C = SCfg<DN, DR, VROPE>;
   extern __shared__ __align__(128) uint8_t smem[];
   uint16_t* Qs = reinterpret_cast<uint16_t*>(smem);
   uint16_t* Qro = reinterpret_cast<uint16_t*>(smem + C::Q_BYTES);
@@ -250,7 +251,7 @@ __global__ void __launch_bounds__(THREADS, 1) split_decode_kernel(const KernelAr
   for (int e = 0; e < 2; ++e)
     lt[e] = red_l[2 * t4 + e] + red_l[NH + 2 * t4 + e] + red_l[2 * NH + 2 * t4 + e] +
             red_l[3 * NH + 2 * t4 + e];
-  float* wo = a.ws_o + int64_t(ch.part) * NH * DN;
+  float* wo = a.ws_o + int64_t(ch.part) * NH * C::DV;
 #pragma unroll
   for (int mt = 0; mt < C::MT; ++mt) {
     const int d0 = warp * C::DVW + mt * 16 + g;
@@ -258,8 +259,22 @@ __global__ void __launch_bounds__(THREADS, 1) split_decode_kernel(const KernelAr
     for (int e = 0; e < 2; ++e) {
       const int h = 2 * t4 + e;
       const float inv = 1.f / lt[e];
-      wo[h * DN + d0] = o[mt][e] * inv;
-      wo[h * DN + d0 + 8] = o[mt][2 + e] * inv;
+      wo[h * C::DV + d0] = o[mt][e] * inv;
+      wo[h * C::DV + d0 + 8] = o[mt][2 + e] * inv;
+    }
+  }
+  if (VROPE) {
+    // the chunk lies in one segment: R(+delta) restores its output phase
+    // before the merge (RedKnot-MLA paper, RoPE-orthogonality paragraph)
+    __syncthreads();
+    const float* cs = a.rope_cs + int64_t(ch.seg) * DR;
+    for (int idx = tid; idx < NH * (DR / 2); idx += THREADS) {
+      const int h = idx / (DR / 2), k = idx - h * (DR / 2);
+      float* w2 = wo + h * C::DV + DN + 2 * k;
+      const float c = cs[2 * k], sn = cs[2 * k + 1];
+      const float x = w2[0], y = w2[1];
+      w2[0] = x * c - y * sn;
+      w2[1] = fmaf(x, sn, y * c);
     }
   }
   if (warp == 0 && g == 0) {
@@ -282,15 +297,30 @@ __global__ void __launch_bounds__(THREADS, 1) split_decode_kernel(const KernelAr
     for (int j = 0; j < ch.nparts; ++j)
       ssum += __expf(__ldcg(a.ws_lse + int64_t(ch.part_first + j) * NH + h) - m);
     const int head = a.global_heads[hbase + h];
-    uint16_t* dst = a.out + (frow * a.H + head) * DN;
-    for (int d = tid; d < DN; d += THREADS) {
-      float acc = 0.f;
+    uint16_t* dst = a.out + (frow * a.H + head) * C::DV;
+    for (int d = 2 * tid; d < C::DV; d += 2 * THREADS) {
+      float acc0 = 0.f, acc1 = 0.f;
       for (int j = 0; j < ch.nparts; ++j) {
         const int64_t pj = ch.part_first + j;
         const float w = __expf(__ldcg(a.ws_lse + pj * NH + h) - m);
-        acc += w * __ldcg(a.ws_o + (pj * NH + h) * DN + d);
+        acc0 += w * __ldcg(a.ws_o + (pj * NH + h) * C::DV + d);
+        acc1 += w * __ldcg(a.ws_o + (pj * NH + h) * C::DV + d + 1);
       }
-      dst[d] = f32_to_bf16(acc / ssum);
+      acc0 /= ssum;
+      acc1 /= ssum;
+      if (VROPE && d >= DN) {
+        // inverse output RoPE R(-p) at the request's row p = 256 a + b
+        const int k = (d - DN) >> 1, p = rq.q_row_begin;
+        const float* hi = a.pos_cs_hi + int64_t(p >> 8) * DR + 2 * k;
+        const float* lo = a.pos_cs_lo + int64_t(p & 255) * DR + 2 * k;
+        const float pc = fmaf(hi[0], lo[0], -hi[1] * lo[1]);
+        const float ps = fmaf(hi[1], lo[0], hi[0] * lo[1]);
+        const float x = acc0, y = acc1;
+        acc0 = fmaf(x, pc, y * ps);
+        acc1 = fmaf(-x, ps, y * pc);
+      }
+      dst[d] = f32_to_bf16(acc0);
+      dst[d + 1] = f32_to_bf16(acc1);
     }
     if (tid == 0) a.lse[frow * a.H + head] = m + logf(ssum);
   }
@@ -632,10 +662,10 @@ __global__ void __launch_bounds__(DT_THREADS, 1) split_decode_tma_kernel(const K
   }
 }
 
-template <int DN, int DR>
+template <int DN, int DR, bool VROPE>
 cudaError_t launch_t(const KernelArgs& a, cudaStream_t s) {
-  using C = SCfg<DN, DR>;
-  auto k = split_decode_kernel<DN, DR>;
+  using C = SCfg<DN, DR, VROPE>;
+  auto k = split_decode_kernel<DN, DR, VROPE>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(C::SMEM));
   if (e != cudaSuccess) return e;
@@ -689,8 +719,9 @@ cudaError_t launch_split_decode(const rk_seg_attn_plan_s& plan, const KernelArgs
     split_decode_tma_kernel<<<a.num_chunks, DT_THREADS, DT_SMEM, s>>>(a);
     return cudaGetLastError();
   }
-  if (plan.d_nope == 512 && plan.d_rope == 64) return launch_t<512, 64>(a, s);
-  if (plan.d_nope == 128 && plan.d_rope == 32) return launch_t<128, 32>(a, s);
+  if (plan.v_rope && plan.d_nope == 448 && plan.d_rope == 64) return launch_t<448, 64, true>(a, s);
+  if (plan.d_nope == 512 && plan.d_rope == 64) return launch_t<512, 64, false>(a, s);
+  if (plan.d_nope == 128 && plan.d_rope == 32) return launch_t<128, 32, false>(a, s);
   return cudaErrorInvalidValue;
 }
 

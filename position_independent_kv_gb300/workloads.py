@@ -21,7 +21,9 @@ latent  bf16 [n, d_nope + d_rope]  row = [c_nope | k_rope], k_rope rotated at
         the row's canonical position 0..n-1 (interleaved pairs).
 q       bf16 [rows, H, d_nope + d_rope]  q_rope rotated at the row's absolute
         request position.
-out     bf16 [rows, H, d_nope]  pre-filled with the cached Local values.
+out     bf16 [rows, H, d_v]  pre-filled with the cached Local values; d_v =
+        d_nope, or d_k for the workloads whose value carries a rotary part
+        (`v_rope`: V is the whole latent row).
 lse     fp32 [rows, H]  pre-filled with LSE_SENTINEL.
 """
 from __future__ import annotations
@@ -83,6 +85,7 @@ class Workload:
     lse_init: torch.Tensor | None = None   # fp32 [rows, H]
     latent_pool: torch.Tensor | None = None
     notes: dict = field(default_factory=dict)
+    v_rope: bool = False                   # V = the whole latent row (d_v = d_k)
 
     @property
     def d_k(self) -> int:
@@ -90,7 +93,7 @@ class Workload:
 
     @property
     def d_v(self) -> int:
-        return self.d_nope
+        return self.d_k if self.v_rope else self.d_nope
 
     @property
     def scale(self) -> float:
@@ -137,6 +140,7 @@ class Spec:
     decode_len_range: tuple[int, int] = (0, 0)
     decode_seg_range: tuple[int, int] = (0, 0)
     rope_base: float = 10000.0
+    v_rope: bool = False
 
 
 SPECS: dict[str, Spec] = {
@@ -168,6 +172,24 @@ SPECS: dict[str, Spec] = {
                    seg_lengths=[2048] * 6, n_new=4096),
     "tiny_wide": Spec("tiny_wide", 8, 128, 32, 4, 10000, ProtectRule(boundary=16),
                       seg_lengths=[256, 256], n_new=64, shuffle=False),
+    # a value that carries a rotary part (V = the whole latent row, output
+    # phase restored): the long-context and decode geometries with a 512-wide
+    # latent row of 448 nope + 64 rope dims, and reduced versions for parity
+    "ctx128k_vrope": Spec("ctx128k_vrope", 128, 448, 64, 4, 256,
+                          ProtectRule(boundary=128, budget=0.25),
+                          seg_lengths=[2048] * 48, n_new=32768, v_rope=True),
+    "decode_vrope": Spec("decode_vrope", 64, 448, 64, 4, 256, ProtectRule(none=True),
+                         decode_requests=64, decode_len_range=(8192, 65536),
+                         decode_seg_range=(4, 32), v_rope=True),
+    "flash_vrope_mini": Spec("flash_vrope_mini", 64, 448, 64, 4, 256,
+                             ProtectRule(boundary=24, p_random=0.10),
+                             seg_lengths=[300, 257, 190], n_new=77, v_rope=True),
+    "ctx128k_vrope_mini": Spec("ctx128k_vrope_mini", 128, 448, 64, 4, 256,
+                               ProtectRule(boundary=24, budget=0.25),
+                               seg_lengths=[130] * 5, n_new=203, v_rope=True),
+    "decode_vrope_mini": Spec("decode_vrope_mini", 64, 448, 64, 4, 256, ProtectRule(none=True),
+                              decode_requests=5, decode_len_range=(300, 1500),
+                              decode_seg_range=(2, 6), v_rope=True),
 }
 
 
@@ -225,7 +247,8 @@ def make_geometry(name: str, seed: int = 0) -> Workload:
         req.perm = rng.permutation(req.T).astype(np.int64)
     return Workload(name=name, H=spec.H, d_nope=spec.d_nope, d_rope=spec.d_rope,
                     rope_base=spec.rope_base, sink=spec.sink, window=spec.window,
-                    head_role=_roles(spec.H), requests=requests, rule=spec.rule)
+                    head_role=_roles(spec.H), requests=requests, rule=spec.rule,
+                    v_rope=spec.v_rope)
 
 
 def _randn_bf16(shape, gen: torch.Generator, device, std: float, chunk_rows: int = 2048) -> torch.Tensor:

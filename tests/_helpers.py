@@ -75,7 +75,7 @@ def oracle_rows(wl, prot_rows, rows_per_req=None):
         li = wl.lse_init[fl].double().cpu().numpy()
         Oo, Lo = O.seg_attn_request(q, segs, req.T, req.q_row_begin, wl.head_role, wl.d_nope,
                                     wl.rope_base, wl.scale, wl.sink, wl.window, prot_rows[r],
-                                    oi, li, rows=rows, sampled=True)
+                                    oi, li, rows=rows, sampled=True, v_rope=wl.v_rope)
         res.append((flat, Oo, Lo))
     return res
 

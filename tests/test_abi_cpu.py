@@ -60,7 +60,7 @@ def _host_plan(name, **over):
     kw = dict(segments=segs, seg_begin=begins, q_row_begin=[r.q_row_begin for r in wl.requests],
               num_heads=wl.H, d_nope=wl.d_nope, d_rope=wl.d_rope, rope_base=wl.rope_base,
               softmax_scale=wl.scale, head_role=wl.head_role, sink=wl.sink, window=wl.window,
-              bitmap=bm, flags=B.RK_PLAN_HOST_ONLY)
+              bitmap=bm, flags=B.RK_PLAN_HOST_ONLY | (B.RK_PLAN_V_ROPE if wl.v_rope else 0))
     kw.update(over)
     return wl, B.SegAttnPlan(**kw)
 
@@ -120,7 +120,8 @@ def test_lse_merge_argument_errors():
 
 
 @pytest.mark.parametrize("name", ["tiny", "flash_mini", "varlen_mini", "ctx128k_mini",
-                                  "decode_mini", "tiny_wide", "flash", "decode"])
+                                  "decode_mini", "tiny_wide", "flash", "decode",
+                                  "flash_vrope_mini", "ctx128k_vrope_mini", "decode_vrope_mini"])
 def test_plan_counts_attended_pairs(name):
     """The plan's pair accounting equals the oracle's visibility rule summed
     over the computed rows (Global heads) and the protected computed rows
@@ -168,3 +169,30 @@ def test_pair_plan_work_bounds(name):
     assert a["dense_tiles"] == b["dense_tiles"]
     assert a["performed_pairs"] <= b["performed_pairs"] * 9 // 8
     assert a["performed_pairs"] >= a["pairs_global"] + a["pairs_local"]
+
+
+def test_vrope_plan_rules():
+    """RK_PLAN_V_ROPE: the value is the whole latent row (d_v = d_k = 512 for
+    d = (448, 64)); it runs on the 4-CTA kernel and the split decode kernel
+    only, and needs exactly those dims."""
+    V = B.RK_PLAN_HOST_ONLY | B.RK_PLAN_V_ROPE
+    wl, plan = _host_plan("flash_vrope_mini", flags=V)
+    info = plan.info
+    assert info["kernel"] == 3 and info["d_v"] == 512 and info["d_nope"] == 448
+    assert _host_plan("flash_mini")[1].info["d_v"] == 512
+    assert _host_plan("tiny")[1].info["d_v"] == 128
+    for name, flags in [("flash_mini", V),                          # (512, 64) with the flag
+                        ("flash_vrope_mini", B.RK_PLAN_HOST_ONLY),  # (448, 64) without it
+                        ("flash_vrope_mini", V | B.RK_PLAN_LEGACY_MMA),
+                        ("flash_vrope_mini", V | B.RK_PLAN_SINGLE_CTA),
+                        ("flash_vrope_mini", V | B.RK_PLAN_CTA_PAIR)]:
+        with pytest.raises(B.RkError) as ei:
+            _host_plan(name, flags=flags)
+        assert ei.value.status == 5, (name, flags)
+    # decode: same geometry as decode_mini; the partials are d_k wide
+    _, pd = _host_plan("decode_vrope_mini", flags=V)
+    _, pn = _host_plan("decode_mini")
+    assert pd.info["split_chunks"] == pn.info["split_chunks"] > 0
+    parts = pd.info["split_chunks"]
+    body = ((parts * 8 * 512 * 4 + parts * 8 * 4 + 255) // 256) * 256
+    assert body < pd.workspace_bytes <= body + 256 + 4 * parts
