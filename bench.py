@@ -59,8 +59,9 @@ def workload_desc(name: str) -> str:
     else:
         prot = f"protected: query rows + boundary {r.boundary}"
     out = f", {int(round(100 * sp.outlier_frac))}% outlier rows x8" if sp.outlier_frac else ""
+    vr = ", V = the whole latent row (output phase restored)" if sp.v_rope else ""
     return (f"{name}: {seg}, H={sp.H} ({sp.H - hg} Local/{hg} Global), d_nope={sp.d_nope}, "
-            f"d_rope={sp.d_rope}, sink={sp.sink}, w={sp.window}, {prot}, "
+            f"d_rope={sp.d_rope}{vr}, sink={sp.sink}, w={sp.window}, {prot}, "
             f"bf16 N(0,1)/sqrt({sp.d_nope + sp.d_rope}){out}, seed 0")
 
 
@@ -222,8 +223,10 @@ def sum_over_ranks(x: float, ws: int) -> float:
     return _reduce(x, ws, "sum")
 
 
-def prefill_flops(info, d_nope, d_rope):
-    per_pair = 2 * (d_nope + d_rope) + 2 * d_nope
+def prefill_flops(info, d_k, d_v):
+    """Algorithmic and performed FLOPs: 2 d_k (scores) + 2 d_v (P V) per
+    attended, resp. issued, (row, head, key) pair."""
+    per_pair = 2 * d_k + 2 * d_v
     return per_pair * (info["pairs_global"] + info["pairs_local"]), per_pair * info["performed_pairs"]
 
 
@@ -252,7 +255,7 @@ def bench_prefill(args, ws, local, pk):
     if plan.workspace_bytes:
         ws_buf = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
     out, lse = wl.out_init, wl.lse_init          # forward overwrites in place
-    alg_flops, perf_flops = prefill_flops(info, wl.d_nope, wl.d_rope)
+    alg_flops, perf_flops = prefill_flops(info, wl.d_k, wl.d_v)
 
     for _ in range(args.warmup):
         plan.forward(wl.q, out, lse, ws_buf, stream=stream)
@@ -359,6 +362,65 @@ def bench_decode(args, local):
     plan.close()
     del flush
     return dict(ms=ms, bytes=byt, gbs=byt / (ms * 1e-3) / 1e9, ok=ok, info=info)
+
+
+def bench_vrope(local: int, pk: dict) -> dict:
+    """The rotary-value path (V = the whole latent row, output phase
+    restored; d = 448 + 64): the long-context prefill (CUDA events, 3 warm-ups,
+    median of 3 launches) and the decode batch (L2 flushed, median of 20)."""
+    import torch
+    from position_independent_kv_gb300 import binding as B
+    from position_independent_kv_gb300.protected import build_bitmap
+    from position_independent_kv_gb300.workloads import make_workload
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    res = {}
+    ok = True
+    for name in ("ctx128k_vrope", "decode_vrope"):
+        wl = make_workload(name, seed=0, device=dev)
+        bm, _ = build_bitmap(wl)
+        plan = B.SegAttnPlan.from_workload(wl, bitmap=bm, stream=stream)
+        ws_buf = torch.empty(max(16, plan.workspace_bytes), dtype=torch.uint8, device=dev)
+        flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev) \
+            if name.startswith("decode") else None
+        out, lse = wl.out_init, wl.lse_init
+        for _ in range(3):
+            plan.forward(wl.q, out, lse, ws_buf, stream=stream)
+        torch.cuda.synchronize(dev)
+        times = []
+        for _ in range(20 if flush is not None else 3):
+            if flush is not None:
+                flush.zero_()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            plan.forward(wl.q, out, lse, ws_buf, stream=stream)
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            times.append(a.elapsed_time(b))
+        ok = ok and plan.device_status(stream=stream) == 0
+        ms = statistics.median(times)
+        info = plan.info
+        if flush is None:
+            alg, perf = prefill_flops(info, wl.d_k, wl.d_v)
+            res["prefill"] = {"workload": workload_desc(name), "ms": round(ms, 3),
+                              "tflops": round(alg / (ms * 1e-3) / 1e12, 1),
+                              "performed_tflops": round(perf / (ms * 1e-3) / 1e12, 1),
+                              "frac_of_peak": round(alg / (ms * 1e-3) / 1e12 / pk["bf16_tflops"], 4),
+                              "kernel": info["kernel"]}
+        else:
+            byt = decode_bytes(wl)
+            gbs = byt / (ms * 1e-3) / 1e9
+            res["decode"] = {"workload": workload_desc(name), "ms": round(ms, 4),
+                             "GB/s": round(gbs, 1), "bytes": byt,
+                             "frac_of_hbm": round(gbs / pk["hbm_gbs"], 4),
+                             "l2": "256 MB flush between iterations"}
+        plan.close()
+        del wl, out, lse, ws_buf, flush
+        torch.cuda.empty_cache()
+    res["status_ok"] = ok
+    res["flop_per_pair"] = 2 * 512 + 2 * 512
+    return res
 
 
 def bench_protected_builder(name: str, local: int) -> dict:
@@ -530,6 +592,9 @@ def run_ours(args):
     proj = None
     if not args.no_projection and rank == 0:
         proj = bench_projection(local, args.projection_workload)
+    vrope = None
+    if not args.no_vrope and rank == 0:
+        vrope = bench_vrope(local, pk)
     line = None
     if rank == 0:
         info = res["info"]
@@ -566,6 +631,8 @@ def run_ours(args):
         if proj:
             proj["frac_of_peak"] = round(proj["tflops"] / peak, 4)
             line["projection"] = proj
+        if vrope:
+            line["v_rope"] = vrope
         if dec:
             line["decode"] = {"workload": "64 requests x 1 row, 4-32 segments, 8K-64K keys, "
                                           "H=64 (56/8), split over segments + fused LSE merge",
@@ -632,6 +699,8 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-projection", action="store_true",
                     help="skip the timing of the projected-state / W_b step")
+    ap.add_argument("--no-vrope", action="store_true",
+                    help="skip the timing of the rotary-value (output-phase restore) path")
     ap.add_argument("--projection-workload", default="ctx128k",
                     help="rows and protected rows of this workload feed the projection step")
     ap.add_argument("--no-builder", action="store_true",

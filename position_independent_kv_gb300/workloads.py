@@ -181,6 +181,9 @@ SPECS: dict[str, Spec] = {
     "decode_vrope": Spec("decode_vrope", 64, 448, 64, 4, 256, ProtectRule(none=True),
                          decode_requests=64, decode_len_range=(8192, 65536),
                          decode_seg_range=(4, 32), v_rope=True),
+    "ctx16k_vrope": Spec("ctx16k_vrope", 128, 448, 64, 4, 256,
+                         ProtectRule(boundary=128, budget=0.25),
+                         seg_lengths=[2048] * 6, n_new=4096, v_rope=True),
     "flash_vrope_mini": Spec("flash_vrope_mini", 64, 448, 64, 4, 256,
                              ProtectRule(boundary=24, p_random=0.10),
                              seg_lengths=[300, 257, 190], n_new=77, v_rope=True),
