@@ -423,6 +423,86 @@ def bench_vrope(local: int, pk: dict) -> dict:
     return res
 
 
+def bench_seg_paged(local: int, pk: dict) -> dict:
+    """SegPagedAttention on GQA pages (Qwen3-32B shape, 1 Global KV head in
+    8): the 128K-token prefill on the paged walk and on the dense + mask arm
+    (CUDA events, 3 warm-ups, median of 3), and 64 decode steps whose Local
+    heads keep only sink and window pages (L2 flushed, median of 20)."""
+    import torch
+    from position_independent_kv_gb300 import binding as B
+    from position_independent_kv_gb300.paged_workloads import make_paged_workload
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    res = {}
+    ok = True
+
+    def timed(plan, pw, out, lse, n, flush=None):
+        for _ in range(3):
+            plan.forward(pw.q, pw.k_pages, pw.v_pages, out, lse, stream=stream)
+        torch.cuda.synchronize(dev)
+        ts = []
+        for _ in range(n):
+            if flush is not None:
+                flush.zero_()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            plan.forward(pw.q, pw.k_pages, pw.v_pages, out, lse, stream=stream)
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            ts.append(a.elapsed_time(b))
+        return statistics.median(ts), plan.device_status(stream=stream) == 0
+
+    pw = make_paged_workload("qwen32b_128k", seed=0, device=dev)
+    out = torch.empty((pw.rows, pw.Hq, 128), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((pw.rows, pw.Hq), dtype=torch.float32, device=dev)
+    for flags, key in ((0, "prefill"), (B.RK_SEGPAGED_DENSE_MASK, "prefill_dense_mask")):
+        plan = B.SegPagedPlan.from_workload(pw, flags=flags, stream=stream)
+        info = plan.info
+        ms, good = timed(plan, pw, out, lse, 3)
+        ok = ok and good
+        alg = 512.0 * info["pairs"]
+        res[key] = {"ms": round(ms, 3), "tflops": round(alg / (ms * 1e-3) / 1e12, 1),
+                    "performed_tflops": round(512.0 * info["performed_pairs"] / (ms * 1e-3) / 1e12, 1),
+                    "frac_of_peak": round(alg / (ms * 1e-3) / 1e12 / pk["bf16_tflops"], 4),
+                    "kv_blocks": info["kv_blocks"], "tiles": info["tiles"]}
+        plan.close()
+    res["prefill"]["workload"] = ("qwen32b_128k: 1 x 131072 tokens, 64 query heads over 8 KV heads "
+                                  "(d 128, 1 Global), per-head pages of 128 tokens, sink 4, w 256, "
+                                  "bf16 N(0,1)/sqrt(128), seed 0")
+    res["dense_mask_over_paged"] = round(res["prefill_dense_mask"]["ms"] / res["prefill"]["ms"], 2)
+    del pw, out, lse
+    torch.cuda.empty_cache()
+    pw = make_paged_workload("qwen32b_decode", seed=0, device=dev)
+    out = torch.empty((pw.rows, pw.Hq, 128), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((pw.rows, pw.Hq), dtype=torch.float32, device=dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    plan = B.SegPagedPlan.from_workload(pw, stream=stream)
+    ms, good = timed(plan, pw, out, lse, 20, flush)
+    ok = ok and good
+    # algorithmic bytes: the K and V rows each KV head's decode row sees, plus q, out, lse
+    byt = 0
+    for T in pw.seq_len:
+        T = int(T)
+        p = T - 1
+        for g in range(pw.Hkv):
+            n = p + 1 if pw.kv_role[g] else (p + 1 if max(0, p - pw.window) <= pw.sink
+                                            else min(pw.sink, p + 1) + pw.window + 1)
+            byt += n * 128 * 2 * 2
+        byt += pw.Hq * (256 + 256 + 4)
+    gbs = byt / (ms * 1e-3) / 1e9
+    res["decode"] = {"workload": "qwen32b_decode: 64 requests x 1 row over 8K-64K tokens, Local "
+                                 "heads keep sink + window pages only", "ms": round(ms, 4),
+                     "GB/s": round(gbs, 1), "bytes": byt, "frac_of_hbm": round(gbs / pk["hbm_gbs"], 4),
+                     "pages": pw.num_pages, "l2": "256 MB flush between iterations"}
+    plan.close()
+    del pw, out, lse, flush
+    torch.cuda.empty_cache()
+    res["status_ok"] = ok
+    res["flop_per_pair"] = 512
+    return res
+
+
 def bench_protected_builder(name: str, local: int) -> dict:
     """rk_protected_build on a workload's geometry (device time per build,
     CUDA events, median of 20 after 3 warm-ups)."""
@@ -595,6 +675,9 @@ def run_ours(args):
     vrope = None
     if not args.no_vrope and rank == 0:
         vrope = bench_vrope(local, pk)
+    paged = None
+    if not args.no_paged and rank == 0:
+        paged = bench_seg_paged(local, pk)
     line = None
     if rank == 0:
         info = res["info"]
@@ -633,6 +716,8 @@ def run_ours(args):
             line["projection"] = proj
         if vrope:
             line["v_rope"] = vrope
+        if paged:
+            line["seg_paged_gqa"] = paged
         if dec:
             line["decode"] = {"workload": "64 requests x 1 row, 4-32 segments, 8K-64K keys, "
                                           "H=64 (56/8), split over segments + fused LSE merge",
@@ -699,6 +784,8 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-projection", action="store_true",
                     help="skip the timing of the projected-state / W_b step")
+    ap.add_argument("--no-paged", action="store_true",
+                    help="skip the timing of SegPagedAttention on GQA pages")
     ap.add_argument("--no-vrope", action="store_true",
                     help="skip the timing of the rotary-value (output-phase restore) path")
     ap.add_argument("--projection-workload", default="ctx128k",

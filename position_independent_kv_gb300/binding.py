@@ -27,12 +27,36 @@ EXPORTS = ["rk_seg_attn_plan", "rk_seg_attn_plan_destroy", "rk_seg_attn_plan_inf
            "rk_seg_attn_workspace_bytes", "rk_seg_attn_forward", "rk_lse_merge",
            "rk_seg_attn_last_device_status", "rk_status_string",
            "rk_seg_attn_forward_noalloc", "rk_seg_attn_forward_host",
-           "rk_protected_workspace_bytes", "rk_protected_build", "rk_project_forward"]
+           "rk_protected_workspace_bytes", "rk_protected_build", "rk_project_forward",
+           "rk_segpaged_plan", "rk_segpaged_forward", "rk_segpaged_plan_info",
+           "rk_segpaged_last_device_status", "rk_segpaged_plan_destroy"]
+
+RK_SEGPAGED_HOST_ONLY = 1
+RK_SEGPAGED_DENSE_MASK = 2
 
 STATUS = {0: "RK_OK", 1: "RK_ERR_NULL", 2: "RK_ERR_INVALID_ARG", 3: "RK_ERR_SEGMENT_OVERLAP",
           4: "RK_ERR_SEGMENT_GAP", 5: "RK_ERR_UNSUPPORTED_DIMS", 6: "RK_ERR_CAPACITY",
           7: "RK_ERR_CUDA", 8: "RK_ERR_DEVICE_TIMEOUT", 9: "RK_ERR_PLAN_MISMATCH",
           10: "RK_ERR_ALIGNMENT", 11: "RK_ERR_WORKSPACE"}
+
+
+class RkSegPagedDesc(C.Structure):
+    _fields_ = [("num_requests", C.c_int32), ("seq_len", C.POINTER(C.c_int64)),
+                ("q_row_begin", C.POINTER(C.c_int64)), ("num_q_heads", C.c_int32),
+                ("num_kv_heads", C.c_int32), ("head_dim", C.c_int32), ("page_size", C.c_int32),
+                ("num_pages", C.c_int64), ("max_blocks", C.c_int32),
+                ("block_table", C.POINTER(C.c_int32)), ("kv_head_role", C.POINTER(C.c_uint8)),
+                ("sink", C.c_int32), ("window", C.c_int32), ("softmax_scale", C.c_float),
+                ("flags", C.c_uint32)]
+
+
+class RkSegPagedInfo(C.Structure):
+    _fields_ = [("rows", C.c_int64), ("tiles", C.c_int64), ("pairs", C.c_int64),
+                ("performed_pairs", C.c_int64), ("kv_blocks", C.c_int64), ("group", C.c_int32),
+                ("reserved", C.c_int32)]
+
+    def as_dict(self):
+        return {k: getattr(self, k) for k, _ in self._fields_ if k != "reserved"}
 
 
 class RkSegment(C.Structure):
@@ -118,6 +142,17 @@ def lib() -> C.CDLL:
         L.rk_lse_merge.restype = C.c_int
         L.rk_seg_attn_last_device_status.argtypes = [C.c_void_p, C.c_void_p]
         L.rk_seg_attn_last_device_status.restype = C.c_int
+        L.rk_segpaged_plan.argtypes = [C.POINTER(RkSegPagedDesc), C.c_void_p,
+                                       C.POINTER(C.c_void_p)]
+        L.rk_segpaged_plan.restype = C.c_int
+        L.rk_segpaged_forward.argtypes = [C.c_void_p] * 7
+        L.rk_segpaged_forward.restype = C.c_int
+        L.rk_segpaged_plan_info.argtypes = [C.c_void_p, C.POINTER(RkSegPagedInfo)]
+        L.rk_segpaged_plan_info.restype = C.c_int
+        L.rk_segpaged_last_device_status.argtypes = [C.c_void_p, C.c_void_p]
+        L.rk_segpaged_last_device_status.restype = C.c_int
+        L.rk_segpaged_plan_destroy.argtypes = [C.c_void_p]
+        L.rk_segpaged_plan_destroy.restype = None
         L.rk_status_string.argtypes = [C.c_int]
         L.rk_status_string.restype = C.c_char_p
         _lib = L
@@ -305,3 +340,70 @@ def protected_workspace_bytes(num_requests: int, num_segments: int) -> int:
 
 def status_string(st: int) -> str:
     return lib().rk_status_string(int(st)).decode()
+
+
+class SegPagedPlan:
+    """rk_segpaged_plan / rk_segpaged_forward (SegPagedAttention on GQA).
+
+    seq_len, q_row_begin: [R]; block_table: int32 [R, Hkv, max_blocks]
+    (physical page or -1); kv_role: uint8 [Hkv] (1 = Global)."""
+
+    def __init__(self, seq_len, q_row_begin, num_q_heads, num_kv_heads, block_table, num_pages,
+                 kv_role, sink, window, softmax_scale, flags=0, stream=None, head_dim=128,
+                 page_size=128):
+        L = lib()
+        sl = np.ascontiguousarray(seq_len, dtype=np.int64)
+        qb = np.ascontiguousarray(q_row_begin, dtype=np.int64)
+        tab = np.ascontiguousarray(block_table, dtype=np.int32)
+        role = np.ascontiguousarray(kv_role, dtype=np.uint8)
+        d = RkSegPagedDesc()
+        d.num_requests = len(sl)
+        d.seq_len = sl.ctypes.data_as(C.POINTER(C.c_int64))
+        d.q_row_begin = qb.ctypes.data_as(C.POINTER(C.c_int64))
+        d.num_q_heads = int(num_q_heads)
+        d.num_kv_heads = int(num_kv_heads)
+        d.head_dim = int(head_dim)
+        d.page_size = int(page_size)
+        d.num_pages = int(num_pages)
+        d.max_blocks = int(tab.shape[-1])
+        d.block_table = tab.ctypes.data_as(C.POINTER(C.c_int32))
+        d.kv_head_role = role.ctypes.data_as(C.POINTER(C.c_uint8))
+        d.sink = int(sink)
+        d.window = int(window)
+        d.softmax_scale = float(softmax_scale)
+        d.flags = int(flags)
+        handle = C.c_void_p()
+        host_only = bool(flags & RK_SEGPAGED_HOST_ONLY)
+        _check(L.rk_segpaged_plan(C.byref(d), 0 if host_only else _stream(stream),
+                                  C.byref(handle)), "rk_segpaged_plan")
+        self._h = handle
+
+    @classmethod
+    def from_workload(cls, pw, flags=0, stream=None):
+        return cls(pw.seq_len, pw.q_row_begin, pw.Hq, pw.Hkv, pw.block_table, pw.num_pages,
+                   pw.kv_role, pw.sink, pw.window, pw.scale, flags=flags, stream=stream)
+
+    @property
+    def info(self) -> dict:
+        inf = RkSegPagedInfo()
+        _check(lib().rk_segpaged_plan_info(self._h, C.byref(inf)), "rk_segpaged_plan_info")
+        return inf.as_dict()
+
+    def forward(self, q, k_pages, v_pages, out, lse, stream=None):
+        _check(lib().rk_segpaged_forward(self._h, _ptr(q), _ptr(k_pages), _ptr(v_pages),
+                                         _ptr(out), _ptr(lse), _stream(stream)),
+               "rk_segpaged_forward")
+
+    def device_status(self, stream=None) -> int:
+        return int(lib().rk_segpaged_last_device_status(self._h, _stream(stream)))
+
+    def close(self):
+        if getattr(self, "_h", None):
+            lib().rk_segpaged_plan_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

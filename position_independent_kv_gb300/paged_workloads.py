@@ -1,0 +1,161 @@
+"""Seeded synthetic inputs for SegPagedAttention on grouped-query attention.
+
+This module only draws numbers and lays out pages; it holds none of the
+method's arithmetic (no masking, no softmax).  The CUDA path and the CPU
+oracle both consume what it returns.
+
+Shapes follow the RedKnot blog ("RedKnot, explained", "Insight 3"): a model
+"shaped like Qwen3-32B" -- 64 query heads over 8 KV heads of dimension 128 --
+with its KV cache stored per KV head in pages; one KV head in eight is
+Global, the rest Local with the MLA workloads' sink 4 and window 256 (the
+blog's worked example).  A page holds 128 tokens of one KV head; the physical
+pages of all (request, KV head, block) triples are a seeded permutation of
+the page pool.  Where `local_pages_only` is set (decode steps), a Local head
+keeps only the pages of its sink and its window, the memory claim of the
+blog; the others are absent (-1) and not allocated.
+
+Tensors: q bf16 [rows, Hq, 128] (RoPE already at absolute positions),
+k_pages / v_pages bf16 [pages, 128, 128], out bf16 [rows, Hq, 128], lse fp32
+[rows, Hq].  Values are i.i.d. N(0, 1) / sqrt(128) drawn in fp32 and cast to
+bf16; q_scale multiplies the queries (a sharper softmax for tests).
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+PAGE = 128
+HEAD_DIM = 128
+
+
+@dataclass
+class PagedSpec:
+    name: str
+    Hq: int
+    Hkv: int
+    seq_len: list[int]
+    q_row_begin: list[int]          # per request; -1 = the last row (decode)
+    sink: int = 4
+    window: int = 256
+    global_every: int = 8           # KV head g is Global when g % global_every == global_every - 1
+    local_pages_only: bool = False
+
+
+PAGED_SPECS: dict[str, PagedSpec] = {
+    # one 128K-token prefill, Qwen3-32B shape
+    "qwen32b_128k": PagedSpec("qwen32b_128k", 64, 8, [131072], [0]),
+    # a 16K-token version for profiling captures
+    "qwen32b_16k": PagedSpec("qwen32b_16k", 64, 8, [16384], [0]),
+    # 64 decode steps over 8K-64K tokens: Local heads keep sink + window pages
+    "qwen32b_decode": PagedSpec("qwen32b_decode", 64, 8, [], [], local_pages_only=True),
+    # reduced versions the oracle evaluates on every row; ragged last blocks,
+    # several group sizes, Global and Local heads
+    "paged_mini": PagedSpec("paged_mini", 16, 2, [1000, 333], [0, 200], global_every=2),
+    "paged_mini_g4": PagedSpec("paged_mini_g4", 16, 4, [777], [0], global_every=2),
+    "paged_mini_g1": PagedSpec("paged_mini_g1", 4, 4, [530], [0], global_every=4),
+    "paged_mini_g16": PagedSpec("paged_mini_g16", 32, 2, [650], [0], global_every=2),
+    "paged_decode_mini": PagedSpec("paged_decode_mini", 16, 2, [], [], global_every=2,
+                                   local_pages_only=True),
+}
+
+
+@dataclass
+class PagedWorkload:
+    name: str
+    Hq: int
+    Hkv: int
+    seq_len: np.ndarray          # int64 [R]
+    q_row_begin: np.ndarray      # int64 [R]
+    kv_role: np.ndarray          # uint8 [Hkv]
+    block_table: np.ndarray      # int32 [R, Hkv, max_blocks]
+    num_pages: int
+    sink: int
+    window: int
+    q: torch.Tensor | None = None
+    k_pages: torch.Tensor | None = None
+    v_pages: torch.Tensor | None = None
+
+    @property
+    def G(self) -> int:
+        return self.Hq // self.Hkv
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(HEAD_DIM)
+
+    @property
+    def rows(self) -> int:
+        return int((self.seq_len - self.q_row_begin).sum())
+
+    def row_offsets(self) -> list[int]:
+        out, acc = [], 0
+        for T, qb in zip(self.seq_len, self.q_row_begin):
+            out.append(acc)
+            acc += int(T - qb)
+        return out
+
+
+def _decode_lengths(name: str, rng: np.random.Generator):
+    if name == "qwen32b_decode":
+        return [int(x) for x in rng.integers(8192, 65537, size=64)]
+    return [int(x) for x in rng.integers(300, 1501, size=5)]
+
+
+def make_paged_geometry(name: str, seed: int = 0) -> PagedWorkload:
+    sp = PAGED_SPECS[name]
+    rng = np.random.default_rng(seed)
+    if sp.seq_len:
+        lens = list(sp.seq_len)
+        qbs = [qb if qb >= 0 else T - 1 for T, qb in zip(lens, sp.q_row_begin)]
+    else:
+        lens = _decode_lengths(name, rng)
+        qbs = [T - 1 for T in lens]
+    role = np.zeros(sp.Hkv, np.uint8)
+    role[sp.global_every - 1::sp.global_every] = 1
+    R = len(lens)
+    max_blocks = max((T + PAGE - 1) // PAGE for T in lens)
+    table = np.full((R, sp.Hkv, max_blocks), -1, np.int32)
+    keep = []
+    for r, T in enumerate(lens):
+        nb = (T + PAGE - 1) // PAGE
+        for g in range(sp.Hkv):
+            blocks = range(nb)
+            if sp.local_pages_only and not role[g]:
+                # the pages the decode row can see: the sink's and the window's
+                lo = max(0, qbs[r] - sp.window) // PAGE
+                sb = (min(sp.sink, T) + PAGE - 1) // PAGE
+                blocks = sorted(set(range(sb)) | set(range(lo, nb)))
+            for b in blocks:
+                keep.append((r, g, b))
+    perm = rng.permutation(len(keep))
+    for i, (r, g, b) in enumerate(keep):
+        table[r, g, b] = int(perm[i])
+    return PagedWorkload(name=name, Hq=sp.Hq, Hkv=sp.Hkv, seq_len=np.array(lens, np.int64),
+                         q_row_begin=np.array(qbs, np.int64), kv_role=role, block_table=table,
+                         num_pages=len(keep), sink=sp.sink, window=sp.window)
+
+
+def _randn_bf16(shape, gen, device, std, chunk=4096):
+    out = torch.empty(shape, dtype=torch.bfloat16, device=device)
+    for s in range(0, shape[0], chunk):
+        e = min(shape[0], s + chunk)
+        t = torch.randn((e - s,) + tuple(shape[1:]), generator=gen, device=device,
+                        dtype=torch.float32)
+        out[s:e] = (t * std).to(torch.bfloat16)
+    return out
+
+
+def make_paged_workload(name: str, seed: int = 0, device="cpu", q_scale: float = 1.0):
+    """Geometry plus seeded bf16 tensors on `device`."""
+    pw = make_paged_geometry(name, seed)
+    device = torch.device(device)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed * 1000003 + 41)
+    std = 1.0 / math.sqrt(HEAD_DIM)
+    pw.k_pages = _randn_bf16((pw.num_pages, PAGE, HEAD_DIM), gen, device, std)
+    pw.v_pages = _randn_bf16((pw.num_pages, PAGE, HEAD_DIM), gen, device, std)
+    pw.q = _randn_bf16((pw.rows, pw.Hq, HEAD_DIM), gen, device, std * q_scale)
+    return pw

@@ -1,0 +1,138 @@
+"""GPU parity of SegPagedAttention (RedKnot blog, "Insight 3") through the C
+ABI against the fp64 oracle on the same seeded pages."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from _helpers import LSE_ABS, MAX_REL
+from position_independent_kv_gb300 import binding as B
+from position_independent_kv_gb300 import build as BUILD
+from position_independent_kv_gb300.paged_workloads import make_paged_workload
+
+pytestmark = pytest.mark.gpu
+
+# Tolerance of this operation, derived from its arithmetic: P is rounded to
+# bf16 before the P.V contraction (the tensor cores take V in bf16 and both
+# operands share the type).  With the stated inputs the softmax is nearly
+# uniform (score std ~ 1/128), every P lies in (0.97, 1] where the bf16 grid
+# step is 2^-8, so each P carries a relative error of RMS 2^-8 / sqrt(12) =
+# 1.1e-3; an output element is a sum of many terms of random sign, so its
+# relative error is that RMS again, and the bf16 rounding of the output adds
+# a relative RMS of up to 2^-9 / sqrt(3) = 1.1e-3 at the bottom of each
+# binade.  Their sum bounds the mean relative error at 2.3e-3 in the limit;
+# 3e-3 leaves room for sampling noise.  Max and LSE bounds are the main
+# path's.
+MEAN_REL = 3e-3
+
+MINI = ["paged_mini", "paged_mini_g4", "paged_mini_g1", "paged_mini_g16", "paged_decode_mini"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    BUILD.build()
+
+
+def run(pw, flags=0):
+    plan = B.SegPagedPlan.from_workload(pw, flags=flags)
+    out = torch.full((pw.rows, pw.Hq, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((pw.rows, pw.Hq), float("nan"), dtype=torch.float32, device="cuda")
+    plan.forward(pw.q, pw.k_pages, pw.v_pages, out, lse)
+    torch.cuda.synchronize()
+    assert plan.device_status() == 0
+    return out, lse, plan
+
+
+def oracle(pw, rows_per_req=None):
+    kp = pw.k_pages.double().cpu().numpy()
+    vp = pw.v_pages.double().cpu().numpy()
+    res = []
+    for r, (T, qb) in enumerate(zip(pw.seq_len, pw.q_row_begin)):
+        off = pw.row_offsets()[r]
+        rows = np.arange(qb, T) if rows_per_req is None else np.asarray(rows_per_req[r])
+        flat = off + (rows - qb)
+        q = pw.q[torch.from_numpy(flat).cuda()].double().cpu().numpy()
+        Oo, Lo = O.seg_paged_request(q, kp, vp, pw.block_table[r], int(T), int(qb), pw.kv_role,
+                                     pw.sink, pw.window, pw.scale, 128, rows=rows, sampled=True)
+        res.append((flat, Oo, Lo))
+    return res
+
+
+def compare(out, lse, ref, label):
+    go = np.concatenate([out[torch.from_numpy(f).cuda()].double().cpu().numpy() for f, _, _ in ref])
+    gl = np.concatenate([lse[torch.from_numpy(f).cuda()].double().cpu().numpy() for f, _, _ in ref])
+    ro = np.concatenate([o for _, o, _ in ref])
+    rl = np.concatenate([l for _, _, l in ref])
+    assert np.isfinite(go).all() and np.isfinite(gl).all(), f"{label}: unwritten or non-finite"
+    err = np.abs(go - ro)
+    st = dict(max_err=float(err.max()), max_ref=float(np.abs(ro).max()),
+              mean_rel=float(err.sum() / np.abs(ro).sum()), lse_err=float(np.abs(gl - rl).max()))
+    assert st["max_err"] <= MAX_REL * st["max_ref"], f"{label}: {st}"
+    assert st["mean_rel"] <= MEAN_REL, f"{label}: {st}"
+    assert st["lse_err"] <= LSE_ABS, f"{label}: {st}"
+    return st
+
+
+@pytest.mark.parametrize("sharp", [False, True], ids=["stated", "sharp"])
+@pytest.mark.parametrize("name", MINI)
+def test_seg_paged_parity_every_row(name, sharp):
+    pw = make_paged_workload(name, seed=0, device="cuda", q_scale=512.0 if sharp else 1.0)
+    out, lse, plan = run(pw)
+    compare(out, lse, oracle(pw), f"{name}/{sharp}")
+
+
+@pytest.mark.parametrize("name", ["paged_mini", "paged_mini_g4"])
+def test_dense_mask_arm_same_results(name):
+    """The dense + mask arm (every block, element masks) gives the same
+    outputs as the paged walk, bit for bit: masked keys contribute exact
+    zeros and the blocks of the paged walk come in the same order."""
+    pw = make_paged_workload(name, seed=1, device="cuda", q_scale=256.0)
+    o1, l1, _ = run(pw)
+    o2, l2, _ = run(pw, B.RK_SEGPAGED_DENSE_MASK)
+    compare(o2, l2, oracle(pw), f"{name}/dense")
+    assert float((o1.float() - o2.float()).abs().max()) <= 2e-2 * float(o1.float().abs().max())
+
+
+@pytest.mark.parametrize("name", MINI)
+def test_seg_paged_visible_key_counts_exact(name):
+    """q = 0: exp(lse) is exactly the number of visible keys of every
+    (row, query head)."""
+    pw = make_paged_workload(name, seed=0, device="cuda")
+    pw.q.zero_()
+    out, lse, plan = run(pw)
+    l = lse.double().cpu().numpy()
+    cnt = np.rint(np.exp(np.minimum(l, 700.0)))
+    offs = pw.row_offsets()
+    for r, (T, qb) in enumerate(zip(pw.seq_len, pw.q_row_begin)):
+        for i, p in enumerate(range(int(qb), int(T))):
+            for hq in range(pw.Hq):
+                g = hq // pw.G
+                want = p + 1 if pw.kv_role[g] else len(O.visible_keys(p, False, pw.sink, pw.window))
+                assert cnt[offs[r] + i, hq] == want, (name, p, hq)
+
+
+@pytest.mark.parametrize("name", ["qwen32b_128k", "qwen32b_decode"])
+def test_seg_paged_full_size_sampled(name):
+    """The benchmark sizes: sampled rows (window edges, block edges, the
+    first and last rows) against the oracle."""
+    pw = make_paged_workload(name, seed=0, device="cuda")
+    out, lse, plan = run(pw)
+    rng = np.random.default_rng(7)
+    rows = []
+    for T, qb in zip(pw.seq_len, pw.q_row_begin):
+        T, qb = int(T), int(qb)
+        if T - qb == 1:
+            rows.append(np.array([qb]))
+            continue
+        pick = {qb, qb + 1, T - 1, 127, 128, 255, 256, 257, 383, 4095, 65535, T // 2}
+        pick |= set(int(x) for x in rng.integers(qb, T, size=6))
+        rows.append(np.array(sorted(x for x in pick if qb <= x < T)))
+    if len(rows) > 8:  # decode: a sample of the requests, the others unchecked
+        for i in range(8, len(rows)):
+            rows[i] = rows[i][:0]
+    ref = oracle(pw, rows)
+    ref = [x for x in ref if len(x[0])]
+    compare(out, lse, ref, name)
+    # every computed row was written
+    assert bool(torch.isfinite(lse).all()) and bool(torch.isfinite(out.float()).all())
