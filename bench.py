@@ -437,8 +437,9 @@ def bench_seg_paged(local: int, pk: dict) -> dict:
     ok = True
 
     def timed(plan, pw, out, lse, n, flush=None):
+        ws = torch.empty(max(16, plan.workspace_bytes), dtype=torch.uint8, device=dev)
         for _ in range(3):
-            plan.forward(pw.q, pw.k_pages, pw.v_pages, out, lse, stream=stream)
+            plan.forward(pw.q, pw.k_pages, pw.v_pages, out, lse, ws, stream=stream)
         torch.cuda.synchronize(dev)
         ts = []
         for _ in range(n):
@@ -447,7 +448,7 @@ def bench_seg_paged(local: int, pk: dict) -> dict:
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
             a.record(stream)
-            plan.forward(pw.q, pw.k_pages, pw.v_pages, out, lse, stream=stream)
+            plan.forward(pw.q, pw.k_pages, pw.v_pages, out, lse, ws, stream=stream)
             b.record(stream)
             torch.cuda.synchronize(dev)
             ts.append(a.elapsed_time(b))
@@ -494,7 +495,8 @@ def bench_seg_paged(local: int, pk: dict) -> dict:
     res["decode"] = {"workload": "qwen32b_decode: 64 requests x 1 row over 8K-64K tokens, Local "
                                  "heads keep sink + window pages only", "ms": round(ms, 4),
                      "GB/s": round(gbs, 1), "bytes": byt, "frac_of_hbm": round(gbs / pk["hbm_gbs"], 4),
-                     "pages": pw.num_pages, "l2": "256 MB flush between iterations"}
+                     "pages": pw.num_pages, "split_parts": plan.info["split_parts"],
+                     "l2": "256 MB flush between iterations"}
     plan.close()
     del pw, out, lse, flush
     torch.cuda.empty_cache()

@@ -99,13 +99,19 @@ typedef struct {
   int64_t pairs;            /* attended (row, query head, key) pairs */
   int64_t performed_pairs;  /* 128 x 128 per issued (tile, key block) */
   int64_t kv_blocks;        /* key blocks read, summed over tiles */
+  int64_t split_parts;      /* parts of split tiles (0 if none) */
   int32_t group;            /* G */
   int32_t reserved;
 } rk_segpaged_info_t;
 
 /* Validate the descriptor, check that every block a computed row can see has
  * a page (RK_ERR_INVALID_ARG otherwise), list the tiles longest first and
- * upload them with a copy of the block table on `stream`.
+ * upload them with a copy of the block table on `stream`.  A tile with few
+ * rows (at most 64 of its 128 query pairs in use, e.g. a decode step) and a
+ * long key walk (more than 64 blocks) is split into parts of 32 blocks
+ * whose normalised partial outputs and LSEs are merged by log-sum-exp in
+ * the workspace by the last part to finish (the RedKnot-MLA paper's
+ * numerically stable merge, RoPE-orthogonality paragraph).
  * Errors: RK_ERR_NULL, RK_ERR_INVALID_ARG, RK_ERR_UNSUPPORTED_DIMS (head_dim,
  * page_size or G), RK_ERR_CAPACITY, RK_ERR_CUDA.  On error *out is NULL. */
 rk_status_t rk_segpaged_plan(const rk_segpaged_desc_t* desc, void* stream,
@@ -117,10 +123,18 @@ rk_status_t rk_segpaged_plan(const rk_segpaged_desc_t* desc, void* stream,
  *          aligned; owned by the caller.
  * out      device bf16 [rows, Hq, 128], written on every computed row.
  * lse      device fp32 [rows, Hq], written likewise.
+ * workspace device scratch of rk_segpaged_workspace_bytes(plan) bytes,
+ *          16-byte aligned; contents on entry irrelevant.
  * Asynchronous on `stream`.  Errors: RK_ERR_NULL, RK_ERR_ALIGNMENT,
- * RK_ERR_PLAN_MISMATCH, RK_ERR_CUDA. */
+ * RK_ERR_WORKSPACE, RK_ERR_PLAN_MISMATCH, RK_ERR_CUDA. */
 rk_status_t rk_segpaged_forward(rk_segpaged_plan_t plan, const void* q, const void* k_pages,
-                                const void* v_pages, void* out, float* lse, void* stream);
+                                const void* v_pages, void* out, float* lse, void* workspace,
+                                size_t workspace_bytes, void* stream);
+
+/* Bytes of device workspace rk_segpaged_forward needs (0 when no tile is
+ * split; then workspace may be NULL).  Forwards sharing a workspace must be
+ * ordered on one stream. */
+size_t rk_segpaged_workspace_bytes(rk_segpaged_plan_t plan);
 
 /* Plan counts.  Errors: RK_ERR_NULL. */
 rk_status_t rk_segpaged_plan_info(rk_segpaged_plan_t plan, rk_segpaged_info_t* info);

@@ -29,7 +29,8 @@ EXPORTS = ["rk_seg_attn_plan", "rk_seg_attn_plan_destroy", "rk_seg_attn_plan_inf
            "rk_seg_attn_forward_noalloc", "rk_seg_attn_forward_host",
            "rk_protected_workspace_bytes", "rk_protected_build", "rk_project_forward",
            "rk_segpaged_plan", "rk_segpaged_forward", "rk_segpaged_plan_info",
-           "rk_segpaged_last_device_status", "rk_segpaged_plan_destroy"]
+           "rk_segpaged_last_device_status", "rk_segpaged_plan_destroy",
+           "rk_segpaged_workspace_bytes"]
 
 RK_SEGPAGED_HOST_ONLY = 1
 RK_SEGPAGED_DENSE_MASK = 2
@@ -52,8 +53,8 @@ class RkSegPagedDesc(C.Structure):
 
 class RkSegPagedInfo(C.Structure):
     _fields_ = [("rows", C.c_int64), ("tiles", C.c_int64), ("pairs", C.c_int64),
-                ("performed_pairs", C.c_int64), ("kv_blocks", C.c_int64), ("group", C.c_int32),
-                ("reserved", C.c_int32)]
+                ("performed_pairs", C.c_int64), ("kv_blocks", C.c_int64),
+                ("split_parts", C.c_int64), ("group", C.c_int32), ("reserved", C.c_int32)]
 
     def as_dict(self):
         return {k: getattr(self, k) for k, _ in self._fields_ if k != "reserved"}
@@ -145,12 +146,14 @@ def lib() -> C.CDLL:
         L.rk_segpaged_plan.argtypes = [C.POINTER(RkSegPagedDesc), C.c_void_p,
                                        C.POINTER(C.c_void_p)]
         L.rk_segpaged_plan.restype = C.c_int
-        L.rk_segpaged_forward.argtypes = [C.c_void_p] * 7
+        L.rk_segpaged_forward.argtypes = [C.c_void_p] * 7 + [C.c_size_t, C.c_void_p]
         L.rk_segpaged_forward.restype = C.c_int
         L.rk_segpaged_plan_info.argtypes = [C.c_void_p, C.POINTER(RkSegPagedInfo)]
         L.rk_segpaged_plan_info.restype = C.c_int
         L.rk_segpaged_last_device_status.argtypes = [C.c_void_p, C.c_void_p]
         L.rk_segpaged_last_device_status.restype = C.c_int
+        L.rk_segpaged_workspace_bytes.argtypes = [C.c_void_p]
+        L.rk_segpaged_workspace_bytes.restype = C.c_size_t
         L.rk_segpaged_plan_destroy.argtypes = [C.c_void_p]
         L.rk_segpaged_plan_destroy.restype = None
         L.rk_status_string.argtypes = [C.c_int]
@@ -389,10 +392,15 @@ class SegPagedPlan:
         _check(lib().rk_segpaged_plan_info(self._h, C.byref(inf)), "rk_segpaged_plan_info")
         return inf.as_dict()
 
-    def forward(self, q, k_pages, v_pages, out, lse, stream=None):
+    @property
+    def workspace_bytes(self) -> int:
+        return int(lib().rk_segpaged_workspace_bytes(self._h))
+
+    def forward(self, q, k_pages, v_pages, out, lse, workspace=None, stream=None):
+        ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
         _check(lib().rk_segpaged_forward(self._h, _ptr(q), _ptr(k_pages), _ptr(v_pages),
-                                         _ptr(out), _ptr(lse), _stream(stream)),
-               "rk_segpaged_forward")
+                                         _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes,
+                                         _stream(stream)), "rk_segpaged_forward")
 
     def device_status(self, stream=None) -> int:
         return int(lib().rk_segpaged_last_device_status(self._h, _stream(stream)))

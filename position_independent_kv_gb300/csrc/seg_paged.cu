@@ -9,7 +9,7 @@
 //
 // A tile is 128 query pairs: 128 / G consecutive rows x the G query heads of
 // one KV head, so each key page is read once for the whole group.  One CTA
-// per tile (192 threads):
+// per tile (320 threads):
 //   warp 0     TMA producer: for each key block its K page and, one block
 //              behind, its V page (each a 32 KB box of 128 tokens x 128
 //              dims, chunk-major, 128-byte swizzled) through a six-slot ring.
@@ -17,13 +17,21 @@
 //              B = K from shared memory) into one of two S buffers in tensor
 //              memory, then O += P_{j-1} V_{j-1} (A = P from tensor memory,
 //              B = V in MN-major form, N = 128).
-//   warps 2-5  one thread per query pair (its TMEM lane): writes its query
-//              row into shared memory (the A operand), masks the edge
-//              blocks, keeps the running max in the log2 domain with a lazy
-//              rescale of O when it grows by more than 2^8, writes P (bf16)
-//              to tensor memory, and finally normalises and stores O and the
-//              LSE.
+//   warps 2-9  two threads per query pair (its TMEM lane), one in each
+//              warpgroup, each taking half of the 128 keys of a block and
+//              half of the 128 output columns: write the query row into
+//              shared memory (the A operand), mask the edge blocks, agree on
+//              the block's row max through shared memory (a per-block
+//              bar.red vote that also lets every warp leave together after a
+//              failed wait), keep the running max in the log2 domain with a
+//              lazy rescale of O when it grows by more than 2^8, write P
+//              (bf16) to tensor memory, and finally normalise and store O and
+//              the LSE.
 // Tensor memory (512 columns): O (128) | S (2 x 128) | P (64, bf16 pairs).
+// A tile with few rows and a long walk (a decode step of a Global head) is
+// split into parts of a few blocks on separate CTAs; each part leaves its
+// normalised partial output and LSE in the workspace and the last part of
+// the tile merges them by log-sum-exp (parts without a visible key weigh 0).
 // Every wait is bounded (2 s); on expiry the CTA records
 // RK_ERR_DEVICE_TIMEOUT and every role stops; the producer waits (bounded)
 // for its copies in flight and tensor memory is released after the MMA pipe
@@ -42,8 +50,8 @@ namespace sp {
 constexpr int PAGE = 128;                   // tokens per page (= keys per block)
 constexpr int DH = 128;                     // head dim
 constexpr uint32_t CHUNK = 16384;           // 128 rows x 64 bf16
-constexpr int THREADS = 192;
-constexpr int RING = 6;
+constexpr int THREADS = 320;
+constexpr int RING = 5;
 constexpr uint32_t SLOT = 2 * CHUNK;        // one K or V page
 constexpr uint32_t OFF_Q = 0;
 constexpr uint32_t OFF_RING = 2 * CHUNK;
@@ -51,16 +59,17 @@ constexpr uint32_t OFF_BAR = OFF_RING + RING * SLOT;
 enum {
   B_FULL = 0,
   B_EMPTY = RING,
-  B_QFULL = 2 * RING,       // queries in shared memory (one arrival per lane warp)
+  B_QFULL = 2 * RING,       // queries in shared memory (one arrival per lane warp, 8)
   B_SFULL,                   // 2: S buffer j & 1 written
-  B_SFREE = B_SFULL + 2,     // 2: S buffer read (one arrival per lane warp)
-  B_PREADY = B_SFREE + 2,    // P_j written and O rescaled (one arrival per lane warp)
+  B_SFREE = B_SFULL + 2,     // 2: S buffer read (one arrival per lane warp, 8)
+  B_PREADY = B_SFREE + 2,    // P_j written and O rescaled (one arrival per lane warp, 8)
   B_ODONE,                   // O += P_j V_j done
   B_FINAL,
   NBAR
 };
 constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
-constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;
+constexpr uint32_t OFF_X = (OFF_MISC + 16 + 15) & ~15u;  // row max [2 buffers][2 halves][128], sums [2][128]
+constexpr uint32_t SMEM_BYTES = OFF_X + (4 + 2) * 128 * 4 + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory");
 constexpr uint32_t T_O = 0, T_S = 128, T_P = 384;
 
@@ -71,11 +80,16 @@ struct Req {
   int64_t table_off;     // offset of the request's [Hkv][max_blocks] block table
 };
 
-// 128 / G rows from p0 of KV head g; key blocks [0, sink_blocks) then
-// [win_lo, hi] (sink_blocks = 0: [win_lo, hi] only).
+// 128 / G rows from p0 of KV head g; its key walk is blocks [0, sink_blocks)
+// then [win_lo, hi] (sink_blocks = 0: [win_lo, hi] only), and this CTA takes
+// walk steps [jb, je).  A split tile's parts are part_first ..
+// part_first + nparts - 1; their partials sit at workspace lanes
+// lane0 + (part - part_first) * rows * G + m.
 struct Tile {
   int32_t req, g, p0, rows;
-  int32_t sink_blocks, win_lo, hi, pad;
+  int32_t sink_blocks, win_lo, hi, jb;
+  int32_t je, part, part_first, nparts;
+  int32_t group, lane0, pad0, pad1;
 };
 
 struct Args {
@@ -90,6 +104,9 @@ struct Args {
   int32_t Hq, G, max_blocks;
   int32_t sink, window;
   float scale_log2;
+  float* ws_o;           // [lanes][128] normalised partial outputs of split tiles
+  float* ws_lse;         // [lanes]
+  int32_t* ws_ticket;    // [split tiles]
 };
 
 struct Maps {
@@ -111,19 +128,19 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const Tile t = a.tiles[blockIdx.x];
   const Req rq = a.reqs[t.req];
-  const int nb = t.sink_blocks + (t.hi - t.win_lo + 1);
+  const int nb = t.je - t.jb;  // this CTA's walk steps
 
   if (tid == 0) {
     for (int i = 0; i < RING; ++i) {
       tc::mbar_init(&bar[B_FULL + i], 1);
       tc::mbar_init(&bar[B_EMPTY + i], 1);
     }
-    tc::mbar_init(&bar[B_QFULL], 4);
+    tc::mbar_init(&bar[B_QFULL], 8);
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(&bar[B_SFULL + b], 1);
-      tc::mbar_init(&bar[B_SFREE + b], 4);
+      tc::mbar_init(&bar[B_SFREE + b], 8);
     }
-    tc::mbar_init(&bar[B_PREADY], 4);
+    tc::mbar_init(&bar[B_PREADY], 8);
     tc::mbar_init(&bar[B_ODONE], 1);
     tc::mbar_init(&bar[B_FINAL], 1);
     misc[1] = 0;
@@ -157,8 +174,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       };
       // K_j, then V_{j-1}: the order in which the issuer consumes them
       for (int j = 0; j <= nb && ok; ++j) {
-        if (j < nb) ok = load(&mp.k, tab[block_of(t, j)]);
-        if (ok && j >= 1) ok = load(&mp.v, tab[block_of(t, j - 1)]);
+        if (j < nb) ok = load(&mp.k, tab[block_of(t, t.jb + j)]);
+        if (ok && j >= 1) ok = load(&mp.v, tab[block_of(t, t.jb + j - 1)]);
       }
       // copies in flight land before the CTA may exit
       for (uint32_t k = (cnt > RING ? cnt - RING : 0); k < cnt; ++k)
@@ -216,8 +233,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else {
     // ------------------------------------------- softmax and epilogue ----
-    const int quarter = warp & 3;
+    const int lw = warp - 2;           // 0..7
+    const int hf = lw >> 2;            // half of the keys and of the output columns
+    const int quarter = warp & 3;      // TMEM lane quarter this warp may access
     const int m = quarter * 32 + lane;
+    const int lid = lw * 32 + lane;    // 0..255
     const int r = m / a.G, h = m - r * a.G;
     const int p = t.p0 + r;
     const bool valid = r < t.rows;
@@ -227,62 +247,71 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int sink = a.sink, window = a.window;
     const int64_t row = rq.row_base + (p - rq.q_row_begin);
     const int head = t.g * a.G + h;
-    // this lane's query row -> shared memory: two 64-dim chunks of 128 rows,
-    // 128-byte swizzle (A operand of the score MMAs); rows past the
-    // request's end are zero
+    float* xmax = reinterpret_cast<float*>(sm + OFF_X);          // [2][2][128]
+    float* xsum = xmax + 4 * 128;                                 // [2][128]
+    // this thread's half of the query row -> shared memory: 64-dim chunk hf
+    // of 128 rows, 128-byte swizzle (A operand of the score MMAs); rows past
+    // the request's end are zero
     {
-      const uint4* src = valid ? reinterpret_cast<const uint4*>(a.q + (row * a.Hq + head) * DH)
+      const uint4* src = valid ? reinterpret_cast<const uint4*>(a.q + (row * a.Hq + head) * DH) + 8 * hf
                                : nullptr;
 #pragma unroll
-      for (int u = 0; u < 16; ++u) {
+      for (int u = 0; u < 8; ++u) {
         const uint4 v = src ? __ldg(src + u) : make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(sm + OFF_Q + (u >> 3) * CHUNK + m * 128 +
-                                  (((u & 7) ^ (m & 7)) << 4)) = v;
+        *reinterpret_cast<uint4*>(sm + OFF_Q + hf * CHUNK + m * 128 + ((u ^ (m & 7)) << 4)) = v;
       }
       tc::fence_proxy_async();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&bar[B_QFULL]);
     }
     float m_run = -INFINITY, l_run = 0.f;
-    bool ok = true;
-    for (int j = 0; j < nb && ok; ++j) {
+    bool okw = true;
+    for (int j = 0; j < nb; ++j) {
       const int b = j & 1;
-      const int k0 = block_of(t, j) * PAGE;
-      ok = __all_sync(0xffffffffu, tt::wait_bar(c, B_SFULL + b, (j >> 1) & 1));
-      if (!ok) break;
-      tc::tc_fence_after();
-      uint32_t s[4][32];
+      const int k0 = block_of(t, t.jb + j) * PAGE + 64 * hf;  // this thread's 64 keys
+      if (okw) okw = __all_sync(0xffffffffu, tt::wait_bar(c, B_SFULL + b, (j >> 1) & 1));
+      uint32_t s[2][32];
+      float mx = -INFINITY;
+      if (okw) {
+        tc::tc_fence_after();
+        tc::tmem_ld32(lt + T_S + 128 * b + 64 * hf, s[0]);
+        tc::tmem_ld32(lt + T_S + 128 * b + 64 * hf + 32, s[1]);
+        tc::tmem_wait_ld();
+        tc::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&bar[B_SFREE + b]);
+        // every key of this half block visible for this row?  (then no masks)
+        const bool full = valid && k0 + 63 <= p && (glob || k0 >= p - window || k0 + 64 <= sink);
+        float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        if (__all_sync(0xffffffffu, full)) {
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) tc::tmem_ld32(lt + T_S + 128 * b + 32 * q4, s[q4]);
-      tc::tmem_wait_ld();
-      tc::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&bar[B_SFREE + b]);
-
-      // every key of the block visible for this row?  (then no masks)
-      const bool full = valid && k0 + PAGE - 1 <= p &&
-                        (glob || k0 >= p - window || k0 + PAGE <= sink);
-      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-      if (__all_sync(0xffffffffu, full)) {
+          for (int q2 = 0; q2 < 2; ++q2)
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4)
+            for (int i = 0; i < 32; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], __uint_as_float(s[q2][i]));
+        } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], __uint_as_float(s[q4][i]));
-      } else {
+          for (int q2 = 0; q2 < 2; ++q2) {
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int key = k0 + 32 * q4 + i;
-            bool vis = valid && key <= p;
-            if (!glob) vis = vis && (key < sink || key >= p - window);
-            const float x = vis ? __uint_as_float(s[q4][i]) : -INFINITY;
-            s[q4][i] = __float_as_uint(x);
-            mx4[i & 3] = fmaxf(mx4[i & 3], x);
+            for (int i = 0; i < 32; ++i) {
+              const int key = k0 + 32 * q2 + i;
+              bool vis = valid && key <= p;
+              if (!glob) vis = vis && (key < sink || key >= p - window);
+              const float x = vis ? __uint_as_float(s[q2][i]) : -INFINITY;
+              s[q2][i] = __float_as_uint(x);
+              mx4[i & 3] = fmaxf(mx4[i & 3], x);
+            }
           }
         }
+        mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * sl2;
+        xmax[(b * 2 + hf) * 128 + m] = mx;
       }
-      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * sl2;
+      // every lane warp votes each block: the halves exchange their maxima,
+      // and a failed wait anywhere makes all of them leave together
+      if (!tc::named_and(2, 256, okw)) {
+        okw = false;
+        break;
+      }
+      mx = fmaxf(mx, xmax[(b * 2 + (hf ^ 1)) * 128 + m]);
       bool need = false;
       float alpha = 1.f;
       if (mx > m_run + 8.f) {  // lazy rescale: only when the max grows by more than 2^8
@@ -294,51 +323,116 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       const float nbias = (m_run == -INFINITY) ? 0.f : -m_run;
       float ls4[4] = {0.f, 0.f, 0.f, 0.f};
-      // P in place: pair i of column block q4 goes to word 16 q4 + i
+      // P in place: keys 2i, 2i + 1 of column block q2 go to word 16 q2 + i
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
+      for (int q2 = 0; q2 < 2; ++q2) {
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float p0 = fast_exp2(fmaf(__uint_as_float(s[q4][2 * i]), sl2, nbias));
-          const float p1 = fast_exp2(fmaf(__uint_as_float(s[q4][2 * i + 1]), sl2, nbias));
+          const float p0 = fast_exp2(fmaf(__uint_as_float(s[q2][2 * i]), sl2, nbias));
+          const float p1 = fast_exp2(fmaf(__uint_as_float(s[q2][2 * i + 1]), sl2, nbias));
           ls4[i & 3] += p0 + p1;
-          s[q4 >> 1][16 * (q4 & 1) + i] = pack_bf16x2(p0, p1);
+          s[0][16 * q2 + i] = pack_bf16x2(p0, p1);
         }
       }
       l_run = l_run * alpha + ((ls4[0] + ls4[1]) + (ls4[2] + ls4[3]));
       // the previous P.V must be done before P and O are touched
-      if (j >= 1) ok = __all_sync(0xffffffffu, tt::wait_bar(c, B_ODONE, (j - 1) & 1));
-      if (!ok) break;
-      tc::tc_fence_after();
-      tc::tmem_st32(lt + T_P, s[0]);
-      tc::tmem_st32(lt + T_P + 32, s[1]);
-      if (__any_sync(0xffffffffu, need)) {
+      if (j >= 1) okw = __all_sync(0xffffffffu, tt::wait_bar(c, B_ODONE, (j - 1) & 1));
+      if (okw) {
+        tc::tc_fence_after();
+        tc::tmem_st32(lt + T_P + 32 * hf, s[0]);
+        if (__any_sync(0xffffffffu, need)) {
 #pragma unroll 1
-        for (int q8 = 0; q8 < 4; ++q8) {
-          uint32_t o[32];
-          tc::tmem_ld32(lt + T_O + 32 * q8, o);
-          tc::tmem_wait_ld();
+          for (int q8 = 0; q8 < 2; ++q8) {
+            uint32_t o[32];
+            tc::tmem_ld32(lt + T_O + 64 * hf + 32 * q8, o);
+            tc::tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tc::tmem_st32(lt + T_O + 32 * q8, o);
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tc::tmem_st32(lt + T_O + 64 * hf + 32 * q8, o);
+          }
         }
+        tc::tmem_wait_st();
+        tc::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&bar[B_PREADY]);
       }
-      tc::tmem_wait_st();
-      tc::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&bar[B_PREADY]);
     }
     // ---- epilogue ----
+    bool ok = okw;
     if (ok) ok = __all_sync(0xffffffffu, tt::wait_bar(c, B_FINAL, 0));
     tc::tc_fence_after();
-    if (ok) {
-      const bool st = valid && l_run > 0.f;
-      const float inv = st ? 1.f / l_run : 0.f;
-      uint16_t* dst = st ? a.out + (row * a.Hq + head) * DH : nullptr;
+    xsum[hf * 128 + m] = l_run;
+    ok = tc::named_and(3, 256, ok);  // every lane warp; also publishes the sums
+    const float l_tot = l_run + xsum[(hf ^ 1) * 128 + m];
+    if (t.nparts > 1) {
+      if (ok) {
+        const int nl = t.rows * a.G;  // lanes in use
+        const int64_t slot = int64_t(t.lane0) + int64_t(t.part - t.part_first) * nl + m;
+        const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
+        float4* w4 = valid ? reinterpret_cast<float4*>(a.ws_o + slot * DH + 64 * hf) : nullptr;
+        // tcgen05.ld is warp-aligned: every lane loads, only the used ones store
 #pragma unroll 1
-      for (int q8 = 0; q8 < 4; ++q8) {
+        for (int q8 = 0; q8 < 2; ++q8) {
+          uint32_t o[32];
+          tc::tmem_ld32(lt + T_O + 64 * hf + 32 * q8, o);
+          tc::tmem_wait_ld();
+          if (valid) {
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              w4[8 * q8 + u] = make_float4(__uint_as_float(o[4 * u]) * inv, __uint_as_float(o[4 * u + 1]) * inv,
+                                           __uint_as_float(o[4 * u + 2]) * inv, __uint_as_float(o[4 * u + 3]) * inv);
+          }
+        }
+        if (valid && hf == 0)
+          a.ws_lse[slot] = l_tot > 0.f ? m_run * 0.6931471805599453f + logf(l_tot) : -INFINITY;
+        __threadfence();
+        tc::named_sync(1, 256);
+        volatile int* last = reinterpret_cast<volatile int*>(misc + 2);
+        if (lid == 0) *last = atomicAdd(a.ws_ticket + t.group, 1) == t.nparts - 1;
+        tc::named_sync(1, 256);
+        if (*last) {
+          __threadfence();
+          // log-sum-exp merge of the parts (-inf parts weigh 0), spread over
+          // the 256 lane threads: item = (used lane, group of 8 dims)
+          for (int it = lid; it < nl * 16; it += 256) {
+            const int l = it >> 4, d0 = (it & 15) * 8;
+            const int64_t s0 = int64_t(t.lane0) + l;
+            float mxp = -INFINITY;
+            for (int q = 0; q < t.nparts; ++q) mxp = fmaxf(mxp, __ldcg(a.ws_lse + s0 + int64_t(q) * nl));
+            float wsum = 0.f;
+            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            for (int q = 0; q < t.nparts; ++q) {
+              const float lq = __ldcg(a.ws_lse + s0 + int64_t(q) * nl);
+              if (lq == -INFINITY) continue;
+              const float wq = __expf(lq - mxp);
+              wsum += wq;
+              const float4* src = reinterpret_cast<const float4*>(a.ws_o + (s0 + int64_t(q) * nl) * DH + d0);
+              const float4 x = __ldcg(src), y = __ldcg(src + 1);
+              acc[0] += wq * x.x; acc[1] += wq * x.y; acc[2] += wq * x.z; acc[3] += wq * x.w;
+              acc[4] += wq * y.x; acc[5] += wq * y.y; acc[6] += wq * y.z; acc[7] += wq * y.w;
+            }
+            const float winv = wsum > 0.f ? 1.f / wsum : 0.f;
+            const int lr = l / a.G, lh = l - lr * a.G;
+            const int64_t orow = rq.row_base + (t.p0 + lr - rq.q_row_begin);
+            const int ohead = t.g * a.G + lh;
+            uint4 v;
+            v.x = pack_bf16x2(acc[0] * winv, acc[1] * winv);
+            v.y = pack_bf16x2(acc[2] * winv, acc[3] * winv);
+            v.z = pack_bf16x2(acc[4] * winv, acc[5] * winv);
+            v.w = pack_bf16x2(acc[6] * winv, acc[7] * winv);
+            *reinterpret_cast<uint4*>(a.out + (orow * a.Hq + ohead) * DH + d0) = v;
+            if (d0 == 0) a.lse[orow * a.Hq + ohead] = wsum > 0.f ? mxp + logf(wsum) : -INFINITY;
+          }
+        }
+      }
+    } else if (ok) {
+      const bool st = valid && l_tot > 0.f;
+      const float inv = st ? 1.f / l_tot : 0.f;
+      uint16_t* dst = st ? a.out + (row * a.Hq + head) * DH + 64 * hf : nullptr;
+#pragma unroll 1
+      for (int q8 = 0; q8 < 2; ++q8) {
         uint32_t o[32];
-        tc::tmem_ld32(lt + T_O + 32 * q8, o);
+        tc::tmem_ld32(lt + T_O + 64 * hf + 32 * q8, o);
         tc::tmem_wait_ld();
         if (st) {
           uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * q8);
@@ -353,7 +447,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
       }
-      if (st) a.lse[row * a.Hq + head] = m_run * 0.6931471805599453f + logf(l_run);
+      if (st && hf == 0) a.lse[row * a.Hq + head] = m_run * 0.6931471805599453f + logf(l_tot);
     }
   }
 
@@ -376,6 +470,8 @@ struct rk_segpaged_plan_s {
   int32_t Hq = 0, Hkv = 0, G = 0, sink = 0, window = 0, max_blocks = 0;
   float scale = 0.f;
   int64_t num_pages = 0, rows = 0;
+  int64_t split_lanes = 0, split_tiles = 0;
+  size_t workspace_bytes = 0;
   rk_segpaged_info_t info{};
   std::vector<rk::sp::Req> reqs;
   std::vector<rk::sp::Tile> tiles;
@@ -391,6 +487,7 @@ struct rk_segpaged_plan_s {
 namespace {
 
 using rk::sp::PAGE;
+constexpr int kSplitBlocks = 32;  // walk steps per part of a split tile
 
 void sp_free(rk_segpaged_plan_s* p) {
   cudaFree(p->d_reqs);
@@ -506,6 +603,27 @@ rk_status_t sp_build(const rk_segpaged_desc_t* d, rk_segpaged_plan_s* p) {
         }
         info.kv_blocks += nb;
         info.performed_pairs += int64_t(nb) * 128 * PAGE;
+        t.jb = 0;
+        t.je = nb;
+        t.part = t.part_first = 0;
+        t.nparts = 1;
+        if (t.rows * G <= 64 && nb > 2 * kSplitBlocks) {
+          // a long walk of few rows: parts of kSplitBlocks steps, merged at the end
+          const int np = (nb + kSplitBlocks - 1) / kSplitBlocks;
+          t.nparts = np;
+          t.group = static_cast<int32_t>(p->split_tiles++);
+          t.lane0 = static_cast<int32_t>(p->split_lanes);
+          p->split_lanes += int64_t(np) * t.rows * G;
+          info.split_parts += np;
+          for (int q = 0; q < np; ++q) {
+            rk::sp::Tile u = t;
+            u.part = q;
+            u.jb = q * kSplitBlocks;
+            u.je = std::min(nb, (q + 1) * kSplitBlocks);
+            list.push_back({u.je - u.jb, u});
+          }
+          continue;
+        }
         list.push_back({nb, t});
       }
     }
@@ -519,6 +637,13 @@ rk_status_t sp_build(const rk_segpaged_desc_t* d, rk_segpaged_plan_s* p) {
   p->rows = rows;
   info.rows = rows;
   info.tiles = static_cast<int64_t>(p->tiles.size());
+  if (p->split_lanes > INT32_MAX / 2 || p->split_tiles > INT32_MAX / 2) return RK_ERR_CAPACITY;
+  if (p->split_tiles) {
+    size_t b = static_cast<size_t>(p->split_lanes) * (rk::sp::DH + 1) * sizeof(float);
+    b = (b + 255) & ~size_t(255);
+    b += static_cast<size_t>(p->split_tiles) * sizeof(int32_t);
+    p->workspace_bytes = (b + 255) & ~size_t(255);
+  }
   return RK_OK;
 }
 
@@ -558,12 +683,17 @@ extern "C" rk_status_t rk_segpaged_plan(const rk_segpaged_desc_t* desc, void* st
 
 extern "C" rk_status_t rk_segpaged_forward(rk_segpaged_plan_t p, const void* q, const void* k_pages,
                                            const void* v_pages, void* out, float* lse,
+                                           void* workspace, size_t workspace_bytes,
                                            void* stream) {
   if (!p || !q || !k_pages || !v_pages || !out || !lse) return RK_ERR_NULL;
   if (p->host_only) return RK_ERR_PLAN_MISMATCH;
   auto mis = [](const void* x) { return (reinterpret_cast<uintptr_t>(x) & 15) != 0; };
   if (mis(q) || mis(k_pages) || mis(v_pages) || mis(out) || (reinterpret_cast<uintptr_t>(lse) & 3))
     return RK_ERR_ALIGNMENT;
+  if (p->workspace_bytes) {
+    if (!workspace || workspace_bytes < p->workspace_bytes) return RK_ERR_WORKSPACE;
+    if (mis(workspace)) return RK_ERR_ALIGNMENT;
+  }
   int cur = -1;
   if (cudaGetDevice(&cur) != cudaSuccess) return RK_ERR_CUDA;
   if (cur != p->device) return RK_ERR_PLAN_MISMATCH;
@@ -594,12 +724,28 @@ extern "C" rk_status_t rk_segpaged_forward(rk_segpaged_plan_t p, const void* q, 
   a.window = p->window;
   a.scale_log2 = p->scale * 1.4426950408889634f;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (p->split_tiles) {
+    char* w = static_cast<char*>(workspace);
+    a.ws_o = reinterpret_cast<float*>(w);
+    size_t off = static_cast<size_t>(p->split_lanes) * rk::sp::DH * sizeof(float);
+    a.ws_lse = reinterpret_cast<float*>(w + off);
+    off += static_cast<size_t>(p->split_lanes) * sizeof(float);
+    off = (off + 255) & ~size_t(255);
+    a.ws_ticket = reinterpret_cast<int32_t*>(w + off);
+    if (cudaMemsetAsync(a.ws_ticket, 0, static_cast<size_t>(p->split_tiles) * sizeof(int32_t), s) !=
+        cudaSuccess)
+      return RK_ERR_CUDA;
+  }
   if (cudaFuncSetAttribute(rk::sp::seg_paged_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(rk::sp::SMEM_BYTES)) != cudaSuccess)
     return RK_ERR_CUDA;
   rk::sp::seg_paged_kernel<<<static_cast<unsigned>(p->tiles.size()), rk::sp::THREADS,
                              rk::sp::SMEM_BYTES, s>>>(a, mp);
   return cudaGetLastError() == cudaSuccess ? RK_OK : RK_ERR_CUDA;
+}
+
+extern "C" size_t rk_segpaged_workspace_bytes(rk_segpaged_plan_t p) {
+  return p ? p->workspace_bytes : 0;
 }
 
 extern "C" rk_status_t rk_segpaged_plan_info(rk_segpaged_plan_t p, rk_segpaged_info_t* info) {

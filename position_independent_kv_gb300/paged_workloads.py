@@ -59,6 +59,9 @@ PAGED_SPECS: dict[str, PagedSpec] = {
     "paged_mini_g16": PagedSpec("paged_mini_g16", 32, 2, [650], [0], global_every=2),
     "paged_decode_mini": PagedSpec("paged_decode_mini", 16, 2, [], [], global_every=2,
                                    local_pages_only=True),
+    # decode rows over 8.5K-12K tokens: the Global heads' walks are split
+    "paged_decode_long_mini": PagedSpec("paged_decode_long_mini", 16, 2, [], [],
+                                        global_every=2, local_pages_only=True),
 }
 
 
@@ -101,6 +104,8 @@ class PagedWorkload:
 def _decode_lengths(name: str, rng: np.random.Generator):
     if name == "qwen32b_decode":
         return [int(x) for x in rng.integers(8192, 65537, size=64)]
+    if name == "paged_decode_long_mini":
+        return [int(x) for x in rng.integers(8500, 12001, size=3)]
     return [int(x) for x in rng.integers(300, 1501, size=5)]
 
 

@@ -25,7 +25,8 @@ pytestmark = pytest.mark.gpu
 # path's.
 MEAN_REL = 3e-3
 
-MINI = ["paged_mini", "paged_mini_g4", "paged_mini_g1", "paged_mini_g16", "paged_decode_mini"]
+MINI = ["paged_mini", "paged_mini_g4", "paged_mini_g1", "paged_mini_g16", "paged_decode_mini",
+        "paged_decode_long_mini"]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -38,7 +39,10 @@ def run(pw, flags=0):
     plan = B.SegPagedPlan.from_workload(pw, flags=flags)
     out = torch.full((pw.rows, pw.Hq, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
     lse = torch.full((pw.rows, pw.Hq), float("nan"), dtype=torch.float32, device="cuda")
-    plan.forward(pw.q, pw.k_pages, pw.v_pages, out, lse)
+    ws = None
+    if plan.workspace_bytes:
+        ws = torch.full((plan.workspace_bytes,), 0xA5, dtype=torch.uint8, device="cuda")
+    plan.forward(pw.q, pw.k_pages, pw.v_pages, out, lse, ws)
     torch.cuda.synchronize()
     assert plan.device_status() == 0
     return out, lse, plan

@@ -25,7 +25,8 @@ def _plan(pw, flags=0, **over):
 
 
 @pytest.mark.parametrize("name", ["paged_mini", "paged_mini_g4", "paged_mini_g1",
-                                  "paged_mini_g16", "paged_decode_mini", "qwen32b_16k"])
+                                  "paged_mini_g16", "paged_decode_mini", "paged_decode_long_mini",
+                                  "qwen32b_16k"])
 def test_pair_counts_and_blocks(name):
     pw = make_paged_geometry(name, 0)
     info = _plan(pw).info
@@ -97,5 +98,31 @@ def test_host_only_refuses_forward():
     pw = make_paged_geometry("paged_mini", 0)
     plan = _plan(pw)
     with pytest.raises(B.RkError) as ei:
-        plan.forward(0x1000, 0x2000, 0x3000, 0x4000, 0x5000, stream=0)
+        plan.forward(0x1000, 0x2000, 0x3000, 0x4000, 0x5000, None, stream=0)
     assert ei.value.status == 9
+
+
+def test_decode_split_parts_and_workspace():
+    """Decode rows of Global heads with long walks (more than 64 blocks) are
+    split into parts of 32 blocks; the workspace holds one fp32 partial and
+    one LSE per used lane of every part, plus a ticket per split tile."""
+    pw = make_paged_geometry("paged_decode_long_mini", 0)
+    plan = _plan(pw)
+    info = plan.info
+    parts = 0
+    lanes = 0
+    split = 0
+    for T in pw.seq_len:
+        nb = (int(T) + PAGE - 1) // PAGE
+        for g in range(pw.Hkv):
+            if pw.kv_role[g] and nb > 64:
+                np_ = (nb + 31) // 32
+                parts += np_
+                lanes += np_ * pw.G
+                split += 1
+    assert info["split_parts"] == parts
+    want = ((lanes * 129 * 4 + 255) // 256) * 256 + split * 4
+    assert split > 0 and plan.workspace_bytes == ((want + 255) // 256) * 256
+    pq = make_paged_geometry("qwen32b_decode", 0)
+    qi = _plan(pq).info
+    assert qi["split_parts"] > 64 and qi["tiles"] > qi["split_parts"]
