@@ -423,7 +423,7 @@ def bench_vrope(local: int, pk: dict) -> dict:
     return res
 
 
-def bench_seg_paged(local: int, pk: dict) -> dict:
+def bench_seg_paged(local: int, pk: dict, prefill: str = "qwen32b_128k") -> dict:
     """SegPagedAttention on GQA pages (Qwen3-32B shape, 1 Global KV head in
     8): the 128K-token prefill on the paged walk and on the dense + mask arm
     (CUDA events, 3 warm-ups, median of 3), and 64 decode steps whose Local
@@ -454,7 +454,7 @@ def bench_seg_paged(local: int, pk: dict) -> dict:
             ts.append(a.elapsed_time(b))
         return statistics.median(ts), plan.device_status(stream=stream) == 0
 
-    pw = make_paged_workload("qwen32b_128k", seed=0, device=dev)
+    pw = make_paged_workload(prefill, seed=0, device=dev)
     out = torch.empty((pw.rows, pw.Hq, 128), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((pw.rows, pw.Hq), dtype=torch.float32, device=dev)
     for flags, key in ((0, "prefill"), (B.RK_SEGPAGED_DENSE_MASK, "prefill_dense_mask")):
@@ -468,9 +468,9 @@ def bench_seg_paged(local: int, pk: dict) -> dict:
                     "frac_of_peak": round(alg / (ms * 1e-3) / 1e12 / pk["bf16_tflops"], 4),
                     "kv_blocks": info["kv_blocks"], "tiles": info["tiles"]}
         plan.close()
-    res["prefill"]["workload"] = ("qwen32b_128k: 1 x 131072 tokens, 64 query heads over 8 KV heads "
-                                  "(d 128, 1 Global), per-head pages of 128 tokens, sink 4, w 256, "
-                                  "bf16 N(0,1)/sqrt(128), seed 0")
+    res["prefill"]["workload"] = (f"{prefill}: 1 x {int(pw.seq_len[0])} tokens, 64 query heads over "
+                                  "8 KV heads (d 128, 1 Global), per-head pages of 128 tokens, "
+                                  "sink 4, w 256, bf16 N(0,1)/sqrt(128), seed 0")
     res["dense_mask_over_paged"] = round(res["prefill_dense_mask"]["ms"] / res["prefill"]["ms"], 2)
     del pw, out, lse
     torch.cuda.empty_cache()
@@ -679,7 +679,7 @@ def run_ours(args):
         vrope = bench_vrope(local, pk)
     paged = None
     if not args.no_paged and rank == 0:
-        paged = bench_seg_paged(local, pk)
+        paged = bench_seg_paged(local, pk, args.paged_prefill)
     line = None
     if rank == 0:
         info = res["info"]
@@ -788,6 +788,8 @@ def main():
                     help="skip the timing of the projected-state / W_b step")
     ap.add_argument("--no-paged", action="store_true",
                     help="skip the timing of SegPagedAttention on GQA pages")
+    ap.add_argument("--paged-prefill", default="qwen32b_128k",
+                    help="paged workload of the SegPagedAttention prefill timing")
     ap.add_argument("--no-vrope", action="store_true",
                     help="skip the timing of the rotary-value (output-phase restore) path")
     ap.add_argument("--projection-workload", default="ctx128k",

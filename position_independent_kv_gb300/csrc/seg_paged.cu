@@ -12,22 +12,25 @@
 // per tile (320 threads):
 //   warp 0     TMA producer: for each key block its K page and, one block
 //              behind, its V page (each a 32 KB box of 128 tokens x 128
-//              dims, chunk-major, 128-byte swizzled) through a six-slot ring.
-//   warp 1     MMA issuer: S_j = Q K_j^T (M = 128, N = 128 keys, A = Q and
-//              B = K from shared memory) into one of two S buffers in tensor
-//              memory, then O += P_{j-1} V_{j-1} (A = P from tensor memory,
+//              dims, chunk-major, 128-byte swizzled) through a six-slot ring
+//              (a box takes ~3 us from issue to arrival, so the bytes in
+//              flight set the pace).
+//   warp 1     MMA issuer: S_j = Q K_j^T (M = 128, N = 128 keys, A = Q from
+//              tensor memory, B = K from shared memory) into one of two S
+//              buffers, then O += P_{j-1} V_{j-1} (A = P from tensor memory,
 //              B = V in MN-major form, N = 128).
 //   warps 2-9  two threads per query pair (its TMEM lane), one in each
 //              warpgroup, each taking half of the 128 keys of a block and
 //              half of the 128 output columns: write the query row into
-//              shared memory (the A operand), mask the edge blocks, agree on
+//              tensor memory (the A operand), mask the edge blocks, agree on
 //              the block's row max through shared memory (a per-block
 //              bar.red vote that also lets every warp leave together after a
 //              failed wait), keep the running max in the log2 domain with a
 //              lazy rescale of O when it grows by more than 2^8, write P
 //              (bf16) to tensor memory, and finally normalise and store O and
 //              the LSE.
-// Tensor memory (512 columns): O (128) | S (2 x 128) | P (64, bf16 pairs).
+// Tensor memory (512 columns): O (128) | S (2 x 128) | P (64) | Q (64), P and
+// Q as bf16 pairs.
 // A tile with few rows and a long walk (a decode step of a Global head) is
 // split into parts of a few blocks on separate CTAs; each part leaves its
 // normalised partial output and LSE in the workspace and the last part of
@@ -51,15 +54,14 @@ constexpr int PAGE = 128;                   // tokens per page (= keys per block
 constexpr int DH = 128;                     // head dim
 constexpr uint32_t CHUNK = 16384;           // 128 rows x 64 bf16
 constexpr int THREADS = 320;
-constexpr int RING = 5;
+constexpr int RING = 6;
 constexpr uint32_t SLOT = 2 * CHUNK;        // one K or V page
-constexpr uint32_t OFF_Q = 0;
-constexpr uint32_t OFF_RING = 2 * CHUNK;
+constexpr uint32_t OFF_RING = 0;
 constexpr uint32_t OFF_BAR = OFF_RING + RING * SLOT;
 enum {
   B_FULL = 0,
   B_EMPTY = RING,
-  B_QFULL = 2 * RING,       // queries in shared memory (one arrival per lane warp, 8)
+  B_QFULL = 2 * RING,       // queries in tensor memory (one arrival per lane warp, 8)
   B_SFULL,                   // 2: S buffer j & 1 written
   B_SFREE = B_SFULL + 2,     // 2: S buffer read (one arrival per lane warp, 8)
   B_PREADY = B_SFREE + 2,    // P_j written and O rescaled (one arrival per lane warp, 8)
@@ -71,7 +73,7 @@ constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
 constexpr uint32_t OFF_X = (OFF_MISC + 16 + 15) & ~15u;  // row max [2 buffers][2 halves][128], sums [2][128]
 constexpr uint32_t SMEM_BYTES = OFF_X + (4 + 2) * 128 * 4 + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory");
-constexpr uint32_t T_O = 0, T_S = 128, T_P = 384;
+constexpr uint32_t T_O = 0, T_S = 128, T_P = 384, T_Q = 448;
 
 struct Req {
   int32_t T;
@@ -188,7 +190,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc::tc_fence_after();
       const uint32_t idS = tc::idesc_bf16(128, 128, false, false);
       const uint32_t idPV = tc::idesc_bf16(128, 128, false, true);
-      const uint32_t qa = smem_u32(sm + OFF_Q), ra = smem_u32(sm + OFF_RING);
+      const uint32_t ra = smem_u32(sm + OFF_RING);
       uint32_t cnt = 0;
       auto pv = [&](int jj) {
         if (!tt::wait_bar(c, B_PREADY, jj & 1)) return false;
@@ -217,11 +219,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!ok) break;
         tc::tc_fence_after();
         const uint32_t base = ra + slot * SLOT;
+        // A = Q[128 rows x 16 dims] from tensor memory (8 columns per step)
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc)
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            tc::mma_ss(tbase + T_S + 128 * b, tc::sdesc_sw128(qa + cc * CHUNK + 32 * k, 16, 1024),
+            tc::mma_ts(tbase + T_S + 128 * b, tbase + T_Q + 8 * (4 * cc + k),
                        tc::sdesc_sw128(base + cc * CHUNK + 32 * k, 16, 1024), idS, (cc | k) != 0);
         tc::mma_commit(&bar[B_EMPTY + slot]);
         ++cnt;
@@ -249,18 +252,24 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int head = t.g * a.G + h;
     float* xmax = reinterpret_cast<float*>(sm + OFF_X);          // [2][2][128]
     float* xsum = xmax + 4 * 128;                                 // [2][128]
-    // this thread's half of the query row -> shared memory: 64-dim chunk hf
-    // of 128 rows, 128-byte swizzle (A operand of the score MMAs); rows past
-    // the request's end are zero
+    // this thread's half of the query row (dims 64 hf .. 64 hf + 63) ->
+    // tensor memory, 32-bit column c = dims 2c, 2c + 1 (A operand of the
+    // score MMAs); rows past the request's end are zero
     {
+      uint32_t w[32];
       const uint4* src = valid ? reinterpret_cast<const uint4*>(a.q + (row * a.Hq + head) * DH) + 8 * hf
                                : nullptr;
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const uint4 v = src ? __ldg(src + u) : make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(sm + OFF_Q + hf * CHUNK + m * 128 + ((u ^ (m & 7)) << 4)) = v;
+        w[4 * u] = v.x;
+        w[4 * u + 1] = v.y;
+        w[4 * u + 2] = v.z;
+        w[4 * u + 3] = v.w;
       }
-      tc::fence_proxy_async();
+      tc::tmem_st32(lt + T_Q + 32 * hf, w);
+      tc::tmem_wait_st();
+      tc::tc_fence_before();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&bar[B_QFULL]);
     }
