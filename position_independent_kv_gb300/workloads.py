@@ -172,6 +172,17 @@ SPECS: dict[str, Spec] = {
                    seg_lengths=[2048] * 6, n_new=4096),
     "tiny_wide": Spec("tiny_wide", 8, 128, 32, 4, 10000, ProtectRule(boundary=16),
                       seg_lengths=[256, 256], n_new=64, shuffle=False),
+    # degenerate cases of the method: no sink and a zero window (a Local row
+    # sees only itself), one-row segments, decode requests of a few rows,
+    # the smallest head count, many short segments with one row per Local tile
+    "edge_sink0_w0": Spec("edge_sink0_w0", 64, 512, 64, 0, 0, ProtectRule(boundary=8, p_random=0.5),
+                          seg_lengths=[37, 1, 64], n_new=5),
+    "edge_tiny_decode": Spec("edge_tiny_decode", 64, 512, 64, 4, 256, ProtectRule(none=True),
+                             decode_requests=6, decode_len_range=(1, 9), decode_seg_range=(1, 3)),
+    "edge_h8": Spec("edge_h8", 8, 512, 64, 4, 16, ProtectRule(boundary=4, budget=0.25),
+                    seg_lengths=[40, 75], n_new=13),
+    "edge_many_segs": Spec("edge_many_segs", 128, 512, 64, 2, 7, ProtectRule(boundary=1, budget=0.10),
+                           seg_len_range=(1, 9), n_segments=40, n_new=30),
     # a value that carries a rotary part (V = the whole latent row, output
     # phase restored): the long-context and decode geometries with a 512-wide
     # latent row of 448 nope + 64 rope dims, and reduced versions for parity
@@ -214,7 +225,7 @@ def make_geometry(name: str, seed: int = 0) -> Workload:
         doc = 0
         for _ in range(spec.decode_requests):
             L = int(rng.integers(lo, hi + 1))
-            S = int(rng.integers(slo, shi + 1))
+            S = min(int(rng.integers(slo, shi + 1)), L)   # at least one row per segment
             lens = _composition(rng, L, S)
             order = rng.permutation(S)
             segs = []

@@ -196,3 +196,17 @@ def test_vrope_plan_rules():
     parts = pd.info["split_chunks"]
     body = ((parts * 8 * 512 * 4 + parts * 8 * 4 + 255) // 256) * 256
     assert body < pd.workspace_bytes <= body + 256 + 4 * parts
+
+
+@pytest.mark.parametrize("name", ["edge_sink0_w0", "edge_tiny_decode", "edge_h8", "edge_many_segs"])
+def test_edge_plans_count_attended_pairs(name):
+    """The degenerate geometries plan with the exact attended-pair counts
+    (H = 8 takes the mma.sync tiles, the others the 4-CTA kernel)."""
+    test_plan_counts_attended_pairs(name)
+    _, plan = _host_plan(name)
+    assert plan.info["kernel"] == (0 if name == "edge_h8" else 3)
+
+
+def test_lse_merge_no_rows_is_a_no_op():
+    L = B.lib()
+    assert L.rk_lse_merge(16, 32, 3, 0, 4, 8, 64, 128, None) == 0
