@@ -7,34 +7,43 @@
 // "Insight 1": Global heads see every k <= p, Local heads k <= p with
 // k < sink or k >= p - w.
 //
-// A tile is 128 query pairs: 128 / G consecutive rows x the G query heads of
-// one KV head, so each key page is read once for the whole group.  One CTA
-// per tile (320 threads):
-//   warp 0     TMA producer: for each key block its K page and, one block
-//              behind, its V page (each a 32 KB box of 128 tokens x 128
-//              dims, chunk-major, 128-byte swizzled) through a six-slot ring
-//              (a box takes ~3 us from issue to arrival, so the bytes in
-//              flight set the pace).
-//   warp 1     MMA issuer: S_j = Q K_j^T (M = 128, N = 128 keys, A = Q from
-//              tensor memory, B = K from shared memory) into one of two S
-//              buffers, then O += P_{j-1} V_{j-1} (A = P from tensor memory,
-//              B = V in MN-major form, N = 128).
-//   warps 2-9  two threads per query pair (its TMEM lane), one in each
-//              warpgroup, each taking half of the 128 keys of a block and
-//              half of the 128 output columns: write the query row into
-//              tensor memory (the A operand), mask the edge blocks, agree on
-//              the block's row max through shared memory (a per-block
-//              bar.red vote that also lets every warp leave together after a
-//              failed wait), keep the running max in the log2 domain with a
-//              lazy rescale of O when it grows by more than 2^8, write P
-//              (bf16) to tensor memory, and finally normalise and store O and
-//              the LSE.
-// Tensor memory (512 columns): O (128) | S (2 x 128) | P (64) | Q (64), P and
-// Q as bf16 pairs.
-// A tile with few rows and a long walk (a decode step of a Global head) is
-// split into parts of a few blocks on separate CTAs; each part leaves its
-// normalised partial output and LSE in the workspace and the last part of
-// the tile merges them by log-sum-exp (parts without a visible key weigh 0).
+// A sub-tile is 128 query pairs: 128 / G consecutive rows x the G query heads
+// of one KV head, so every key page is read once for the whole group.  Two
+// kernels share the tile list format:
+//
+// seg_paged_two_kernel, for tiles with more than 64 pairs in use (never
+// split): a tile is two sub-tiles (the second the next 128 / G rows) that walk the union of
+// their key blocks, so a page serves 2 x 128 / G rows.  One CTA per tile
+// (320 threads):
+//   warp 0     TMA producer: for each key block its K page, then its V page
+//              (each a 32 KB box of 128 tokens x 128 dims, chunk-major,
+//              128-byte swizzled), through a four-slot ring.
+//   warp 1     MMA issuer, alternating the sub-tiles A and B so that one's
+//              softmax runs under the other's MMAs: PV_A(j), S_A(j+1),
+//              PV_B(j), S_B(j+1), ... with S_X = Q_X K^T (M = 128, N = 128
+//              keys, A = Q_X and B = K from shared memory) and O_X += P_X V
+//              (A = P_X from tensor memory, B = V in MN-major form).
+//   warps 2-5  sub-tile A, warps 6-9 sub-tile B: one thread per query pair
+//              (its TMEM lane) writes its query row into shared memory, masks
+//              the edge blocks, keeps the running max in the log2 domain with
+//              a lazy rescale of O when it grows by more than 2^8, writes P
+//              (bf16) over the first half of its S columns, and finally
+//              normalises and stores O and the LSE.
+// Tensor memory (512 columns): S_A / P_A (128) | S_B / P_B (128) | O_A (128) |
+// O_B (128).  P_X overwrites S_X after the lanes have read it; the next S_X
+// is issued after the P.V that reads P_X, and the MMAs of one thread run in
+// issue order.
+//
+// seg_paged_one_kernel, for tiles with at most 64 pairs in use (decode
+// steps): one sub-tile per CTA whose query pairs each have two lane threads,
+// one per warpgroup, taking half of a block's keys and half of the output
+// columns (the row max is agreed through shared memory with a per-block
+// bar.red vote that also lets every warp leave together after a failed
+// wait); Q in tensor memory, S double-buffered, a six-slot K/V ring.  A long
+// walk (a decode step of a Global head) is split into parts of 32 blocks on
+// separate CTAs; each part leaves its normalised partial output and LSE in
+// the workspace and the last part merges them by log-sum-exp (parts without
+// a visible key weigh 0).
 // Every wait is bounded (2 s); on expiry the CTA records
 // RK_ERR_DEVICE_TIMEOUT and every role stops; the producer waits (bounded)
 // for its copies in flight and tensor memory is released after the MMA pipe
@@ -53,27 +62,6 @@ namespace sp {
 constexpr int PAGE = 128;                   // tokens per page (= keys per block)
 constexpr int DH = 128;                     // head dim
 constexpr uint32_t CHUNK = 16384;           // 128 rows x 64 bf16
-constexpr int THREADS = 320;
-constexpr int RING = 6;
-constexpr uint32_t SLOT = 2 * CHUNK;        // one K or V page
-constexpr uint32_t OFF_RING = 0;
-constexpr uint32_t OFF_BAR = OFF_RING + RING * SLOT;
-enum {
-  B_FULL = 0,
-  B_EMPTY = RING,
-  B_QFULL = 2 * RING,       // queries in tensor memory (one arrival per lane warp, 8)
-  B_SFULL,                   // 2: S buffer j & 1 written
-  B_SFREE = B_SFULL + 2,     // 2: S buffer read (one arrival per lane warp, 8)
-  B_PREADY = B_SFREE + 2,    // P_j written and O rescaled (one arrival per lane warp, 8)
-  B_ODONE,                   // O += P_j V_j done
-  B_FINAL,
-  NBAR
-};
-constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
-constexpr uint32_t OFF_X = (OFF_MISC + 16 + 15) & ~15u;  // row max [2 buffers][2 halves][128], sums [2][128]
-constexpr uint32_t SMEM_BYTES = OFF_X + (4 + 2) * 128 * 4 + 1024;
-static_assert(SMEM_BYTES <= 232448, "shared memory");
-constexpr uint32_t T_O = 0, T_S = 128, T_P = 384, T_Q = 448;
 
 struct Req {
   int32_t T;
@@ -82,11 +70,12 @@ struct Req {
   int64_t table_off;     // offset of the request's [Hkv][max_blocks] block table
 };
 
-// 128 / G rows from p0 of KV head g; its key walk is blocks [0, sink_blocks)
-// then [win_lo, hi] (sink_blocks = 0: [win_lo, hi] only), and this CTA takes
-// walk steps [jb, je).  A split tile's parts are part_first ..
-// part_first + nparts - 1; their partials sit at workspace lanes
-// lane0 + (part - part_first) * rows * G + m.
+// rows (up to 2 x 128 / G) from p0 of KV head g: sub-tile A the first
+// 128 / G of them, sub-tile B the rest; the key walk is blocks
+// [0, sink_blocks) then [win_lo, hi] (sink_blocks = 0: [win_lo, hi] only),
+// and this CTA takes walk steps [jb, je).  A split tile's parts are
+// part_first .. part_first + nparts - 1; their partials sit at workspace
+// lanes lane0 + (part - part_first) * rows * G + m.
 struct Tile {
   int32_t req, g, p0, rows;
   int32_t sink_blocks, win_lo, hi, jb;
@@ -119,8 +108,338 @@ __device__ __forceinline__ int block_of(const Tile& t, int j) {
   return j < t.sink_blocks ? j : t.win_lo + (j - t.sink_blocks);
 }
 
+// ---- two sub-tiles of 128 pairs per CTA (tiles with more than 64 pairs in use)
+namespace two {
+
+constexpr int THREADS = 320;
+constexpr int RING = 4;
+constexpr uint32_t SLOT = 2 * CHUNK;        // one K or V page
+constexpr uint32_t OFF_Q = 0;               // Q_A, Q_B: 2 x 32 KB
+constexpr uint32_t OFF_RING = 4 * CHUNK;
+constexpr uint32_t OFF_BAR = OFF_RING + RING * SLOT;
+enum {
+  B_FULL = 0,
+  B_EMPTY = RING,
+  B_QFULL = 2 * RING,        // queries in shared memory (one arrival per lane warp, 8)
+  B_SFULL,                   // 2 (A, B): S_X(j) written
+  B_PREADY = B_SFULL + 2,    // 2: P_X(j) written and O_X rescaled (one arrival per warp of X, 4)
+  B_ODONE = B_PREADY + 2,    // 2: O_X += P_X(j) V(j) done
+  B_FINAL = B_ODONE + 2,
+  NBAR
+};
+constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
+constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;
+static_assert(SMEM_BYTES <= 232448, "shared memory");
+constexpr uint32_t T_S = 0, T_O = 256;      // sub-tile X: S/P at 128 X, O at 256 + 128 X
+
 __global__ void __launch_bounds__(THREADS, 1)
-    seg_paged_kernel(const __grid_constant__ Args a, const __grid_constant__ Maps mp) {
+    seg_paged_two_kernel(const __grid_constant__ Args a, const __grid_constant__ Maps mp) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
+  uint32_t* misc = reinterpret_cast<uint32_t*>(sm + OFF_MISC);
+  const tt::Ctx c{bar, reinterpret_cast<volatile uint32_t*>(misc + 1), a.status};
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const Tile t = a.tiles[blockIdx.x];
+  const Req rq = a.reqs[t.req];
+  const int nb = t.je - t.jb;                 // this CTA's walk steps
+  const int RT = 128 / a.G;                   // rows of a sub-tile
+  const bool has_b = t.rows > RT;             // sub-tile B in use
+
+  if (tid == 0) {
+    for (int i = 0; i < RING; ++i) {
+      tc::mbar_init(&bar[B_FULL + i], 1);
+      tc::mbar_init(&bar[B_EMPTY + i], 1);
+    }
+    tc::mbar_init(&bar[B_QFULL], 8);
+    for (int x = 0; x < 2; ++x) {
+      tc::mbar_init(&bar[B_SFULL + x], 1);
+      tc::mbar_init(&bar[B_PREADY + x], 4);
+      tc::mbar_init(&bar[B_ODONE + x], 1);
+    }
+    tc::mbar_init(&bar[B_FINAL], 1);
+    misc[1] = 0;
+    tc::fence_barrier_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(misc, 512);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tbase = misc[0];
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer --
+    if (lane == 0) {
+      tc::prefetch_tmap(&mp.k);
+      tc::prefetch_tmap(&mp.v);
+      const int32_t* tab = a.table + rq.table_off + int64_t(t.g) * a.max_blocks;
+      uint32_t cnt = 0;
+      bool ok = true;
+      auto load = [&](const CUtensorMap* map, int page) {
+        const int slot = cnt % RING;
+        if (!tt::wait_bar(c, B_EMPTY + slot, ((cnt / RING) & 1) ^ 1)) return false;
+        tc::mbar_arrive_expect_tx(&bar[B_FULL + slot], SLOT);
+        tc::tma_load_4d(smem_u32(sm + OFF_RING + slot * SLOT), map, &bar[B_FULL + slot], 0, 0, 0,
+                        page);
+        ++cnt;
+        return true;
+      };
+      // K_j, then V_j: the order in which the issuer first needs them
+      for (int j = 0; j < nb && ok; ++j) {
+        const int page = tab[block_of(t, t.jb + j)];
+        ok = load(&mp.k, page);
+        if (ok) ok = load(&mp.v, page);
+      }
+      // copies in flight land before the CTA may exit
+      for (uint32_t k = (cnt > RING ? cnt - RING : 0); k < cnt; ++k)
+        tt::drain_bar(c, B_FULL + k % RING, (k / RING) & 1);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------- MMA issuer ---
+    if (lane == 0) {
+      bool ok = tt::wait_bar(c, B_QFULL, 0);
+      tc::tc_fence_after();
+      const uint32_t idS = tc::idesc_bf16(128, 128, false, false);
+      const uint32_t idPV = tc::idesc_bf16(128, 128, false, true);
+      const uint32_t qa = smem_u32(sm + OFF_Q), ra = smem_u32(sm + OFF_RING);
+      const int nx = has_b ? 2 : 1;
+      // slot of K_j is 2j mod RING, of V_j 2j + 1 mod RING (loads alternate)
+      auto full = [&](uint32_t ld) {
+        const bool r = tt::wait_bar(c, B_FULL + ld % RING, (ld / RING) & 1);
+        tc::tc_fence_after();
+        return r;
+      };
+      auto score = [&](int x, int j) {
+        const uint32_t base = ra + ((2u * j) % RING) * SLOT;
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc)
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            tc::mma_ss(tbase + T_S + 128 * x,
+                       tc::sdesc_sw128(qa + (2 * x + cc) * CHUNK + 32 * k, 16, 1024),
+                       tc::sdesc_sw128(base + cc * CHUNK + 32 * k, 16, 1024), idS, (cc | k) != 0);
+        tc::mma_commit(&bar[B_SFULL + x]);
+      };
+      auto pv = [&](int x, int j) {
+        const uint32_t base = ra + ((2u * j + 1) % RING) * SLOT;
+        // B = V[16 keys x 128 dims]: two 64-dim chunks 16 KB apart (LBO)
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          tc::mma_ts(tbase + T_O + 128 * x, tbase + T_S + 128 * x + 8 * k,
+                     tc::sdesc_sw128(base + 2048 * k, CHUNK, 1024), idPV, (j > 0 || k > 0) ? 1u : 0u);
+        tc::mma_commit(&bar[B_ODONE + x]);
+      };
+      if (ok && nb > 0) {
+        ok = full(0);
+        if (ok) {
+          for (int x = 0; x < nx; ++x) score(x, 0);
+          tc::mma_commit(&bar[B_EMPTY + 0]);  // K_0 read by every score MMA
+        }
+      }
+      for (int j = 0; j < nb && ok; ++j) {
+        ok = full(2u * j + 1);              // V_j
+        const bool more = j + 1 < nb;
+        for (int x = 0; x < nx && ok; ++x) {
+          ok = tt::wait_bar(c, B_PREADY + x, j & 1);
+          if (!ok) break;
+          tc::tc_fence_after();
+          pv(x, j);
+          if (more) {
+            if (x == 0) ok = full(2u * j + 2);  // K_{j+1}
+            if (!ok) break;
+            score(x, j + 1);
+          }
+        }
+        if (!ok) break;
+        tc::mma_commit(&bar[B_EMPTY + (2u * j + 1) % RING]);          // V_j
+        if (more) tc::mma_commit(&bar[B_EMPTY + (2u * j + 2) % RING]);  // K_{j+1}
+      }
+      tc::mma_commit(&bar[B_FINAL]);
+    }
+  } else {
+    // ------------------------------------------- softmax and epilogue ----
+    const int lw = warp - 2;           // 0..7
+    const int x = lw >> 2;             // sub-tile
+    const int quarter = warp & 3;      // TMEM lane quarter this warp may access
+    const int m = quarter * 32 + lane;
+    const int r = m / a.G, h = m - r * a.G;
+    const int p = t.p0 + x * RT + r;
+    const bool active = x == 0 || has_b;  // this warpgroup's sub-tile exists
+    const bool valid = x * RT + r < t.rows;
+    const bool glob = a.role[t.g] != 0;
+    const uint32_t lt = tbase + (static_cast<uint32_t>(quarter * 32) << 16);
+    const uint32_t tS = lt + T_S + 128 * x, tO = lt + T_O + 128 * x;
+    const float sl2 = a.scale_log2;
+    const int sink = a.sink, window = a.window;
+    const int64_t row = rq.row_base + (p - rq.q_row_begin);
+    const int head = t.g * a.G + h;
+    // this lane's query row -> shared memory: two 64-dim chunks of 128 rows,
+    // 128-byte swizzle (A operand of the score MMAs); rows past the tile's
+    // end are zero
+    {
+      const uint4* src = valid ? reinterpret_cast<const uint4*>(a.q + (row * a.Hq + head) * DH)
+                               : nullptr;
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const uint4 v = src ? __ldg(src + u) : make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(sm + OFF_Q + (2 * x + (u >> 3)) * CHUNK + m * 128 +
+                                  (((u & 7) ^ (m & 7)) << 4)) = v;
+      }
+      tc::fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&bar[B_QFULL]);
+    }
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = active;
+    for (int j = 0; j < nb && ok; ++j) {
+      const int k0 = block_of(t, t.jb + j) * PAGE;
+      ok = __all_sync(0xffffffffu, tt::wait_bar(c, B_SFULL + x, j & 1));
+      if (!ok) break;
+      tc::tc_fence_after();
+      uint32_t s[4][32];
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) tc::tmem_ld32(tS + 32 * q4, s[q4]);
+      tc::tmem_wait_ld();
+      // every key of the block visible for this row?  (then no masks)
+      const bool full = valid && k0 + PAGE - 1 <= p &&
+                        (glob || k0 >= p - window || k0 + PAGE <= sink);
+      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      if (__all_sync(0xffffffffu, full)) {
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], __uint_as_float(s[q4][i]));
+      } else {
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int key = k0 + 32 * q4 + i;
+            bool vis = valid && key <= p;
+            if (!glob) vis = vis && (key < sink || key >= p - window);
+            const float xv = vis ? __uint_as_float(s[q4][i]) : -INFINITY;
+            s[q4][i] = __float_as_uint(xv);
+            mx4[i & 3] = fmaxf(mx4[i & 3], xv);
+          }
+        }
+      }
+      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * sl2;
+      bool need = false;
+      float alpha = 1.f;
+      if (mx > m_run + 8.f) {  // lazy rescale: only when the max grows by more than 2^8
+        if (m_run != -INFINITY) {
+          need = true;
+          alpha = fast_exp2(m_run - mx);
+        }
+        m_run = mx;
+      }
+      const float nbias = (m_run == -INFINITY) ? 0.f : -m_run;
+      float ls4[4] = {0.f, 0.f, 0.f, 0.f};
+      // P in place: keys 2i, 2i + 1 of column block q4 go to word 16 q4 + i
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float p0 = fast_exp2(fmaf(__uint_as_float(s[q4][2 * i]), sl2, nbias));
+          const float p1 = fast_exp2(fmaf(__uint_as_float(s[q4][2 * i + 1]), sl2, nbias));
+          ls4[i & 3] += p0 + p1;
+          s[q4 >> 1][16 * (q4 & 1) + i] = pack_bf16x2(p0, p1);
+        }
+      }
+      l_run = l_run * alpha + ((ls4[0] + ls4[1]) + (ls4[2] + ls4[3]));
+      // S_X(j) was issued after P_X(j-1).V, and its completion (above)
+      // implies that of every earlier MMA: P and O are free
+      tc::tmem_st32(tS, s[0]);
+      tc::tmem_st32(tS + 32, s[1]);
+      if (__any_sync(0xffffffffu, need)) {
+#pragma unroll 1
+        for (int q8 = 0; q8 < 4; ++q8) {
+          uint32_t o[32];
+          tc::tmem_ld32(tO + 32 * q8, o);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tc::tmem_st32(tO + 32 * q8, o);
+        }
+      }
+      tc::tmem_wait_st();
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&bar[B_PREADY + x]);
+    }
+    // ---- epilogue ----
+    if (ok) ok = __all_sync(0xffffffffu, tt::wait_bar(c, B_FINAL, 0));
+    tc::tc_fence_after();
+    // tiles of this kernel are never split
+    if (ok) {
+      const bool st = valid && l_run > 0.f;
+      const float inv = st ? 1.f / l_run : 0.f;
+      uint16_t* dst = st ? a.out + (row * a.Hq + head) * DH : nullptr;
+#pragma unroll 1
+      for (int q8 = 0; q8 < 4; ++q8) {
+        uint32_t o[32];
+        tc::tmem_ld32(tO + 32 * q8, o);
+        tc::tmem_wait_ld();
+        if (st) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * q8);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            uint4 v;
+            v.x = pack_bf16x2(__uint_as_float(o[8 * u + 0]) * inv, __uint_as_float(o[8 * u + 1]) * inv);
+            v.y = pack_bf16x2(__uint_as_float(o[8 * u + 2]) * inv, __uint_as_float(o[8 * u + 3]) * inv);
+            v.z = pack_bf16x2(__uint_as_float(o[8 * u + 4]) * inv, __uint_as_float(o[8 * u + 5]) * inv);
+            v.w = pack_bf16x2(__uint_as_float(o[8 * u + 6]) * inv, __uint_as_float(o[8 * u + 7]) * inv);
+            d4[u] = v;
+          }
+        }
+      }
+      if (st) a.lse[row * a.Hq + head] = m_run * 0.6931471805599453f + logf(l_run);
+    }
+  }
+
+  // ------------------------------------------------------------ teardown --
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tt::drain_bar(c, B_FINAL, 0);  // the MMA pipe is empty before TMEM is released
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tbase, 512);
+  }
+}
+
+}  // namespace two
+
+// ---- one sub-tile, two lane warpgroups (decode steps, split parts, small tiles)
+namespace one {
+
+constexpr int THREADS = 320;
+constexpr int RING = 6;
+constexpr uint32_t SLOT = 2 * CHUNK;        // one K or V page
+constexpr uint32_t OFF_RING = 0;
+constexpr uint32_t OFF_BAR = OFF_RING + RING * SLOT;
+enum {
+  B_FULL = 0,
+  B_EMPTY = RING,
+  B_QFULL = 2 * RING,       // queries in tensor memory (one arrival per lane warp, 8)
+  B_SFULL,                   // 2: S buffer j & 1 written
+  B_SFREE = B_SFULL + 2,     // 2: S buffer read (one arrival per lane warp, 8)
+  B_PREADY = B_SFREE + 2,    // P_j written and O rescaled (one arrival per lane warp, 8)
+  B_ODONE,                   // O += P_j V_j done
+  B_FINAL,
+  NBAR
+};
+constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
+constexpr uint32_t OFF_X = (OFF_MISC + 16 + 15) & ~15u;  // row max [2 buffers][2 halves][128], sums [2][128]
+constexpr uint32_t SMEM_BYTES = OFF_X + (4 + 2) * 128 * 4 + 1024;
+static_assert(SMEM_BYTES <= 232448, "shared memory");
+constexpr uint32_t T_O = 0, T_S = 128, T_P = 384, T_Q = 448;
+
+__global__ void __launch_bounds__(THREADS, 1)
+    seg_paged_one_kernel(const __grid_constant__ Args a, const __grid_constant__ Maps mp) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
@@ -470,6 +789,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
+}  // namespace one
+
 }  // namespace sp
 }  // namespace rk
 
@@ -483,11 +804,13 @@ struct rk_segpaged_plan_s {
   size_t workspace_bytes = 0;
   rk_segpaged_info_t info{};
   std::vector<rk::sp::Req> reqs;
-  std::vector<rk::sp::Tile> tiles;
+  std::vector<rk::sp::Tile> tiles;      // two sub-tiles per CTA
+  std::vector<rk::sp::Tile> tiles_one;  // one sub-tile per CTA (<= 64 pairs in use)
   std::vector<int32_t> table;
   std::vector<uint8_t> role;
   rk::sp::Req* d_reqs = nullptr;
   rk::sp::Tile* d_tiles = nullptr;
+  rk::sp::Tile* d_tiles_one = nullptr;
   int32_t* d_table = nullptr;
   uint8_t* d_role = nullptr;
   int32_t* d_status = nullptr;
@@ -501,11 +824,13 @@ constexpr int kSplitBlocks = 32;  // walk steps per part of a split tile
 void sp_free(rk_segpaged_plan_s* p) {
   cudaFree(p->d_reqs);
   cudaFree(p->d_tiles);
+  cudaFree(p->d_tiles_one);
   cudaFree(p->d_table);
   cudaFree(p->d_role);
   cudaFree(p->d_status);
   p->d_reqs = nullptr;
   p->d_tiles = nullptr;
+  p->d_tiles_one = nullptr;
   p->d_table = nullptr;
   p->d_role = nullptr;
   p->d_status = nullptr;
@@ -551,7 +876,7 @@ rk_status_t sp_build(const rk_segpaged_desc_t* d, rk_segpaged_plan_s* p) {
   for (int g = 0; g < Hkv; ++g)
     if (d->kv_head_role[g] > 1) return RK_ERR_INVALID_ARG;
   const bool dense = (d->flags & RK_SEGPAGED_DENSE_MASK) != 0;
-  const int RT = 128 / G;
+  const int RT = 256 / G;  // rows of a tile: two sub-tiles of 128 / G rows
   p->Hq = d->num_q_heads;
   p->Hkv = Hkv;
   p->G = G;
@@ -567,7 +892,7 @@ rk_status_t sp_build(const rk_segpaged_desc_t* d, rk_segpaged_plan_s* p) {
   rk_segpaged_info_t& info = p->info;
   info = rk_segpaged_info_t{};
   info.group = G;
-  std::vector<std::pair<int64_t, rk::sp::Tile>> list;
+  std::vector<std::pair<int64_t, rk::sp::Tile>> list, list_one;
   int64_t rows = 0;
   for (int r = 0; r < R; ++r) {
     const int64_t T = d->seq_len[r], qb = d->q_row_begin[r];
@@ -611,12 +936,13 @@ rk_status_t sp_build(const rk_segpaged_desc_t* d, rk_segpaged_plan_s* p) {
           if (tab[b] < 0 || tab[b] >= d->num_pages) return RK_ERR_INVALID_ARG;
         }
         info.kv_blocks += nb;
-        info.performed_pairs += int64_t(nb) * 128 * PAGE;
+        info.performed_pairs += int64_t(nb) * (t.rows > RT / 2 ? 256 : 128) * PAGE;
         t.jb = 0;
         t.je = nb;
         t.part = t.part_first = 0;
         t.nparts = 1;
-        if (t.rows * G <= 64 && nb > 2 * kSplitBlocks) {
+        const bool small = t.rows * G <= 64;  // at most 64 pairs in use: one-sub-tile kernel
+        if (small && nb > 2 * kSplitBlocks) {
           // a long walk of few rows: parts of kSplitBlocks steps, merged at the end
           const int np = (nb + kSplitBlocks - 1) / kSplitBlocks;
           t.nparts = np;
@@ -629,23 +955,26 @@ rk_status_t sp_build(const rk_segpaged_desc_t* d, rk_segpaged_plan_s* p) {
             u.part = q;
             u.jb = q * kSplitBlocks;
             u.je = std::min(nb, (q + 1) * kSplitBlocks);
-            list.push_back({u.je - u.jb, u});
+            list_one.push_back({u.je - u.jb, u});
           }
           continue;
         }
-        list.push_back({nb, t});
+        (small ? list_one : list).push_back({nb, t});
       }
     }
     rows += T - qb;
   }
-  if (rows * d->num_q_heads > (int64_t(1) << 40) || list.size() > INT32_MAX / 2)
+  if (rows * d->num_q_heads > (int64_t(1) << 40) || list.size() > INT32_MAX / 2 ||
+      list_one.size() > INT32_MAX / 2)
     return RK_ERR_CAPACITY;
-  std::stable_sort(list.begin(), list.end(),
-                   [](const auto& x, const auto& y) { return x.first > y.first; });
+  auto longest_first = [](const auto& x, const auto& y) { return x.first > y.first; };
+  std::stable_sort(list.begin(), list.end(), longest_first);
+  std::stable_sort(list_one.begin(), list_one.end(), longest_first);
   for (auto& e : list) p->tiles.push_back(e.second);
+  for (auto& e : list_one) p->tiles_one.push_back(e.second);
   p->rows = rows;
   info.rows = rows;
-  info.tiles = static_cast<int64_t>(p->tiles.size());
+  info.tiles = static_cast<int64_t>(p->tiles.size() + p->tiles_one.size());
   if (p->split_lanes > INT32_MAX / 2 || p->split_tiles > INT32_MAX / 2) return RK_ERR_CAPACITY;
   if (p->split_tiles) {
     size_t b = static_cast<size_t>(p->split_lanes) * (rk::sp::DH + 1) * sizeof(float);
@@ -671,6 +1000,7 @@ extern "C" rk_status_t rk_segpaged_plan(const rk_segpaged_desc_t* desc, void* st
     if (cudaGetDevice(&p->device) != cudaSuccess) st = RK_ERR_CUDA;
     if (st == RK_OK) st = sp_upload(p->reqs, &p->d_reqs, s);
     if (st == RK_OK) st = sp_upload(p->tiles, &p->d_tiles, s);
+    if (st == RK_OK) st = sp_upload(p->tiles_one, &p->d_tiles_one, s);
     if (st == RK_OK) st = sp_upload(p->table, &p->d_table, s);
     if (st == RK_OK) st = sp_upload(p->role, &p->d_role, s);
     if (st == RK_OK) {
@@ -706,7 +1036,7 @@ extern "C" rk_status_t rk_segpaged_forward(rk_segpaged_plan_t p, const void* q, 
   int cur = -1;
   if (cudaGetDevice(&cur) != cudaSuccess) return RK_ERR_CUDA;
   if (cur != p->device) return RK_ERR_PLAN_MISMATCH;
-  if (p->tiles.empty()) return RK_OK;
+  if (p->tiles.empty() && p->tiles_one.empty()) return RK_OK;
   rk::sp::Maps mp{};
   {
     // a page viewed as (64 dims, 128 tokens, 2 chunks, pages): one page per box
@@ -745,12 +1075,27 @@ extern "C" rk_status_t rk_segpaged_forward(rk_segpaged_plan_t p, const void* q, 
         cudaSuccess)
       return RK_ERR_CUDA;
   }
-  if (cudaFuncSetAttribute(rk::sp::seg_paged_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(rk::sp::SMEM_BYTES)) != cudaSuccess)
-    return RK_ERR_CUDA;
-  rk::sp::seg_paged_kernel<<<static_cast<unsigned>(p->tiles.size()), rk::sp::THREADS,
-                             rk::sp::SMEM_BYTES, s>>>(a, mp);
-  return cudaGetLastError() == cudaSuccess ? RK_OK : RK_ERR_CUDA;
+  if (!p->tiles.empty()) {
+    namespace k2 = rk::sp::two;
+    if (cudaFuncSetAttribute(k2::seg_paged_two_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(k2::SMEM_BYTES)) != cudaSuccess)
+      return RK_ERR_CUDA;
+    a.tiles = p->d_tiles;
+    k2::seg_paged_two_kernel<<<static_cast<unsigned>(p->tiles.size()), k2::THREADS, k2::SMEM_BYTES,
+                               s>>>(a, mp);
+    if (cudaGetLastError() != cudaSuccess) return RK_ERR_CUDA;
+  }
+  if (!p->tiles_one.empty()) {
+    namespace k1 = rk::sp::one;
+    if (cudaFuncSetAttribute(k1::seg_paged_one_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(k1::SMEM_BYTES)) != cudaSuccess)
+      return RK_ERR_CUDA;
+    a.tiles = p->d_tiles_one;
+    k1::seg_paged_one_kernel<<<static_cast<unsigned>(p->tiles_one.size()), k1::THREADS,
+                               k1::SMEM_BYTES, s>>>(a, mp);
+    if (cudaGetLastError() != cudaSuccess) return RK_ERR_CUDA;
+  }
+  return RK_OK;
 }
 
 extern "C" size_t rk_segpaged_workspace_bytes(rk_segpaged_plan_t p) {

@@ -44,7 +44,8 @@ def test_pair_counts_and_blocks(name):
                 cnt = np.where(lo <= pw.sink, p + 1, np.minimum(pw.sink, p + 1) + p - lo + 1)
                 pairs += G * int(cnt.sum())
     assert info["pairs"] == pairs and info["rows"] == pw.rows and info["group"] == G
-    assert info["performed_pairs"] == info["kv_blocks"] * 128 * PAGE >= pairs
+    assert info["kv_blocks"] * 128 * PAGE <= info["performed_pairs"] <= info["kv_blocks"] * 256 * PAGE
+    assert info["performed_pairs"] >= pairs
     # the dense + mask arm walks every block up to each tile's last row
     if not (pw.block_table < 0).any():
         dense = _plan(pw, B.RK_SEGPAGED_DENSE_MASK).info
@@ -57,7 +58,7 @@ def test_qwen_128k_work():
     pw = make_paged_geometry("qwen32b_128k", 0)
     a = _plan(pw).info
     d = _plan(pw, B.RK_SEGPAGED_DENSE_MASK).info
-    assert a["tiles"] == 8 * 131072 // 16
+    assert a["tiles"] == 8 * 131072 // 32
     assert d["kv_blocks"] > 7 * a["kv_blocks"] // 2
     assert a["pairs"] == d["pairs"]
 
