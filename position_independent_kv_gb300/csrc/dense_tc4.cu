@@ -55,7 +55,7 @@ using tt::wait_bar;
 constexpr int TNK = 128;                   // keys per key tile
 constexpr uint32_t CHUNK = 16384;          // 128 rows x 64 bf16
 constexpr uint32_t HCHUNK = 8192;          // 64 rows x 64 bf16
-constexpr int THREADS = 192;
+constexpr int THREADS = 256;   // warps 6 and 7: the rope writers of the score pair
 
 // S pair: rotated q_rope hi and lo (K-major operands), a staging buffer for
 // P and the records, the key ring
@@ -83,8 +83,11 @@ enum {
   // SFREE, ROPE and PREADY take one arrival per lane warp of both CTAs of a
   // pair, made by lane 0 after the warp has synchronised
   B_SFREE = B_SFULL + 2,  // 2: S buffer read by both S CTAs' softmax lanes
-  B_ROPE = B_SFREE + 2,   // rotated q_rope of the next segment written (the first
-                          // event also publishes the queries in tensor memory)
+  B_ROPE = B_SFREE + 2,   // rotated q_rope of the next segment written (one arrival
+                          // per rope warp of both S CTAs)
+  B_QREADY,               // queries in tensor memory (one arrival per lane warp)
+  B_SWITCH,               // the last score MMAs of a segment are done (one phase per
+                          // segment switch, so the rope warps wait on every phase)
   B_SFINAL,
   B_PEMPTY,             // 2 (S CTAs): P buffer consumed by the output MMAs
   B_VFULL = B_PEMPTY + 2,
@@ -161,7 +164,9 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
       tc::mbar_init(&bar[B_PFULL + b], 1);
       tc::mbar_init(&bar[B_PREADY + b], 2 * 4);
     }
-    tc::mbar_init(&bar[B_ROPE], 2 * 4);
+    tc::mbar_init(&bar[B_ROPE], 2 * 2);
+    tc::mbar_init(&bar[B_QREADY], 2 * 4);
+    tc::mbar_init(&bar[B_SWITCH], 1);
     tc::mbar_init(&bar[B_SFINAL], 1);
     tc::mbar_init(&bar[B_ODONE], 1);
     tc::mbar_init(&bar[B_OFINAL], 1);
@@ -212,8 +217,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
         const uint32_t idS = tc::idesc_bf16(256, 128, false, false);
         const uint32_t ropa = smem_u32(sm + OFF_ROPE), ka = smem_u32(sm + OFF_KRING);
         uint32_t rope_ev = 0;
-        // the first event also publishes the queries in tensor memory
-        bool ok = wait_bar<true>(c, B_ROPE, rope_ev++ & 1);
+        bool ok = wait_bar<true>(c, B_QREADY, 0) && wait_bar<true>(c, B_ROPE, rope_ev++ & 1);
         uint32_t cnt = 0;
         int j = 0, prev_seg = -1;
         KeyTile cur{0, 0, 0, -1};
@@ -251,8 +255,94 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
           prev_seg = cur.j;
           ++j;
           have = next_key_tile<TNK>(cur, segs, nseg, 0, r0hi, r1lo, r1hi);
+          // a new segment follows: the rope warps may rewrite q_rope' once
+          // these MMAs are done
+          if (have && cur.j != prev_seg) tc::mma_commit_2sm(&bar[B_SWITCH], 0x3);
         }
         tc::mma_commit_2sm(&bar[B_SFINAL], 0x3);
+      }
+    } else if (warp >= 6) {
+      // ------------------------------------- S pair: rope writers -------
+      // q_rope' = R(-delta) q_rope as bf16 hi and lo rows of two K-major
+      // 128-byte-swizzled operands (RedKnot-MLA paper, RoPE-orthogonality
+      // paragraph), rewritten at every segment switch of the key walk as
+      // soon as the last score MMAs of the old segment are done; each lane
+      // keeps the raw q_rope of its two rows in registers
+      const int m0 = 64 * (warp - 6) + lane;
+      uint32_t raw[2][32];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const tt::RowInfo ri = tt::row_info(a, t, rq, m0 + 32 * e);
+        const uint16_t* qrow = ri.p >= 0 ? a.q + (ri.frow * a.H + ri.head) * DK : nullptr;
+        if (qrow) {
+          const uint4* s4 = reinterpret_cast<const uint4*>(qrow + 64 * NCH);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const uint4 v = __ldg(s4 + u);
+            raw[e][4 * u] = v.x;
+            raw[e][4 * u + 1] = v.y;
+            raw[e][4 * u + 2] = v.z;
+            raw[e][4 * u + 3] = v.w;
+          }
+        } else {
+#pragma unroll
+          for (int u = 0; u < 32; ++u) raw[e][u] = 0;
+        }
+      }
+      auto put_rope = [&](int seg) {
+        const float4* cs4 =
+            reinterpret_cast<const float4*>(a.rope_cs + static_cast<int64_t>(rq.seg_first + seg) * 64);
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int m = m0 + 32 * e;
+          const uint32_t sw = static_cast<uint32_t>(m & 7);
+          uint8_t* rrow = sm + OFF_ROPE + m * 128;
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            uint32_t hi[4], lo[4];
+#pragma unroll
+            for (int v2 = 0; v2 < 2; ++v2) {
+              const float4 w = __ldg(cs4 + 2 * u + v2);  // (cos, sin) of pairs 4u + 2 v2, + 1
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const int jj = 4 * u + 2 * v2 + h;
+                const float co = h ? w.z : w.x, si = h ? w.w : w.y;
+                const float x = __uint_as_float(raw[e][jj] << 16);
+                const float y = __uint_as_float(raw[e][jj] & 0xffff0000u);
+                const float xr = fmaf(x, co, y * si), yr = fmaf(-x, si, y * co);
+                const uint32_t hw = pack_bf16x2(xr, yr);
+                hi[2 * v2 + h] = hw;
+                lo[2 * v2 + h] = pack_bf16x2(xr - __uint_as_float(hw << 16),
+                                             yr - __uint_as_float(hw & 0xffff0000u));
+              }
+            }
+            *reinterpret_cast<uint4*>(rrow + ((u ^ sw) << 4)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4*>(rrow + CHUNK + ((u ^ sw) << 4)) =
+                make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          }
+        }
+        tc::fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive_cluster(cbar(B_ROPE, 0));
+      };
+      KeyTile kt{0, 0, 0, -1};
+      bool have = next_key_tile<TNK>(kt, segs, nseg, 0, r0hi, r1lo, r1hi);
+      if (have) put_rope(kt.j);
+      uint32_t sw_ev = 0;
+      bool ok = true;
+      while (ok && have) {
+        KeyTile nx = kt;
+        const bool have_next = next_key_tile<TNK>(nx, segs, nseg, 0, r0hi, r1lo, r1hi);
+        if (have_next && nx.j != kt.j) {
+          // the old segment's score MMAs are done: none reads q_rope' any more
+          ok = __all_sync(0xffffffffu, wait_bar(c, B_SWITCH, sw_ev++ & 1));
+          if (ok) {
+            tc::tc_fence_after();
+            put_rope(nx.j);
+          }
+        }
+        kt = nx;
+        have = have_next;
       }
     } else {
       // ------------------- S pair: queries, rotation and online softmax ---
@@ -287,52 +377,11 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
         tc::tmem_st32(lt + T_Q + 32 * i, w);
       }
       tc::tmem_wait_st();
-      // q_rope' = R(-delta) q_rope as bf16 hi and lo rows of two K-major
-      // 128-byte-swizzled operands (RedKnot-MLA paper, RoPE-orthogonality
-      // paragraph)
-      auto put_rope = [&](int seg) {
-        const float* cs = a.rope_cs + static_cast<int64_t>(rq.seg_first + seg) * 64;
-        uint32_t raw[32];
-        if (qrow) {
-          const uint4* s4 = reinterpret_cast<const uint4*>(qrow + 64 * NCH);
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const uint4 v = __ldg(s4 + u);
-            raw[4 * u] = v.x;
-            raw[4 * u + 1] = v.y;
-            raw[4 * u + 2] = v.z;
-            raw[4 * u + 3] = v.w;
-          }
-        } else {
-#pragma unroll
-          for (int u = 0; u < 32; ++u) raw[u] = 0;
-        }
-        uint32_t hi[32];
-#pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
-          const float x = __uint_as_float(raw[jj] << 16), y = __uint_as_float(raw[jj] & 0xffff0000u);
-          const float co = __ldg(cs + 2 * jj), si = __ldg(cs + 2 * jj + 1);
-          const float xr = fmaf(x, co, y * si), yr = fmaf(-x, si, y * co);
-          hi[jj] = pack_bf16x2(xr, yr);
-          raw[jj] = pack_bf16x2(xr - __uint_as_float(hi[jj] << 16),
-                                yr - __uint_as_float(hi[jj] & 0xffff0000u));
-        }
-        uint8_t* rrow = sm + OFF_ROPE + m * 128;
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          *reinterpret_cast<uint4*>(rrow + ((u ^ sw) << 4)) =
-              make_uint4(hi[4 * u], hi[4 * u + 1], hi[4 * u + 2], hi[4 * u + 3]);
-          *reinterpret_cast<uint4*>(rrow + CHUNK + ((u ^ sw) << 4)) =
-              make_uint4(raw[4 * u], raw[4 * u + 1], raw[4 * u + 2], raw[4 * u + 3]);
-        }
-        tc::fence_proxy_async();
-      };
-      KeyTile kt{0, 0, 0, -1};
-      bool have = next_key_tile<TNK>(kt, segs, nseg, 0, r0hi, r1lo, r1hi);
-      put_rope(kt.j);
       tc::tc_fence_before();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive_cluster(cbar(B_ROPE, 0));
+      if (lane == 0) tc::mbar_arrive_cluster(cbar(B_QREADY, 0));
+      KeyTile kt{0, 0, 0, -1};
+      bool have = next_key_tile<TNK>(kt, segs, nseg, 0, r0hi, r1lo, r1hi);
       float m_run = -INFINITY, l_run = 0.f;
       int j = 0;
       bool ok = true;
@@ -348,12 +397,6 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
         float alpha = 1.f;
         if (okw) {
           tc::tc_fence_after();
-          // S_j is complete, so no score MMA still reads the rotated q_rope
-          if (have_next && nx.j != kt.j) {
-            put_rope(nx.j);
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive_cluster(cbar(B_ROPE, 0));
-          }
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) tc::tmem_ld32(lt + T_S + 128 * b + 32 * q4, s[q4]);
           tc::tmem_wait_ld();
@@ -506,7 +549,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
         }
         tc::mma_commit_2sm(&bar[B_OFINAL], 0xC);
       }
-    } else {
+    } else if (warp < 6) {
       // ------------------------------- O pair: rescale and epilogue ------
       const int quarter = warp & 3;
       const int m = quarter * 32 + lane;
