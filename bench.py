@@ -300,8 +300,17 @@ def bench_prefill(args, ws, local, pk):
         h_lat = torch.empty(wl.latent_pool.shape, dtype=wl.latent_pool.dtype, pin_memory=True)
         h_lat.copy_(wl.latent_pool)
         torch.cuda.synchronize(dev)
-        h2d = sum(t.numel() * t.element_size() for t in (h_q, h_out, h_lse, h_lat))
-        d2h = out.numel() * out.element_size() + lse.numel() * lse.element_size()
+        # in: q, lse and the latents (out is not uploaded: no kernel reads it);
+        # out: lse and the written elements of out (whole protected rows, the
+        # Global heads of the others)
+        h2d = sum(t.numel() * t.element_size() for t in (h_q, h_lse, h_lat))
+        row_bytes = wl.d_v * out.element_size()
+        if info["num_local_heads"]:
+            prot = info["protected_local_rows"]
+            written = (prot * wl.H + (info["rows"] - prot) * info["num_global_heads"]) * row_bytes
+        else:
+            written = out.numel() * out.element_size()
+        d2h = written + lse.numel() * lse.element_size()
         steps = max(1, min(args.steps, 3))
         barrier(ws)
         torch.cuda.synchronize(dev)

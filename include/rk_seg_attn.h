@@ -223,9 +223,13 @@ rk_status_t rk_seg_attn_forward(rk_seg_attn_plan_t plan, const void* q, void* ou
 /* The same forward with q, out and lse starting and ending in host memory:
  * the copies to and from the device run inside the call, overlapped with
  * the kernels.  The computed rows are taken in eight consecutive ranges;
- * a range is copied in on a plan-owned stream, its tiles run on `stream` as
- * soon as it (and every earlier range) is on the device, and it is copied
- * back on a second plan-owned stream once the tiles that write it are done.
+ * a range's q and lse rows are copied in on a plan-owned stream, its tiles
+ * run on `stream` as soon as it (and every earlier range) is on the device,
+ * and its results are copied back on a second plan-owned stream once the
+ * tiles that write it are done.  Only written elements of out travel: the
+ * whole row where every head is written (protected rows, or every row when
+ * all heads are Global) and the Global heads' columns of the other rows;
+ * out is never copied in, since no kernel reads it.
  * (The pages have no counterpart; this is how a host-resident query batch
  * meets the device-resident document latents.)
  * q_host, out_host, lse_host  host arrays of the shapes of q, out, lse
@@ -233,7 +237,9 @@ rk_status_t rk_seg_attn_forward(rk_seg_attn_plan_t plan, const void* q, void* ou
  *            lse.  Page-locked memory lets the copies overlap; pageable
  *            memory is accepted and is copied synchronously.
  * q, out, lse device arrays of the full sizes (as for rk_seg_attn_forward);
- *            the call overwrites them with the host contents first.
+ *            q and lse are overwritten with the host contents first; out
+ *            receives the written elements, its other elements are left
+ *            unspecified.
  * workspace  as for rk_seg_attn_forward.
  * Asynchronous on `stream`: work queued on `stream` before the call runs
  * first, and `stream` continues only after out_host and lse_host hold the

@@ -264,8 +264,9 @@ class SegAttnPlan:
 
     def forward_host(self, q_host, out_host, lse_host, q, out, lse, workspace=None, stream=None):
         """rk_seg_attn_forward_host: q_host/out_host/lse_host are host tensors
-        (pinned for overlap); q/out/lse are device tensors of the same shapes
-        that the call fills from the host first."""
+        (pinned for overlap); q/out/lse are device tensors of the same shapes.
+        q and lse go to the device; only the elements the kernels write come
+        back into out_host (out is never uploaded)."""
         ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
         st = lib().rk_seg_attn_forward_host(self._h, _ptr(q_host), _ptr(out_host), _ptr(lse_host),
                                             _ptr(q), _ptr(out), _ptr(lse), _ptr(workspace),

@@ -340,6 +340,13 @@ static rk_status_t build_plan(const rk_seg_attn_desc_t* d, rk_seg_attn_plan_s* p
       if (prot[q]) p->local_rows.push_back(static_cast<int32_t>(q));
     const int64_t nprot = static_cast<int64_t>(p->local_rows.size() - lr_first);
     if (HL) info.protected_local_rows += nprot;
+    for (size_t i = lr_first; i < p->local_rows.size(); ++i) {
+      const int64_t f = rq.row_base + (p->local_rows[i] - qb);
+      if (!p->full_rows.empty() && p->full_rows.back().second == f)
+        ++p->full_rows.back().second;
+      else
+        p->full_rows.push_back({f, f + 1});
+    }
 
     // algorithmic pairs
     for (int64_t q = qb; q < Tr; ++q) info.pairs_global += int64_t(HG) * (q + 1);
@@ -816,10 +823,9 @@ extern "C" rk_status_t rk_seg_attn_forward_host(rk_seg_attn_plan_t p, const void
     int64_t r0, r1;
     range(c, r0, r1);
     if (r1 > r0) {
+      // q and lse go in; out does not (no kernel reads it)
       const int64_t n = r1 - r0;
       good = ok(cudaMemcpyAsync(qd + r0 * qrow, qh + r0 * qrow, n * qrow, cudaMemcpyHostToDevice,
-                                p->copy_in)) &&
-             ok(cudaMemcpyAsync(od + r0 * orow, oh + r0 * orow, n * orow, cudaMemcpyHostToDevice,
                                 p->copy_in)) &&
              ok(cudaMemcpyAsync(ld + r0 * lrow, lh + r0 * lrow, n * lrow, cudaMemcpyHostToDevice,
                                 p->copy_in));
@@ -856,6 +862,23 @@ extern "C" rk_status_t rk_seg_attn_forward_host(rk_seg_attn_plan_t p, const void
     for (int c = 0; c < NC && good; ++c) good = ok(cudaEventRecord(p->ev_k[c], s));
   }
   good = good && ok(cudaEventRecord(p->ev_split, s));
+  // Only the elements the kernels write come back: whole rows where every
+  // head is written (protected rows; every row when all heads are Global)
+  // and the Global heads' columns of the other rows; the host keeps the rest
+  // of out_host as it was.  lse comes back whole (it went in whole).
+  const int HG = static_cast<int>(p->global_heads.size());
+  const bool all_global = p->local_heads.empty();
+  const size_t hbytes = static_cast<size_t>(p->d_v) * 2;
+  // Global heads c0 + s g (g < H / s) are one strided copy per range;
+  // otherwise one copy per run of consecutive Global heads
+  int gstride = 0;
+  if (HG > 0 && !all_global && p->H % HG == 0) {
+    const int sdiv = p->H / HG;
+    bool ev = p->global_heads[0] < sdiv;
+    for (int g = 0; g < HG && ev; ++g) ev = p->global_heads[g] == p->global_heads[0] + sdiv * g;
+    if (ev) gstride = sdiv;
+  }
+  size_t run = 0;  // first run of full rows not yet copied
   // range c is final once the kernels of ranges c and c + 1 (and any split
   // chunks) are done
   for (int c = 0; c < NC && good; ++c) {
@@ -863,12 +886,38 @@ extern "C" rk_status_t rk_seg_attn_forward_host(rk_seg_attn_plan_t p, const void
     range(c, r0, r1);
     good = ok(cudaStreamWaitEvent(p->copy_out, p->ev_k[std::min(c + 1, NC - 1)], 0));
     if (good && a.num_chunks) good = ok(cudaStreamWaitEvent(p->copy_out, p->ev_split, 0));
-    if (good && r1 > r0) {
-      const int64_t n = r1 - r0;
-      good = ok(cudaMemcpyAsync(oh + r0 * orow, od + r0 * orow, n * orow, cudaMemcpyDeviceToHost,
-                                p->copy_out)) &&
-             ok(cudaMemcpyAsync(lh + r0 * lrow, ld + r0 * lrow, n * lrow, cudaMemcpyDeviceToHost,
-                                p->copy_out));
+    if (!good || r1 <= r0) continue;
+    const int64_t n = r1 - r0;
+    good = ok(cudaMemcpyAsync(lh + r0 * lrow, ld + r0 * lrow, n * lrow, cudaMemcpyDeviceToHost,
+                              p->copy_out));
+    if (all_global) {
+      good = good && ok(cudaMemcpyAsync(oh + r0 * orow, od + r0 * orow, n * orow,
+                                        cudaMemcpyDeviceToHost, p->copy_out));
+      continue;
+    }
+    if (good && gstride > 0) {
+      const size_t off = r0 * orow + p->global_heads[0] * hbytes;
+      good = ok(cudaMemcpy2DAsync(oh + off, gstride * hbytes, od + off, gstride * hbytes, hbytes,
+                                  static_cast<size_t>(n) * HG, cudaMemcpyDeviceToHost,
+                                  p->copy_out));
+    } else {
+      for (int g = 0; g < HG && good;) {
+        int e = g + 1;
+        while (e < HG && p->global_heads[e] == p->global_heads[e - 1] + 1) ++e;
+        const size_t off = r0 * orow + p->global_heads[g] * hbytes;
+        good = ok(cudaMemcpy2DAsync(oh + off, orow, od + off, orow, (e - g) * hbytes,
+                                    static_cast<size_t>(n), cudaMemcpyDeviceToHost, p->copy_out));
+        g = e;
+      }
+    }
+    while (good && run < p->full_rows.size() && p->full_rows[run].first < r1) {
+      const int64_t f0 = std::max(r0, p->full_rows[run].first);
+      const int64_t f1 = std::min(r1, p->full_rows[run].second);
+      if (f1 > f0)
+        good = ok(cudaMemcpyAsync(oh + f0 * orow, od + f0 * orow, (f1 - f0) * orow,
+                                  cudaMemcpyDeviceToHost, p->copy_out));
+      if (p->full_rows[run].second > r1) break;  // continues in the next range
+      ++run;
     }
   }
   // the caller's stream resumes when everything is back on the host

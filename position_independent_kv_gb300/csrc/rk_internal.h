@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
 #include <vector>
 
 #include "rk_seg_attn.h"
@@ -154,6 +155,10 @@ struct rk_seg_attn_plan_s {
   std::vector<float> pos_cs_hi, pos_cs_lo;
   std::vector<rk::DenseTile> tiles;
   std::vector<int32_t> local_rows;
+  // runs [first, end) of flattened computed rows whose every head is written
+  // (protected rows); the host forward copies back these rows whole and only
+  // the Global heads of the others
+  std::vector<std::pair<int64_t, int64_t>> full_rows;
   std::vector<int32_t> global_heads, local_heads;
   std::vector<rk::SplitChunk> chunks;
   std::vector<rk::TcTile> tc_tiles;
