@@ -1,10 +1,11 @@
 """rk_seg_attn_forward_host: the forward with q, out and lse in host memory
 (copies overlapped with the kernels) gives the device forward's results bit
 for bit, for every prefill kernel and for decode."""
+import numpy as np
 import pytest
 import torch
 
-from _helpers import run_gpu
+from _helpers import compare, oracle_rows, run_gpu, sample_rows
 from position_independent_kv_gb300 import binding as B
 from position_independent_kv_gb300 import build as BUILD
 from position_independent_kv_gb300.protected import build_bitmap
@@ -61,5 +62,31 @@ def test_host_forward_pageable_memory():
     out, lse, plan, _, _ = run_gpu(wl)
     ho, hl, plan2 = _host_forward(wl, 0, pinned=False)
     assert torch.equal(ho, out.cpu()) and torch.equal(hl, lse.cpu())
+    plan.close()
+    plan2.close()
+
+
+# Global head sets other than one head per group of eight: three runs of
+# consecutive heads (one strided copy per run comes back) and every fourth
+# head (one strided copy per row range); five Global heads also tile the
+# 128 query pairs of a Global tile unevenly (25 rows x 5 heads)
+ROLES = {"runs": [0, 1, 2, 9, 33], "stride4": list(range(1, 64, 4))}
+
+
+@pytest.mark.parametrize("roles", list(ROLES))
+@pytest.mark.parametrize("kernel", ["default", "cta_pair"])
+def test_host_forward_other_global_heads(roles, kernel):
+    wl = make_workload("flash_mini", seed=2, device="cuda", q_scale=4.0)
+    role = np.zeros(wl.H, np.uint8)
+    role[ROLES[roles]] = 1
+    wl.head_role = role
+    out, lse, plan, _, prot_rows = run_gpu(wl, flags=KERNELS[kernel])
+    rng = np.random.default_rng(5)
+    rows = [sample_rows(req, prot_rows[r], rng, wl.window, wl.sink, cap=24)
+            for r, req in enumerate(wl.requests)]
+    compare(wl, out, lse, prot_rows, oracle_rows(wl, prot_rows, rows), rows, label=roles)
+    ho, hl, plan2 = _host_forward(wl, KERNELS[kernel])
+    assert torch.equal(ho, out.cpu()), "out differs from the device forward"
+    assert torch.equal(hl, lse.cpu()), "lse differs from the device forward"
     plan.close()
     plan2.close()
