@@ -97,7 +97,9 @@ typedef struct {
   int64_t rows;             /* computed rows */
   int64_t tiles;            /* work tiles: (request, KV head, 128 / G rows) */
   int64_t pairs;            /* attended (row, query head, key) pairs */
-  int64_t performed_pairs;  /* 128 x 128 per issued (tile, key block) */
+  int64_t performed_pairs;  /* 16, 128 or 256 pairs x 128 keys per issued
+                               (tile, key block): decode, one or two
+                               sub-tiles */
   int64_t kv_blocks;        /* key blocks read, summed over tiles */
   int64_t split_parts;      /* parts of split tiles (0 if none) */
   int32_t group;            /* G */
@@ -107,11 +109,12 @@ typedef struct {
 /* Validate the descriptor, check that every block a computed row can see has
  * a page (RK_ERR_INVALID_ARG otherwise), list the tiles longest first and
  * upload them with a copy of the block table on `stream`.  A tile with few
- * rows (at most 64 of its 128 query pairs in use, e.g. a decode step) and a
- * long key walk (more than 64 blocks) is split into parts of 32 blocks
- * whose normalised partial outputs and LSEs are merged by log-sum-exp in
- * the workspace by the last part to finish (the RedKnot-MLA paper's
- * numerically stable merge, RoPE-orthogonality paragraph).
+ * query pairs in use and a long key walk is split into parts: at most 16
+ * pairs (a decode step) and more than 24 blocks, parts of 16 blocks; 17 to
+ * 64 pairs and more than 64 blocks, parts of 32 blocks.  The parts'
+ * normalised partial outputs and LSEs are merged by log-sum-exp in the
+ * workspace by the last part to finish (the RedKnot-MLA paper's numerically
+ * stable merge, RoPE-orthogonality paragraph).
  * Errors: RK_ERR_NULL, RK_ERR_INVALID_ARG, RK_ERR_UNSUPPORTED_DIMS (head_dim,
  * page_size or G), RK_ERR_CAPACITY, RK_ERR_CUDA.  On error *out is NULL. */
 rk_status_t rk_segpaged_plan(const rk_segpaged_desc_t* desc, void* stream,

@@ -8,7 +8,7 @@
 // k < sink or k >= p - w.
 //
 // A sub-tile is 128 query pairs: 128 / G consecutive rows x the G query heads
-// of one KV head, so every key page is read once for the whole group.  Two
+// of one KV head, so every key page is read once for the whole group.  Three
 // kernels share the tile list format:
 //
 // seg_paged_two_kernel, for tiles with more than 64 pairs in use (never
@@ -34,16 +34,21 @@
 // is issued after the P.V that reads P_X, and the MMAs of one thread run in
 // issue order.
 //
-// seg_paged_one_kernel, for tiles with at most 64 pairs in use (decode
-// steps): one sub-tile per CTA whose query pairs each have two lane threads,
+// seg_paged_one_kernel, for tiles with 17 to 64 pairs in use (the last rows
+// of a request): one sub-tile per CTA whose query pairs each have two lane threads,
 // one per warpgroup, taking half of a block's keys and half of the output
 // columns (the row max is agreed through shared memory with a per-block
 // bar.red vote that also lets every warp leave together after a failed
 // wait); Q in tensor memory, S double-buffered, a six-slot K/V ring.  A long
-// walk (a decode step of a Global head) is split into parts of 32 blocks on
-// separate CTAs; each part leaves its normalised partial output and LSE in
-// the workspace and the last part merges them by log-sum-exp (parts without
-// a visible key weigh 0).
+// walk is split into parts of 32 blocks on separate CTAs; each part leaves
+// its normalised partial output and LSE in the workspace and the last part
+// merges them by log-sum-exp (parts without a visible key weigh 0).
+//
+// seg_paged_dec_kernel, for tiles with at most 16 pairs in use (decode
+// steps): a persistent mma.sync kernel, one CTA per SM, with the pairs on
+// the 16-row side of the tile and each of eight warps owning 16 keys of
+// every block (details at the kernel); walks of more than 24 blocks are
+// split into parts of 16 blocks, merged like the one-sub-tile kernel's.
 // Every wait is bounded (2 s); on expiry the CTA records
 // RK_ERR_DEVICE_TIMEOUT and every role stops; the producer waits (bounded)
 // for its copies in flight and tensor memory is released after the MMA pipe
@@ -95,6 +100,7 @@ struct Args {
   int32_t Hq, G, max_blocks;
   int32_t sink, window;
   float scale_log2;
+  int32_t num_tiles;     // tiles of the launch (the decode kernel strides over them)
   float* ws_o;           // [lanes][128] normalised partial outputs of split tiles
   float* ws_lse;         // [lanes]
   int32_t* ws_ticket;    // [split tiles]
@@ -106,6 +112,45 @@ struct Maps {
 
 __device__ __forceinline__ int block_of(const Tile& t, int j) {
   return j < t.sink_blocks ? j : t.win_lo + (j - t.sink_blocks);
+}
+
+// Log-sum-exp merge of a split tile's parts (RedKnot-MLA paper, the
+// numerically stable merge of the RoPE-orthogonality paragraph): every part
+// left its normalised output and its natural-log LSE at workspace lanes
+// lane0 + part * nl + pair; parts without a visible key (LSE -inf) weigh 0.
+// Run by the last part to finish, spread over `nthr` threads (item = pair,
+// group of 8 dims).
+__device__ void merge_parts(const Args& a, const Tile& t, const Req& rq, int tid, int nthr) {
+  const int nl = t.rows * a.G;
+  for (int it = tid; it < nl * 16; it += nthr) {
+    const int l = it >> 4, d0 = (it & 15) * 8;
+    const int64_t s0 = int64_t(t.lane0) + l;
+    float mxp = -INFINITY;
+    for (int q = 0; q < t.nparts; ++q) mxp = fmaxf(mxp, __ldcg(a.ws_lse + s0 + int64_t(q) * nl));
+    float wsum = 0.f;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int q = 0; q < t.nparts; ++q) {
+      const float lq = __ldcg(a.ws_lse + s0 + int64_t(q) * nl);
+      if (lq == -INFINITY) continue;
+      const float wq = __expf(lq - mxp);
+      wsum += wq;
+      const float4* src = reinterpret_cast<const float4*>(a.ws_o + (s0 + int64_t(q) * nl) * DH + d0);
+      const float4 x = __ldcg(src), y = __ldcg(src + 1);
+      acc[0] += wq * x.x; acc[1] += wq * x.y; acc[2] += wq * x.z; acc[3] += wq * x.w;
+      acc[4] += wq * y.x; acc[5] += wq * y.y; acc[6] += wq * y.z; acc[7] += wq * y.w;
+    }
+    const float winv = wsum > 0.f ? 1.f / wsum : 0.f;
+    const int lr = l / a.G, lh = l - lr * a.G;
+    const int64_t orow = rq.row_base + (t.p0 + lr - rq.q_row_begin);
+    const int ohead = t.g * a.G + lh;
+    uint4 v;
+    v.x = pack_bf16x2(acc[0] * winv, acc[1] * winv);
+    v.y = pack_bf16x2(acc[2] * winv, acc[3] * winv);
+    v.z = pack_bf16x2(acc[4] * winv, acc[5] * winv);
+    v.w = pack_bf16x2(acc[6] * winv, acc[7] * winv);
+    *reinterpret_cast<uint4*>(a.out + (orow * a.Hq + ohead) * DH + d0) = v;
+    if (d0 == 0) a.lse[orow * a.Hq + ohead] = wsum > 0.f ? mxp + logf(wsum) : -INFINITY;
+  }
 }
 
 // ---- two sub-tiles of 128 pairs per CTA (tiles with more than 64 pairs in use)
@@ -720,37 +765,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc::named_sync(1, 256);
         if (*last) {
           __threadfence();
-          // log-sum-exp merge of the parts (-inf parts weigh 0), spread over
-          // the 256 lane threads: item = (used lane, group of 8 dims)
-          for (int it = lid; it < nl * 16; it += 256) {
-            const int l = it >> 4, d0 = (it & 15) * 8;
-            const int64_t s0 = int64_t(t.lane0) + l;
-            float mxp = -INFINITY;
-            for (int q = 0; q < t.nparts; ++q) mxp = fmaxf(mxp, __ldcg(a.ws_lse + s0 + int64_t(q) * nl));
-            float wsum = 0.f;
-            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            for (int q = 0; q < t.nparts; ++q) {
-              const float lq = __ldcg(a.ws_lse + s0 + int64_t(q) * nl);
-              if (lq == -INFINITY) continue;
-              const float wq = __expf(lq - mxp);
-              wsum += wq;
-              const float4* src = reinterpret_cast<const float4*>(a.ws_o + (s0 + int64_t(q) * nl) * DH + d0);
-              const float4 x = __ldcg(src), y = __ldcg(src + 1);
-              acc[0] += wq * x.x; acc[1] += wq * x.y; acc[2] += wq * x.z; acc[3] += wq * x.w;
-              acc[4] += wq * y.x; acc[5] += wq * y.y; acc[6] += wq * y.z; acc[7] += wq * y.w;
-            }
-            const float winv = wsum > 0.f ? 1.f / wsum : 0.f;
-            const int lr = l / a.G, lh = l - lr * a.G;
-            const int64_t orow = rq.row_base + (t.p0 + lr - rq.q_row_begin);
-            const int ohead = t.g * a.G + lh;
-            uint4 v;
-            v.x = pack_bf16x2(acc[0] * winv, acc[1] * winv);
-            v.y = pack_bf16x2(acc[2] * winv, acc[3] * winv);
-            v.z = pack_bf16x2(acc[4] * winv, acc[5] * winv);
-            v.w = pack_bf16x2(acc[6] * winv, acc[7] * winv);
-            *reinterpret_cast<uint4*>(a.out + (orow * a.Hq + ohead) * DH + d0) = v;
-            if (d0 == 0) a.lse[orow * a.Hq + ohead] = wsum > 0.f ? mxp + logf(wsum) : -INFINITY;
-          }
+          merge_parts(a, t, rq, lid, 256);
         }
       }
     } else if (ok) {
@@ -791,6 +806,306 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 }  // namespace one
 
+// ---- tiles of at most 16 query pairs (decode steps) on mma.sync ------------
+// A persistent kernel (one CTA per SM) walks the tile list with a stride of
+// the grid, so the page ring stays full across tile boundaries.  The query
+// pairs (row r, head h) -> pair r G + h sit on the 16-row side of the
+// m16n8k16 tile, the keys on its 8-column side.  Warp 8 streams the K and V
+// pages (32 KB boxes, chunk-major, 128-byte swizzled) through a six-slot
+// ring; compute warp w (0..7) takes keys 16 w .. 16 w + 15 of every block:
+// S = Q K^T on its 16 keys, its own online softmax, O += P V with P taken
+// straight from the score fragments.  At the end of a tile the eight warps'
+// partial states are merged through shared memory (log-sum-exp), eight pairs
+// per pass; a split part leaves its normalised result in the workspace and
+// the last part merges the parts.
+namespace dec {
+
+constexpr int CW = 8;                          // compute warps
+constexpr int THREADS = 32 * (CW + 1);         // + the producer warp
+constexpr int RING = 6;
+constexpr uint32_t SLOT = 2 * CHUNK;           // one K or V page
+constexpr uint32_t OFF_RING = 0;
+constexpr uint32_t OFF_MERGE = OFF_RING + RING * SLOT;   // [CW][8 pairs][128] fp32
+constexpr uint32_t OFF_ML = OFF_MERGE + CW * 8 * DH * 4;  // m [CW][16], l [CW][16]
+constexpr uint32_t OFF_BAR = OFF_ML + 2 * CW * 16 * 4;
+enum { B_FULL = 0, B_EMPTY = RING, NBAR = 2 * RING };
+constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
+constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;
+static_assert(SMEM_BYTES <= 232448, "shared memory");
+static_assert(OFF_MERGE % 16 == 0 && OFF_ML % 16 == 0 && OFF_BAR % 8 == 0, "alignment");
+
+__device__ __forceinline__ uint32_t ldg32(const uint16_t* p) {
+  return __ldg(reinterpret_cast<const uint32_t*>(p));
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+    seg_paged_dec_kernel(const __grid_constant__ Args a, const __grid_constant__ Maps mp) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
+  uint32_t* misc = reinterpret_cast<uint32_t*>(sm + OFF_MISC);
+  const tt::Ctx c{bar, reinterpret_cast<volatile uint32_t*>(misc + 1), a.status};
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  if (tid == 0) {
+    for (int i = 0; i < RING; ++i) {
+      tc::mbar_init(&bar[B_FULL + i], 1);
+      tc::mbar_init(&bar[B_EMPTY + i], CW);
+    }
+    misc[1] = 0;
+    tc::fence_barrier_init();
+  }
+  __syncthreads();
+
+  if (warp == CW) {
+    // ------------------------------------------------------ TMA producer --
+    if (lane == 0) {
+      tc::prefetch_tmap(&mp.k);
+      tc::prefetch_tmap(&mp.v);
+      uint32_t cnt = 0;
+      bool ok = true;
+      auto load = [&](const CUtensorMap* map, int page) {
+        const int slot = cnt % RING;
+        if (!tt::wait_bar(c, B_EMPTY + slot, ((cnt / RING) & 1) ^ 1)) return false;
+        tc::mbar_arrive_expect_tx(&bar[B_FULL + slot], SLOT);
+        tc::tma_load_4d(smem_u32(sm + OFF_RING + slot * SLOT), map, &bar[B_FULL + slot], 0, 0, 0,
+                        page);
+        ++cnt;
+        return true;
+      };
+      for (int ti = blockIdx.x; ti < a.num_tiles && ok; ti += gridDim.x) {
+        const Tile t = a.tiles[ti];
+        const int32_t* tab = a.table + a.reqs[t.req].table_off + int64_t(t.g) * a.max_blocks;
+        for (int j = t.jb; j < t.je && ok; ++j) {
+          const int page = tab[block_of(t, j)];
+          ok = load(&mp.k, page) && load(&mp.v, page);
+        }
+      }
+      // copies in flight land before the CTA may exit
+      for (uint32_t k = (cnt > RING ? cnt - RING : 0); k < cnt; ++k)
+        tt::drain_bar(c, B_FULL + k % RING, (k / RING) & 1);
+    }
+  } else {
+    // --------------------------------------------------- compute warps ---
+    const int g8 = lane >> 2, t4 = lane & 3;
+    const uint32_t ring = smem_u32(sm + OFF_RING);
+    float* mbuf = reinterpret_cast<float*>(sm + OFF_MERGE);  // [CW][8][DH]
+    float* mlm = reinterpret_cast<float*>(sm + OFF_ML);      // [CW][16]
+    float* mll = mlm + CW * 16;                              // [CW][16]
+    const float sl2 = a.scale_log2;
+    const int sink = a.sink, window = a.window;
+    // ldmatrix row addresses of this lane (matrix lane >> 3, row lane & 7):
+    // scores read K rows 16 warp + 8 ((lane >> 3) >> 1) + (lane & 7) at
+    // dim unit (lane >> 3) & 1 of a k-step; P.V reads V rows
+    // 16 warp + 8 ((lane >> 3) & 1) + (lane & 7) at dim unit (lane >> 3) >> 1
+    const int mi = lane >> 3;
+    const uint32_t krow = 16 * warp + 8 * (mi >> 1) + (lane & 7);
+    const uint32_t vrow = 16 * warp + 8 * (mi & 1) + (lane & 7);
+    uint32_t cnt = 0;
+    bool ok = true;
+    for (int ti = blockIdx.x; ti < a.num_tiles; ti += gridDim.x) {
+      const Tile t = a.tiles[ti];
+      const Req rq = a.reqs[t.req];
+      const bool glob = a.role[t.g] != 0;
+      const int np = t.rows * a.G;  // pairs in use (<= 16)
+      // this lane's two pairs: rows g8 and g8 + 8 of the fragments
+      int pp[2];
+      bool pv[2];
+      uint32_t qa[8][4];
+      {
+        const uint16_t* qr[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int n = g8 + 8 * e;
+          const int r = n / a.G, h = n - r * a.G;
+          pv[e] = n < np;
+          pp[e] = t.p0 + r;
+          const int64_t row = rq.row_base + (pp[e] - rq.q_row_begin);
+          qr[e] = pv[e] ? a.q + (row * a.Hq + t.g * a.G + h) * DH : nullptr;
+        }
+        // A fragments of Q: k-step kk covers dims 16 kk .. 16 kk + 15
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const int d = 16 * kk + 2 * t4;
+          qa[kk][0] = qr[0] ? ldg32(qr[0] + d) : 0u;
+          qa[kk][1] = qr[1] ? ldg32(qr[1] + d) : 0u;
+          qa[kk][2] = qr[0] ? ldg32(qr[0] + d + 8) : 0u;
+          qa[kk][3] = qr[1] ? ldg32(qr[1] + d + 8) : 0u;
+        }
+      }
+      float o[16][4];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+      float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+
+      for (int j = t.jb; j < t.je && ok; ++j) {
+        const int kb = block_of(t, j) * PAGE;
+        // ---- S = Q K^T on this warp's 16 keys ----
+        int slot = cnt % RING;
+        ok = __all_sync(0xffffffffu, tt::wait_bar(c, B_FULL + slot, (cnt / RING) & 1));
+        if (!ok) break;
+        float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        {
+          const uint32_t base = ring + slot * SLOT + krow * 128;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t unit = 2 * (kk & 3) + (mi & 1);
+            uint32_t b[4];
+            ldsm_x4(b, base + (kk >> 2) * CHUNK + ((unit ^ (krow & 7)) << 4));
+            mma16816(s[0], qa[kk], b[0], b[1]);
+            mma16816(s[1], qa[kk], b[2], b[3]);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&bar[B_EMPTY + slot]);
+        ++cnt;
+        // ---- mask, online softmax (log2 domain) ----
+        float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e = 0; e < 2; ++e)
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int key = kb + 16 * warp + 8 * nt + 2 * t4 + u;
+              bool vis = pv[e] && key <= pp[e];
+              if (!glob) vis = vis && (key < sink || key >= pp[e] - window);
+              const float x = vis ? s[nt][2 * e + u] * sl2 : -INFINITY;
+              s[nt][2 * e + u] = x;
+              mx[e] = fmaxf(mx[e], x);
+            }
+        float alpha[2], nb[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          mx[e] = fmaxf(mx[e], __shfl_xor_sync(0xffffffffu, mx[e], 1));
+          mx[e] = fmaxf(mx[e], __shfl_xor_sync(0xffffffffu, mx[e], 2));
+          const float mn = fmaxf(m_run[e], mx[e]);
+          alpha[e] = (m_run[e] == -INFINITY) ? 1.f : fast_exp2(m_run[e] - mn);
+          nb[e] = (mn == -INFINITY) ? 0.f : -mn;
+          m_run[e] = mn;
+        }
+        uint32_t pa[4];
+        float ls[2] = {0.f, 0.f};
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const float p0 = fast_exp2(s[nt][2 * e] + nb[e]);
+            const float p1 = fast_exp2(s[nt][2 * e + 1] + nb[e]);
+            ls[e] += p0 + p1;
+            pa[2 * nt + e] = pack_bf16x2(p0, p1);
+          }
+#pragma unroll
+        for (int e = 0; e < 2; ++e) l_run[e] = l_run[e] * alpha[e] + ls[e];
+        if (alpha[0] != 1.f || alpha[1] != 1.f) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            o[i][0] *= alpha[0];
+            o[i][1] *= alpha[0];
+            o[i][2] *= alpha[1];
+            o[i][3] *= alpha[1];
+          }
+        }
+        // ---- O += P V on this warp's 16 keys ----
+        slot = cnt % RING;
+        ok = __all_sync(0xffffffffu, tt::wait_bar(c, B_FULL + slot, (cnt / RING) & 1));
+        if (!ok) break;
+        {
+          const uint32_t base = ring + slot * SLOT + vrow * 128;
+#pragma unroll
+          for (int d2 = 0; d2 < 8; ++d2) {
+            const uint32_t unit = 2 * (d2 & 3) + (mi >> 1);
+            uint32_t b[4];
+            ldsm_x4_t(b, base + (d2 >> 2) * CHUNK + ((unit ^ (vrow & 7)) << 4));
+            mma16816(o[2 * d2], pa, b[0], b[1]);
+            mma16816(o[2 * d2 + 1], pa, b[2], b[3]);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&bar[B_EMPTY + slot]);
+        ++cnt;
+      }
+      // every compute warp agrees before the merge (a failed wait anywhere
+      // makes all of them leave the tile loop together)
+      ok = tc::named_and(1, 32 * CW, ok);
+      if (!ok) break;
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        l_run[e] += __shfl_xor_sync(0xffffffffu, l_run[e], 1);
+        l_run[e] += __shfl_xor_sync(0xffffffffu, l_run[e], 2);
+      }
+      const bool split = t.nparts > 1;
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        if (e == 1 && np <= 8) break;
+        // this warp's state of pairs 8 e .. 8 e + 7
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          *reinterpret_cast<float2*>(mbuf + (warp * 8 + g8) * DH + 8 * i + 2 * t4) =
+              make_float2(o[i][2 * e], o[i][2 * e + 1]);
+        if (t4 == 0) {
+          mlm[warp * 16 + g8 + 8 * e] = m_run[e];
+          mll[warp * 16 + g8 + 8 * e] = l_run[e];
+        }
+        tc::named_sync(1, 32 * CW);
+        {
+          const int n = 8 * e + (tid >> 5), d0 = 4 * (tid & 31);
+          if (n < np) {
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < CW; ++w) M = fmaxf(M, mlm[w * 16 + n]);
+            float L = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int w = 0; w < CW; ++w) {
+              const float mw = mlm[w * 16 + n];
+              const float wt = (mw == -INFINITY) ? 0.f : fast_exp2(mw - M);
+              L += wt * mll[w * 16 + n];
+              const float4 x = *reinterpret_cast<const float4*>(mbuf + (w * 8 + (n & 7)) * DH + d0);
+              acc[0] += wt * x.x;
+              acc[1] += wt * x.y;
+              acc[2] += wt * x.z;
+              acc[3] += wt * x.w;
+            }
+            const float inv = L > 0.f ? 1.f / L : 0.f;
+            const float lse = L > 0.f ? M * 0.6931471805599453f + logf(L) : -INFINITY;
+            const int r = n / a.G, h = n - r * a.G;
+            if (split) {
+              const int64_t sl = int64_t(t.lane0) + int64_t(t.part - t.part_first) * np + n;
+              *reinterpret_cast<float4*>(a.ws_o + sl * DH + d0) =
+                  make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
+              if (d0 == 0) a.ws_lse[sl] = lse;
+            } else if (L > 0.f) {
+              const int64_t row = rq.row_base + (t.p0 + r - rq.q_row_begin);
+              const int64_t oi = row * a.Hq + t.g * a.G + h;
+              *reinterpret_cast<uint2*>(a.out + oi * DH + d0) =
+                  make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv),
+                             pack_bf16x2(acc[2] * inv, acc[3] * inv));
+              if (d0 == 0) a.lse[oi] = lse;
+            }
+          }
+        }
+        tc::named_sync(1, 32 * CW);  // the buffer is free for the next pass or tile
+      }
+      if (split) {
+        __threadfence();
+        volatile int* last = reinterpret_cast<volatile int*>(misc + 2);
+        if (tid == 0) *last = atomicAdd(a.ws_ticket + t.group, 1) == t.nparts - 1;
+        tc::named_sync(1, 32 * CW);
+        const bool im_last = *last != 0;
+        tc::named_sync(1, 32 * CW);  // the flag is read before the next tile may set it
+        if (im_last) {
+          __threadfence();
+          merge_parts(a, t, rq, tid, 32 * CW);
+        }
+      }
+    }
+  }
+  __syncthreads();
+}
+
+}  // namespace dec
+
 }  // namespace sp
 }  // namespace rk
 
@@ -806,11 +1121,14 @@ struct rk_segpaged_plan_s {
   std::vector<rk::sp::Req> reqs;
   std::vector<rk::sp::Tile> tiles;      // two sub-tiles per CTA
   std::vector<rk::sp::Tile> tiles_one;  // one sub-tile per CTA (<= 64 pairs in use)
+  std::vector<rk::sp::Tile> tiles_dec;  // <= 16 pairs in use (decode steps), persistent kernel
+  int32_t num_sms = 0;
   std::vector<int32_t> table;
   std::vector<uint8_t> role;
   rk::sp::Req* d_reqs = nullptr;
   rk::sp::Tile* d_tiles = nullptr;
   rk::sp::Tile* d_tiles_one = nullptr;
+  rk::sp::Tile* d_tiles_dec = nullptr;
   int32_t* d_table = nullptr;
   uint8_t* d_role = nullptr;
   int32_t* d_status = nullptr;
@@ -819,18 +1137,21 @@ struct rk_segpaged_plan_s {
 namespace {
 
 using rk::sp::PAGE;
-constexpr int kSplitBlocks = 32;  // walk steps per part of a split tile
+constexpr int kSplitBlocks = 32;  // walk steps per part of a split tile (<= 64 pairs)
+constexpr int kDecSplit = 16;     // walk steps per part of a split tile of <= 16 pairs
 
 void sp_free(rk_segpaged_plan_s* p) {
   cudaFree(p->d_reqs);
   cudaFree(p->d_tiles);
   cudaFree(p->d_tiles_one);
+  cudaFree(p->d_tiles_dec);
   cudaFree(p->d_table);
   cudaFree(p->d_role);
   cudaFree(p->d_status);
   p->d_reqs = nullptr;
   p->d_tiles = nullptr;
   p->d_tiles_one = nullptr;
+  p->d_tiles_dec = nullptr;
   p->d_table = nullptr;
   p->d_role = nullptr;
   p->d_status = nullptr;
@@ -892,7 +1213,7 @@ rk_status_t sp_build(const rk_segpaged_desc_t* d, rk_segpaged_plan_s* p) {
   rk_segpaged_info_t& info = p->info;
   info = rk_segpaged_info_t{};
   info.group = G;
-  std::vector<std::pair<int64_t, rk::sp::Tile>> list, list_one;
+  std::vector<std::pair<int64_t, rk::sp::Tile>> list, list_one, list_dec;
   int64_t rows = 0;
   for (int r = 0; r < R; ++r) {
     const int64_t T = d->seq_len[r], qb = d->q_row_begin[r];
@@ -936,15 +1257,17 @@ rk_status_t sp_build(const rk_segpaged_desc_t* d, rk_segpaged_plan_s* p) {
           if (tab[b] < 0 || tab[b] >= d->num_pages) return RK_ERR_INVALID_ARG;
         }
         info.kv_blocks += nb;
-        info.performed_pairs += int64_t(nb) * (t.rows > RT / 2 ? 256 : 128) * PAGE;
+        const bool tiny = t.rows * G <= 16;   // at most 16 pairs in use: decode kernel
+        const bool small = t.rows * G <= 64;  // at most 64 pairs in use: one-sub-tile kernel
+        info.performed_pairs += int64_t(nb) * (tiny ? 16 : t.rows > RT / 2 ? 256 : 128) * PAGE;
         t.jb = 0;
         t.je = nb;
         t.part = t.part_first = 0;
         t.nparts = 1;
-        const bool small = t.rows * G <= 64;  // at most 64 pairs in use: one-sub-tile kernel
-        if (small && nb > 2 * kSplitBlocks) {
-          // a long walk of few rows: parts of kSplitBlocks steps, merged at the end
-          const int np = (nb + kSplitBlocks - 1) / kSplitBlocks;
+        const int split_len = tiny ? kDecSplit : kSplitBlocks;
+        if (small && nb > (tiny ? 3 * kDecSplit / 2 : 2 * kSplitBlocks)) {
+          // a long walk of few rows: parts of split_len steps, merged at the end
+          const int np = (nb + split_len - 1) / split_len;
           t.nparts = np;
           t.group = static_cast<int32_t>(p->split_tiles++);
           t.lane0 = static_cast<int32_t>(p->split_lanes);
@@ -953,28 +1276,30 @@ rk_status_t sp_build(const rk_segpaged_desc_t* d, rk_segpaged_plan_s* p) {
           for (int q = 0; q < np; ++q) {
             rk::sp::Tile u = t;
             u.part = q;
-            u.jb = q * kSplitBlocks;
-            u.je = std::min(nb, (q + 1) * kSplitBlocks);
-            list_one.push_back({u.je - u.jb, u});
+            u.jb = q * split_len;
+            u.je = std::min(nb, (q + 1) * split_len);
+            (tiny ? list_dec : list_one).push_back({u.je - u.jb, u});
           }
           continue;
         }
-        (small ? list_one : list).push_back({nb, t});
+        (tiny ? list_dec : small ? list_one : list).push_back({nb, t});
       }
     }
     rows += T - qb;
   }
   if (rows * d->num_q_heads > (int64_t(1) << 40) || list.size() > INT32_MAX / 2 ||
-      list_one.size() > INT32_MAX / 2)
+      list_one.size() > INT32_MAX / 2 || list_dec.size() > INT32_MAX / 2)
     return RK_ERR_CAPACITY;
   auto longest_first = [](const auto& x, const auto& y) { return x.first > y.first; };
   std::stable_sort(list.begin(), list.end(), longest_first);
   std::stable_sort(list_one.begin(), list_one.end(), longest_first);
+  std::stable_sort(list_dec.begin(), list_dec.end(), longest_first);
   for (auto& e : list) p->tiles.push_back(e.second);
   for (auto& e : list_one) p->tiles_one.push_back(e.second);
+  for (auto& e : list_dec) p->tiles_dec.push_back(e.second);
   p->rows = rows;
   info.rows = rows;
-  info.tiles = static_cast<int64_t>(p->tiles.size() + p->tiles_one.size());
+  info.tiles = static_cast<int64_t>(p->tiles.size() + p->tiles_one.size() + p->tiles_dec.size());
   if (p->split_lanes > INT32_MAX / 2 || p->split_tiles > INT32_MAX / 2) return RK_ERR_CAPACITY;
   if (p->split_tiles) {
     size_t b = static_cast<size_t>(p->split_lanes) * (rk::sp::DH + 1) * sizeof(float);
@@ -1001,6 +1326,10 @@ extern "C" rk_status_t rk_segpaged_plan(const rk_segpaged_desc_t* desc, void* st
     if (st == RK_OK) st = sp_upload(p->reqs, &p->d_reqs, s);
     if (st == RK_OK) st = sp_upload(p->tiles, &p->d_tiles, s);
     if (st == RK_OK) st = sp_upload(p->tiles_one, &p->d_tiles_one, s);
+    if (st == RK_OK) st = sp_upload(p->tiles_dec, &p->d_tiles_dec, s);
+    if (st == RK_OK &&
+        cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device) != cudaSuccess)
+      st = RK_ERR_CUDA;
     if (st == RK_OK) st = sp_upload(p->table, &p->d_table, s);
     if (st == RK_OK) st = sp_upload(p->role, &p->d_role, s);
     if (st == RK_OK) {
@@ -1036,7 +1365,7 @@ extern "C" rk_status_t rk_segpaged_forward(rk_segpaged_plan_t p, const void* q, 
   int cur = -1;
   if (cudaGetDevice(&cur) != cudaSuccess) return RK_ERR_CUDA;
   if (cur != p->device) return RK_ERR_PLAN_MISMATCH;
-  if (p->tiles.empty() && p->tiles_one.empty()) return RK_OK;
+  if (p->tiles.empty() && p->tiles_one.empty() && p->tiles_dec.empty()) return RK_OK;
   rk::sp::Maps mp{};
   {
     // a page viewed as (64 dims, 128 tokens, 2 chunks, pages): one page per box
@@ -1093,6 +1422,18 @@ extern "C" rk_status_t rk_segpaged_forward(rk_segpaged_plan_t p, const void* q, 
     a.tiles = p->d_tiles_one;
     k1::seg_paged_one_kernel<<<static_cast<unsigned>(p->tiles_one.size()), k1::THREADS,
                                k1::SMEM_BYTES, s>>>(a, mp);
+    if (cudaGetLastError() != cudaSuccess) return RK_ERR_CUDA;
+  }
+  if (!p->tiles_dec.empty()) {
+    namespace kd = rk::sp::dec;
+    if (cudaFuncSetAttribute(kd::seg_paged_dec_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kd::SMEM_BYTES)) != cudaSuccess)
+      return RK_ERR_CUDA;
+    a.tiles = p->d_tiles_dec;
+    a.num_tiles = static_cast<int32_t>(p->tiles_dec.size());
+    // persistent: one CTA per SM strides over the tiles (longest first)
+    const int grid = std::max(1, std::min<int>(a.num_tiles, p->num_sms));
+    kd::seg_paged_dec_kernel<<<static_cast<unsigned>(grid), kd::THREADS, kd::SMEM_BYTES, s>>>(a, mp);
     if (cudaGetLastError() != cudaSuccess) return RK_ERR_CUDA;
   }
   return RK_OK;

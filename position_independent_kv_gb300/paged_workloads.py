@@ -62,6 +62,20 @@ PAGED_SPECS: dict[str, PagedSpec] = {
     # decode rows over 8.5K-12K tokens: the Global heads' walks are split
     "paged_decode_long_mini": PagedSpec("paged_decode_long_mini", 16, 2, [], [],
                                         global_every=2, local_pages_only=True),
+    # decode steps of other group sizes: 16 query pairs (every row of the
+    # decode kernel's fragments), one pair, four pairs
+    "paged_decode_g16_long": PagedSpec("paged_decode_g16_long", 32, 2, [], [], global_every=2,
+                                       local_pages_only=True),
+    "paged_decode_g1_long": PagedSpec("paged_decode_g1_long", 4, 4, [], [], global_every=4,
+                                      local_pages_only=True),
+    "paged_decode_g4": PagedSpec("paged_decode_g4", 8, 2, [], [], global_every=2,
+                                 local_pages_only=True),
+    # prefills whose last tile has at most 16 query pairs over several rows
+    # (13 rows x G 1, 7 rows x G 2), and 4 rows x G 4 at the end of a 3.5K
+    # prompt (a Global walk of 28 blocks split in two parts)
+    "paged_tail_g1": PagedSpec("paged_tail_g1", 2, 2, [525], [0], global_every=2),
+    "paged_tail_g2": PagedSpec("paged_tail_g2", 4, 2, [391], [0], global_every=2),
+    "paged_tail_g4_split": PagedSpec("paged_tail_g4_split", 8, 2, [3500], [3496], global_every=2),
 }
 
 
@@ -104,7 +118,7 @@ class PagedWorkload:
 def _decode_lengths(name: str, rng: np.random.Generator):
     if name == "qwen32b_decode":
         return [int(x) for x in rng.integers(8192, 65537, size=64)]
-    if name == "paged_decode_long_mini":
+    if name.endswith("_long_mini") or name.endswith("_long"):
         return [int(x) for x in rng.integers(8500, 12001, size=3)]
     return [int(x) for x in rng.integers(300, 1501, size=5)]
 

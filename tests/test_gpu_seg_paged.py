@@ -26,7 +26,8 @@ pytestmark = pytest.mark.gpu
 MEAN_REL = 3e-3
 
 MINI = ["paged_mini", "paged_mini_g4", "paged_mini_g1", "paged_mini_g16", "paged_decode_mini",
-        "paged_decode_long_mini"]
+        "paged_decode_long_mini", "paged_decode_g16_long", "paged_decode_g1_long", "paged_decode_g4", "paged_tail_g1",
+        "paged_tail_g2", "paged_tail_g4_split"]
 
 
 @pytest.fixture(scope="module", autouse=True)

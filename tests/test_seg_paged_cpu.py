@@ -26,6 +26,8 @@ def _plan(pw, flags=0, **over):
 
 @pytest.mark.parametrize("name", ["paged_mini", "paged_mini_g4", "paged_mini_g1",
                                   "paged_mini_g16", "paged_decode_mini", "paged_decode_long_mini",
+                                  "paged_decode_g16_long", "paged_decode_g1_long", "paged_decode_g4", "paged_tail_g1",
+                                  "paged_tail_g2", "paged_tail_g4_split",
                                   "qwen32b_16k"])
 def test_pair_counts_and_blocks(name):
     pw = make_paged_geometry(name, 0)
@@ -44,7 +46,8 @@ def test_pair_counts_and_blocks(name):
                 cnt = np.where(lo <= pw.sink, p + 1, np.minimum(pw.sink, p + 1) + p - lo + 1)
                 pairs += G * int(cnt.sum())
     assert info["pairs"] == pairs and info["rows"] == pw.rows and info["group"] == G
-    assert info["kv_blocks"] * 128 * PAGE <= info["performed_pairs"] <= info["kv_blocks"] * 256 * PAGE
+    # 16, 128 or 256 query pairs per issued block (decode, one or two sub-tiles)
+    assert info["kv_blocks"] * 16 * PAGE <= info["performed_pairs"] <= info["kv_blocks"] * 256 * PAGE
     assert info["performed_pairs"] >= pairs
     # the dense + mask arm walks every block up to each tile's last row
     if not (pw.block_table < 0).any():
@@ -104,9 +107,10 @@ def test_host_only_refuses_forward():
 
 
 def test_decode_split_parts_and_workspace():
-    """Decode rows of Global heads with long walks (more than 64 blocks) are
-    split into parts of 32 blocks; the workspace holds one fp32 partial and
-    one LSE per used lane of every part, plus a ticket per split tile."""
+    """Decode rows (at most 16 query pairs) of Global heads with long walks
+    (more than 24 blocks) are split into parts of 16 blocks; the workspace
+    holds one fp32 partial and one LSE per used pair of every part, plus a
+    ticket per split tile."""
     pw = make_paged_geometry("paged_decode_long_mini", 0)
     plan = _plan(pw)
     info = plan.info
@@ -116,8 +120,8 @@ def test_decode_split_parts_and_workspace():
     for T in pw.seq_len:
         nb = (int(T) + PAGE - 1) // PAGE
         for g in range(pw.Hkv):
-            if pw.kv_role[g] and nb > 64:
-                np_ = (nb + 31) // 32
+            if pw.kv_role[g] and nb > 24:
+                np_ = (nb + 15) // 16
                 parts += np_
                 lanes += np_ * pw.G
                 split += 1
