@@ -109,9 +109,9 @@ typedef struct {
 /* Validate the descriptor, check that every block a computed row can see has
  * a page (RK_ERR_INVALID_ARG otherwise), list the tiles longest first and
  * upload them with a copy of the block table on `stream`.  A tile with few
- * query pairs in use and a long key walk is split into parts: at most 16
- * pairs (a decode step) and more than 24 blocks, parts of 16 blocks; 17 to
- * 64 pairs and more than 64 blocks, parts of 32 blocks.  The parts'
+ * query pairs in use and a long key walk is split into parts of 32 blocks:
+ * at most 16 pairs (a decode step) and more than 48 blocks, or 17 to 64
+ * pairs and more than 64 blocks.  The parts'
  * normalised partial outputs and LSEs are merged by log-sum-exp in the
  * workspace by the last part to finish (the RedKnot-MLA paper's numerically
  * stable merge, RoPE-orthogonality paragraph).

@@ -47,8 +47,8 @@
 // seg_paged_dec_kernel, for tiles with at most 16 pairs in use (decode
 // steps): a persistent mma.sync kernel, one CTA per SM, with the pairs on
 // the 16-row side of the tile and each of eight warps owning 16 keys of
-// every block (details at the kernel); walks of more than 24 blocks are
-// split into parts of 16 blocks, merged like the one-sub-tile kernel's.
+// every block (details at the kernel); walks of more than 48 blocks are
+// split into parts of 32 blocks, merged like the one-sub-tile kernel's.
 // Every wait is bounded (2 s); on expiry the CTA records
 // RK_ERR_DEVICE_TIMEOUT and every role stops; the producer waits (bounded)
 // for its copies in flight and tensor memory is released after the MMA pipe
@@ -1138,7 +1138,7 @@ namespace {
 
 using rk::sp::PAGE;
 constexpr int kSplitBlocks = 32;  // walk steps per part of a split tile (<= 64 pairs)
-constexpr int kDecSplit = 16;     // walk steps per part of a split tile of <= 16 pairs
+constexpr int kDecSplit = 32;     // walk steps per part of a split tile of <= 16 pairs
 
 void sp_free(rk_segpaged_plan_s* p) {
   cudaFree(p->d_reqs);

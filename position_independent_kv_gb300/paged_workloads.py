@@ -71,11 +71,11 @@ PAGED_SPECS: dict[str, PagedSpec] = {
     "paged_decode_g4": PagedSpec("paged_decode_g4", 8, 2, [], [], global_every=2,
                                  local_pages_only=True),
     # prefills whose last tile has at most 16 query pairs over several rows
-    # (13 rows x G 1, 7 rows x G 2), and 4 rows x G 4 at the end of a 3.5K
-    # prompt (a Global walk of 28 blocks split in two parts)
+    # (13 rows x G 1, 7 rows x G 2), and 4 rows x G 4 at the end of a 7K
+    # prompt (a Global walk of 55 blocks split in two parts)
     "paged_tail_g1": PagedSpec("paged_tail_g1", 2, 2, [525], [0], global_every=2),
     "paged_tail_g2": PagedSpec("paged_tail_g2", 4, 2, [391], [0], global_every=2),
-    "paged_tail_g4_split": PagedSpec("paged_tail_g4_split", 8, 2, [3500], [3496], global_every=2),
+    "paged_tail_g4_split": PagedSpec("paged_tail_g4_split", 8, 2, [7000], [6996], global_every=2),
 }
 
 

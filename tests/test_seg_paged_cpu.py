@@ -108,7 +108,7 @@ def test_host_only_refuses_forward():
 
 def test_decode_split_parts_and_workspace():
     """Decode rows (at most 16 query pairs) of Global heads with long walks
-    (more than 24 blocks) are split into parts of 16 blocks; the workspace
+    (more than 48 blocks) are split into parts of 32 blocks; the workspace
     holds one fp32 partial and one LSE per used pair of every part, plus a
     ticket per split tile."""
     pw = make_paged_geometry("paged_decode_long_mini", 0)
@@ -120,8 +120,8 @@ def test_decode_split_parts_and_workspace():
     for T in pw.seq_len:
         nb = (int(T) + PAGE - 1) // PAGE
         for g in range(pw.Hkv):
-            if pw.kv_role[g] and nb > 24:
-                np_ = (nb + 15) // 16
+            if pw.kv_role[g] and nb > 48:
+                np_ = (nb + 31) // 32
                 parts += np_
                 lanes += np_ * pw.G
                 split += 1
