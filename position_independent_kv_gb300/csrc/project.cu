@@ -10,8 +10,10 @@
 //     z[t, g] = W_aG(g) O_G[t] + (row t protected ? W_aL(g) O_L[t] : z_off[t, g])
 //     y[t]    = W_b z[t]
 // (the inverse output rotation is the identity: the values carry no rotary
-// part).  Two passes of one tcgen05 GEMM kernel (M = 128 rows, N = 256
-// columns, K in 64-wide chunks through a 4-stage TMA ring):
+// part).  Two passes of one tcgen05 GEMM kernel on CTA pairs (M = 256 rows,
+// 128 per CTA; N = 256 columns, 128 of the B rows loaded by each CTA;
+// cta_group::2 MMAs issued by the first CTA; K in stages of two 64-wide
+// chunks, one 32 KB box per operand and CTA, through a 3-stage ring):
 //   pass z: A = the group's head outputs O[t, 8g + i, :], B = W_a rows; the
 //           Global heads' chunks accumulate in tensor-memory columns 0..255,
 //           the Local heads' chunks in 256..511, the latter only for row
@@ -31,10 +33,12 @@ using tt::drain_bar;
 using tt::wait_bar;
 
 constexpr int PJ_THREADS = 192;
-constexpr uint32_t PJ_A = 16384;           // 128 rows x 64 bf16
-constexpr uint32_t PJ_B = 32768;           // 256 rows x 64 bf16
+constexpr int PJ_KC = 2;                   // 64-wide K chunks per stage (one box each)
+constexpr uint32_t PJ_C = 16384;           // 128 rows x 64 bf16: one chunk of A or B
+constexpr uint32_t PJ_A = PJ_KC * PJ_C;    // this CTA's rows
+constexpr uint32_t PJ_B = PJ_KC * PJ_C;    // this CTA's half of N
 constexpr uint32_t PJ_STAGE = PJ_A + PJ_B;
-constexpr int PJ_ST = 4;
+constexpr int PJ_ST = 3;
 constexpr uint32_t PJ_OFF_BAR = PJ_ST * PJ_STAGE;
 enum { P_FULL = 0, P_EMPTY = PJ_ST, P_DONE = 2 * PJ_ST, P_NBAR };
 constexpr uint32_t PJ_SMEM = PJ_OFF_BAR + P_NBAR * 8 + 16 + 1024;
@@ -80,7 +84,7 @@ __device__ __forceinline__ void chunk_of(const ProjArgs& a, int g, int c, int& a
   cb = i * 8 + k;             // W_a viewed as (64, G d_g, 64 chunks)
 }
 
-__global__ void __launch_bounds__(PJ_THREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PJ_THREADS, 1)
     project_kernel(const __grid_constant__ ProjArgs a, const __grid_constant__ CUtensorMap ma,
                    const __grid_constant__ CUtensorMap mb) {
   extern __shared__ uint8_t smem_raw[];
@@ -90,22 +94,28 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
   uint32_t* misc = reinterpret_cast<uint32_t*>(sm + PJ_OFF_BAR + P_NBAR * 8);
   const Ctx c{bar, reinterpret_cast<volatile uint32_t*>(misc + 1), a.status};
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // tile: (row tile, group, column tile) in pass z; (row tile, column tile) in pass y
-  const int nt = blockIdx.x % a.n_tiles;
-  const int g = a.mode == 0 ? (blockIdx.x / a.n_tiles) % a.groups : 0;
-  const int64_t mt = a.mode == 0 ? blockIdx.x / (a.n_tiles * a.groups) : blockIdx.x / a.n_tiles;
-  const int64_t m0 = mt * 128;
-  // does the row tile hold a protected row?  (pass z runs the Local chunks only then)
+  const uint32_t r = tc::cluster_ctarank();  // this CTA's rows and half of the columns
+  auto cbar = [&](int i, uint32_t rank) { return tc::mapa_shared(smem_u32(&bar[i]), rank); };
+  // pair tile: (row tile of 256, group, column tile of 256) in pass z;
+  // (row tile, column tile) in pass y
+  const int pt = static_cast<int>(blockIdx.x >> 1);
+  const int nt = pt % a.n_tiles;
+  const int g = a.mode == 0 ? (pt / a.n_tiles) % a.groups : 0;
+  const int64_t mt = a.mode == 0 ? pt / (a.n_tiles * a.groups) : pt / a.n_tiles;
+  const int64_t mp = mt * 256;       // the pair's first row
+  const int64_t m0 = mp + 128 * r;   // this CTA's first row
+  // does the pair's row tile hold a protected row?  (pass z runs the Local
+  // chunks only then; both CTAs take the same decision)
   bool any_prot = false;
   if (a.mode == 0) {
-    for (int w = 0; w < 4; ++w) {
-      const int64_t word = (m0 >> 5) + w;
+    for (int w = 0; w < 8; ++w) {
+      const int64_t word = (mp >> 5) + w;
       if (word * 32 < a.rows && a.prot[word]) any_prot = true;
     }
   }
   const int ng = a.mode == 0 ? __popc(static_cast<uint32_t>(a.role_mask[g])) : 0;
   const int nchunks = a.mode == 0 ? 8 * ng + (any_prot ? 8 * (8 - ng) : 0) : a.dg / 64;
-  const int32_t brow = a.mode == 0 ? g * a.dg + nt * 256 : nt * 256;
+  const int32_t brow = (a.mode == 0 ? g * a.dg + nt * 256 : nt * 256) + 128 * static_cast<int32_t>(r);
 
   if (tid == 0) {
     for (int i = 0; i < PJ_ST; ++i) {
@@ -117,11 +127,12 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
     tc::fence_barrier_init();
   }
   if (warp == 1) {
-    tc::tmem_alloc(misc, 512);
-    tc::tmem_relinquish();
+    tc::tmem_alloc_2sm(misc, 512);
+    tc::tmem_relinquish_2sm();
   }
   tc::tc_fence_before();
   __syncthreads();
+  tc::cluster_sync();  // both CTAs' barriers are initialised before any remote use
   tc::tc_fence_after();
   const uint32_t tbase = misc[0];
 
@@ -129,43 +140,50 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
     if (lane == 0) {
       bool ok = true;
       int k = 0;
-      for (; k < nchunks && ok; ++k) {
+      const int nst = nchunks / PJ_KC;
+      for (; k < nst && ok; ++k) {
         const int s = k % PJ_ST;
         ok = wait_bar(c, P_EMPTY + s, ((k / PJ_ST) & 1) ^ 1);
         if (!ok) break;
         int acc, ca, cb;
-        chunk_of(a, g, k, acc, ca, cb);
-        tc::mbar_arrive_expect_tx(&bar[P_FULL + s], PJ_STAGE);
+        chunk_of(a, g, PJ_KC * k, acc, ca, cb);
+        // the leader's barrier counts both CTAs' boxes
+        if (r == 0) tc::mbar_arrive_expect_tx(&bar[P_FULL + s], 2 * PJ_STAGE);
         const uint32_t dst = smem_u32(sm + s * PJ_STAGE);
-        tc::tma_load_3d(dst, &ma, &bar[P_FULL + s], 0, static_cast<int32_t>(m0), ca);
-        tc::tma_load_3d(dst + PJ_A, &mb, &bar[P_FULL + s], 0, brow, cb);
+        tc::tma_load_3d_2sm(dst, &ma, cbar(P_FULL + s, 0), 0, static_cast<int32_t>(m0), ca);
+        tc::tma_load_3d_2sm(dst + PJ_A, &mb, cbar(P_FULL + s, 0), 0, brow, cb);
       }
-      for (int j = (k > PJ_ST ? k - PJ_ST : 0); j < k; ++j)
-        drain_bar(c, P_FULL + j % PJ_ST, (j / PJ_ST) & 1);
+      // the pair's copies in flight land before either CTA may exit
+      if (r == 0)
+        for (int j = (k > PJ_ST ? k - PJ_ST : 0); j < k; ++j)
+          drain_bar(c, P_FULL + j % PJ_ST, (j / PJ_ST) & 1);
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      const uint32_t id = tc::idesc_bf16(128, 256, false, false);
+    if (lane == 0 && r == 0) {
+      const uint32_t id = tc::idesc_bf16(256, 256, false, false);
       bool ok = true;
       bool first[2] = {true, true};
-      for (int k = 0; k < nchunks && ok; ++k) {
+      const int nst = nchunks / PJ_KC;
+      for (int k = 0; k < nst && ok; ++k) {
         const int s = k % PJ_ST;
         ok = wait_bar(c, P_FULL + s, (k / PJ_ST) & 1);
         if (!ok) break;
         tc::tc_fence_after();
         int acc, ca, cb;
-        chunk_of(a, g, k, acc, ca, cb);
+        chunk_of(a, g, PJ_KC * k, acc, ca, cb);
         const uint32_t base = smem_u32(sm + s * PJ_STAGE);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          tc::mma_ss(tbase + 256 * acc, tc::sdesc_sw128(base + 32 * kk, 16, 1024),
-                     tc::sdesc_sw128(base + PJ_A + 32 * kk, 16, 1024), id,
-                     (first[acc] && kk == 0) ? 0u : 1u);
-        }
+        for (int kc = 0; kc < PJ_KC; ++kc)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            tc::mma_ss_2sm(tbase + 256 * acc, tc::sdesc_sw128(base + kc * PJ_C + 32 * kk, 16, 1024),
+                           tc::sdesc_sw128(base + PJ_A + kc * PJ_C + 32 * kk, 16, 1024), id,
+                           (first[acc] && kc == 0 && kk == 0) ? 0u : 1u);
+          }
         first[acc] = false;
-        tc::mma_commit(&bar[P_EMPTY + s]);
+        tc::mma_commit_2sm(&bar[P_EMPTY + s], 0x3);
       }
-      tc::mma_commit(&bar[P_DONE]);
+      tc::mma_commit_2sm(&bar[P_DONE], 0x3);
     }
   } else {
     // ------------------------------------------------------ epilogue -----
@@ -234,10 +252,12 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
   }
   tc::tc_fence_before();
   __syncthreads();
+  if (warp == 1) drain_bar(c, P_DONE, 0);  // the pair's MMA pipe is empty
+  __syncthreads();
+  tc::cluster_sync();  // no CTA leaves while the other may still use its memory
   if (warp == 1) {
-    drain_bar(c, P_DONE, 0);
     tc::tc_fence_after();
-    tc::tmem_dealloc(tbase, 512);
+    tc::tmem_dealloc_2sm(tbase, 512);
   }
 }
 
@@ -263,8 +283,8 @@ extern "C" rk_status_t rk_project_forward(const rk_project_desc_t* d, const void
     return RK_ERR_ALIGNMENT;
   const int64_t rows = d->rows, H = d->num_heads, G = H / 8, dg = d->d_g, dm = d->d_model;
   if (rows > (int64_t(1) << 31) - 256) return RK_ERR_CAPACITY;
-  const int64_t mtiles = (rows + 127) / 128;
-  if (mtiles * G * (dg / 256) > INT32_MAX || mtiles * (dm / 256) > INT32_MAX)
+  const int64_t mtiles = (rows + 255) / 256;  // row tiles of a CTA pair
+  if (2 * mtiles * G * (dg / 256) > INT32_MAX || 2 * mtiles * (dm / 256) > INT32_MAX)
     return RK_ERR_CAPACITY;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   CUtensorMap ma{}, mb{};
@@ -288,16 +308,16 @@ extern "C" rk_status_t rk_project_forward(const rk_project_desc_t* d, const void
   {
     const uint64_t da[3] = {64, static_cast<uint64_t>(rows), static_cast<uint64_t>(H * 8)};
     const uint64_t sa[2] = {static_cast<uint64_t>(H) * 1024, 128};
-    const uint32_t ba[3] = {64, 128, 1};
+    const uint32_t ba[3] = {64, 128, PJ_KC};
     const uint64_t db[3] = {64, static_cast<uint64_t>(G * dg), 64};
     const uint64_t sb[2] = {8 * 1024, 128};
-    const uint32_t bb[3] = {64, 256, 1};
+    const uint32_t bb[3] = {64, 128, PJ_KC};
     if (!make_tmap_bf16(&ma, o, 3, da, sa, ba) || !make_tmap_bf16(&mb, w_a, 3, db, sb, bb))
       return RK_ERR_CUDA;
     pa.mode = 0;
     pa.n_tiles = static_cast<int32_t>(dg / 256);
     pa.out = static_cast<uint16_t*>(z);
-    project_kernel<<<static_cast<unsigned>(mtiles * G * (dg / 256)), PJ_THREADS, PJ_SMEM, s>>>(
+    project_kernel<<<static_cast<unsigned>(2 * mtiles * G * (dg / 256)), PJ_THREADS, PJ_SMEM, s>>>(
         pa, ma, mb);
     if (cudaGetLastError() != cudaSuccess) return RK_ERR_CUDA;
   }
@@ -306,17 +326,17 @@ extern "C" rk_status_t rk_project_forward(const rk_project_desc_t* d, const void
     const uint64_t kc = static_cast<uint64_t>(G * dg / 64);
     const uint64_t da[3] = {64, static_cast<uint64_t>(rows), kc};
     const uint64_t sa[2] = {static_cast<uint64_t>(G * dg) * 2, 128};
-    const uint32_t ba[3] = {64, 128, 1};
+    const uint32_t ba[3] = {64, 128, PJ_KC};
     const uint64_t db[3] = {64, static_cast<uint64_t>(dm), kc};
     const uint64_t sb[2] = {static_cast<uint64_t>(G * dg) * 2, 128};
-    const uint32_t bb[3] = {64, 256, 1};
+    const uint32_t bb[3] = {64, 128, PJ_KC};
     if (!make_tmap_bf16(&ma, z, 3, da, sa, ba) || !make_tmap_bf16(&mb, w_b, 3, db, sb, bb))
       return RK_ERR_CUDA;
     pa.mode = 1;
     pa.dg = static_cast<int32_t>(G * dg);  // K of pass y
     pa.n_tiles = static_cast<int32_t>(dm / 256);
     pa.out = static_cast<uint16_t*>(y);
-    project_kernel<<<static_cast<unsigned>(mtiles * (dm / 256)), PJ_THREADS, PJ_SMEM, s>>>(
+    project_kernel<<<static_cast<unsigned>(2 * mtiles * (dm / 256)), PJ_THREADS, PJ_SMEM, s>>>(
         pa, ma, mb);
     if (cudaGetLastError() != cudaSuccess) return RK_ERR_CUDA;
   }

@@ -36,7 +36,7 @@ def _make(rows, H, dg, dm, role, p_prot, seed):
     rng = np.random.default_rng(seed)
     prot = rng.random(rows) < p_prot
     if rows > 200:
-        prot[128:256] = False   # a row tile without protected rows (Local part skipped)
+        prot[256:512] = False   # a 256-row tile without protected rows (Local part skipped)
     words = np.zeros((rows + 31) // 32, np.uint32)
     for r in np.nonzero(prot)[0]:
         words[r // 32] |= np.uint32(1) << np.uint32(r % 32)
