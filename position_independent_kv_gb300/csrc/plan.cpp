@@ -75,15 +75,16 @@ void free_device(rk_seg_attn_plan_s* p) {
   p->ev_fork = p->ev_join = nullptr;
   if (p->copy_in) cudaStreamDestroy(p->copy_in);
   if (p->copy_out) cudaStreamDestroy(p->copy_out);
-  for (cudaEvent_t* e : {&p->ev_start, &p->ev_split, &p->ev_done})
+  if (p->compute2) cudaStreamDestroy(p->compute2);
+  for (cudaEvent_t* e : {&p->ev_start, &p->ev_split, &p->ev_done, &p->ev_c2})
     if (*e) cudaEventDestroy(*e);
   for (int c = 0; c < rk_seg_attn_plan_s::kHostChunks; ++c) {
     if (p->ev_in[c]) cudaEventDestroy(p->ev_in[c]);
     if (p->ev_k[c]) cudaEventDestroy(p->ev_k[c]);
     p->ev_in[c] = p->ev_k[c] = nullptr;
   }
-  p->copy_in = p->copy_out = nullptr;
-  p->ev_start = p->ev_split = p->ev_done = nullptr;
+  p->copy_in = p->copy_out = p->compute2 = nullptr;
+  p->ev_start = p->ev_split = p->ev_done = p->ev_c2 = nullptr;
   p->d_tc_pairs_chunked = nullptr;
   p->d_segs = nullptr;
   p->d_reqs = nullptr;
@@ -698,8 +699,9 @@ extern "C" rk_status_t rk_seg_attn_plan(const rk_seg_attn_desc_t* desc, void* st
     }
     if (st == RK_OK) {
       bool okc = cudaStreamCreateWithFlags(&p->copy_in, cudaStreamNonBlocking) == cudaSuccess &&
-                 cudaStreamCreateWithFlags(&p->copy_out, cudaStreamNonBlocking) == cudaSuccess;
-      for (cudaEvent_t* e : {&p->ev_start, &p->ev_split, &p->ev_done})
+                 cudaStreamCreateWithFlags(&p->copy_out, cudaStreamNonBlocking) == cudaSuccess &&
+                 cudaStreamCreateWithFlags(&p->compute2, cudaStreamNonBlocking) == cudaSuccess;
+      for (cudaEvent_t* e : {&p->ev_start, &p->ev_split, &p->ev_done, &p->ev_c2})
         okc = okc && cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess;
       for (int c = 0; c < rk_seg_attn_plan_s::kHostChunks && okc; ++c)
         okc = cudaEventCreateWithFlags(&p->ev_in[c], cudaEventDisableTiming) == cudaSuccess &&
@@ -837,20 +839,28 @@ extern "C" rk_status_t rk_seg_attn_forward_host(rk_seg_attn_plan_t p, const void
   if (good) good = bind_workspace(*p, a, workspace, s) == RK_OK;
   const bool pipelined = !p->tc_pairs_chunked.empty() && a.num_tiles == 0 && a.num_tc_tiles == 0;
   if (pipelined) {
-    // the tile pairs of row range c run once rows 0 .. c are on the device
+    // the tile pairs of row range c run once rows 0 .. c are on the device;
+    // the ranges alternate between the caller's stream and a second
+    // plan-owned stream, so one range's tiles start on the SMs that the
+    // previous range's longest tiles leave idle (the ranges' pairs write
+    // disjoint tiles)
+    good = good && ok(cudaStreamWaitEvent(p->compute2, p->ev_start, 0));
     for (int c = 0; c < NC && good; ++c) {
-      good = ok(cudaStreamWaitEvent(s, p->ev_in[c], 0));
+      cudaStream_t cs = (c & 1) ? p->compute2 : s;
+      good = ok(cudaStreamWaitEvent(cs, p->ev_in[c], 0));
       const int32_t b = p->chunk_pair_begin[c], e = p->chunk_pair_begin[c + 1];
       if (good && e > b) {
         rk::KernelArgs ac = a;
         ac.tc_pairs = p->d_tc_pairs_chunked + b;
         ac.num_tc_pairs = e - b;
         ac.num_chunks = 0;
-        good = ok(p->kernel == 3 ? rk::launch_dense_tc4(*p, ac, q, s)
-                                 : rk::launch_dense_tc2(*p, ac, q, s));
+        good = ok(p->kernel == 3 ? rk::launch_dense_tc4(*p, ac, q, cs)
+                                 : rk::launch_dense_tc2(*p, ac, q, cs));
       }
-      good = good && ok(cudaEventRecord(p->ev_k[c], s));
+      good = good && ok(cudaEventRecord(p->ev_k[c], cs));
     }
+    good = good && ok(cudaEventRecord(p->ev_c2, p->compute2)) &&
+           ok(cudaStreamWaitEvent(s, p->ev_c2, 0));
     if (good && a.num_chunks) {
       rk::KernelArgs ac = a;
       ac.num_tc_pairs = 0;
@@ -884,7 +894,8 @@ extern "C" rk_status_t rk_seg_attn_forward_host(rk_seg_attn_plan_t p, const void
   for (int c = 0; c < NC && good; ++c) {
     int64_t r0, r1;
     range(c, r0, r1);
-    good = ok(cudaStreamWaitEvent(p->copy_out, p->ev_k[std::min(c + 1, NC - 1)], 0));
+    good = ok(cudaStreamWaitEvent(p->copy_out, p->ev_k[c], 0)) &&
+           ok(cudaStreamWaitEvent(p->copy_out, p->ev_k[std::min(c + 1, NC - 1)], 0));
     if (good && a.num_chunks) good = ok(cudaStreamWaitEvent(p->copy_out, p->ev_split, 0));
     if (!good || r1 <= r0) continue;
     const int64_t n = r1 - r0;

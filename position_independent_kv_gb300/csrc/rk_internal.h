@@ -199,8 +199,8 @@ struct rk_seg_attn_plan_s {
   std::vector<rk::TcPair> tc_pairs_chunked;
   int32_t chunk_pair_begin[kHostChunks + 1] = {};
   rk::TcPair* d_tc_pairs_chunked = nullptr;
-  cudaStream_t copy_in = nullptr, copy_out = nullptr;
-  cudaEvent_t ev_start = nullptr, ev_split = nullptr, ev_done = nullptr;
+  cudaStream_t copy_in = nullptr, copy_out = nullptr, compute2 = nullptr;
+  cudaEvent_t ev_start = nullptr, ev_split = nullptr, ev_done = nullptr, ev_c2 = nullptr;
   cudaEvent_t ev_in[kHostChunks] = {}, ev_k[kHostChunks] = {};
 };
 
