@@ -671,14 +671,16 @@ extern "C" rk_status_t rk_seg_attn_plan(const rk_seg_attn_desc_t* desc, void* st
       }
       if (st == RK_OK) st = upload(p->segmaps, &p->d_segmaps, s);
     }
-    if (st == RK_OK && !p->chunks.empty() && p->d_nope == 512 && p->d_rope == 64 &&
+    if (st == RK_OK && !p->chunks.empty() && p->d_rope == 64 &&
+        (p->d_nope == 512 || (p->v_rope && p->d_nope == 448)) &&
         !(desc->flags & RK_PLAN_LEGACY_MMA)) {
       // split-over-segments chunks stream 32-row boxes of whole latent rows
+      const uint32_t nch = static_cast<uint32_t>((p->d_nope + p->d_rope) / 64);
       p->decmaps.resize(p->segs.size());
       for (size_t i = 0; i < p->segs.size() && st == RK_OK; ++i) {
-        const uint64_t dims[3] = {64, static_cast<uint64_t>(p->segs[i].n), 9};
-        const uint64_t strides[2] = {576 * 2, 128};
-        const uint32_t box[3] = {64, 32, 9};
+        const uint64_t dims[3] = {64, static_cast<uint64_t>(p->segs[i].n), nch};
+        const uint64_t strides[2] = {static_cast<uint64_t>(nch) * 128, 128};
+        const uint32_t box[3] = {64, 32, nch};
         if (!rk::make_tmap_bf16(&p->decmaps[i], p->segs[i].latent, 3, dims, strides, box))
           st = RK_ERR_CUDA;
       }

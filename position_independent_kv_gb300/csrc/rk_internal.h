@@ -125,7 +125,7 @@ struct KernelArgs {
   const CUtensorMap* segmaps; // kSegMaps per segment
   const uint8_t* head_role;   // [H]
   int32_t g_ingroup;          // Global heads are 8g + g_ingroup for every group g, or -1
-  const CUtensorMap* decmaps; // per segment: latent viewed (64, n, 9 chunks), box 32 rows x 9 chunks
+  const CUtensorMap* decmaps; // per segment: latent viewed (64, n, d_k / 64 chunks), box 32 rows x all chunks
   const TcPair* tc_pairs;
   int32_t num_tc_pairs;
   int32_t v_rope;             // V is the whole latent row (d_v = d_k), output phase restored

@@ -328,38 +328,56 @@ __global__ void __launch_bounds__(THREADS, 1) split_decode_kernel(const KernelAr
 
 
 // ---------------------------------------------------------------------------
-// d = (512, 64) version fed by TMA: each stage is one 3-D box of 32 keys x 9
-// chunks of 64 dims (36 KB of whole 1152-byte latent rows, laid out
+// Version fed by TMA for latent rows of NCH nope chunks + one rope chunk of
+// 64 dims (d = 512 + 64, or 448 + 64 with the rotary value): each stage is
+// one 3-D box of 32 keys x (NCH + 1) chunks (whole latent rows, laid out
 // chunk-major with the 128-byte swizzle), five stages deep, so that four
-// stages (144 KB) stay in flight while one is computed; fragment addresses
-// apply the same XOR swizzle, so the ldmatrix reads are conflict-free.  Eight
-// warps: the scores of the 32 keys are split over two key halves x four
-// quarters of d_k (each warp holds only its quarter of Q^T in registers),
-// and each warp takes 64 output rows of P.V.
+// stages stay in flight while one is computed; fragment addresses apply the
+// same XOR swizzle, so the ldmatrix reads are conflict-free.  Eight warps:
+// the scores of the 32 keys are split over two key halves x four quarters
+// of the 4 NCH + 8 k-steps (nope, then q_rope' hi and lo), each warp holding
+// only its quarter of Q^T in registers, and each warp takes 64 of the 512
+// output rows of P.V (V = the first 8 chunks: c_nope, or the whole row).
 constexpr int DT_TK = 32;
 constexpr int DT_ST = 5;                       // stages per CTA
 constexpr int DT_THREADS = 256;
 constexpr uint32_t DT_CH = DT_TK * 128;        // one 64-dim chunk of a stage
-constexpr uint32_t DT_STAGE = 9 * DT_CH;       // 36,864 B
 constexpr uint64_t DT_WAIT_NS = 2000000000ull;
-constexpr int DT_QS = 512 + 128 + 8;
 constexpr int DT_PS = DT_TK + 8;
-// shared-memory layout (byte offsets from the 1024-aligned base)
-constexpr size_t DT_OFF_Q = size_t(DT_ST) * DT_STAGE;
-constexpr size_t DT_OFF_QRO = DT_OFF_Q + size_t(NH) * DT_QS * 2;
-constexpr size_t DT_OFF_P = DT_OFF_QRO + size_t(NH) * 64 * 2;
-constexpr size_t DT_OFF_RED = DT_OFF_P + size_t(NH) * DT_PS * 2;       // red_m [2][NH], red_l [2][NH]
-constexpr size_t DT_OFF_FLAG = DT_OFF_RED + size_t(4) * NH * 4;
-constexpr size_t DT_OFF_BAR = (DT_OFF_FLAG + 16 + 7) & ~size_t(7);
-constexpr size_t DT_OFF_PART = (DT_OFF_BAR + size_t(DT_ST) * 8 + 15) & ~size_t(15);
-constexpr size_t DT_PART_BYTES = size_t(2) * 3 * 32 * 16;  // [key half][d_k quarter 1..3][lane] float4
-constexpr size_t DT_SMEM = 1024 + DT_OFF_PART + DT_PART_BYTES;
-static_assert(DT_OFF_Q % 16 == 0 && DT_OFF_QRO % 16 == 0 && DT_OFF_P % 16 == 0,
-              "cp.async / ldmatrix targets are 16-byte aligned");
-static_assert(DT_OFF_PART % 16 == 0 && DT_OFF_BAR % 8 == 0, "float4 and mbarrier alignment");
-static_assert(DT_SMEM <= 227 * 1024, "shared memory");
+constexpr int DT_DV = 512;
 
+template <int NCH>
+struct TCfg {
+  static constexpr int DN = 64 * NCH;
+  static constexpr int DK = DN + 64;
+  static constexpr int NKQ = NCH + 2;             // k-steps per quarter of d_k (+ rope lo)
+  static constexpr uint32_t STAGE = (NCH + 1) * DT_CH;
+  static constexpr int QS = DN + 128 + 8;         // [nope | rope hi | rope lo] + padding
+  // shared-memory layout (byte offsets from the 1024-aligned base)
+  static constexpr size_t OFF_Q = size_t(DT_ST) * STAGE;
+  static constexpr size_t OFF_QRO = OFF_Q + size_t(NH) * QS * 2;
+  static constexpr size_t OFF_P = OFF_QRO + size_t(NH) * 64 * 2;
+  static constexpr size_t OFF_RED = OFF_P + size_t(NH) * DT_PS * 2;  // red_m [2][NH], red_l [2][NH]
+  static constexpr size_t OFF_FLAG = OFF_RED + size_t(4) * NH * 4;
+  static constexpr size_t OFF_BAR = (OFF_FLAG + 16 + 7) & ~size_t(7);
+  static constexpr size_t OFF_PART = (OFF_BAR + size_t(DT_ST) * 8 + 15) & ~size_t(15);
+  static constexpr size_t PART_BYTES = size_t(2) * 3 * 32 * 16;  // [key half][quarter 1..3][lane] float4
+  static constexpr size_t SMEM = 1024 + OFF_PART + PART_BYTES;
+  static_assert(OFF_Q % 16 == 0 && OFF_QRO % 16 == 0 && OFF_P % 16 == 0,
+                "cp.async / ldmatrix targets are 16-byte aligned");
+  static_assert(OFF_PART % 16 == 0 && OFF_BAR % 8 == 0, "float4 and mbarrier alignment");
+  static_assert(SMEM <= 227 * 1024, "shared memory");
+  static_assert(NCH >= 7 && NCH <= 8, "the last quarter holds 1 or 2 nope k-steps");
+};
+
+template <int NCH, bool VROPE>
 __global__ void __launch_bounds__(DT_THREADS, 1) split_decode_tma_kernel(const KernelArgs a) {
+  using T = TCfg<NCH>;
+  constexpr uint32_t DT_STAGE = T::STAGE;
+  constexpr int DT_QS = T::QS;
+  constexpr size_t DT_OFF_Q = T::OFF_Q, DT_OFF_QRO = T::OFF_QRO, DT_OFF_P = T::OFF_P,
+                   DT_OFF_RED = T::OFF_RED, DT_OFF_FLAG = T::OFF_FLAG, DT_OFF_BAR = T::OFF_BAR,
+                   DT_OFF_PART = T::OFF_PART;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
@@ -400,13 +418,13 @@ __global__ void __launch_bounds__(DT_THREADS, 1) split_decode_tma_kernel(const K
   }
   // ---- query rows of the 8 heads ----
   {
-    constexpr int CH_N = 512 / 8, CH = CH_N + 8;
+    constexpr int CH_N = T::DN / 8, CH = CH_N + 8;
     for (int idx = tid; idx < NH * CH; idx += DT_THREADS) {
       const int h = idx / CH, c = idx - h * CH;
       const uint16_t* src = a.q;
       int bytes = 0;
       if (h < nh) {
-        src = a.q + (frow * a.H + a.global_heads[hbase + h]) * 576 + c * 8;
+        src = a.q + (frow * a.H + a.global_heads[hbase + h]) * T::DK + c * 8;
         bytes = 16;
       }
       const uint32_t dst = (c < CH_N) ? smem_u32(Qs + h * DT_QS + c * 8)
@@ -427,20 +445,22 @@ __global__ void __launch_bounds__(DT_THREADS, 1) split_decode_tma_kernel(const K
       const float xr = fmaf(x, c, y * s), yr = fmaf(-x, s, y * c);
       const uint32_t hi = pack_bf16x2(xr, yr);
       const float xh = __uint_as_float(hi << 16), yh = __uint_as_float(hi & 0xffff0000u);
-      *reinterpret_cast<uint32_t*>(Qs + h * DT_QS + 512 + 2 * j) = hi;
-      *reinterpret_cast<uint32_t*>(Qs + h * DT_QS + 576 + 2 * j) = pack_bf16x2(xr - xh, yr - yh);
+      *reinterpret_cast<uint32_t*>(Qs + h * DT_QS + T::DN + 2 * j) = hi;
+      *reinterpret_cast<uint32_t*>(Qs + h * DT_QS + T::DN + 64 + 2 * j) =
+          pack_bf16x2(xr - xh, yr - yh);
     }
   }
   __syncthreads();
-  // this warp's 10 k-steps of Q^T (k-steps 10 dq .. 10 dq + 9 of the 40:
-  // nope 0..31, rope hi 32..35, rope lo 36..39) as mma B fragments
+  // this warp's NKQ k-steps of Q^T (k-steps NKQ dq .. NKQ dq + NKQ - 1 of
+  // the 4 NKQ: nope, rope hi, rope lo) as mma B fragments; ten are loaded
+  // (for NKQ = 9 the last one is not used)
   uint32_t qb[10][2];
   {
     const uint32_t base = smem_u32(Qs + (lane & 7) * DT_QS + 8 * (lane >> 3));
 #pragma unroll
     for (int i = 0; i < 5; ++i) {
       uint32_t r[4];
-      ldsm_x4(r, base + (5 * dq + i) * 64);
+      ldsm_x4(r, base + (T::NKQ * dq + 2 * i) * 32);
       qb[2 * i][0] = r[0];
       qb[2 * i][1] = r[1];
       qb[2 * i + 1][0] = r[2];
@@ -476,30 +496,36 @@ __global__ void __launch_bounds__(DT_THREADS, 1) split_decode_tma_kernel(const K
         const uint32_t unit = ((static_cast<uint32_t>(kk) & 3u) << 1) | hl;
         return rb + static_cast<uint32_t>(kk >> 2) * DT_CH + ((unit ^ rs) << 4);
       };
+      constexpr int NKQ = T::NKQ, NR = NCH - 6;  // nope k-steps of the last quarter
       if (dq < 3) {
 #pragma unroll
-        for (int j = 0; j < 10; j += 2) {
-          uint32_t a0[4], a1[4];
-          ldsm_x4(a0, kaddr(10 * dq + j));
-          ldsm_x4(a1, kaddr(10 * dq + j + 1));
+        for (int j = 0; j < NKQ; j += 2) {
+          uint32_t a0[4];
+          ldsm_x4(a0, kaddr(NKQ * dq + j));
           mma16816(sc, a0, qb[j][0], qb[j][1]);
-          mma16816(sd, a1, qb[j + 1][0], qb[j + 1][1]);
+          if (j + 1 < NKQ) {
+            uint32_t a1[4];
+            ldsm_x4(a1, kaddr(NKQ * dq + j + 1));
+            mma16816(sd, a1, qb[j + 1][0], qb[j + 1][1]);
+          }
         }
       } else {
-        {
-          uint32_t a0[4], a1[4];
-          ldsm_x4(a0, kaddr(30));
-          ldsm_x4(a1, kaddr(31));
-          mma16816(sc, a0, qb[0][0], qb[0][1]);
-          mma16816(sd, a1, qb[1][0], qb[1][1]);
+#pragma unroll
+        for (int i = 0; i < NR; ++i) {
+          uint32_t a0[4];
+          ldsm_x4(a0, kaddr(3 * NKQ + i));
+          if (i & 1)
+            mma16816(sd, a0, qb[i][0], qb[i][1]);
+          else
+            mma16816(sc, a0, qb[i][0], qb[i][1]);
         }
-        // the rope chunk meets q_rope' hi (k-steps 32..35) and lo (36..39)
+        // the rope chunk (k-steps 4 NCH ..) meets q_rope' hi and lo
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           uint32_t af[4];
-          ldsm_x4(af, kaddr(32 + kk));
-          mma16816(sc, af, qb[2 + kk][0], qb[2 + kk][1]);
-          mma16816(sd, af, qb[6 + kk][0], qb[6 + kk][1]);
+          ldsm_x4(af, kaddr(4 * NCH + kk));
+          mma16816(sc, af, qb[NR + kk][0], qb[NR + kk][1]);
+          mma16816(sd, af, qb[NR + 4 + kk][0], qb[NR + 4 + kk][1]);
         }
       }
 #pragma unroll
@@ -618,7 +644,7 @@ __global__ void __launch_bounds__(DT_THREADS, 1) split_decode_tma_kernel(const K
   float lt[2];
 #pragma unroll
   for (int e = 0; e < 2; ++e) lt[e] = red_l[2 * t4 + e] + red_l[NH + 2 * t4 + e];
-  float* wo = a.ws_o + int64_t(ch.part) * NH * 512;
+  float* wo = a.ws_o + int64_t(ch.part) * NH * DT_DV;
 #pragma unroll
   for (int mt = 0; mt < 4; ++mt) {
     const int d0 = 64 * warp + mt * 16 + g;
@@ -626,8 +652,22 @@ __global__ void __launch_bounds__(DT_THREADS, 1) split_decode_tma_kernel(const K
     for (int e = 0; e < 2; ++e) {
       const int h = 2 * t4 + e;
       const float inv = 1.f / lt[e];
-      wo[h * 512 + d0] = o[mt][e] * inv;
-      wo[h * 512 + d0 + 8] = o[mt][2 + e] * inv;
+      wo[h * DT_DV + d0] = o[mt][e] * inv;
+      wo[h * DT_DV + d0 + 8] = o[mt][2 + e] * inv;
+    }
+  }
+  if (VROPE) {
+    // the chunk lies in one segment: R(+delta) restores its output phase
+    // before the merge (RedKnot-MLA paper, RoPE-orthogonality paragraph)
+    __syncthreads();
+    const float* cs = a.rope_cs + int64_t(ch.seg) * 64;
+    for (int idx = tid; idx < NH * 32; idx += DT_THREADS) {
+      const int h = idx >> 5, k = idx & 31;
+      float* w2 = wo + h * DT_DV + T::DN + 2 * k;
+      const float c = cs[2 * k], sn = cs[2 * k + 1];
+      const float x = w2[0], y = w2[1];
+      w2[0] = x * c - y * sn;
+      w2[1] = fmaf(x, sn, y * c);
     }
   }
   if (warp == 0 && g == 0) {
@@ -648,15 +688,30 @@ __global__ void __launch_bounds__(DT_THREADS, 1) split_decode_tma_kernel(const K
     for (int j = 0; j < ch.nparts; ++j)
       ssum += __expf(__ldcg(a.ws_lse + int64_t(ch.part_first + j) * NH + h) - m);
     const int head = a.global_heads[hbase + h];
-    uint16_t* dst = a.out + (frow * a.H + head) * 512;
-    for (int d = tid; d < 512; d += DT_THREADS) {
-      float acc = 0.f;
+    uint16_t* dst = a.out + (frow * a.H + head) * DT_DV;
+    for (int d = 2 * tid; d < DT_DV; d += 2 * DT_THREADS) {
+      float acc0 = 0.f, acc1 = 0.f;
       for (int j = 0; j < ch.nparts; ++j) {
         const int64_t pj = ch.part_first + j;
         const float w = __expf(__ldcg(a.ws_lse + pj * NH + h) - m);
-        acc += w * __ldcg(a.ws_o + (pj * NH + h) * 512 + d);
+        acc0 += w * __ldcg(a.ws_o + (pj * NH + h) * DT_DV + d);
+        acc1 += w * __ldcg(a.ws_o + (pj * NH + h) * DT_DV + d + 1);
       }
-      dst[d] = f32_to_bf16(acc / ssum);
+      acc0 /= ssum;
+      acc1 /= ssum;
+      if (VROPE && d >= T::DN) {
+        // inverse output RoPE R(-p) at the request's row p = 256 a + b
+        const int k = (d - T::DN) >> 1, p = rq.q_row_begin;
+        const float* hi = a.pos_cs_hi + int64_t(p >> 8) * 64 + 2 * k;
+        const float* lo = a.pos_cs_lo + int64_t(p & 255) * 64 + 2 * k;
+        const float pc = fmaf(hi[0], lo[0], -hi[1] * lo[1]);
+        const float ps = fmaf(hi[1], lo[0], hi[0] * lo[1]);
+        const float x = acc0, y = acc1;
+        acc0 = fmaf(x, pc, y * ps);
+        acc1 = fmaf(-x, ps, y * pc);
+      }
+      dst[d] = f32_to_bf16(acc0);
+      dst[d + 1] = f32_to_bf16(acc1);
     }
     if (tid == 0) a.lse[frow * a.H + head] = m + logf(ssum);
   }
@@ -670,6 +725,17 @@ cudaError_t launch_t(const KernelArgs& a, cudaStream_t s) {
                                        static_cast<int>(C::SMEM));
   if (e != cudaSuccess) return e;
   k<<<a.num_chunks, THREADS, C::SMEM, s>>>(a);
+  return cudaGetLastError();
+}
+
+template <int NCH, bool VROPE>
+cudaError_t launch_tma(const KernelArgs& a, cudaStream_t s) {
+  auto k = split_decode_tma_kernel<NCH, VROPE>;
+  constexpr size_t smem = TCfg<NCH>::SMEM;
+  cudaError_t e =
+      cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  k<<<a.num_chunks, DT_THREADS, smem, s>>>(a);
   return cudaGetLastError();
 }
 
@@ -711,14 +777,10 @@ __global__ void lse_merge_kernel(const float* __restrict__ o_parts,
 
 cudaError_t launch_split_decode(const rk_seg_attn_plan_s& plan, const KernelArgs& a,
                                 cudaStream_t s) {
-  if (plan.d_nope == 512 && plan.d_rope == 64 && a.decmaps) {
-    cudaError_t e = cudaFuncSetAttribute(split_decode_tma_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(DT_SMEM));
-    if (e != cudaSuccess) return e;
-    split_decode_tma_kernel<<<a.num_chunks, DT_THREADS, DT_SMEM, s>>>(a);
-    return cudaGetLastError();
-  }
+  if (!plan.v_rope && plan.d_nope == 512 && plan.d_rope == 64 && a.decmaps)
+    return launch_tma<8, false>(a, s);
+  if (plan.v_rope && plan.d_nope == 448 && plan.d_rope == 64 && a.decmaps)
+    return launch_tma<7, true>(a, s);
   if (plan.v_rope && plan.d_nope == 448 && plan.d_rope == 64) return launch_t<448, 64, true>(a, s);
   if (plan.d_nope == 512 && plan.d_rope == 64) return launch_t<512, 64, false>(a, s);
   if (plan.d_nope == 128 && plan.d_rope == 32) return launch_t<128, 32, false>(a, s);
