@@ -680,25 +680,47 @@ __global__ void __launch_bounds__(DT_THREADS, 1) split_decode_tma_kernel(const K
   __syncthreads();
   if (!flag[0]) return;
   __threadfence();
-  for (int h = 0; h < nh; ++h) {
+  // ---- last CTA of the request: log-sum-exp merge of all partials ----
+  // warp h finds head h's maximum and sum over the parts and writes each
+  // part's weight exp(lse_j - m) / sum once into the idle stage ring (every
+  // stage has landed and been consumed)
+  const int np = ch.nparts;
+  float* wts = reinterpret_cast<float*>(Kst);  // [NH][np]
+  const bool in_smem = size_t(np) * NH * 4 <= size_t(DT_ST) * DT_STAGE;
+  if (warp < nh) {
+    const int h = warp;
     float m = -INFINITY;
-    for (int j = 0; j < ch.nparts; ++j)
+    for (int j = lane; j < np; j += 32)
       m = fmaxf(m, __ldcg(a.ws_lse + int64_t(ch.part_first + j) * NH + h));
+#pragma unroll
+    for (int off = 16; off; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
     float ssum = 0.f;
-    for (int j = 0; j < ch.nparts; ++j)
+    for (int j = lane; j < np; j += 32)
       ssum += __expf(__ldcg(a.ws_lse + int64_t(ch.part_first + j) * NH + h) - m);
+#pragma unroll
+    for (int off = 16; off; off >>= 1) ssum += __shfl_xor_sync(0xffffffffu, ssum, off);
+    if (in_smem)
+      for (int j = lane; j < np; j += 32)
+        wts[h * np + j] = __expf(__ldcg(a.ws_lse + int64_t(ch.part_first + j) * NH + h) - m) / ssum;
+    if (lane == 0) {
+      red_m[h] = m;
+      red_l[h] = ssum;
+    }
+  }
+  __syncthreads();
+  for (int h = 0; h < nh; ++h) {
+    const float m = red_m[h], ssum = red_l[h], inv = 1.f / ssum;
     const int head = a.global_heads[hbase + h];
     uint16_t* dst = a.out + (frow * a.H + head) * DT_DV;
     for (int d = 2 * tid; d < DT_DV; d += 2 * DT_THREADS) {
       float acc0 = 0.f, acc1 = 0.f;
-      for (int j = 0; j < ch.nparts; ++j) {
+      for (int j = 0; j < np; ++j) {
         const int64_t pj = ch.part_first + j;
-        const float w = __expf(__ldcg(a.ws_lse + pj * NH + h) - m);
-        acc0 += w * __ldcg(a.ws_o + (pj * NH + h) * DT_DV + d);
-        acc1 += w * __ldcg(a.ws_o + (pj * NH + h) * DT_DV + d + 1);
+        const float w = in_smem ? wts[h * np + j] : __expf(__ldcg(a.ws_lse + pj * NH + h) - m) * inv;
+        const float2 x = __ldcg(reinterpret_cast<const float2*>(a.ws_o + (pj * NH + h) * DT_DV + d));
+        acc0 = fmaf(w, x.x, acc0);
+        acc1 = fmaf(w, x.y, acc1);
       }
-      acc0 /= ssum;
-      acc1 /= ssum;
       if (VROPE && d >= T::DN) {
         // inverse output RoPE R(-p) at the request's row p = 256 a + b
         const int k = (d - T::DN) >> 1, p = rq.q_row_begin;
