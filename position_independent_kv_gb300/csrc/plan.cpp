@@ -990,8 +990,12 @@ cudaError_t launch_forward(const rk_seg_attn_plan_s& p, const KernelArgs& a, con
   }
   if (a.num_tiles) e = launch_dense_mma(p, a, ts);
   if (e == cudaSuccess && a.num_tc_tiles) e = launch_dense_tc(p, a, q, ts);
+  // beside split chunks (decode) the few short Local tiles run on CTA pairs,
+  // which leave more SMs to the split kernel than 4-CTA clusters (the pair
+  // kernel has no rotary-value form)
   if (e == cudaSuccess && a.num_tc_pairs)
-    e = p.kernel == 3 ? launch_dense_tc4(p, a, q, ts) : launch_dense_tc2(p, a, q, ts);
+    e = (p.kernel == 3 && (!a.num_chunks || p.v_rope)) ? launch_dense_tc4(p, a, q, ts)
+                                                        : launch_dense_tc2(p, a, q, ts);
   if (e == cudaSuccess && a.num_chunks) e = launch_split_decode(p, a, s);
   if (ts != s) {
     const cudaError_t e1 = cudaEventRecord(p.ev_join, ts);
