@@ -224,7 +224,8 @@ rk_status_t rk_seg_attn_forward(rk_seg_attn_plan_t plan, const void* q, void* ou
  * the copies to and from the device run inside the call, overlapped with
  * the kernels.  The computed rows are taken in eight consecutive ranges;
  * a range's q and lse rows are copied in on a plan-owned stream, its tiles
- * run on `stream` as soon as it (and every earlier range) is on the device,
+ * run as soon as it (and every earlier range) is on the device, alternately
+ * on `stream` and on a second plan-owned stream,
  * and its results are copied back on a second plan-owned stream once the
  * tiles that write it are done.  Only written elements of out travel: the
  * whole row where every head is written (protected rows, or every row when
