@@ -226,7 +226,7 @@ rk_status_t rk_seg_attn_forward(rk_seg_attn_plan_t plan, const void* q, void* ou
  * a range's q and lse rows are copied in on a plan-owned stream, its tiles
  * run as soon as it (and every earlier range) is on the device, alternately
  * on `stream` and on a second plan-owned stream,
- * and its results are copied back on a second plan-owned stream once the
+ * and its results are copied back on a third plan-owned stream once the
  * tiles that write it are done.  Only written elements of out travel: the
  * whole row where every head is written (protected rows, or every row when
  * all heads are Global) and the Global heads' columns of the other rows;
