@@ -373,6 +373,68 @@ def bench_decode(args, local):
     return dict(ms=ms, bytes=byt, gbs=byt / (ms * 1e-3) / 1e9, ok=ok, info=info)
 
 
+def bench_other_prefill(local: int, pk: dict, names=("flash", "varlen", "tiny")) -> dict:
+    """The other prefill-shaped workloads on the default plan: device time per
+    forward (CUDA events on the launching stream, 3 warm-ups, median of 20);
+    algorithmic and performed TFLOP/s, attended pairs/s and the fraction of
+    the bf16 peak.  Tiny fits in L2, so L2 is flushed (256 MB write) before
+    each of its iterations; the others read more than L2 per forward."""
+    import torch
+    from position_independent_kv_gb300 import binding as B
+    from position_independent_kv_gb300.protected import build_bitmap
+    from position_independent_kv_gb300.workloads import make_workload
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    res = {}
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    for name in names:
+        wl = make_workload(name, seed=0, device=dev)
+        bm, _ = build_bitmap(wl)
+        plan = B.SegAttnPlan.from_workload(wl, bitmap=bm, stream=stream)
+        ws_buf = torch.empty(max(16, plan.workspace_bytes), dtype=torch.uint8, device=dev)
+        out, lse = wl.out_init, wl.lse_init
+        in_bytes = (wl.q.numel() * wl.q.element_size() + out.numel() * out.element_size())
+        do_flush = in_bytes < 2 * 129 * 1024 * 1024
+        for _ in range(3):
+            plan.forward(wl.q, out, lse, ws_buf, stream=stream)
+        torch.cuda.synchronize(dev)
+        times = []
+        for _ in range(20):
+            if do_flush:
+                flush.zero_()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            plan.forward(wl.q, out, lse, ws_buf, stream=stream)
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            times.append(a.elapsed_time(b))
+        ok = plan.device_status(stream=stream) == 0
+        info = plan.info
+        ms = statistics.median(times)
+        alg, perf = prefill_flops(info, wl.d_k, wl.d_v)
+        pairs = info["pairs_global"] + info["pairs_local"]
+        kernel = {0: "mma_sync", 1: "tcgen05", 2: "tcgen05_pair", 3: "tcgen05_quad",
+                  4: "tcgen05_small"}.get(info["kernel"], str(info["kernel"]))
+        res[name] = {"workload": workload_desc(name), "ms": round(ms, 4),
+                     "tflops": round(alg / (ms * 1e-3) / 1e12, 2),
+                     "performed_tflops": round(perf / (ms * 1e-3) / 1e12, 2),
+                     "pairs_per_s": pairs / (ms * 1e-3),
+                     "frac_of_peak": round(alg / (ms * 1e-3) / 1e12 / pk["bf16_tflops"], 4),
+                     "performed_frac_of_peak": round(perf / (ms * 1e-3) / 1e12 / pk["bf16_tflops"], 4),
+                     "flop_per_pair": 2 * wl.d_k + 2 * wl.d_v, "attended_pairs": pairs,
+                     "performed_pairs": info["performed_pairs"], "kernel": kernel,
+                     "dense_tile_pairs": info.get("tc_pairs", info["dense_tiles"]),
+                     "l2": "256 MB flush between iterations" if do_flush else
+                           f"inputs larger than L2 ({in_bytes / 1e9:.2f} GB of Q + O), no flush",
+                     "status_ok": ok}
+        plan.close()
+        del wl, out, lse, ws_buf
+        torch.cuda.empty_cache()
+    del flush
+    return res
+
+
 def bench_vrope(local: int, pk: dict) -> dict:
     """The rotary-value path (V = the whole latent row, output phase
     restored; d = 448 + 64): the long-context prefill (CUDA events, 3 warm-ups,
@@ -683,6 +745,9 @@ def run_ours(args):
     proj = None
     if not args.no_projection and rank == 0:
         proj = bench_projection(local, args.projection_workload)
+    others = None
+    if not args.no_others and rank == 0:
+        others = bench_other_prefill(local, pk)
     vrope = None
     if not args.no_vrope and rank == 0:
         vrope = bench_vrope(local, pk)
@@ -725,6 +790,8 @@ def run_ours(args):
         if proj:
             proj["frac_of_peak"] = round(proj["tflops"] / peak, 4)
             line["projection"] = proj
+        if others:
+            line["configs"] = others
         if vrope:
             line["v_rope"] = vrope
         if paged:
@@ -799,6 +866,8 @@ def main():
                     help="skip the timing of SegPagedAttention on GQA pages")
     ap.add_argument("--paged-prefill", default="qwen32b_128k",
                     help="paged workload of the SegPagedAttention prefill timing")
+    ap.add_argument("--no-others", action="store_true",
+                    help="skip the timing of the flash-like, variable-length and tiny workloads")
     ap.add_argument("--no-vrope", action="store_true",
                     help="skip the timing of the rotary-value (output-phase restore) path")
     ap.add_argument("--projection-workload", default="ctx128k",

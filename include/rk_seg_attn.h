@@ -277,8 +277,9 @@ rk_status_t rk_lse_merge(const float* o_parts, const float* lse_parts, int32_t P
  * All calls on a device share that array and it keeps the previous call's
  * contents (each call clears what must start at zero); calls whose kernels
  * overlap on the GPU race on it, so order them on one stream.  The first
- * call on a device looks up the array's address with that device current;
- * make that first call before any stream capture.
+ * call on a device looks up the array's address with that device current,
+ * and a call that finds a new context on the device (after cudaDeviceReset)
+ * looks it up again; make those calls before any stream capture.
  * Errors: as rk_seg_attn_forward, plus RK_ERR_CAPACITY (before any launch)
  * when rk_seg_attn_workspace_bytes(plan) > RK_NOALLOC_SCRATCH_BYTES. */
 rk_status_t rk_seg_attn_forward_noalloc(rk_seg_attn_plan_t plan, const void* q, void* out,

@@ -18,11 +18,16 @@
 //  * calls whose kernels overlap on the GPU (different streams without an
 //    ordering between them) race on the array: order them;
 //  * the first call on a device looks up the array's device address
-//    (cudaGetSymbolAddress) with that device current and caches it; make
-//    that first call before any stream capture;
+//    (cudaGetSymbolAddress) with that device current and caches it with the
+//    id of the device's current context; a later call that finds another
+//    context there (after cudaDeviceReset the module is loaded again and the
+//    array has a new address) looks it up again.  Make the first call on a
+//    device, and the first call after a reset, before any stream capture;
 //  * a plan whose scratch needs more than the array holds is refused with
 //    RK_ERR_CAPACITY before anything is launched.
 // The kernels and their arguments are exactly those of rk_seg_attn_forward.
+
+#include <cudaTypedefs.h>
 
 #include <mutex>
 
@@ -31,22 +36,50 @@
 namespace {
 
 constexpr size_t kScratchBytes = RK_NOALLOC_SCRATCH_BYTES;
-constexpr int kSplitHeads = 8;
 constexpr int kMaxDevices = 128;
 
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
 std::mutex g_mu;
 void* g_addr[kMaxDevices] = {};
+unsigned long long g_ctx[kMaxDevices] = {};
 
-// Device address of g_scratch on the current device `dev` (cached).
+// Id of the calling thread's current context (driver entry points, so the
+// library keeps no link-time dependency on libcuda).
+bool current_context_id(unsigned long long* id) {
+  static PFN_cuCtxGetCurrent_v4000 get_cur = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_cur = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(f);
+  });
+  CUcontext ctx = nullptr;
+  if (!get_cur || !get_id || get_cur(&ctx) != CUDA_SUCCESS || !ctx) return false;
+  return get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of g_scratch on the current device `dev`, looked up once
+// per device and context.
 rk_status_t scratch_address(int dev, void** out) {
   if (dev < 0 || dev >= kMaxDevices) return RK_ERR_CAPACITY;
+  unsigned long long ctx = 0;
+  if (!current_context_id(&ctx)) return RK_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_addr[dev]) {
+  if (!g_addr[dev] || g_ctx[dev] != ctx) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || !p) return RK_ERR_CUDA;
     g_addr[dev] = p;
+    g_ctx[dev] = ctx;
   }
   *out = g_addr[dev];
   return RK_OK;
@@ -72,15 +105,8 @@ extern "C" rk_status_t rk_seg_attn_forward_noalloc(rk_seg_attn_plan_t p, const v
     void* base = nullptr;
     rk_status_t st = scratch_address(cur, &base);
     if (st != RK_OK) return st;
-    char* w = static_cast<char*>(base);
-    a.ws_o = reinterpret_cast<float*>(w);
-    size_t off = static_cast<size_t>(p->num_parts) * kSplitHeads * p->d_v * sizeof(float);
-    a.ws_lse = reinterpret_cast<float*>(w + off);
-    off += static_cast<size_t>(p->num_parts) * kSplitHeads * sizeof(float);
-    off = (off + 255) & ~size_t(255);
-    a.ws_ticket = reinterpret_cast<int32_t*>(w + off);
-    if (cudaMemsetAsync(a.ws_ticket, 0, p->num_mgroups * sizeof(int32_t), s) != cudaSuccess)
-      return RK_ERR_CUDA;
+    st = rk::bind_workspace(*p, a, base, s);  // the layout rk_seg_attn_forward uses
+    if (st != RK_OK) return st;
   }
   return rk::launch_forward(*p, a, q, s) == cudaSuccess ? RK_OK : RK_ERR_CUDA;
 }

@@ -745,11 +745,9 @@ extern "C" size_t rk_seg_attn_workspace_bytes(rk_seg_attn_plan_t p) {
   return p ? p->workspace_bytes : 0;
 }
 
-namespace {
+namespace rk {
 
-// Point the split-decode arguments at the caller's workspace and clear the
-// merge tickets on stream s.
-rk_status_t bind_workspace(const rk_seg_attn_plan_s& p, rk::KernelArgs& a, void* workspace,
+rk_status_t bind_workspace(const rk_seg_attn_plan_s& p, KernelArgs& a, void* workspace,
                            cudaStream_t s) {
   if (!p.num_parts) return RK_OK;
   char* w = static_cast<char*>(workspace);
@@ -763,6 +761,10 @@ rk_status_t bind_workspace(const rk_seg_attn_plan_s& p, rk::KernelArgs& a, void*
              ? RK_OK
              : RK_ERR_CUDA;
 }
+
+}  // namespace rk
+
+namespace {
 
 rk_status_t check_forward_args(const rk_seg_attn_plan_s* p, const void* q, const void* out,
                                const float* lse, const void* workspace, size_t ws_bytes) {
@@ -790,7 +792,7 @@ extern "C" rk_status_t rk_seg_attn_forward(rk_seg_attn_plan_t p, const void* q, 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   rk::KernelArgs a{};
   rk::fill_args(*p, a, q, out, lse);
-  st = bind_workspace(*p, a, workspace, s);
+  st = rk::bind_workspace(*p, a, workspace, s);
   if (st != RK_OK) return st;
   return rk::launch_forward(*p, a, q, s) == cudaSuccess ? RK_OK : RK_ERR_CUDA;
 }
@@ -838,7 +840,7 @@ extern "C" rk_status_t rk_seg_attn_forward_host(rk_seg_attn_plan_t p, const void
   }
   rk::KernelArgs a{};
   rk::fill_args(*p, a, q, out, lse);
-  if (good) good = bind_workspace(*p, a, workspace, s) == RK_OK;
+  if (good) good = rk::bind_workspace(*p, a, workspace, s) == RK_OK;
   const bool pipelined = !p->tc_pairs_chunked.empty() && a.num_tiles == 0 && a.num_tc_tiles == 0;
   if (pipelined) {
     // the tile pairs of row range c run once rows 0 .. c are on the device;

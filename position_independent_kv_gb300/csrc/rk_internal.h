@@ -219,6 +219,11 @@ cudaError_t launch_dense_tc4(const rk_seg_attn_plan_s& plan, const KernelArgs& a
 // Fill the kernel arguments shared by every launch of a forward.
 void fill_args(const rk_seg_attn_plan_s& plan, KernelArgs& a, const void* q, void* out,
                float* lse);
+// Point the split-decode arguments at `workspace` (the layout that
+// rk_seg_attn_workspace_bytes sizes: partial outputs, partial LSEs, then the
+// merge tickets at a 256-byte boundary) and clear the tickets on stream s.
+rk_status_t bind_workspace(const rk_seg_attn_plan_s& plan, KernelArgs& a, void* workspace,
+                           cudaStream_t s);
 // Launch every kernel of a forward (split chunks, then prefill tiles).
 cudaError_t launch_forward(const rk_seg_attn_plan_s& plan, const KernelArgs& a, const void* q,
                            cudaStream_t stream);

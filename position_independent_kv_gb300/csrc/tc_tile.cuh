@@ -23,7 +23,8 @@ struct Ctx {
 // CLUSTER: acquire at cluster scope (the phase is completed by arrivals
 // from other CTAs that publish shared-memory data).
 template <bool CLUSTER = false>
-__device__ __forceinline__ bool wait_bar(const Ctx& c, int i, uint32_t parity) {
+__device__ __forceinline__ bool wait_bar(const Ctx& c, int i, uint32_t parity,
+                                         uint64_t limit_ns = WAIT_NS) {
   uint64_t* b = c.bar + i;
   uint32_t it = 0;
   uint64_t t0 = 0;
@@ -36,7 +37,7 @@ __device__ __forceinline__ bool wait_bar(const Ctx& c, int i, uint32_t parity) {
       const uint64_t now = tc::global_ns();
       if (t0 == 0) {
         t0 = now;
-      } else if (now - t0 > WAIT_NS) {
+      } else if (now - t0 > limit_ns) {
         *c.abort = 1;
         atomicCAS(c.status, 0, static_cast<int32_t>(RK_ERR_DEVICE_TIMEOUT));
         return false;
@@ -47,11 +48,12 @@ __device__ __forceinline__ bool wait_bar(const Ctx& c, int i, uint32_t parity) {
 }
 
 // Bounded wait that ignores the abort flag (drains work in flight).
-__device__ __forceinline__ void drain_bar(const Ctx& c, int i, uint32_t parity) {
+__device__ __forceinline__ void drain_bar(const Ctx& c, int i, uint32_t parity,
+                                          uint64_t limit_ns = WAIT_NS) {
   uint64_t* b = c.bar + i;
   const uint64_t t0 = tc::global_ns();
   while (!tc::mbar_try_wait(b, parity)) {
-    if (tc::global_ns() - t0 > WAIT_NS) {
+    if (tc::global_ns() - t0 > limit_ns) {
       atomicCAS(c.status, 0, static_cast<int32_t>(RK_ERR_DEVICE_TIMEOUT));
       return;
     }

@@ -18,6 +18,16 @@ MAX_REL = 1e-2     # max |err| <= MAX_REL * max |ref|   (per tensor)
 MEAN_REL = 2e-3    # sum |err| / sum |ref| <= MEAN_REL  (per tensor)
 LSE_ABS = 1e-3     # |lse - lse_ref| <= LSE_ABS
 
+# (label, stats) of every comparison made in this session; the conftest
+# prints them at the end of the run so the margins to the bounds are visible.
+PARITY_STATS: list = []
+
+
+def record_stats(label: str, stats: dict, max_rel=MAX_REL, mean_rel=MEAN_REL, lse_abs=LSE_ABS):
+    """Keep one comparison's error statistics with the bounds it was held to."""
+    PARITY_STATS.append((label, dict(stats, max_bound=max_rel * stats["max_ref"],
+                                     mean_bound=mean_rel, lse_bound=lse_abs)))
+
 
 def run_gpu(wl, flags=0, stream=None):
     bm, prot_rows = build_bitmap(wl)
@@ -128,6 +138,7 @@ def compare(wl, out, lse, prot_rows, ref, rows_per_req, label=""):
     stats = dict(max_err=float(err.max()), max_ref=float(np.abs(ro).max()),
                  mean_rel=float(err.sum() / np.abs(ro).sum()),
                  lse_err=float(np.abs(gl - rl).max()), n=int(go.shape[0]))
+    record_stats(label, stats)
     assert np.isfinite(go).all() and np.isfinite(gl).all(), f"{label}: non-finite output"
     assert stats["max_err"] <= MAX_REL * stats["max_ref"], f"{label}: {stats}"
     assert stats["mean_rel"] <= MEAN_REL, f"{label}: {stats}"

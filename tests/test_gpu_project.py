@@ -4,6 +4,8 @@ import numpy as np
 import pytest
 import torch
 
+from _helpers import record_stats
+
 from oracle.project import project_state
 from position_independent_kv_gb300 import binding as B
 from position_independent_kv_gb300 import build as BUILD
@@ -60,6 +62,10 @@ def _check(got, ref, label, mean_rel=MEAN_REL):
     got = got.double().cpu().numpy()
     assert np.isfinite(got).all(), f"{label}: unwritten outputs"
     err = np.abs(got - ref)
+    record_stats(f"project {label}", dict(max_err=float(err.max()), max_ref=float(np.abs(ref).max()),
+                                          mean_rel=float(err.sum() / np.abs(ref).sum()),
+                                          lse_err=0.0, n=int(err.size)),
+                 mean_rel=mean_rel)
     assert err.max() <= MAX_REL * np.abs(ref).max(), f"{label}: max err {err.max()}"
     assert err.sum() <= mean_rel * np.abs(ref).sum(), f"{label}: mean rel {err.sum() / np.abs(ref).sum()}"
 

@@ -5,25 +5,19 @@ import pytest
 import torch
 
 import oracle as O
-from _helpers import LSE_ABS, MAX_REL
+from _helpers import LSE_ABS, MAX_REL, record_stats
 from position_independent_kv_gb300 import binding as B
 from position_independent_kv_gb300 import build as BUILD
 from position_independent_kv_gb300.paged_workloads import make_paged_workload
 
 pytestmark = pytest.mark.gpu
 
-# Tolerance of this operation, derived from its arithmetic: P is rounded to
-# bf16 before the P.V contraction (the tensor cores take V in bf16 and both
-# operands share the type).  With the stated inputs the softmax is nearly
-# uniform (score std ~ 1/128), every P lies in (0.97, 1] where the bf16 grid
-# step is 2^-8, so each P carries a relative error of RMS 2^-8 / sqrt(12) =
-# 1.1e-3; an output element is a sum of many terms of random sign, so its
-# relative error is that RMS again, and the bf16 rounding of the output adds
-# a relative RMS of up to 2^-9 / sqrt(3) = 1.1e-3 at the bottom of each
-# binade.  Their sum bounds the mean relative error at 2.3e-3 in the limit;
-# 3e-3 leaves room for sampling noise.  Max and LSE bounds are the main
-# path's.
-MEAN_REL = 3e-3
+# The stated bound for bf16 in / fp32 accumulate: mean relative error 2e-3,
+# max error 1e-2 max|ref|, LSE 1e-3 absolute.  Two bf16 roundings set most of
+# the mean error on the stated inputs: P before the P.V contraction (the
+# tensor cores take V in bf16 and both operands share the type) and the
+# stored output, together about 1.9e-3 here, as on the MLA path.
+from _helpers import MEAN_REL  # noqa: E402
 
 MINI = ["paged_mini", "paged_mini_g4", "paged_mini_g1", "paged_mini_g16", "paged_decode_mini",
         "paged_decode_long_mini", "paged_decode_g16_long", "paged_decode_g1_long", "paged_decode_g4", "paged_tail_g1",
@@ -72,7 +66,9 @@ def compare(out, lse, ref, label):
     assert np.isfinite(go).all() and np.isfinite(gl).all(), f"{label}: unwritten or non-finite"
     err = np.abs(go - ro)
     st = dict(max_err=float(err.max()), max_ref=float(np.abs(ro).max()),
-              mean_rel=float(err.sum() / np.abs(ro).sum()), lse_err=float(np.abs(gl - rl).max()))
+              mean_rel=float(err.sum() / np.abs(ro).sum()), lse_err=float(np.abs(gl - rl).max()),
+              n=int(go.size))
+    record_stats(f"seg_paged {label}", st, mean_rel=MEAN_REL)
     assert st["max_err"] <= MAX_REL * st["max_ref"], f"{label}: {st}"
     assert st["mean_rel"] <= MEAN_REL, f"{label}: {st}"
     assert st["lse_err"] <= LSE_ABS, f"{label}: {st}"

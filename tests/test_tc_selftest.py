@@ -79,55 +79,52 @@ def test_tcgen05_cta_pair(selftest_lib, mode):
         f"{ref[0, :4].tolist()}; row 128 {got[128, :4].tolist()} vs {ref[128, :4].tolist()}")
 
 
-def test_data_movement_probes(selftest_lib):
-    """Hardware probes behind the prefill kernels' data movement (run with -s
-    to see the tables): TMA streaming throughput over all SMs by box shape for
-    per-CTA loads, CTA-pair loads completing on the leader's barrier, and
-    per-CTA loads whose arrival is forwarded to the leader; then the round trip
-    of remote mbarrier arrives between the CTAs of a pair.  Asserts only that
-    every probe runs to completion without an expired wait."""
+def test_bounded_wait_expires_cleanly(selftest_lib):
+    """The kernels' bounded wait run out on purpose, with no copy and no MMA
+    in flight: a waiter on a barrier that nothing completes gives up after
+    its limit and records RK_ERR_DEVICE_TIMEOUT (8); the CTA's other roles,
+    waiting with the kernels' own 2 s bound, give up at once through the
+    abort flag and leave their bar.red vote together; tensor memory is freed;
+    the launch returns.  The context stays usable: a following forward
+    through the C ABI matches the oracle and reports a clean status."""
+    import numpy as np
+    from _helpers import compare, oracle_rows, run_gpu
+    from position_independent_kv_gb300.workloads import make_workload
     L = selftest_lib
-    L.rk_tma_stream_probe.argtypes = [ctypes.c_void_p] + [ctypes.c_int] * 6 + [ctypes.c_void_p] * 2
-    L.rk_tma_stream_probe.restype = ctypes.c_int
-    L.rk_tma_pair_probe.argtypes = [ctypes.c_void_p] + [ctypes.c_int] * 7 + [ctypes.c_void_p] * 2
-    L.rk_tma_pair_probe.restype = ctypes.c_int
-    L.rk_remote_arrive_probe.argtypes = [ctypes.c_int] * 3 + [ctypes.c_void_p] * 3
-    L.rk_remote_arrive_probe.restype = ctypes.c_int
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    ctas = sms - (sms & 1)
-    rows = 131072
-    g = torch.Generator(device="cuda").manual_seed(7)
-    lat = torch.randn(rows, 576, device="cuda", generator=g).to(torch.bfloat16)
-    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    L.rk_tc_timeout_selftest.argtypes = [ctypes.c_int, ctypes.c_ulonglong] + [ctypes.c_void_p] * 4
+    L.rk_tc_timeout_selftest.restype = ctypes.c_int
     stream = torch.cuda.current_stream().cuda_stream
-    clk = 2.07e9  # the part's maximum SM clock, for B/clk/SM
-    print(f"\nTMA streaming, {ctas} CTAs, [{rows}, 576] bf16, box 64 dims x rows x chunks")
-    print("box           bytes  slots  per-CTA  pair  forwarded   (B/clk/SM)")
-    for br, bc, slots in [(64, 3, 5), (128, 2, 4), (64, 4, 3), (64, 9, 2), (128, 4, 3)]:
-        bb = 128 * br * bc
-        n = max(16, int(24e6 // bb))
-        res = []
-        for mode in (0, 1, 2):
-            best = None
-            for _ in range(2):
-                e0, e1 = torch.cuda.Event(True), torch.cuda.Event(True)
-                e0.record()
-                rc = L.rk_tma_pair_probe(lat.data_ptr(), rows, br, bc, slots, n, mode, ctas,
-                                         status.data_ptr(), stream)
-                e1.record()
-                torch.cuda.synchronize()
-                assert rc == 0
-                ms = e0.elapsed_time(e1)
-                best = ms if best is None else min(best, ms)
-            assert int(status.item()) == 0, "a bounded wait expired"
-            res.append(ctas * n * bb / (best * 1e-3) / ctas / clk)
-        print(f"{br:3d} x {bc}     {bb // 1024:3d} KB  {slots:4d}  {res[0]:7.1f} {res[1]:5.1f} {res[2]:8.1f}")
-    ns = torch.zeros(1, dtype=torch.int64, device="cuda")
-    for relaxed in (0, 1):
-        n = 20000
-        assert L.rk_remote_arrive_probe(n, relaxed, ctas, status.data_ptr(), ns.data_ptr(),
-                                        stream) == 0
+
+    def run(mode, limit_ns):
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        ended = torch.zeros(3, dtype=torch.int32, device="cuda")
+        ns = torch.zeros(3, dtype=torch.int64, device="cuda")
+        e0, e1 = torch.cuda.Event(True), torch.cuda.Event(True)
+        e0.record()
+        rc = L.rk_tc_timeout_selftest(mode, limit_ns, status.data_ptr(), ended.data_ptr(),
+                                      ns.data_ptr(), stream)
+        e1.record()
         torch.cuda.synchronize()
-        assert int(status.item()) == 0, "a bounded wait expired"
-        print(f"remote mbarrier arrive round trip ({'relaxed' if relaxed else 'release'}): "
-              f"{int(ns.item()) / n:.1f} ns")
+        assert rc == 0
+        return int(status.item()), ended.tolist(), ns.tolist(), e0.elapsed_time(e1)
+
+    # every barrier completed: every wait passes, no error
+    st, ended, ns, _ = run(1, 20_000)
+    assert st == 0 and ended == [1, 1, 1], (st, ended)
+    # nothing completes barrier 0: its waiter gives up after 20 us, the other
+    # roles follow it long before their own 2 s bound
+    limit = 20_000
+    st, ended, ns, ms = run(0, limit)
+    assert st == 8, f"status {st}, want RK_ERR_DEVICE_TIMEOUT"
+    assert ended == [2, 2, 2], ended
+    assert ns[0] >= limit, ns
+    assert max(ns) < 100_000_000, f"a role kept waiting after the abort: {ns} ns"
+    assert ms < 1000.0
+    print(f"\nbounded wait: first waiter gave up after {ns[0] / 1e3:.1f} us, "
+          f"the others after {ns[1] / 1e3:.1f} / {ns[2] / 1e3:.1f} us; launch {ms:.3f} ms")
+    # the context is intact: a normal forward is correct and its status clean
+    wl = make_workload("tiny", seed=0, device="cuda")
+    out, lse, plan, bm, prot = run_gpu(wl)
+    ref = oracle_rows(wl, prot)
+    rows = [np.arange(r.q_row_begin, r.T) for r in wl.requests]
+    compare(wl, out, lse, prot, ref, rows, label="tiny after an expired wait")

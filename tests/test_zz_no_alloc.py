@@ -2,7 +2,10 @@
 device memory when they issue it (engines that reserve all memory up front).
 It keeps the split-over-segments scratch in the library's static device
 array; its results must match rk_seg_attn_forward with a caller workspace,
-on two calls in a row (the array keeps the previous call's contents).
+bit for bit, on two calls in a row (the array keeps the previous call's
+contents).  Both entry points run the same kernels on the same plan and the
+split merge adds its parts in a fixed order, so any difference would be a
+scratch-layout or clearing mistake.
 
 This file is collected last on purpose."""
 import math
@@ -11,7 +14,6 @@ import numpy as np
 import pytest
 import torch
 
-from _helpers import LSE_ABS, MAX_REL, MEAN_REL
 from position_independent_kv_gb300 import binding as B
 from position_independent_kv_gb300 import build as BUILD
 from position_independent_kv_gb300.protected import build_bitmap
@@ -26,15 +28,6 @@ def built():
     BUILD.build()
 
 
-def _within(a_out, a_lse, r_out, r_lse, comp):
-    go = a_out[comp].double()
-    ro = r_out[comp].double()
-    err = (go - ro).abs()
-    assert float(err.max()) <= MAX_REL * float(ro.abs().max())
-    assert float(err.sum() / ro.abs().sum()) <= MEAN_REL
-    assert float((a_lse[comp].double() - r_lse[comp].double()).abs().max()) <= LSE_ABS
-
-
 @pytest.mark.parametrize("name", ["decode_mini", "decode"])
 def test_noalloc_matches_workspace_forward(name):
     wl = make_workload(name, seed=4, device="cuda", q_scale=2304.0)
@@ -45,14 +38,13 @@ def test_noalloc_matches_workspace_forward(name):
     r_out, r_lse = wl.out_init.clone(), wl.lse_init.clone()
     plan.forward(wl.q, r_out, r_lse, ws)
     torch.cuda.synchronize()
-    # every row of a decode request is its new row: all heads are recomputed
-    comp = torch.ones(wl.rows, wl.H, dtype=torch.bool, device="cuda")
     for call in range(2):
         out, lse = wl.out_init.clone(), wl.lse_init.clone()
         plan.forward_noalloc(wl.q, out, lse)
         torch.cuda.synchronize()
         assert plan.device_status() == 0
-        _within(out, lse, r_out, r_lse, comp)
+        assert torch.equal(out, r_out), f"call {call}: out differs"
+        assert torch.equal(lse, r_lse), f"call {call}: lse differs"
 
 
 def test_noalloc_refuses_oversized_scratch():
