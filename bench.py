@@ -78,6 +78,7 @@ def peaks():
 
 PLAN_FLAGS = {"auto": 0, "pair": 8, "single": 4, "legacy": 2}
 KERNEL_SOURCES = {"mma_sync": ["dense_mma.cu", "common.cuh"],
+                  "tcgen05_small": ["dense_tcs.cu", "tc_tile.cuh", "tc_ptx.cuh", "common.cuh"],
                   "tcgen05": ["dense_tc.cu", "tc_ptx.cuh", "common.cuh"],
                   "tcgen05_pair": ["dense_tc2.cu", "tc_tile.cuh", "tc_ptx.cuh", "common.cuh"],
                   "tcgen05_quad": ["dense_tc4.cu", "tc_tile.cuh", "tc_ptx.cuh", "common.cuh"]}
@@ -757,7 +758,8 @@ def run_ours(args):
     line = None
     if rank == 0:
         info = res["info"]
-        kernel = {0: "mma_sync", 1: "tcgen05", 2: "tcgen05_pair", 3: "tcgen05_quad"}[info["kernel"]]
+        kernel = {0: "mma_sync", 1: "tcgen05", 2: "tcgen05_pair", 3: "tcgen05_quad",
+                  4: "tcgen05_small"}[info["kernel"]]
         peak = pk["bf16_tflops"]
         line = {
             "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": ws,

@@ -73,7 +73,7 @@ typedef enum {
 #define RK_PLAN_HOST_ONLY 1u    /* build and validate on the host only: no
                                    device memory, forward refuses the plan */
 #define RK_PLAN_LEGACY_MMA 2u   /* run the prefill tiles on the mma.sync
-                                   kernel instead of the tcgen05 kernel */
+                                   kernel instead of a tcgen05 kernel */
 #define RK_PLAN_SINGLE_CTA 4u   /* run each tcgen05 tile on its own two CTAs
                                    (one per half of d_v) */
 #define RK_PLAN_DEVICE_BITMAP 16u /* protected_bitmap is a device pointer
@@ -172,7 +172,9 @@ typedef struct {
   int64_t latent_bytes;      /* bytes of every segment latent */
   int32_t kernel;            /* 0 = mma.sync tiles, 1 = tcgen05 tiles,
                                 2 = tcgen05 tiles paired on CTA pairs,
-                                3 = tcgen05 tile pairs on 4-CTA clusters */
+                                3 = tcgen05 tile pairs on 4-CTA clusters,
+                                4 = tcgen05 tiles for small heads (d_nope 128,
+                                    d_rope 32), one CTA per tile */
   int32_t d_v;               /* output columns: d_nope, or d_k with RK_PLAN_V_ROPE */
 } rk_plan_info_t;
 

@@ -196,6 +196,13 @@ static rk_status_t build_plan(const rk_seg_attn_desc_t* d, rk_seg_attn_plan_s* p
       p->kernel = (d->flags & RK_PLAN_SINGLE_CTA) ? 1 : (d->flags & RK_PLAN_CTA_PAIR) ? 2 : 3;
       p->tile_m = kTcM;
     }
+    // small heads (d_nope 128, d_rope 32): one tcgen05 CTA per tile of 128
+    // query pairs of the generic work list
+    if (!(d->flags & RK_PLAN_LEGACY_MMA) && !v_rope && d->d_nope == 128 && d->d_rope == 32 &&
+        d->num_heads <= kTcM) {
+      p->kernel = 4;
+      p->tile_m = kTcM;
+    }
     // the rotary value runs on the 4-CTA kernel only
     if (v_rope) {
       if (!(hg_ok && h_ok)) return RK_ERR_UNSUPPORTED_DIMS;
@@ -316,8 +323,8 @@ static rk_status_t build_plan(const rk_seg_attn_desc_t* d, rk_seg_attn_plan_s* p
     info.latent_bytes += p->segs[i].n * int64_t(d->d_nope + d->d_rope) * 2;
 
   const int TM = p->tile_m;
-  const bool tc = p->kernel >= 1;
-  const int TN = tc ? kTcN : kMmaTileN;
+  const bool tc = p->kernel >= 1 && p->kernel <= 3;  // tcgen05 tiles of the TcTile kind
+  const int TN = (tc || p->kernel == 4) ? kTcN : kMmaTileN;
   const int64_t sink = d->sink, window = d->window;
   std::vector<std::pair<int64_t, DenseTile>> tiles;  // (cost, tile)
   std::vector<std::pair<int64_t, TcTile>> tc_list;   // (cost, tile)
@@ -653,7 +660,22 @@ extern "C" rk_status_t rk_seg_attn_plan(const rk_seg_attn_desc_t* desc, void* st
     if (st == RK_OK) st = upload(p->tc_pairs, &p->d_tc_pairs, s);
     if (st == RK_OK) st = upload(p->tc_pairs_chunked, &p->d_tc_pairs_chunked, s);
     if (st == RK_OK) st = upload(p->head_role, &p->d_head_role, s);
-    if (st == RK_OK && p->kernel >= 1) {
+    if (st == RK_OK && p->kernel == 4) {
+      // small heads: map 0 of each segment is the latent as [n, d_k]
+      // row-major, box 64 dims x 128 rows (dims past d_k read as zero)
+      p->segmaps.resize(rk::kSegMaps * p->segs.size());
+      const uint64_t dk = static_cast<uint64_t>(p->d_nope + p->d_rope);
+      for (size_t i = 0; i < p->segs.size() && st == RK_OK; ++i) {
+        const uint64_t dims[2] = {dk, static_cast<uint64_t>(p->segs[i].n)};
+        const uint64_t strides[1] = {dk * 2};
+        const uint32_t box[2] = {64, 128};
+        if (!rk::make_tmap_bf16(&p->segmaps[rk::kSegMaps * i], p->segs[i].latent, 2, dims,
+                                strides, box))
+          st = RK_ERR_CUDA;
+      }
+      if (st == RK_OK) st = upload(p->segmaps, &p->d_segmaps, s);
+    }
+    if (st == RK_OK && p->kernel >= 1 && p->kernel <= 3) {
       // TMA maps of each segment latent, viewing a row as d_k / 64 chunks
       // of 64 bf16: (64, n, d_k / 64) so that a box lands chunk-major in
       // shared memory; map 4 takes whole rows
@@ -990,7 +1012,7 @@ cudaError_t launch_forward(const rk_seg_attn_plan_s& p, const KernelArgs& a, con
     if (e != cudaSuccess) return e;
     ts = p.side;
   }
-  if (a.num_tiles) e = launch_dense_mma(p, a, ts);
+  if (a.num_tiles) e = p.kernel == 4 ? launch_dense_tcs(p, a, ts) : launch_dense_mma(p, a, ts);
   if (e == cudaSuccess && a.num_tc_tiles) e = launch_dense_tc(p, a, q, ts);
   // beside split chunks (decode) the few short Local tiles run on CTA pairs,
   // which leave more SMs to the split kernel than 4-CTA clusters (the pair

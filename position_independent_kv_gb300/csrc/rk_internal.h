@@ -216,6 +216,8 @@ cudaError_t launch_dense_tc2(const rk_seg_attn_plan_s& plan, const KernelArgs& a
                              const void* q, cudaStream_t stream);
 cudaError_t launch_dense_tc4(const rk_seg_attn_plan_s& plan, const KernelArgs& a,
                              const void* q, cudaStream_t stream);
+cudaError_t launch_dense_tcs(const rk_seg_attn_plan_s& plan, const KernelArgs& a,
+                             cudaStream_t stream);
 // Fill the kernel arguments shared by every launch of a forward.
 void fill_args(const rk_seg_attn_plan_s& plan, KernelArgs& a, const void* q, void* out,
                float* lse);

@@ -207,6 +207,20 @@ def test_edge_plans_count_attended_pairs(name):
     assert plan.info["kernel"] == (0 if name == "edge_h8" else 3)
 
 
+@pytest.mark.parametrize("name", ["tiny", "tiny_wide"])
+def test_small_head_plans_take_the_tcgen05_tiles(name):
+    """d = (128, 32) plans on the small-head tcgen05 kernel (4) by default and
+    on the mma.sync tiles with RK_PLAN_LEGACY_MMA; both count the same
+    attended pairs, the tcgen05 tiles 128 query pairs x 128 keys each."""
+    wl, plan = _host_plan(name)
+    _, legacy = _host_plan(name, flags=B.RK_PLAN_HOST_ONLY | B.RK_PLAN_LEGACY_MMA)
+    assert plan.info["kernel"] == 4 and legacy.info["kernel"] == 0
+    for k in ("pairs_global", "pairs_local", "protected_local_rows"):
+        assert plan.info[k] == legacy.info[k]
+    assert plan.info["performed_pairs"] % (128 * 128) == 0
+    assert plan.info["performed_pairs"] >= plan.info["pairs_global"] + plan.info["pairs_local"]
+
+
 def test_lse_merge_no_rows_is_a_no_op():
     L = B.lib()
     assert L.rk_lse_merge(16, 32, 3, 0, 4, 8, 64, 128, None) == 0
