@@ -60,6 +60,8 @@ def workload_desc(name: str) -> str:
         prot = f"protected: query rows + boundary {r.boundary}"
     out = f", {int(round(100 * sp.outlier_frac))}% outlier rows x8" if sp.outlier_frac else ""
     vr = ", V = the whole latent row (output phase restored)" if sp.v_rope else ""
+    if sp.q_tail:
+        vr += f", only the last {sp.q_tail} rows computed"
     return (f"{name}: {seg}, H={sp.H} ({sp.H - hg} Local/{hg} Global), d_nope={sp.d_nope}, "
             f"d_rope={sp.d_rope}{vr}, sink={sp.sink}, w={sp.window}, {prot}, "
             f"bf16 N(0,1)/sqrt({sp.d_nope + sp.d_rope}){out}, seed 0")

@@ -141,6 +141,7 @@ class Spec:
     decode_seg_range: tuple[int, int] = (0, 0)
     rope_base: float = 10000.0
     v_rope: bool = False
+    q_tail: int = 0          # prefill: compute only the last q_tail rows (0 = all)
 
 
 SPECS: dict[str, Spec] = {
@@ -170,6 +171,15 @@ SPECS: dict[str, Spec] = {
     # (inputs larger than L2, a few GB on the device)
     "ctx16k": Spec("ctx16k", 128, 512, 64, 4, 256, ProtectRule(boundary=128, budget=0.25),
                    seg_lengths=[2048] * 6, n_new=4096),
+    # the long-context geometry with only its last 2048 rows computed: the
+    # longest causal tiles (the steady state of the full workload) in a
+    # capture of a few GB
+    "ctx128k_tail2k": Spec("ctx128k_tail2k", 128, 512, 64, 4, 256,
+                           ProtectRule(boundary=128, budget=0.25),
+                           seg_lengths=[2048] * 48, n_new=32768, q_tail=2048),
+    "ctx128k_vrope_tail2k": Spec("ctx128k_vrope_tail2k", 128, 448, 64, 4, 256,
+                                 ProtectRule(boundary=128, budget=0.25),
+                                 seg_lengths=[2048] * 48, n_new=32768, q_tail=2048, v_rope=True),
     "tiny_wide": Spec("tiny_wide", 8, 128, 32, 4, 10000, ProtectRule(boundary=16),
                       seg_lengths=[256, 256], n_new=64, shuffle=False),
     # degenerate cases of the method: no sink and a zero window (a Local row
@@ -255,7 +265,9 @@ def make_geometry(name: str, seed: int = 0) -> Workload:
             pos += lens[j]
         segs = [Segment(doc=j, n=lens[j], delta=deltas[j], is_new=False) for j in range(S)]
         segs.append(Segment(doc=S, n=spec.n_new, delta=pos, is_new=True))
-        requests.append(Request(segments=segs, T=pos + spec.n_new, q_row_begin=0))
+        T = pos + spec.n_new
+        qb = T - spec.q_tail if spec.q_tail else 0
+        requests.append(Request(segments=segs, T=T, q_row_begin=qb))
     for req in requests:
         req.u = rng.random(req.T)
         req.perm = rng.permutation(req.T).astype(np.int64)
