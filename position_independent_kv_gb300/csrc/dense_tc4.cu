@@ -86,8 +86,8 @@ enum {
   B_ROPE = B_SFREE + 2,   // rotated q_rope of the next segment written (one arrival
                           // per rope warp of both S CTAs)
   B_QREADY,               // queries in tensor memory (one arrival per lane warp)
-  B_SWITCH,               // the last score MMAs of a segment are done (one phase per
-                          // segment switch, so the rope warps wait on every phase)
+  B_SWITCH,               // the rope MMAs of a segment's last tile are done (one phase
+                          // per segment switch, so the rope warps wait on every phase)
   B_SFINAL,
   B_PEMPTY,             // 2 (S CTAs): P buffer consumed by the output MMAs
   B_VFULL = B_PEMPTY + 2,
@@ -235,29 +235,33 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
           if (!ok) break;
           tc::tc_fence_after();
           const uint32_t base = ka + slot * KSLOT;
-          // B = K[64 keys of each CTA x 16 dims]: the nope chunks, then the rope chunk
+          KeyTile nx = cur;
+          const bool have_next = next_key_tile<TNK>(nx, segs, nseg, 0, r0hi, r1lo, r1hi);
+          // B = K[64 keys of each CTA x 16 dims]: the rope chunk first (q_rope'
+          // hi and lo), then the nope chunks
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint64_t bd = tc::sdesc_sw128(base + NCH * HCHUNK + 32 * k, 16, 1024);
+            tc::mma_ss_2sm(ts, tc::sdesc_sw128(ropa + 32 * k, 16, 1024), bd, idS, k != 0);
+            tc::mma_ss_2sm(ts, tc::sdesc_sw128(ropa + CHUNK + 32 * k, 16, 1024), bd, idS, 1);
+          }
+          // the last tile of a segment: the rope warps may rewrite q_rope' for
+          // the next segment once these rope MMAs are done, while the nope
+          // MMAs below still run
+          if (have_next && nx.j != cur.j) tc::mma_commit_2sm(&bar[B_SWITCH], 0x3);
 #pragma unroll
           for (int cc = 0; cc < NCH; ++cc)
 #pragma unroll
             for (int k = 0; k < 4; ++k)
               tc::mma_ts_2sm(ts, tbase + T_Q + 8 * (4 * cc + k),
-                             tc::sdesc_sw128(base + cc * HCHUNK + 32 * k, 16, 1024), idS,
-                             (cc | k) != 0);
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint64_t bd = tc::sdesc_sw128(base + NCH * HCHUNK + 32 * k, 16, 1024);
-            tc::mma_ss_2sm(ts, tc::sdesc_sw128(ropa + 32 * k, 16, 1024), bd, idS, 1);
-            tc::mma_ss_2sm(ts, tc::sdesc_sw128(ropa + CHUNK + 32 * k, 16, 1024), bd, idS, 1);
-          }
+                             tc::sdesc_sw128(base + cc * HCHUNK + 32 * k, 16, 1024), idS, 1);
           tc::mma_commit_2sm(&bar[B_KEMPTY + slot], 0x3);
           ++cnt;
           tc::mma_commit_2sm(&bar[B_SFULL + b], 0x3);
           prev_seg = cur.j;
           ++j;
-          have = next_key_tile<TNK>(cur, segs, nseg, 0, r0hi, r1lo, r1hi);
-          // a new segment follows: the rope warps may rewrite q_rope' once
-          // these MMAs are done
-          if (have && cur.j != prev_seg) tc::mma_commit_2sm(&bar[B_SWITCH], 0x3);
+          cur = nx;
+          have = have_next;
         }
         tc::mma_commit_2sm(&bar[B_SFINAL], 0x3);
       }
@@ -266,8 +270,10 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
       // q_rope' = R(-delta) q_rope as bf16 hi and lo rows of two K-major
       // 128-byte-swizzled operands (RedKnot-MLA paper, RoPE-orthogonality
       // paragraph), rewritten at every segment switch of the key walk as
-      // soon as the last score MMAs of the old segment are done; each lane
-      // keeps the raw q_rope of its two rows in registers
+      // soon as the rope MMAs of the old segment's last tile are done (each
+      // tile's chain takes the rope chunk first, so the rewrite overlaps that
+      // tile's nope MMAs); each lane keeps the raw q_rope of its two rows in
+      // registers
       const int m0 = 64 * (warp - 6) + lane;
       uint32_t raw[2][32];
 #pragma unroll
@@ -334,7 +340,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
         KeyTile nx = kt;
         const bool have_next = next_key_tile<TNK>(nx, segs, nseg, 0, r0hi, r1lo, r1hi);
         if (have_next && nx.j != kt.j) {
-          // the old segment's score MMAs are done: none reads q_rope' any more
+          // the old segment's rope MMAs are done: none reads q_rope' any more
           ok = __all_sync(0xffffffffu, wait_bar(c, B_SWITCH, sw_ev++ & 1));
           if (ok) {
             tc::tc_fence_after();
