@@ -432,8 +432,14 @@ static rk_status_t build_plan(const rk_seg_attn_desc_t* d, rk_seg_attn_plan_s* p
         tiles.push_back({kt, t});
       }
     }
-    // Local heads on protected rows
-    if (HL && nprot && tc) {
+    // Local heads on protected rows.  A request whose only computed row is
+    // its new row (decode) runs its Local heads as mma.sync tiles of 64
+    // pairs x 32 keys: one row x the Local heads over at most w + 1 + sink
+    // keys is too little work to fill a tcgen05 tile pair, whose partner
+    // would be idle (tiles of two requests share no keys).  The rotary value
+    // has no mma.sync form and keeps the 4-CTA tiles.
+    const bool local_mma = tc && split && !v_rope;
+    if (HL && nprot && tc && !local_mma) {
       const int rows_per = kTcM / H;  // 1 or 2 rows of every head per tile
       int64_t i = 0;
       while (i < nprot) {
@@ -470,12 +476,14 @@ static rk_status_t build_plan(const rk_seg_attn_desc_t* d, rk_seg_attn_plan_s* p
         i += pb >= 0 ? 2 : 1;
       }
     } else if (HL && nprot) {
+      const int LTM = local_mma ? kMmaTileM : TM;
+      const int LTN = local_mma ? kMmaTileN : TN;
       const int64_t npairs = nprot * HL;
       const int64_t pair_base = static_cast<int64_t>(lr_first) * HL;
       int64_t i = 0;
       while (i < npairs) {
         const int64_t p_first = p->local_rows[lr_first + i / HL];
-        int64_t e = std::min<int64_t>(npairs, i + TM);
+        int64_t e = std::min<int64_t>(npairs, i + LTM);
         // cut the tile where the next row is too far away to share a window
         for (int64_t k = i + 1; k < e; ++k) {
           if ((k % HL) == 0 && p->local_rows[lr_first + k / HL] - p_first > window / 2 + 1) {
@@ -501,9 +509,9 @@ static rk_status_t build_plan(const rk_seg_attn_desc_t* d, rk_seg_attn_plan_s* p
         int64_t kt = 0;
         for (int j = 0; j < rq.seg_count; ++j) {
           const DevSeg& s = p->segs[rq.seg_first + j];
-          kt += key_tiles_in_segment(t, s.delta, s.n, TN);
+          kt += key_tiles_in_segment(t, s.delta, s.n, LTN);
         }
-        info.performed_pairs += kt * TN * TM;
+        info.performed_pairs += kt * LTN * LTM;
         tiles.push_back({kt, t});
         i = e;
       }
