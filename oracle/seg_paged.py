@@ -20,12 +20,22 @@ i // (Hq / Hkv); keys already carry their RoPE at absolute positions; every
 computed row p of every query head is evaluated.  The visibility rule and the
 dense softmax are the ones of `seg_attn` (imported, so both oracles read the
 blog's window rule one way).
+
+Relocated documents (`block_delta`): a document cached alone has its keys'
+RoPE at positions 0..n-1; placed at request offset delta, its pages are
+reused as they are.  Reading: `block_delta[b]` is the offset of the document
+that logical block b belongs to (every KV head alike), so a key stored at
+absolute token k of block b carries its RoPE at position k - block_delta[b].
+The oracle relocates each such key physically, K(k) = R(delta) K_stored
+(blog "Insight 1", the relocation equation K(p_new) = R(p_new) R(p_old)^-1
+K(p_old)), with RoPE on all head dims as interleaved pairs, theta_j =
+base^(-2j/d) (the `rotate` of `seg_attn`), and then attends as above.
 """
 from __future__ import annotations
 
 import numpy as np
 
-from .seg_attn import attend, visible_keys
+from .seg_attn import attend, rotate, visible_keys
 
 
 def gather_head(pages: np.ndarray, table_row, n_tokens: int, page_size: int, need=None):
@@ -44,9 +54,18 @@ def gather_head(pages: np.ndarray, table_row, n_tokens: int, page_size: int, nee
     return out
 
 
+def relocate_blocks(K: np.ndarray, block_delta, page_size: int, base: float) -> np.ndarray:
+    """K [T, d] of one KV head with every key of block b moved from its stored
+    RoPE position k - block_delta[b] to its absolute position k: R(+delta)."""
+    T = K.shape[0]
+    pos = np.array([block_delta[k // page_size] for k in range(T)], dtype=np.float64)
+    return rotate(K, pos, base)
+
+
 def seg_paged_request(q: np.ndarray, k_pages: np.ndarray, v_pages: np.ndarray,
                       table: np.ndarray, T: int, q_row_begin: int, kv_role, sink: int,
-                      window: int, scale: float, page_size: int, rows=None, sampled=False):
+                      window: int, scale: float, page_size: int, rows=None, sampled=False,
+                      block_delta=None, rope_base: float = 10000.0):
     """One request.
 
     q         fp64 [T - q_row_begin, Hq, d]  (row i = absolute row q_row_begin + i)
@@ -55,6 +74,8 @@ def seg_paged_request(q: np.ndarray, k_pages: np.ndarray, v_pages: np.ndarray,
     kv_role   [Hkv] 0 Local, 1 Global
     rows      absolute rows to evaluate (default every computed row); with
               `sampled` q holds only those rows, in that order.
+    block_delta  optional [max_blocks] document offset of each logical block
+              (keys stored with RoPE at k - delta); rope_base its RoPE base.
 
     Returns O [n_rows, Hq, d], lse [n_rows, Hq]."""
     kv_role = np.asarray(kv_role).astype(bool)
@@ -71,6 +92,8 @@ def seg_paged_request(q: np.ndarray, k_pages: np.ndarray, v_pages: np.ndarray,
         for g in range(Hkv):
             need[g, visible_keys(int(p), bool(kv_role[g]), sink, window)] = True
     K = [gather_head(k_pages, table[g], T, page_size, need[g]) for g in range(Hkv)]
+    if block_delta is not None:
+        K = [relocate_blocks(k, block_delta, page_size, rope_base) for k in K]
     V = [gather_head(v_pages, table[g], T, page_size) for g in range(Hkv)]
     d = q.shape[2]
     O = np.empty((len(rows), Hq, d))

@@ -14,6 +14,13 @@ the page pool.  Where `local_pages_only` is set (decode steps), a Local head
 keeps only the pages of its sink and its window, the memory claim of the
 blog; the others are absent (-1) and not allocated.
 
+Relocated documents (`docs` > 0): the first whole pages of each prompt are
+split into `docs` documents of seeded page-multiple lengths (a fixed length
+when `doc_tokens` is set); each was cached alone, so its keys carry their RoPE
+at positions 0..n-1, and `block_delta[r, b]` holds the offset of the document
+of block b (0 for the blocks after the documents).  Only the offsets are
+drawn here; the keys themselves are i.i.d. as for the other workloads.
+
 Tensors: q bf16 [rows, Hq, 128] (RoPE already at absolute positions),
 k_pages / v_pages bf16 [pages, 128, 128], out bf16 [rows, Hq, 128], lse fp32
 [rows, Hq].  Values are i.i.d. N(0, 1) / sqrt(128) drawn in fp32 and cast to
@@ -42,6 +49,8 @@ class PagedSpec:
     window: int = 256
     global_every: int = 8           # KV head g is Global when g % global_every == global_every - 1
     local_pages_only: bool = False
+    docs: int = 0                   # relocated documents per prompt (0: none)
+    doc_tokens: int = 0             # fixed document length (0: seeded page multiples)
 
 
 PAGED_SPECS: dict[str, PagedSpec] = {
@@ -76,6 +85,18 @@ PAGED_SPECS: dict[str, PagedSpec] = {
     "paged_tail_g1": PagedSpec("paged_tail_g1", 2, 2, [525], [0], global_every=2),
     "paged_tail_g2": PagedSpec("paged_tail_g2", 4, 2, [391], [0], global_every=2),
     "paged_tail_g4_split": PagedSpec("paged_tail_g4_split", 8, 2, [7000], [6996], global_every=2),
+    # relocated documents (keys cached at canonical positions, the query
+    # turns by -delta): several group sizes, ragged tails, decode rows
+    "paged_reloc_mini": PagedSpec("paged_reloc_mini", 16, 2, [1000, 700], [0, 300],
+                                  global_every=2, docs=3),
+    "paged_reloc_g8": PagedSpec("paged_reloc_g8", 64, 8, [900], [0], docs=4),
+    "paged_reloc_g1": PagedSpec("paged_reloc_g1", 4, 4, [530], [0], global_every=4, docs=2),
+    "paged_reloc_decode": PagedSpec("paged_reloc_decode", 16, 2, [], [], global_every=2,
+                                    local_pages_only=True, docs=3),
+    # the 128K prefill with its first 96K tokens as 48 relocated documents of
+    # 2048 tokens (the MLA long-context geometry's documents) and a 32K tail
+    "qwen32b_reloc_128k": PagedSpec("qwen32b_reloc_128k", 64, 8, [131072], [0], docs=48,
+                                    doc_tokens=2048),
 }
 
 
@@ -91,6 +112,8 @@ class PagedWorkload:
     num_pages: int
     sink: int
     window: int
+    block_delta: np.ndarray | None = None   # int64 [R, max_blocks] document offsets, or None
+    rope_base: float = 10000.0
     q: torch.Tensor | None = None
     k_pages: torch.Tensor | None = None
     v_pages: torch.Tensor | None = None
@@ -152,9 +175,25 @@ def make_paged_geometry(name: str, seed: int = 0) -> PagedWorkload:
     perm = rng.permutation(len(keep))
     for i, (r, g, b) in enumerate(keep):
         table[r, g, b] = int(perm[i])
+    delta = None
+    if sp.docs:
+        delta = np.zeros((R, max_blocks), np.int64)
+        for r, T in enumerate(lens):
+            if sp.doc_tokens:
+                nb_docs = min(sp.docs * sp.doc_tokens, T) // PAGE
+                cuts = [d * (sp.doc_tokens // PAGE) for d in range(sp.docs) if
+                        d * (sp.doc_tokens // PAGE) < nb_docs]
+            else:
+                nb_docs = max(0, T // PAGE - 1)   # whole pages, the last one left to the tail
+                nd = min(sp.docs, nb_docs)
+                cuts = ([0] + sorted(rng.choice(np.arange(1, nb_docs), size=nd - 1,
+                                                replace=False).tolist()) if nd > 1 else [0])
+            for i, c in enumerate(cuts):
+                e = cuts[i + 1] if i + 1 < len(cuts) else nb_docs
+                delta[r, c:e] = c * PAGE
     return PagedWorkload(name=name, Hq=sp.Hq, Hkv=sp.Hkv, seq_len=np.array(lens, np.int64),
                          q_row_begin=np.array(qbs, np.int64), kv_role=role, block_table=table,
-                         num_pages=len(keep), sink=sp.sink, window=sp.window)
+                         num_pages=len(keep), sink=sp.sink, window=sp.window, block_delta=delta)
 
 
 def _randn_bf16(shape, gen, device, std, chunk=4096):

@@ -130,3 +130,62 @@ def test_local_heads_drop_pages_outside_sink_and_window():
     t3[0, p // ps] = -1
     with pytest.raises(AssertionError):
         O.seg_paged_request(q, kp, vp, t3, T, p, roles, sink, window, 0.5, ps)
+
+
+def _rope_complex(x: np.ndarray, pos: np.ndarray, base: float) -> np.ndarray:
+    """R(pos) on the last axis written with complex numbers: pair j (dims 2j,
+    2j + 1) is the complex number x_2j + i x_2j+1 turned by exp(i pos theta_j),
+    theta_j = base^(-2j/d).  An independent statement of the RoPE rotation."""
+    d = x.shape[-1]
+    theta = base ** (-2.0 * np.arange(d // 2) / d)
+    z = (x[..., 0::2] + 1j * x[..., 1::2]) * np.exp(1j * pos[..., None] * theta)
+    out = np.empty_like(x)
+    out[..., 0::2] = z.real
+    out[..., 1::2] = z.imag
+    return out
+
+
+@pytest.mark.parametrize("roles", [(1, 0), (0, 1)])
+def test_relocated_documents_equal_keys_at_absolute_positions(roles):
+    """Blog "Insight 1": a document cached alone (keys with RoPE at 0..n-1)
+    and placed at offset delta attends exactly as if its keys had been
+    computed at positions delta..delta+n-1.  Keys are built from raw vectors
+    x_k both ways with the complex-number rotation; the oracle given the
+    canonical pages and the block offsets must match the oracle given the
+    absolute pages, and the opposite turn must not."""
+    rng = np.random.default_rng(77)
+    T, Hq, Hkv, d, ps, base = 40, 4, 2, 8, 8, 100.0
+    delta = np.array([0, 0, 16, 16, 0])         # documents: blocks 0-1 at 0, 2-3 at 16; tail 4
+    tok_delta = np.repeat(delta, ps)[:T]
+    X = rng.standard_normal((Hkv, T, d))
+    V = rng.standard_normal((Hkv, T, d))
+    k_abs = _rope_complex(X, np.arange(T, dtype=np.float64)[None, :].repeat(Hkv, 0), base)
+    k_can = _rope_complex(X, (np.arange(T) - tok_delta).astype(np.float64)[None, :].repeat(Hkv, 0),
+                          base)
+    nb = T // ps
+    table = np.array([[g * nb + b for b in range(nb)] for g in range(Hkv)])
+
+    def pages(K):
+        return np.stack([K[g, b * ps:(b + 1) * ps] for g in range(Hkv) for b in range(nb)])
+
+    q = rng.standard_normal((T, Hq, d)) * 2.0
+    role = np.array(roles, np.uint8)
+    args = (table, T, 0, role, 2, 6, 0.5, ps)
+    O_ref, L_ref = O.seg_paged_request(q, pages(k_abs), pages(V), *args)
+    O_rel, L_rel = O.seg_paged_request(q, pages(k_can), pages(V), *args, block_delta=delta,
+                                       rope_base=base)
+    assert np.abs(O_rel - O_ref).max() < 1e-12 and np.abs(L_rel - L_ref).max() < 1e-12
+    O_bad, _ = O.seg_paged_request(q, pages(k_can), pages(V), *args, block_delta=-delta,
+                                   rope_base=base)
+    assert np.abs(O_bad - O_ref).max() > 1e-3
+
+
+def test_zero_offsets_change_nothing():
+    rng = np.random.default_rng(78)
+    K, V, kp, vp, table = _case(rng, 23, 4, 2, 4, 4, None)
+    q = rng.standard_normal((23, 4, 4))
+    role = np.array([1, 0], np.uint8)
+    a = O.seg_paged_request(q, kp, vp, table, 23, 0, role, 2, 5, 0.7, 4)
+    b = O.seg_paged_request(q, kp, vp, table, 23, 0, role, 2, 5, 0.7, 4,
+                            block_delta=np.zeros(table.shape[1], np.int64))
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
