@@ -16,7 +16,8 @@
  * Conventions
  * -----------
  * bf16       IEEE bfloat16 stored as uint16.
- * head_dim   d = 128.  Keys carry their RoPE at absolute positions already.
+ * head_dim   d = 128.  Keys carry their RoPE at absolute positions, unless
+ *            their block belongs to a relocated document (block_delta below).
  * pages      k_pages and v_pages are bf16 [num_pages, page_size, d] with
  *            page_size = 128: a page holds 128 consecutive tokens of ONE KV
  *            head.  Logical block b of a sequence covers tokens
@@ -71,7 +72,21 @@ extern "C" {
  * kv_head_role   [Hkv] 0 = Local, 1 = Global.
  * sink, window   Local visibility: k <= p with k < sink or k >= p - window.
  * softmax_scale  s > 0.
- * flags          RK_SEGPAGED_* bits. */
+ * flags          RK_SEGPAGED_* bits.
+ * block_delta    [R][max_blocks] or NULL.  Relocated documents (RedKnot blog,
+ *                "Insight 1": a document cached alone and reused at offset
+ *                delta; RedKnot-MLA paper, RoPE-orthogonality paragraph: the
+ *                query turns by -delta instead of the cache being rewritten):
+ *                the keys of logical block b of request r, in every KV head,
+ *                carry their RoPE at position k - block_delta[r][b] instead of
+ *                k.  Entries must lie in [-2^31, 2^31).  NULL: every key at its
+ *                absolute position.  A plan with offsets runs every tile on the
+ *                one-sub-tile kernel, whose query operand is R(-delta) q kept
+ *                as bf16 hi + lo parts (rewritten at each change of offset
+ *                along the key walk; a zero offset skips the lo part).
+ * rope_base      RoPE base of the keys and queries (pairs (2j, 2j + 1) over
+ *                all 128 dims, theta_j = base^(-2j/128)); read only with
+ *                block_delta. */
 typedef struct {
   int32_t num_requests;
   const int64_t* seq_len;
@@ -88,6 +103,8 @@ typedef struct {
   int32_t window;
   float softmax_scale;
   uint32_t flags;
+  const int64_t* block_delta;
+  double rope_base;
 } rk_segpaged_desc_t;
 
 typedef struct rk_segpaged_plan_s* rk_segpaged_plan_t;

@@ -48,7 +48,8 @@ class RkSegPagedDesc(C.Structure):
                 ("num_pages", C.c_int64), ("max_blocks", C.c_int32),
                 ("block_table", C.POINTER(C.c_int32)), ("kv_head_role", C.POINTER(C.c_uint8)),
                 ("sink", C.c_int32), ("window", C.c_int32), ("softmax_scale", C.c_float),
-                ("flags", C.c_uint32)]
+                ("flags", C.c_uint32), ("block_delta", C.POINTER(C.c_int64)),
+                ("rope_base", C.c_double)]
 
 
 class RkSegPagedInfo(C.Structure):
@@ -350,11 +351,12 @@ class SegPagedPlan:
     """rk_segpaged_plan / rk_segpaged_forward (SegPagedAttention on GQA).
 
     seq_len, q_row_begin: [R]; block_table: int32 [R, Hkv, max_blocks]
-    (physical page or -1); kv_role: uint8 [Hkv] (1 = Global)."""
+    (physical page or -1); kv_role: uint8 [Hkv] (1 = Global); block_delta:
+    int64 [R, max_blocks] offsets of relocated documents, or None."""
 
     def __init__(self, seq_len, q_row_begin, num_q_heads, num_kv_heads, block_table, num_pages,
                  kv_role, sink, window, softmax_scale, flags=0, stream=None, head_dim=128,
-                 page_size=128):
+                 page_size=128, block_delta=None, rope_base=10000.0):
         L = lib()
         sl = np.ascontiguousarray(seq_len, dtype=np.int64)
         qb = np.ascontiguousarray(q_row_begin, dtype=np.int64)
@@ -376,6 +378,12 @@ class SegPagedPlan:
         d.window = int(window)
         d.softmax_scale = float(softmax_scale)
         d.flags = int(flags)
+        dl = None
+        if block_delta is not None:
+            dl = np.ascontiguousarray(block_delta, dtype=np.int64)
+            assert dl.shape == (len(sl), tab.shape[-1])
+            d.block_delta = dl.ctypes.data_as(C.POINTER(C.c_int64))
+        d.rope_base = float(rope_base)
         handle = C.c_void_p()
         host_only = bool(flags & RK_SEGPAGED_HOST_ONLY)
         _check(L.rk_segpaged_plan(C.byref(d), 0 if host_only else _stream(stream),
@@ -385,7 +393,8 @@ class SegPagedPlan:
     @classmethod
     def from_workload(cls, pw, flags=0, stream=None):
         return cls(pw.seq_len, pw.q_row_begin, pw.Hq, pw.Hkv, pw.block_table, pw.num_pages,
-                   pw.kv_role, pw.sink, pw.window, pw.scale, flags=flags, stream=stream)
+                   pw.kv_role, pw.sink, pw.window, pw.scale, flags=flags, stream=stream,
+                   block_delta=pw.block_delta, rope_base=pw.rope_base)
 
     @property
     def info(self) -> dict:

@@ -55,6 +55,9 @@
 // has drained.
 
 #include <algorithm>
+#include <climits>
+#include <cmath>
+#include <map>
 #include <new>
 #include <vector>
 
@@ -73,6 +76,7 @@ struct Req {
   int32_t q_row_begin;
   int64_t row_base;      // first flattened row of the request
   int64_t table_off;     // offset of the request's [Hkv][max_blocks] block table
+  int64_t blk_off;       // offset of the request's [max_blocks] offset indices
 };
 
 // rows (up to 2 x 128 / G) from p0 of KV head g: sub-tile A the first
@@ -104,6 +108,9 @@ struct Args {
   float* ws_o;           // [lanes][128] normalised partial outputs of split tiles
   float* ws_lse;         // [lanes]
   int32_t* ws_ticket;    // [split tiles]
+  const int32_t* blk_cs; // relocated documents: [R][max_blocks] index of the block's offset
+                         // (index 0 is the zero offset)
+  const float* cs;       // [offsets][64][2] cos, sin of delta * theta_j
 };
 
 struct Maps {
@@ -482,7 +489,18 @@ constexpr uint32_t OFF_X = (OFF_MISC + 16 + 15) & ~15u;  // row max [2 buffers][
 constexpr uint32_t SMEM_BYTES = OFF_X + (4 + 2) * 128 * 4 + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory");
 constexpr uint32_t T_O = 0, T_S = 128, T_P = 384, T_Q = 448;
+// relocated documents: P overwrites the first half of its S buffer (the next
+// S into that buffer is issued after the P.V that reads P, and one thread's
+// MMAs run in issue order), which frees the columns for the query as bf16
+// hi and lo parts of R(-delta) q
+constexpr uint32_t T_QH = 384, T_QL = 448;
 
+// Offset index of walk step j of tile t (relocated documents).
+__device__ __forceinline__ int32_t cs_of(const Args& a, const Tile& t, const Req& rq, int j) {
+  return a.blk_cs[rq.blk_off + block_of(t, t.jb + j)];
+}
+
+template <bool RELOC>
 __global__ void __launch_bounds__(THREADS, 1)
     seg_paged_one_kernel(const __grid_constant__ Args a, const __grid_constant__ Maps mp) {
   extern __shared__ uint8_t smem_raw[];
@@ -555,6 +573,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t idS = tc::idesc_bf16(128, 128, false, false);
       const uint32_t idPV = tc::idesc_bf16(128, 128, false, true);
       const uint32_t ra = smem_u32(sm + OFF_RING);
+      // relocated documents, tiles of at most 64 pairs in use (memory-bound
+      // decode and tail tiles): P enters P.V as bf16 hi + lo parts
+      const bool psplit = RELOC && t.rows * a.G <= 64;
       uint32_t cnt = 0;
       auto pv = [&](int jj) {
         if (!tt::wait_bar(c, B_PREADY, jj & 1)) return false;
@@ -563,33 +584,64 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!tt::wait_bar(c, B_FULL + slot, (cnt / RING) & 1)) return false;
         tc::tc_fence_after();
         const uint32_t base = ra + slot * SLOT;
+        const uint32_t tp = RELOC ? T_S + 128 * (jj & 1) : T_P;
         // B = V[16 keys x 128 dims]: two 64-dim chunks 16 KB apart (LBO)
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-          tc::mma_ts(tbase + T_O, tbase + T_P + 8 * k, tc::sdesc_sw128(base + 2048 * k, CHUNK, 1024),
+          tc::mma_ts(tbase + T_O, tbase + tp + 8 * k, tc::sdesc_sw128(base + 2048 * k, CHUNK, 1024),
                      idPV, (jj > 0 || k > 0) ? 1u : 0u);
+        if (psplit) {
+          // the lo part of P: half h of the keys at columns 64 + 32 h of the
+          // buffer, keys 32..63 of the half before keys 0..31
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t lc = 64 + 32 * (k >> 2) + (((k >> 1) & 1) ? 0 : 16) + 8 * (k & 1);
+            tc::mma_ts(tbase + T_O, tbase + tp + lc, tc::sdesc_sw128(base + 2048 * k, CHUNK, 1024),
+                       idPV, 1u);
+          }
+        }
         tc::mma_commit(&bar[B_EMPTY + slot]);
         ++cnt;
         tc::mma_commit(&bar[B_ODONE]);
         return true;
       };
+      uint32_t qph = 1;        // query phases consumed (the first above)
+      int32_t cs_prev = -1;    // relocated documents: offset index of the last step
       for (int j = 0; j < nb && ok; ++j) {
         const int b = j & 1;
         ok = tt::wait_bar(c, B_SFREE + b, ((j >> 1) & 1) ^ 1);
         if (!ok) break;
+        int32_t csj = 0;
+        if (RELOC) {
+          // a new offset: the lanes rewrite R(-delta) q once S of the last
+          // step is done (no S MMA still reads the old query)
+          csj = cs_of(a, t, rq, j);
+          if (j > 0 && csj != cs_prev) ok = tt::wait_bar(c, B_QFULL, qph++ & 1);
+          cs_prev = csj;
+          if (!ok) break;
+        }
         tc::tc_fence_after();
         const int slot = cnt % RING;
         ok = tt::wait_bar(c, B_FULL + slot, (cnt / RING) & 1);
         if (!ok) break;
         tc::tc_fence_after();
         const uint32_t base = ra + slot * SLOT;
-        // A = Q[128 rows x 16 dims] from tensor memory (8 columns per step)
+        // A = Q[128 rows x 16 dims] from tensor memory (8 columns per step);
+        // relocated documents: the hi part, then (offset not zero) the lo part
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc)
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            tc::mma_ts(tbase + T_S + 128 * b, tbase + T_Q + 8 * (4 * cc + k),
+            tc::mma_ts(tbase + T_S + 128 * b, tbase + (RELOC ? T_QH : T_Q) + 8 * (4 * cc + k),
                        tc::sdesc_sw128(base + cc * CHUNK + 32 * k, 16, 1024), idS, (cc | k) != 0);
+        if (RELOC && csj != 0) {
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc)
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              tc::mma_ts(tbase + T_S + 128 * b, tbase + T_QL + 8 * (4 * cc + k),
+                         tc::sdesc_sw128(base + cc * CHUNK + 32 * k, 16, 1024), idS, 1);
+        }
         tc::mma_commit(&bar[B_EMPTY + slot]);
         ++cnt;
         tc::mma_commit(&bar[B_SFULL + b]);
@@ -614,29 +666,62 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int sink = a.sink, window = a.window;
     const int64_t row = rq.row_base + (p - rq.q_row_begin);
     const int head = t.g * a.G + h;
+    const bool psplit = RELOC && t.rows * a.G <= 64;  // P.V with P as hi + lo (see the issuer)
     float* xmax = reinterpret_cast<float*>(sm + OFF_X);          // [2][2][128]
     float* xsum = xmax + 4 * 128;                                 // [2][128]
     // this thread's half of the query row (dims 64 hf .. 64 hf + 63) ->
     // tensor memory, 32-bit column c = dims 2c, 2c + 1 (A operand of the
     // score MMAs); rows past the request's end are zero
+    uint32_t qw[32];
     {
-      uint32_t w[32];
       const uint4* src = valid ? reinterpret_cast<const uint4*>(a.q + (row * a.Hq + head) * DH) + 8 * hf
                                : nullptr;
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const uint4 v = src ? __ldg(src + u) : make_uint4(0, 0, 0, 0);
-        w[4 * u] = v.x;
-        w[4 * u + 1] = v.y;
-        w[4 * u + 2] = v.z;
-        w[4 * u + 3] = v.w;
+        qw[4 * u] = v.x;
+        qw[4 * u + 1] = v.y;
+        qw[4 * u + 2] = v.z;
+        qw[4 * u + 3] = v.w;
       }
-      tc::tmem_st32(lt + T_Q + 32 * hf, w);
+    }
+    // relocated documents: R(-delta) q for the offset with index ci (RedKnot
+    // blog, "Insight 1"; the query turns instead of the cached keys), this
+    // thread's 32 rotation pairs (pair 32 hf + i: dims 2i, 2i + 1 of its
+    // half), as bf16 hi and lo parts
+    auto put_q = [&](int32_t ci) {
+      if (RELOC) {
+        const float4* cs4 = reinterpret_cast<const float4*>(a.cs + int64_t(ci) * 128 + 64 * hf);
+        // two passes (hi, then lo) keep one 32-word array live at a time
+#pragma unroll 1
+        for (int part = 0; part < 2; ++part) {
+          uint32_t w32[32];
+#pragma unroll
+          for (int u = 0; u < 16; ++u) {
+            const float4 w = __ldg(cs4 + u);  // (cos, sin) of pairs 2u, 2u + 1 of the half
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int i = 2 * u + e;
+              const float co = e ? w.z : w.x, si = e ? w.w : w.y;
+              const float x = __uint_as_float(qw[i] << 16), y = __uint_as_float(qw[i] & 0xffff0000u);
+              const float xr = fmaf(x, co, y * si), yr = fmaf(-x, si, y * co);
+              const uint32_t hw = pack_bf16x2(xr, yr);
+              w32[i] = part == 0 ? hw
+                                 : pack_bf16x2(xr - __uint_as_float(hw << 16),
+                                               yr - __uint_as_float(hw & 0xffff0000u));
+            }
+          }
+          tc::tmem_st32(lt + (part == 0 ? T_QH : T_QL) + 32 * hf, w32);
+        }
+      } else {
+        tc::tmem_st32(lt + T_Q + 32 * hf, qw);
+      }
       tc::tmem_wait_st();
       tc::tc_fence_before();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&bar[B_QFULL]);
-    }
+    };
+    put_q(RELOC && nb > 0 ? cs_of(a, t, rq, 0) : 0);
     float m_run = -INFINITY, l_run = 0.f;
     bool okw = true;
     for (int j = 0; j < nb; ++j) {
@@ -650,6 +735,13 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc::tmem_ld32(lt + T_S + 128 * b + 64 * hf, s[0]);
         tc::tmem_ld32(lt + T_S + 128 * b + 64 * hf + 32, s[1]);
         tc::tmem_wait_ld();
+        // S of this step is done, so no S MMA reads the query any more: a
+        // new offset at the next step gets its R(-delta) q now (the issuer
+        // waits for it before the next S)
+        if (RELOC && j + 1 < nb) {
+          const int32_t cn = cs_of(a, t, rq, j + 1);
+          if (cn != cs_of(a, t, rq, j)) put_q(cn);
+        }
         tc::tc_fence_before();
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&bar[B_SFREE + b]);
@@ -696,7 +788,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       const float nbias = (m_run == -INFINITY) ? 0.f : -m_run;
       float ls4[4] = {0.f, 0.f, 0.f, 0.f};
-      // P in place: keys 2i, 2i + 1 of column block q2 go to word 16 q2 + i
+      // P in place: keys 2i, 2i + 1 of column block q2 go to word 16 q2 + i;
+      // relocated documents also keep the lo parts P - bf16(P): those of
+      // column block 1 in s[1][i] (already read), those of block 0 in lo0
+      // and then s[1][16 + i]
+      uint32_t lo0[16];
 #pragma unroll
       for (int q2 = 0; q2 < 2; ++q2) {
 #pragma unroll
@@ -704,15 +800,29 @@ __global__ void __launch_bounds__(THREADS, 1)
           const float p0 = fast_exp2(fmaf(__uint_as_float(s[q2][2 * i]), sl2, nbias));
           const float p1 = fast_exp2(fmaf(__uint_as_float(s[q2][2 * i + 1]), sl2, nbias));
           ls4[i & 3] += p0 + p1;
-          s[0][16 * q2 + i] = pack_bf16x2(p0, p1);
+          const uint32_t hw = pack_bf16x2(p0, p1);
+          s[0][16 * q2 + i] = hw;
+          if (RELOC) {
+            const uint32_t lw =
+                pack_bf16x2(p0 - __uint_as_float(hw << 16), p1 - __uint_as_float(hw & 0xffff0000u));
+            if (q2 == 0)
+              lo0[i] = lw;
+            else
+              s[1][i] = lw;
+          }
         }
+      }
+      if (RELOC) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) s[1][16 + i] = lo0[i];
       }
       l_run = l_run * alpha + ((ls4[0] + ls4[1]) + (ls4[2] + ls4[3]));
       // the previous P.V must be done before P and O are touched
       if (j >= 1) okw = __all_sync(0xffffffffu, tt::wait_bar(c, B_ODONE, (j - 1) & 1));
       if (okw) {
         tc::tc_fence_after();
-        tc::tmem_st32(lt + T_P + 32 * hf, s[0]);
+        tc::tmem_st32(lt + (RELOC ? T_S + 128 * b : T_P) + 32 * hf, s[0]);
+        if (psplit) tc::tmem_st32(lt + T_S + 128 * b + 64 + 32 * hf, s[1]);
         if (__any_sync(0xffffffffu, need)) {
 #pragma unroll 1
           for (int q8 = 0; q8 < 2; ++q8) {
@@ -1125,6 +1235,11 @@ struct rk_segpaged_plan_s {
   int32_t num_sms = 0;
   std::vector<int32_t> table;
   std::vector<uint8_t> role;
+  bool reloc = false;             // relocated documents: every tile on the one-sub-tile kernel
+  std::vector<int32_t> blk_cs;    // [R][max_blocks] offset index of each block
+  std::vector<float> cs;          // [offsets][64][2] cos, sin of delta * theta_j
+  int32_t* d_blk_cs = nullptr;
+  float* d_cs = nullptr;
   rk::sp::Req* d_reqs = nullptr;
   rk::sp::Tile* d_tiles = nullptr;
   rk::sp::Tile* d_tiles_one = nullptr;
@@ -1148,6 +1263,10 @@ void sp_free(rk_segpaged_plan_s* p) {
   cudaFree(p->d_table);
   cudaFree(p->d_role);
   cudaFree(p->d_status);
+  cudaFree(p->d_blk_cs);
+  cudaFree(p->d_cs);
+  p->d_blk_cs = nullptr;
+  p->d_cs = nullptr;
   p->d_reqs = nullptr;
   p->d_tiles = nullptr;
   p->d_tiles_one = nullptr;
@@ -1197,7 +1316,11 @@ rk_status_t sp_build(const rk_segpaged_desc_t* d, rk_segpaged_plan_s* p) {
   for (int g = 0; g < Hkv; ++g)
     if (d->kv_head_role[g] > 1) return RK_ERR_INVALID_ARG;
   const bool dense = (d->flags & RK_SEGPAGED_DENSE_MASK) != 0;
-  const int RT = 256 / G;  // rows of a tile: two sub-tiles of 128 / G rows
+  // relocated documents: one sub-tile of 128 / G rows per tile, every tile
+  // on the one-sub-tile kernel (its query operand is R(-delta) q as hi + lo)
+  const bool reloc = d->block_delta != nullptr;
+  if (reloc && !(d->rope_base > 1.0) ) return RK_ERR_INVALID_ARG;
+  const int RT = (reloc ? 128 : 256) / G;  // rows of a tile
   p->Hq = d->num_q_heads;
   p->Hkv = Hkv;
   p->G = G;
@@ -1210,6 +1333,33 @@ rk_status_t sp_build(const rk_segpaged_desc_t* d, rk_segpaged_plan_s* p) {
   p->role.assign(d->kv_head_role, d->kv_head_role + Hkv);
   const int64_t tab_n = int64_t(R) * Hkv * d->max_blocks;
   p->table.assign(d->block_table, d->block_table + tab_n);
+  p->reloc = reloc;
+  if (reloc) {
+    // one cos / sin table per distinct offset (index 0: the zero offset),
+    // angles in double precision: delta * base^(-2j / 128), j = 0..63
+    std::map<int64_t, int32_t> index{{0, 0}};
+    std::vector<int64_t> deltas{0};
+    const int64_t nblk = int64_t(R) * d->max_blocks;
+    p->blk_cs.resize(nblk);
+    for (int64_t i = 0; i < nblk; ++i) {
+      const int64_t dl = d->block_delta[i];
+      if (dl < INT32_MIN || dl > INT32_MAX) return RK_ERR_INVALID_ARG;
+      auto it = index.find(dl);
+      if (it == index.end()) {
+        if (deltas.size() >= (1u << 20)) return RK_ERR_CAPACITY;
+        it = index.emplace(dl, static_cast<int32_t>(deltas.size())).first;
+        deltas.push_back(dl);
+      }
+      p->blk_cs[i] = it->second;
+    }
+    p->cs.resize(deltas.size() * 128);
+    for (size_t k = 0; k < deltas.size(); ++k)
+      for (int j = 0; j < 64; ++j) {
+        const double ang = double(deltas[k]) * std::pow(d->rope_base, -2.0 * j / 128.0);
+        p->cs[k * 128 + 2 * j] = static_cast<float>(std::cos(ang));
+        p->cs[k * 128 + 2 * j + 1] = static_cast<float>(std::sin(ang));
+      }
+  }
   rk_segpaged_info_t& info = p->info;
   info = rk_segpaged_info_t{};
   info.group = G;
@@ -1225,6 +1375,7 @@ rk_status_t sp_build(const rk_segpaged_desc_t* d, rk_segpaged_plan_s* p) {
     q.q_row_begin = static_cast<int32_t>(qb);
     q.row_base = rows;
     q.table_off = int64_t(r) * Hkv * d->max_blocks;
+    q.blk_off = int64_t(r) * d->max_blocks;
     p->reqs.push_back(q);
     for (int64_t x = qb; x < T; ++x)
       for (int g = 0; g < Hkv; ++g)
@@ -1257,15 +1408,18 @@ rk_status_t sp_build(const rk_segpaged_desc_t* d, rk_segpaged_plan_s* p) {
           if (tab[b] < 0 || tab[b] >= d->num_pages) return RK_ERR_INVALID_ARG;
         }
         info.kv_blocks += nb;
-        const bool tiny = t.rows * G <= 16;   // at most 16 pairs in use: decode kernel
-        const bool small = t.rows * G <= 64;  // at most 64 pairs in use: one-sub-tile kernel
-        info.performed_pairs += int64_t(nb) * (tiny ? 16 : t.rows > RT / 2 ? 256 : 128) * PAGE;
+        // at most 16 pairs in use: decode kernel; at most 64 (or relocated
+        // documents): one-sub-tile kernel
+        const bool tiny = !reloc && t.rows * G <= 16;
+        const bool small = reloc || t.rows * G <= 64;
+        info.performed_pairs +=
+            int64_t(nb) * (tiny ? 16 : (!reloc && t.rows > RT / 2) ? 256 : 128) * PAGE;
         t.jb = 0;
         t.je = nb;
         t.part = t.part_first = 0;
         t.nparts = 1;
         const int split_len = tiny ? kDecSplit : kSplitBlocks;
-        if (small && nb > (tiny ? 3 * kDecSplit / 2 : 2 * kSplitBlocks)) {
+        if (small && t.rows * G <= 64 && nb > (tiny ? 3 * kDecSplit / 2 : 2 * kSplitBlocks)) {
           // a long walk of few rows: parts of split_len steps, merged at the end
           const int np = (nb + split_len - 1) / split_len;
           t.nparts = np;
@@ -1332,6 +1486,8 @@ extern "C" rk_status_t rk_segpaged_plan(const rk_segpaged_desc_t* desc, void* st
       st = RK_ERR_CUDA;
     if (st == RK_OK) st = sp_upload(p->table, &p->d_table, s);
     if (st == RK_OK) st = sp_upload(p->role, &p->d_role, s);
+    if (st == RK_OK) st = sp_upload(p->blk_cs, &p->d_blk_cs, s);
+    if (st == RK_OK) st = sp_upload(p->cs, &p->d_cs, s);
     if (st == RK_OK) {
       if (cudaMalloc(reinterpret_cast<void**>(&p->d_status), sizeof(int32_t)) != cudaSuccess ||
           cudaMemsetAsync(p->d_status, 0, sizeof(int32_t), s) != cudaSuccess)
@@ -1391,6 +1547,8 @@ extern "C" rk_status_t rk_segpaged_forward(rk_segpaged_plan_t p, const void* q, 
   a.sink = p->sink;
   a.window = p->window;
   a.scale_log2 = p->scale * 1.4426950408889634f;
+  a.blk_cs = p->d_blk_cs;
+  a.cs = p->d_cs;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (p->split_tiles) {
     char* w = static_cast<char*>(workspace);
@@ -1416,12 +1574,12 @@ extern "C" rk_status_t rk_segpaged_forward(rk_segpaged_plan_t p, const void* q, 
   }
   if (!p->tiles_one.empty()) {
     namespace k1 = rk::sp::one;
-    if (cudaFuncSetAttribute(k1::seg_paged_one_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    auto kern = p->reloc ? k1::seg_paged_one_kernel<true> : k1::seg_paged_one_kernel<false>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(k1::SMEM_BYTES)) != cudaSuccess)
       return RK_ERR_CUDA;
     a.tiles = p->d_tiles_one;
-    k1::seg_paged_one_kernel<<<static_cast<unsigned>(p->tiles_one.size()), k1::THREADS,
-                               k1::SMEM_BYTES, s>>>(a, mp);
+    kern<<<static_cast<unsigned>(p->tiles_one.size()), k1::THREADS, k1::SMEM_BYTES, s>>>(a, mp);
     if (cudaGetLastError() != cudaSuccess) return RK_ERR_CUDA;
   }
   if (!p->tiles_dec.empty()) {

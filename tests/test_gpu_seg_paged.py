@@ -52,8 +52,10 @@ def oracle(pw, rows_per_req=None):
         rows = np.arange(qb, T) if rows_per_req is None else np.asarray(rows_per_req[r])
         flat = off + (rows - qb)
         q = pw.q[torch.from_numpy(flat).cuda()].double().cpu().numpy()
+        bd = None if pw.block_delta is None else pw.block_delta[r]
         Oo, Lo = O.seg_paged_request(q, kp, vp, pw.block_table[r], int(T), int(qb), pw.kv_role,
-                                     pw.sink, pw.window, pw.scale, 128, rows=rows, sampled=True)
+                                     pw.sink, pw.window, pw.scale, 128, rows=rows, sampled=True,
+                                     block_delta=bd, rope_base=pw.rope_base)
         res.append((flat, Oo, Lo))
     return res
 
@@ -137,3 +139,68 @@ def test_seg_paged_full_size_sampled(name):
     compare(out, lse, ref, name)
     # every computed row was written
     assert bool(torch.isfinite(lse).all()) and bool(torch.isfinite(out.float()).all())
+
+
+RELOC = ["paged_reloc_mini", "paged_reloc_g8", "paged_reloc_g1", "paged_reloc_decode"]
+
+
+@pytest.mark.parametrize("sharp", [False, True], ids=["stated", "sharp"])
+@pytest.mark.parametrize("name", RELOC)
+def test_relocated_documents_parity_every_row(name, sharp):
+    """Documents cached alone and reused at other offsets (blog "Insight 1"):
+    every row against the oracle, which relocates the keys physically; the
+    sharp queries (score std ~4) make the relocation decisive."""
+    pw = make_paged_workload(name, seed=0, device="cuda", q_scale=512.0 if sharp else 1.0)
+    assert pw.block_delta is not None and (pw.block_delta != 0).any()
+    out, lse, plan = run(pw)
+    compare(out, lse, oracle(pw), f"{name}/reloc/{sharp}")
+
+
+@pytest.mark.parametrize("name", ["paged_reloc_mini", "paged_reloc_decode"])
+def test_relocated_documents_visible_key_counts_exact(name):
+    pw = make_paged_workload(name, seed=0, device="cuda")
+    pw.q.zero_()
+    out, lse, plan = run(pw)
+    cnt = np.rint(np.exp(np.minimum(lse.double().cpu().numpy(), 700.0)))
+    offs = pw.row_offsets()
+    for r, (T, qb) in enumerate(zip(pw.seq_len, pw.q_row_begin)):
+        for i, p in enumerate(range(int(qb), int(T))):
+            for hq in range(pw.Hq):
+                g = hq // pw.G
+                want = p + 1 if pw.kv_role[g] else len(O.visible_keys(p, False, pw.sink, pw.window))
+                assert cnt[offs[r] + i, hq] == want, (name, p, hq)
+
+
+def test_relocated_document_decisive_probe():
+    """A query aimed at one key of a relocated document, as that key sits at
+    its absolute position (R(delta) k_stored): the key must dominate the
+    attention on the GPU as in the oracle, which a missing or wrong-signed
+    turn of the query would not give."""
+    pw = make_paged_workload("paged_reloc_mini", seed=3, device="cuda")
+    r, T = 0, int(pw.seq_len[0])
+    delta = pw.block_delta[r]
+    blk = int(np.nonzero(delta)[0][0])          # first block of a moved document
+    k_tok = blk * 128 + 5
+    p = min(T - 1, k_tok + 40)
+    g = int(np.nonzero(pw.kv_role)[0][0])        # a Global KV head
+    page = int(pw.block_table[r, g, blk])
+    kst = pw.k_pages[page, 5].double().cpu().numpy()
+    th = pw.rope_base ** (-2.0 * np.arange(64) / 128)
+    ang = float(delta[blk]) * th
+    c, s = np.cos(ang), np.sin(ang)
+    kabs = np.empty(128)
+    kabs[0::2] = kst[0::2] * c - kst[1::2] * s
+    kabs[1::2] = kst[0::2] * s + kst[1::2] * c
+    qv = torch.from_numpy(kabs / np.linalg.norm(kabs) * 400.0).to(pw.q.dtype).cuda()
+    row = int(pw.row_offsets()[r] + (p - int(pw.q_row_begin[r])))
+    for h in range(g * pw.G, (g + 1) * pw.G):
+        pw.q[row, h] = qv
+    out, lse, plan = run(pw)
+    ref = oracle(pw, [np.array([p])] + [np.zeros(0, np.int64)] * (len(pw.seq_len) - 1))
+    ref = [x for x in ref if len(x[0])]
+    compare(out, lse, ref, "reloc probe")
+    heads = slice(g * pw.G, (g + 1) * pw.G)
+    assert float(ref[0][2][0, heads].min()) > 5.0        # the probe key dominates in the oracle
+    got = out[row, heads].double().cpu().numpy()
+    vst = pw.v_pages[page, 5].double().cpu().numpy()
+    assert np.abs(got - vst[None, :]).max() < 0.05 * np.abs(vst).max()

@@ -131,3 +131,33 @@ def test_decode_split_parts_and_workspace():
     pq = make_paged_geometry("qwen32b_decode", 0)
     qi = _plan(pq).info
     assert qi["split_parts"] > 64 and qi["tiles"] > qi["split_parts"]
+
+
+@pytest.mark.parametrize("name", ["paged_reloc_mini", "paged_reloc_g8", "paged_reloc_decode",
+                                  "qwen32b_reloc_128k"])
+def test_relocated_plans_use_single_sub_tiles(name):
+    """With document offsets every tile is one sub-tile of 128 / G rows on the
+    one-sub-tile kernel: 128 query pairs per issued block, the same attended
+    pairs and blocks as the plan without offsets."""
+    pw = make_paged_geometry(name, 0)
+    rel = _plan(pw, block_delta=pw.block_delta, rope_base=pw.rope_base).info
+    plain = _plan(pw).info
+    assert rel["pairs"] == plain["pairs"] and rel["rows"] == plain["rows"]
+    assert rel["performed_pairs"] == rel["kv_blocks"] * 128 * PAGE
+    rows_per = 128 // pw.G
+    want_tiles = 0
+    for T, qb in zip(pw.seq_len, pw.q_row_begin):
+        want_tiles += pw.Hkv * ((int(T) - int(qb) + rows_per - 1) // rows_per)
+    assert rel["tiles"] >= want_tiles     # split parts add tiles, never remove them
+
+
+def test_relocated_plan_errors():
+    pw = make_paged_geometry("paged_reloc_mini", 0)
+    bad = pw.block_delta.copy()
+    bad[0, 1] = 1 << 40                            # offset beyond int32
+    with pytest.raises(B.RkError) as ei:
+        _plan(pw, block_delta=bad)
+    assert ei.value.status == 2
+    with pytest.raises(B.RkError) as ei:
+        _plan(pw, block_delta=pw.block_delta, rope_base=0.5)
+    assert ei.value.status == 2
