@@ -548,6 +548,28 @@ def bench_seg_paged(local: int, pk: dict, prefill: str = "qwen32b_128k") -> dict
     res["dense_mask_over_paged"] = round(res["prefill_dense_mask"]["ms"] / res["prefill"]["ms"], 2)
     del pw, out, lse
     torch.cuda.empty_cache()
+    # relocated documents: the first 96K tokens are 48 documents of 2048
+    # tokens cached alone (keys with RoPE at 0..2047), the query turns by
+    # -delta; every tile on the one-sub-tile kernel
+    pw = make_paged_workload("qwen32b_reloc_128k", seed=0, device=dev)
+    out = torch.empty((pw.rows, pw.Hq, 128), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((pw.rows, pw.Hq), dtype=torch.float32, device=dev)
+    plan = B.SegPagedPlan.from_workload(pw, stream=stream)
+    info = plan.info
+    ms, good = timed(plan, pw, out, lse, 3)
+    ok = ok and good
+    alg = 512.0 * info["pairs"]
+    res["prefill_relocated"] = {
+        "workload": "qwen32b_reloc_128k: the 128K prefill with 48 relocated documents of 2048 "
+                    "tokens (keys cached at positions 0..2047, query turned by -delta) and a "
+                    "32K tail", "ms": round(ms, 3),
+        "tflops": round(alg / (ms * 1e-3) / 1e12, 1),
+        "performed_tflops": round(512.0 * info["performed_pairs"] / (ms * 1e-3) / 1e12, 1),
+        "frac_of_peak": round(alg / (ms * 1e-3) / 1e12 / pk["bf16_tflops"], 4),
+        "tiles": info["tiles"]}
+    plan.close()
+    del pw, out, lse
+    torch.cuda.empty_cache()
     pw = make_paged_workload("qwen32b_decode", seed=0, device=dev)
     out = torch.empty((pw.rows, pw.Hq, 128), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((pw.rows, pw.Hq), dtype=torch.float32, device=dev)
