@@ -71,6 +71,10 @@ __device__ __forceinline__ void cp_async_wait() {
 // Next key tile of a work item.  Keys visited: [r0lo, r0hi) u [r1lo, r1hi)
 // intersected with each segment (segments sorted by offset), walked segment
 // by segment so the query rotation changes only at segment boundaries.
+// `skip` (from the plan, 0 = none) names segments [skip & 0xffff, skip >> 16)
+// that meet neither range: the walk jumps over them instead of reading each
+// one's offset, which between a sink and a window far behind it would be a
+// chain of dependent global loads.
 struct KeyTile {
   int j;    // segment index within the request
   int rr;   // range 0 (sink) or 1 (window / causal)
@@ -80,7 +84,9 @@ struct KeyTile {
 
 template <int TN>
 __device__ __forceinline__ bool next_key_tile(KeyTile& t, const DevSeg* segs, int nseg, int r0lo,
-                                              int r0hi, int r1lo, int r1hi) {
+                                              int r0hi, int r1lo, int r1hi,
+                                              uint32_t skip = 0) {
+  const int jlo = static_cast<int>(skip & 0xffffu), jhi = static_cast<int>(skip >> 16);
   int j = t.j, rr = t.rr, k = t.k1;
   while (j < nseg) {
     const int d = segs[j].delta;
@@ -100,6 +106,7 @@ __device__ __forceinline__ bool next_key_tile(KeyTile& t, const DevSeg* segs, in
     } else {
       rr = 0;
       ++j;
+      if (j >= jlo && j < jhi) j = jhi;
     }
     k = -1;
   }

@@ -76,6 +76,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   const DevSeg* segs = a.segs + rq.seg_first;
   const int nseg = rq.seg_count;
   const int r0hi = P.sink_hi, r1lo = P.win_lo, r1hi = P.key_hi;
+  const uint32_t skip = static_cast<uint32_t>(P.skip);
   // the leader's barrier i as a shared::cluster address
   auto lbar = [&](int i) { return tc::mapa_shared(smem_u32(&bar[i]), 0); };
 
@@ -125,7 +126,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         return true;
       };
       KeyTile cur{0, 0, 0, -1}, prev{0, 0, 0, -1};
-      bool have = next_key_tile<TNK>(cur, segs, nseg, 0, r0hi, r1lo, r1hi);
+      bool have = next_key_tile<TNK>(cur, segs, nseg, 0, r0hi, r1lo, r1hi, skip);
       bool has_prev = false;
       const int koff = 64 * static_cast<int>(rank);
       while (ok && (have || has_prev)) {
@@ -138,7 +139,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           ok = load(prev, MAP_V, 0, 4 * half + 2 * static_cast<int>(rank), 2 * CHUNK);
         prev = cur;
         has_prev = have;
-        if (have) have = next_key_tile<TNK>(cur, segs, nseg, 0, r0hi, r1lo, r1hi);
+        if (have) have = next_key_tile<TNK>(cur, segs, nseg, 0, r0hi, r1lo, r1hi, skip);
       }
       // the pair's copies in flight land before either CTA may exit (the
       // teardown cluster barrier holds rank 1 until the leader gets here)
@@ -159,7 +160,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       uint32_t cnt = 0;
       int j = 0, jprev = -1;
       KeyTile cur{0, 0, 0, -1};
-      bool have = next_key_tile<TNK>(cur, segs, nseg, 0, r0hi, r1lo, r1hi);
+      bool have = next_key_tile<TNK>(cur, segs, nseg, 0, r0hi, r1lo, r1hi, skip);
       bool has_prev = false;
       while (ok && (have || has_prev)) {
         if (have) {
@@ -220,7 +221,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         has_prev = have;
         jprev = j;
         if (have) {
-          have = next_key_tile<TNK>(cur, segs, nseg, 0, r0hi, r1lo, r1hi);
+          have = next_key_tile<TNK>(cur, segs, nseg, 0, r0hi, r1lo, r1hi, skip);
           ++j;
         }
       }
@@ -237,7 +238,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     const uint16_t* qrope = ri.p >= 0 ? a.q + (ri.frow * a.H + ri.head) * 576 + 512 : nullptr;
     const uint32_t sfree_l = lbar(B_SFREE), pready_l = lbar(B_PREADY);
     KeyTile kt{0, 0, 0, -1};
-    bool have = next_key_tile<TNK>(kt, segs, nseg, 0, r0hi, r1lo, r1hi);
+    bool have = next_key_tile<TNK>(kt, segs, nseg, 0, r0hi, r1lo, r1hi, skip);
     // q_rope' of the first segment, then release the (empty) S buffer
     tt::write_rope(lt, T_RH, T_RL, qrope, a.rope_cs + static_cast<int64_t>(rq.seg_first + kt.j) * 64);
     tc::tc_fence_before();
@@ -247,7 +248,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     bool ok = true;
     while (ok && have) {
       KeyTile nx = kt;
-      const bool have_next = next_key_tile<TNK>(nx, segs, nseg, 0, r0hi, r1lo, r1hi);
+      const bool have_next = next_key_tile<TNK>(nx, segs, nseg, 0, r0hi, r1lo, r1hi, skip);
       ok = __all_sync(0xffffffffu, wait_bar(c, B_SFULL, j & 1));
       if (!ok) break;
       tc::tc_fence_after();

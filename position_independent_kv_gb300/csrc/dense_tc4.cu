@@ -73,9 +73,14 @@ constexpr uint32_t OFF_P = 0;
 constexpr int VRING = 2;
 constexpr uint32_t VSLOT = 4 * CHUNK;
 constexpr uint32_t OFF_VRING = OFF_P + 2 * PSTRIDE;
+// epilogue: each lane's bf16 output row (1 KB) staged over the P buffers and
+// the value ring (all consumed by then), rows 1040 bytes apart so that a
+// warp's 16-byte stores of one column fall in distinct banks
+constexpr uint32_t OFF_OSTG = 0, OSTRIDE = 1040;
 constexpr uint32_t OFF_BAR = OFF_KRING + KRING * KSLOT;
 static_assert(OFF_KRING % 1024 == 0 && OFF_VRING % 1024 == 0, "operand alignment");
 static_assert(OFF_VRING + VRING * VSLOT <= OFF_BAR, "O-pair layout");
+static_assert(OFF_OSTG + 128 * OSTRIDE <= OFF_VRING + VRING * VSLOT, "output staging");
 enum {
   B_KFULL = 0,
   B_KEMPTY = B_KFULL + KRING,
@@ -96,6 +101,10 @@ enum {
   B_PREADY = B_PFULL + 2,      // 2: O rescaled where needed, P buffer ready for the MMAs
   B_ODONE = B_PREADY + 2,
   B_OFINAL,
+  B_STGFREE,  // (S CTAs) the last bulk copy of P has landed: the staging buffer
+              // may be rewritten (one arrival per tile from the output CTA's
+              // warp 6; a copy that completes on the receiver's barrier is not
+              // covered by the sender's bulk-group waits)
   NBAR
 };
 constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
@@ -109,6 +118,14 @@ constexpr uint32_t T_O = 0;
 // segment maps (kSegMaps per segment)
 constexpr int MAP_K9 = 4;    // 64 rows x all d_k / 64 chunks
 constexpr int MAP_V4 = 5;    // 128 rows x 4 chunks
+
+// Bit i set for each offset base + i (i < 32) inside [lo, hi).
+__device__ __forceinline__ uint32_t span_bits(int lo, int hi, int base) {
+  const int l = min(max(lo - base, 0), 32), h = min(max(hi - base, 0), 32);
+  const uint32_t mh = h >= 32 ? 0xffffffffu : ((1u << h) - 1u);
+  const uint32_t ml = l >= 32 ? 0xffffffffu : ((1u << l) - 1u);
+  return mh & ~ml;
+}
 
 // Turn the rope pairs held in o[0..31] (32 consecutive output columns: pairs
 // H0 .. H0 + 15 of the rope slice) by the angles whose cos / sin are (c[k],
@@ -146,6 +163,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
   const DevSeg* segs = a.segs + rq.seg_first;
   const int nseg = rq.seg_count;
   const int r0hi = P.sink_hi, r1lo = P.win_lo, r1hi = P.key_hi;
+  const uint32_t skip = static_cast<uint32_t>(P.skip);
   auto cbar = [&](int i, uint32_t rank) { return tc::mapa_shared(smem_u32(&bar[i]), rank); };
 
   if (tid == 0) {
@@ -170,6 +188,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
     tc::mbar_init(&bar[B_SFINAL], 1);
     tc::mbar_init(&bar[B_ODONE], 1);
     tc::mbar_init(&bar[B_OFINAL], 1);
+    tc::mbar_init(&bar[B_STGFREE], 1);
     misc[1] = 0;
     if (!spair)  // each P buffer expects one bulk copy per use; armed one use ahead
       for (int b = 0; b < 2; ++b) tc::mbar_arrive_expect_tx(&bar[B_PFULL + b], PREC_BYTES);
@@ -192,7 +211,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
         uint32_t cnt = 0;
         bool ok = true;
         KeyTile cur{0, 0, 0, -1};
-        bool have = next_key_tile<TNK>(cur, segs, nseg, 0, r0hi, r1lo, r1hi);
+        bool have = next_key_tile<TNK>(cur, segs, nseg, 0, r0hi, r1lo, r1hi, skip);
         while (ok && have) {
           const int slot = cnt % KRING;
           ok = wait_bar(c, B_KEMPTY + slot, ((cnt / KRING) & 1) ^ 1);
@@ -204,7 +223,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
                               cbar(B_KFULL + slot, 0), 0,
                               cur.k0 - segs[cur.j].delta + 64 * static_cast<int>(r), 0);
           ++cnt;
-          have = next_key_tile<TNK>(cur, segs, nseg, 0, r0hi, r1lo, r1hi);
+          have = next_key_tile<TNK>(cur, segs, nseg, 0, r0hi, r1lo, r1hi, skip);
         }
         // the pair's copies in flight land before either CTA may exit
         if (r == 0)
@@ -221,7 +240,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
         uint32_t cnt = 0;
         int j = 0, prev_seg = -1;
         KeyTile cur{0, 0, 0, -1};
-        bool have = next_key_tile<TNK>(cur, segs, nseg, 0, r0hi, r1lo, r1hi);
+        bool have = next_key_tile<TNK>(cur, segs, nseg, 0, r0hi, r1lo, r1hi, skip);
         while (ok && have) {
           const int b = j & 1;
           ok = wait_bar<true>(c, B_SFREE + b, ((j >> 1) & 1) ^ 1);
@@ -236,7 +255,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
           tc::tc_fence_after();
           const uint32_t base = ka + slot * KSLOT;
           KeyTile nx = cur;
-          const bool have_next = next_key_tile<TNK>(nx, segs, nseg, 0, r0hi, r1lo, r1hi);
+          const bool have_next = next_key_tile<TNK>(nx, segs, nseg, 0, r0hi, r1lo, r1hi, skip);
           // B = K[64 keys of each CTA x 16 dims]: the rope chunk first (q_rope'
           // hi and lo), then the nope chunks
 #pragma unroll
@@ -298,11 +317,15 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
       auto put_rope = [&](int seg) {
         const float4* cs4 =
             reinterpret_cast<const float4*>(a.rope_cs + static_cast<int64_t>(rq.seg_first + seg) * 64);
-#pragma unroll
+        // one row per pass (not unrolled: the body is long)
+#pragma unroll 1
         for (int e = 0; e < 2; ++e) {
           const int m = m0 + 32 * e;
           const uint32_t sw = static_cast<uint32_t>(m & 7);
           uint8_t* rrow = sm + OFF_ROPE + m * 128;
+          uint32_t cur[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) cur[i] = e ? raw[1][i] : raw[0][i];
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
             uint32_t hi[4], lo[4];
@@ -313,8 +336,8 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
               for (int h = 0; h < 2; ++h) {
                 const int jj = 4 * u + 2 * v2 + h;
                 const float co = h ? w.z : w.x, si = h ? w.w : w.y;
-                const float x = __uint_as_float(raw[e][jj] << 16);
-                const float y = __uint_as_float(raw[e][jj] & 0xffff0000u);
+                const float x = __uint_as_float(cur[jj] << 16);
+                const float y = __uint_as_float(cur[jj] & 0xffff0000u);
                 const float xr = fmaf(x, co, y * si), yr = fmaf(-x, si, y * co);
                 const uint32_t hw = pack_bf16x2(xr, yr);
                 hi[2 * v2 + h] = hw;
@@ -332,23 +355,29 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
         if (lane == 0) tc::mbar_arrive_cluster(cbar(B_ROPE, 0));
       };
       KeyTile kt{0, 0, 0, -1};
-      bool have = next_key_tile<TNK>(kt, segs, nseg, 0, r0hi, r1lo, r1hi);
-      if (have) put_rope(kt.j);
+      bool have = next_key_tile<TNK>(kt, segs, nseg, 0, r0hi, r1lo, r1hi, skip);
+      int seg = have ? kt.j : -1;  // the segment to write q_rope' for next
       uint32_t sw_ev = 0;
-      bool ok = true;
-      while (ok && have) {
-        KeyTile nx = kt;
-        const bool have_next = next_key_tile<TNK>(nx, segs, nseg, 0, r0hi, r1lo, r1hi);
-        if (have_next && nx.j != kt.j) {
-          // the old segment's rope MMAs are done: none reads q_rope' any more
-          ok = __all_sync(0xffffffffu, wait_bar(c, B_SWITCH, sw_ev++ & 1));
-          if (ok) {
-            tc::tc_fence_after();
-            put_rope(nx.j);
+      while (seg >= 0) {
+        put_rope(seg);  // one call site: the body is large
+        seg = -1;
+        while (have) {
+          KeyTile nx = kt;
+          const bool have_next = next_key_tile<TNK>(nx, segs, nseg, 0, r0hi, r1lo, r1hi, skip);
+          const bool sw = have_next && nx.j != kt.j;
+          kt = nx;
+          have = have_next;
+          if (sw) {
+            // the old segment's rope MMAs are done: none reads q_rope' any more
+            if (__all_sync(0xffffffffu, wait_bar(c, B_SWITCH, sw_ev++ & 1))) {
+              tc::tc_fence_after();
+              seg = kt.j;
+            } else {
+              have = false;
+            }
+            break;
           }
         }
-        kt = nx;
-        have = have_next;
       }
     } else {
       // ------------------- S pair: queries, rotation and online softmax ---
@@ -362,32 +391,58 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
       const uint16_t* qrow = ri.p >= 0 ? a.q + (ri.frow * a.H + ri.head) * DK : nullptr;
       const uint32_t orank = crank + 2;
       const uint32_t sw = static_cast<uint32_t>(m & 7);
-      // this lane's nope queries -> tensor memory (32-bit column c = dims 2c, 2c + 1)
+      // this lane's nope queries -> tensor memory (32-bit column c = dims 2c,
+      // 2c + 1).  The loads are coalesced: in step u a warp reads four whole
+      // 128-byte rows of a chunk (lane l: 16-byte unit l & 7 of row 4u + l / 8
+      // of the warp's 32 rows), and a 4 KB slice of the P staging buffer
+      // (unused until the first P) turns them back into one row per lane;
+      // four chunks' loads in flight at a time
+      {
+        uint8_t* qs = sm + OFF_STG + quarter * 4096;
+        const int rsub = lane >> 3, unit = lane & 7;
+        const uint4* qsrc[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          qsrc[u] = reinterpret_cast<const uint4*>(__shfl_sync(
+              0xffffffffu, reinterpret_cast<unsigned long long>(qrow), 4 * u + rsub));
 #pragma unroll 1
-      for (int i = 0; i < NCH; ++i) {
-        uint32_t w[32];
-        if (qrow) {
-          const uint4* s4 = reinterpret_cast<const uint4*>(qrow) + 8 * i;
+        for (int i0 = 0; i0 < NCH; i0 += 4) {
+          uint4 qw[4][8];
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const uint4 v = __ldg(s4 + u);
-            w[4 * u] = v.x;
-            w[4 * u + 1] = v.y;
-            w[4 * u + 2] = v.z;
-            w[4 * u + 3] = v.w;
+          for (int ii = 0; ii < 4; ++ii)
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              qw[ii][u] = (qsrc[u] && i0 + ii < NCH) ? __ldg(qsrc[u] + 8 * (i0 + ii) + unit)
+                                                     : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+          for (int ii = 0; ii < 4; ++ii) {
+            if (i0 + ii >= NCH) break;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const int row = 4 * u + rsub;
+              *reinterpret_cast<uint4*>(qs + row * 128 + ((unit ^ (row & 7)) << 4)) = qw[ii][u];
+            }
+            __syncwarp();
+            uint32_t v[32];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const uint4 x = *reinterpret_cast<const uint4*>(qs + lane * 128 + ((k ^ (lane & 7)) << 4));
+              v[4 * k] = x.x;
+              v[4 * k + 1] = x.y;
+              v[4 * k + 2] = x.z;
+              v[4 * k + 3] = x.w;
+            }
+            __syncwarp();
+            tc::tmem_st32(lt + T_Q + 32 * (i0 + ii), v);
           }
-        } else {
-#pragma unroll
-          for (int u = 0; u < 32; ++u) w[u] = 0;
         }
-        tc::tmem_st32(lt + T_Q + 32 * i, w);
       }
       tc::tmem_wait_st();
       tc::tc_fence_before();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive_cluster(cbar(B_QREADY, 0));
       KeyTile kt{0, 0, 0, -1};
-      bool have = next_key_tile<TNK>(kt, segs, nseg, 0, r0hi, r1lo, r1hi);
+      bool have = next_key_tile<TNK>(kt, segs, nseg, 0, r0hi, r1lo, r1hi, skip);
       float m_run = -INFINITY, l_run = 0.f;
       int j = 0;
       bool ok = true;
@@ -397,7 +452,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
       while (ok && have) {
         const int b = j & 1;
         KeyTile nx = kt;
-        const bool have_next = next_key_tile<TNK>(nx, segs, nseg, 0, r0hi, r1lo, r1hi);
+        const bool have_next = next_key_tile<TNK>(nx, segs, nseg, 0, r0hi, r1lo, r1hi, skip);
         bool okw = __all_sync(0xffffffffu, wait_bar(c, B_SFULL + b, (j >> 1) & 1));
         uint32_t s[4][32];
         float alpha = 1.f;
@@ -422,14 +477,17 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
               for (int i = 0; i < 32; ++i)
                 mx4[i & 3] = fmaxf(mx4[i & 3], __uint_as_float(s[q4][i]));
           } else {
+            // visible keys as offsets from k0: [0, a_hi) u [b_lo, hi) (a Global
+            // head: [0, hi)), one bit per key of each 32-key group
+            const int hi = min(max(min(kt.k1, p + 1) - kt.k0, 0), TNK);
+            const int a_hi = ri.glob ? hi : min(hi, max(sink - kt.k0, 0));
+            const int b_lo = ri.glob ? hi : max(p - window - kt.k0, 0);
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
+              const uint32_t msk = span_bits(0, a_hi, 32 * q4) | span_bits(b_lo, hi, 32 * q4);
 #pragma unroll
               for (int i = 0; i < 32; ++i) {
-                const int key = kt.k0 + 32 * q4 + i;
-                bool vis = key < kt.k1 && key <= p;
-                if (!ri.glob) vis = vis && (key < sink || key >= p - window);
-                const float x = vis ? __uint_as_float(s[q4][i]) : -INFINITY;
+                const float x = ((msk >> i) & 1u) ? __uint_as_float(s[q4][i]) : -INFINITY;
                 s[q4][i] = __float_as_uint(x);
                 mx4[i & 3] = fmaxf(mx4[i & 3], x);
               }
@@ -458,7 +516,8 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
           // j - 2 are done; the staging buffer once the copy of tile j - 1
           // has read it
           okw = __all_sync(0xffffffffu, wait_bar(c, B_PEMPTY + b, ((j >> 1) & 1) ^ 1));
-          if (okw && issuer) tc::bulk_wait_read<0>();  // the staging buffer is free
+          // the staging buffer is free once the copy of tile j - 1 has landed
+          if (okw && issuer && j > 0) okw = wait_bar<true>(c, B_STGFREE, (j - 1) & 1);
         }
         ok = tc::named_and(1, 128, okw);
         if (!ok) break;
@@ -476,7 +535,6 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
         if (issuer) {
           tc::bulk_copy_to_cluster(tc::mapa_shared(smem_u32(sm + OFF_P + b * PSTRIDE), orank),
                                    smem_u32(stg), PREC_BYTES, cbar(B_PFULL + b, orank));
-          tc::bulk_commit_group();
         }
         ++j;
         kt = nx;
@@ -485,7 +543,6 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
       // every output MMA has consumed its P before the cluster may exit
       for (int jj = j - 1; ok && jj >= 0 && jj >= j - 2; --jj)
         ok = __all_sync(0xffffffffu, wait_bar(c, B_PEMPTY + (jj & 1), (jj >> 1) & 1));
-      if (issuer) tc::bulk_wait_read<0>();
       if (ok && ri.store && l_run > 0.f)
         a.lse[ri.frow * a.H + ri.head] = m_run * 0.6931471805599453f + logf(l_run);
     }
@@ -496,7 +553,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
         uint32_t cnt = 0;
         bool ok = true;
         KeyTile cur{0, 0, 0, -1};
-        bool have = next_key_tile<TNK>(cur, segs, nseg, 0, r0hi, r1lo, r1hi);
+        bool have = next_key_tile<TNK>(cur, segs, nseg, 0, r0hi, r1lo, r1hi, skip);
         while (ok && have) {
           const int slot = cnt % VRING;
           ok = wait_bar(c, B_VEMPTY + slot, ((cnt / VRING) & 1) ^ 1);
@@ -508,7 +565,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
                               cbar(B_VFULL + slot, 2), 0, cur.k0 - segs[cur.j].delta,
                               4 * static_cast<int>(r));
           ++cnt;
-          have = next_key_tile<TNK>(cur, segs, nseg, 0, r0hi, r1lo, r1hi);
+          have = next_key_tile<TNK>(cur, segs, nseg, 0, r0hi, r1lo, r1hi, skip);
         }
         if (r == 0)
           for (uint32_t k = (cnt > VRING ? cnt - VRING : 0); k < cnt; ++k)
@@ -523,7 +580,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
         int j = 0;
         bool ok = true;
         KeyTile cur{0, 0, 0, -1};
-        bool have = next_key_tile<TNK>(cur, segs, nseg, 0, r0hi, r1lo, r1hi);
+        bool have = next_key_tile<TNK>(cur, segs, nseg, 0, r0hi, r1lo, r1hi, skip);
         while (ok && have) {
           const int b = j & 1;
           ok = wait_bar<true>(c, B_PREADY + b, (j >> 1) & 1);
@@ -551,9 +608,25 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
           tc::mma_commit_2sm(&bar[B_ODONE], 0xC);
           tc::mma_commit_2sm(&bar[B_PEMPTY + b], 0x3);
           ++j;
-          have = next_key_tile<TNK>(cur, segs, nseg, 0, r0hi, r1lo, r1hi);
+          have = next_key_tile<TNK>(cur, segs, nseg, 0, r0hi, r1lo, r1hi, skip);
         }
         tc::mma_commit_2sm(&bar[B_OFINAL], 0xC);
+      }
+    } else if (warp == 6) {
+      // ---------------- O pair: releases the sender's P staging buffer ---
+      // as soon as each copy has landed (a thread of its own, so that the
+      // release never waits for the rescale / turn work of the lanes).  It
+      // cannot fall two phases behind on a P buffer: the copy of tile j + 2
+      // is sent only after the release of tile j + 1.
+      if (lane == 0) {
+        int j = 0;
+        KeyTile kt{0, 0, 0, -1};
+        bool have = next_key_tile<TNK>(kt, segs, nseg, 0, r0hi, r1lo, r1hi, skip);
+        while (have && wait_bar<true>(c, B_PFULL + (j & 1), (j >> 1) & 1)) {
+          tc::mbar_arrive_cluster(cbar(B_STGFREE, crank - 2));
+          ++j;
+          have = next_key_tile<TNK>(kt, segs, nseg, 0, r0hi, r1lo, r1hi, skip);
+        }
       }
     } else if (warp < 6) {
       // ------------------------------- O pair: rescale and epilogue ------
@@ -566,7 +639,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
       int j = 0;
       bool ok = true;
       KeyTile kt{0, 0, 0, -1};
-      bool have = next_key_tile<TNK>(kt, segs, nseg, 0, r0hi, r1lo, r1hi);
+      bool have = next_key_tile<TNK>(kt, segs, nseg, 0, r0hi, r1lo, r1hi, skip);
       // rotary value: the segment whose canonical frame the output's rope
       // columns (448..511, output column = value column there) are in
       int seg_frame = kt.j;
@@ -622,7 +695,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
         __syncwarp();
         if (lane == 0) tc::mbar_arrive_cluster(cbar(B_PREADY + b, 2));
         ++j;
-        have = next_key_tile<TNK>(kt, segs, nseg, 0, r0hi, r1lo, r1hi);
+        have = next_key_tile<TNK>(kt, segs, nseg, 0, r0hi, r1lo, r1hi, skip);
       }
       if (ok) ok = __all_sync(0xffffffffu, wait_bar(c, B_OFINAL, 0));
       tc::tc_fence_after();
@@ -630,6 +703,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
         const bool st = ri.store && l_fin > 0.f;
         const float inv = st ? 1.f / l_fin : 0.f;
         uint16_t* dst = st ? a.out + (ri.frow * a.H + ri.head) * 512 : nullptr;
+        uint8_t* orow = sm + OFF_OSTG + m * OSTRIDE;
         // rotary value: R(delta_frame - p) restores the last segment's output
         // phase and applies the inverse output RoPE at the row's position p
         // (cos / sin of p theta from the two-level position table)
@@ -650,27 +724,41 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
             es[2 * u + 1] = fmaf(x.w, pc1, -x.z * ps1);
           }
         }
+        // two 32-column loads per wait
 #pragma unroll 1
-        for (int q8 = 0; q8 < 16; ++q8) {
-          uint32_t o[32];
-          tc::tmem_ld32(lt + T_O + 32 * q8, o);
+        for (int q0 = 0; q0 < 16; q0 += 2) {
+          uint32_t o[2][32];
+          tc::tmem_ld32(lt + T_O + 32 * q0, o[0]);
+          tc::tmem_ld32(lt + T_O + 32 * (q0 + 1), o[1]);
           tc::tmem_wait_ld();
-          if (VROPE && st && q8 == 14) turn_pairs<0>(o, ec, es);
-          if (VROPE && st && q8 == 15) turn_pairs<16>(o, ec, es);
+          if (VROPE && st && q0 == 14) {
+            turn_pairs<0>(o[0], ec, es);
+            turn_pairs<16>(o[1], ec, es);
+          }
           if (st) {
-            const int c0 = 32 * q8;
-            const int col = 256 * ((c0 >> 7) & 1) + 128 * (c0 >> 8) + (c0 & 127);
-            uint4* d4 = reinterpret_cast<uint4*>(dst + col);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              uint4 w;
-              w.x = pack_bf16x2(__uint_as_float(o[8 * u + 0]) * inv, __uint_as_float(o[8 * u + 1]) * inv);
-              w.y = pack_bf16x2(__uint_as_float(o[8 * u + 2]) * inv, __uint_as_float(o[8 * u + 3]) * inv);
-              w.z = pack_bf16x2(__uint_as_float(o[8 * u + 4]) * inv, __uint_as_float(o[8 * u + 5]) * inv);
-              w.w = pack_bf16x2(__uint_as_float(o[8 * u + 6]) * inv, __uint_as_float(o[8 * u + 7]) * inv);
-              d4[u] = w;
+            for (int h = 0; h < 2; ++h) {
+              const int c0 = 32 * (q0 + h);
+              const int col = 256 * ((c0 >> 7) & 1) + 128 * (c0 >> 8) + (c0 & 127);
+              uint4* d4 = reinterpret_cast<uint4*>(orow + 2 * col);
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                uint4 w;
+                w.x = pack_bf16x2(__uint_as_float(o[h][8 * u + 0]) * inv, __uint_as_float(o[h][8 * u + 1]) * inv);
+                w.y = pack_bf16x2(__uint_as_float(o[h][8 * u + 2]) * inv, __uint_as_float(o[h][8 * u + 3]) * inv);
+                w.z = pack_bf16x2(__uint_as_float(o[h][8 * u + 4]) * inv, __uint_as_float(o[h][8 * u + 5]) * inv);
+                w.w = pack_bf16x2(__uint_as_float(o[h][8 * u + 6]) * inv, __uint_as_float(o[h][8 * u + 7]) * inv);
+                d4[u] = w;
+              }
             }
           }
+        }
+        // one bulk copy per stored row; its shared-memory reads finish before exit
+        if (st) {
+          tc::fence_proxy_async();
+          tc::bulk_store_global(dst, smem_u32(orow), 1024);
+          tc::bulk_commit_group();
+          tc::bulk_wait_read<0>();
         }
       }
     }

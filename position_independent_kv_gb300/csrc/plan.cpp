@@ -548,6 +548,26 @@ static rk_status_t build_plan(const rk_seg_attn_desc_t* d, rk_seg_attn_plan_s* p
       }
       return kt;
     };
+    // segments of request `req` that meet neither [0, sh) nor [wl, ...):
+    // those from the first one starting at or after sh up to the first one
+    // ending after wl (segments are sorted by offset)
+    auto skip_hint = [&](int req, int64_t sh, int64_t wl) -> int32_t {
+      const DevReq& rq = p->reqs[req];
+      if (wl <= sh || rq.seg_count > 0xffff) return 0;
+      const DevSeg* sg = p->segs.data() + rq.seg_first;
+      int lo = 0, hi = rq.seg_count;
+      while (lo < hi) {  // first segment with delta >= sh
+        const int mid = (lo + hi) / 2;
+        if (sg[mid].delta < sh) lo = mid + 1; else hi = mid;
+      }
+      const int jlo = lo;
+      hi = rq.seg_count;
+      while (lo < hi) {  // first segment ending after wl
+        const int mid = (lo + hi) / 2;
+        if (int64_t(sg[mid].delta) + sg[mid].n <= wl) lo = mid + 1; else hi = mid;
+      }
+      return jlo < lo ? static_cast<int32_t>((static_cast<uint32_t>(lo) << 16) | uint32_t(jlo)) : 0;
+    };
     std::vector<std::pair<int64_t, TcPair>> pairs;
     size_t i = 0;
     while (i < tc_list.size()) {
@@ -582,6 +602,7 @@ static rk_status_t build_plan(const rk_seg_attn_desc_t* d, rk_seg_attn_plan_s* p
         pr.t[1] = A;
         pr.t[1].pad |= 1;
       }
+      pr.skip = skip_hint(A.req, pr.sink_hi, pr.win_lo);
       // both CTAs of a real pair do attention work; a partner without work does not count
       info.performed_pairs += (paired ? 2 : 1) * cost * TN * TM;
       pairs.push_back({cost, pr});

@@ -88,13 +88,15 @@ struct TcTile {
 // the union of their key ranges, [0, sink_hi) u [win_lo, key_hi) with
 // sink_hi <= win_lo.  t[1].pad bit 0 marks a partner without work (its CTA
 // computes on a copy of t[0] and stores nothing).  Each pair runs on four
-// CTAs: two per half of d_v.
+// CTAs: two per half of d_v.  `skip` packs the request's segments
+// [skip & 0xffff, skip >> 16) that lie wholly between the two key ranges
+// (0 = none), for the key walk to jump over.
 struct TcPair {
   TcTile t[2];
   int32_t key_hi;
   int32_t win_lo;
   int32_t sink_hi;
-  int32_t pad;
+  int32_t skip;
 };
 
 struct KernelArgs {
