@@ -57,17 +57,17 @@ constexpr uint32_t CHUNK = 16384;          // 128 rows x 64 bf16
 constexpr uint32_t HCHUNK = 8192;          // 64 rows x 64 bf16
 constexpr int THREADS = 256;   // warps 6 and 7: the rope writers of the score pair
 
-// S pair: rotated q_rope hi and lo (K-major operands), a staging buffer for
-// P and the records, the key ring
+// S pair: rotated q_rope hi and lo (K-major operands), three staging slots
+// for P halves (64 keys x 128 lanes each), the key ring
 constexpr uint32_t OFF_ROPE = 0;
 constexpr uint32_t PBUF = 2 * CHUNK;       // 128 lanes x 128 keys bf16, two 64-key chunks
 constexpr uint32_t RBUF = 128 * 8;         // (alpha, l) per lane, after P
-constexpr uint32_t PREC_BYTES = PBUF + RBUF;
 constexpr uint32_t PSTRIDE = PBUF + 2048;  // 1024-aligned buffers
 constexpr uint32_t OFF_STG = 2 * CHUNK;
+constexpr int NSTG = 3;                    // staging slots; half k of the walk uses slot k % 3
 constexpr int KRING = 2;
 constexpr uint32_t KSLOT = 9 * HCHUNK;     // 64 keys x up to 9 chunks: one box per key tile
-constexpr uint32_t OFF_KRING = OFF_STG + PSTRIDE;
+constexpr uint32_t OFF_KRING = OFF_STG + NSTG * CHUNK;
 // O pair: two P + record buffers, the V ring (128 keys x 4 chunks per slot)
 constexpr uint32_t OFF_P = 0;
 constexpr int VRING = 2;
@@ -80,6 +80,7 @@ constexpr uint32_t OFF_OSTG = 0, OSTRIDE = 1040;
 constexpr uint32_t OFF_BAR = OFF_KRING + KRING * KSLOT;
 static_assert(OFF_KRING % 1024 == 0 && OFF_VRING % 1024 == 0, "operand alignment");
 static_assert(OFF_VRING + VRING * VSLOT <= OFF_BAR, "O-pair layout");
+static_assert(OFF_STG + 4 * 4096 <= OFF_KRING, "query transposition slices");
 static_assert(OFF_OSTG + 128 * OSTRIDE <= OFF_VRING + VRING * VSLOT, "output staging");
 enum {
   B_KFULL = 0,
@@ -97,14 +98,12 @@ enum {
   B_PEMPTY,             // 2 (S CTAs): P buffer consumed by the output MMAs
   B_VFULL = B_PEMPTY + 2,
   B_VEMPTY = B_VFULL + VRING,
-  B_PFULL = B_VEMPTY + VRING,  // 2 (O CTAs): P and records copied in
-  B_PREADY = B_PFULL + 2,      // 2: O rescaled where needed, P buffer ready for the MMAs
+  // 2 + 2 (O CTAs): P keys 0-63 copied in; P keys 64-127 and the records in
+  B_PFULL0 = B_VEMPTY + VRING,
+  B_PFULL1 = B_PFULL0 + 2,
+  B_PREADY = B_PFULL1 + 2,     // 2: O rescaled where needed, P buffer ready for the MMAs
   B_ODONE = B_PREADY + 2,
   B_OFINAL,
-  B_STGFREE,  // (S CTAs) the last bulk copy of P has landed: the staging buffer
-              // may be rewritten (one arrival per tile from the output CTA's
-              // warp 6; a copy that completes on the receiver's barrier is not
-              // covered by the sender's bulk-group waits)
   NBAR
 };
 constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
@@ -179,7 +178,8 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
       tc::mbar_init(&bar[B_SFULL + b], 1);
       tc::mbar_init(&bar[B_SFREE + b], 2 * 4);
       tc::mbar_init(&bar[B_PEMPTY + b], 1);
-      tc::mbar_init(&bar[B_PFULL + b], 1);
+      tc::mbar_init(&bar[B_PFULL0 + b], 1);
+      tc::mbar_init(&bar[B_PFULL1 + b], 1);
       tc::mbar_init(&bar[B_PREADY + b], 2 * 4);
     }
     tc::mbar_init(&bar[B_ROPE], 2 * 2);
@@ -188,10 +188,13 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
     tc::mbar_init(&bar[B_SFINAL], 1);
     tc::mbar_init(&bar[B_ODONE], 1);
     tc::mbar_init(&bar[B_OFINAL], 1);
-    tc::mbar_init(&bar[B_STGFREE], 1);
     misc[1] = 0;
+    misc[2] = 0;  // S CTAs: P halves of the walk landed at the output CTA, in order
     if (!spair)  // each P buffer expects one bulk copy per use; armed one use ahead
-      for (int b = 0; b < 2; ++b) tc::mbar_arrive_expect_tx(&bar[B_PFULL + b], PREC_BYTES);
+      for (int b = 0; b < 2; ++b) {
+        tc::mbar_arrive_expect_tx(&bar[B_PFULL0 + b], CHUNK);
+        tc::mbar_arrive_expect_tx(&bar[B_PFULL1 + b], CHUNK + RBUF);
+      }
     tc::fence_barrier_init();
   }
   if (warp == 1) {
@@ -513,28 +516,33 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
           }
           l_run = l_run * alpha + ((ls4[0] + ls4[1]) + (ls4[2] + ls4[3]));
           // the O pair's P buffer b is free once the output MMAs of tile
-          // j - 2 are done; the staging buffer once the copy of tile j - 1
-          // has read it
+          // j - 2 are done
           okw = __all_sync(0xffffffffu, wait_bar(c, B_PEMPTY + b, ((j >> 1) & 1) ^ 1));
-          // the staging buffer is free once the copy of tile j - 1 has landed
-          if (okw && issuer && j > 0) okw = wait_bar<true>(c, B_STGFREE, (j - 1) & 1);
+          // P half k = 2j + h of the walk is staged in slot k % 3, whose last
+          // copy (half k - 3) must have landed: a shared::cta ->
+          // shared::cluster bulk copy completes on the receiver's barrier
+          // only, so the output CTA counts the halves that have landed
+          if (okw && issuer && j > 0) okw = wait_count(c, &misc[2], static_cast<uint32_t>(2 * j - 1));
         }
         ok = tc::named_and(1, 128, okw);
         if (!ok) break;
-        uint8_t* stg = sm + OFF_STG;
-        // lane m's 128 keys: two 64-key chunks of 8 16-byte units, 128-byte swizzle
+        const int k0 = (2 * j) % NSTG;
+        uint8_t* stg[2] = {sm + OFF_STG + k0 * CHUNK, sm + OFF_STG + (k0 == NSTG - 1 ? 0 : k0 + 1) * CHUNK};
+        // lane m's 128 keys: two 64-key halves of 8 16-byte units, 128-byte swizzle
 #pragma unroll
         for (int h = 0; h < 2; ++h)
 #pragma unroll
           for (int u = 0; u < 8; ++u)
-            *reinterpret_cast<uint4*>(stg + h * CHUNK + m * 128 + ((u ^ sw) << 4)) =
+            *reinterpret_cast<uint4*>(stg[h] + m * 128 + ((u ^ sw) << 4)) =
                 make_uint4(s[h][4 * u], s[h][4 * u + 1], s[h][4 * u + 2], s[h][4 * u + 3]);
-        *reinterpret_cast<float2*>(stg + PBUF + m * 8) = make_float2(alpha, l_run);
+        // the lane's record goes straight to the output CTA, counted with the second half
+        const uint32_t pdst = tc::mapa_shared(smem_u32(sm + OFF_P + b * PSTRIDE), orank);
+        tc::st_async_v2f32(pdst + PBUF + m * 8, alpha, l_run, cbar(B_PFULL1 + b, orank));
         tc::fence_proxy_async();
         tc::named_sync(1, 128);
         if (issuer) {
-          tc::bulk_copy_to_cluster(tc::mapa_shared(smem_u32(sm + OFF_P + b * PSTRIDE), orank),
-                                   smem_u32(stg), PREC_BYTES, cbar(B_PFULL + b, orank));
+          tc::bulk_copy_to_cluster(pdst, smem_u32(stg[0]), CHUNK, cbar(B_PFULL0 + b, orank));
+          tc::bulk_copy_to_cluster(pdst + CHUNK, smem_u32(stg[1]), CHUNK, cbar(B_PFULL1 + b, orank));
         }
         ++j;
         kt = nx;
@@ -613,17 +621,22 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
         tc::mma_commit_2sm(&bar[B_OFINAL], 0xC);
       }
     } else if (warp == 6) {
-      // ---------------- O pair: releases the sender's P staging buffer ---
-      // as soon as each copy has landed (a thread of its own, so that the
-      // release never waits for the rescale / turn work of the lanes).  It
-      // cannot fall two phases behind on a P buffer: the copy of tile j + 2
-      // is sent only after the release of tile j + 1.
+      // ------------- O pair: counts the sender's P halves that have landed
+      // (a thread of its own, so that the count never waits for the rescale
+      // / turn work of the lanes), with a release store into the sender's
+      // counter.  It cannot fall two phases behind on a P barrier: tile
+      // j + 2 is sent only after the count has passed tile j + 1's first half.
       if (lane == 0) {
         int j = 0;
         KeyTile kt{0, 0, 0, -1};
         bool have = next_key_tile<TNK>(kt, segs, nseg, 0, r0hi, r1lo, r1hi, skip);
-        while (have && wait_bar<true>(c, B_PFULL + (j & 1), (j >> 1) & 1)) {
-          tc::mbar_arrive_cluster(cbar(B_STGFREE, crank - 2));
+        const uint32_t cnt = tc::mapa_shared(smem_u32(&misc[2]), crank - 2);
+        while (have) {
+          const uint32_t par = (j >> 1) & 1;
+          if (!wait_bar<true>(c, B_PFULL0 + (j & 1), par)) break;
+          tc::st_release_cluster_u32(cnt, static_cast<uint32_t>(2 * j + 1));
+          if (!wait_bar<true>(c, B_PFULL1 + (j & 1), par)) break;
+          tc::st_release_cluster_u32(cnt, static_cast<uint32_t>(2 * j + 2));
           ++j;
           have = next_key_tile<TNK>(kt, segs, nseg, 0, r0hi, r1lo, r1hi, skip);
         }
@@ -645,14 +658,18 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
       int seg_frame = kt.j;
       while (ok && have) {
         const int b = j & 1;
-        ok = __all_sync(0xffffffffu, wait_bar<true>(c, B_PFULL + b, (j >> 1) & 1));
+        ok = __all_sync(0xffffffffu, wait_bar<true>(c, B_PFULL0 + b, (j >> 1) & 1) &&
+                                         wait_bar<true>(c, B_PFULL1 + b, (j >> 1) & 1));
         if (!ok) break;
         const volatile float* rp =
             reinterpret_cast<const volatile float*>(sm + OFF_P + b * PSTRIDE + PBUF + m * 8);
         const float alpha = rp[0];
         l_fin = rp[1];
         // arm buffer b for tile j + 2 (its copy starts after the MMAs of tile j)
-        if (m == 0) tc::mbar_arrive_expect_tx(&bar[B_PFULL + b], PREC_BYTES);
+        if (m == 0) {
+          tc::mbar_arrive_expect_tx(&bar[B_PFULL0 + b], CHUNK);
+          tc::mbar_arrive_expect_tx(&bar[B_PFULL1 + b], CHUNK + RBUF);
+        }
         const bool scale = __any_sync(0xffffffffu, alpha != 1.f);
         const bool turn = VROPE && kt.j != seg_frame;
         if (scale || turn) {

@@ -211,6 +211,33 @@ __device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst, uint32_t src,
       ::"r"(dst), "r"(src), "r"(bytes), "r"(bar)
       : "memory");
 }
+// 8-byte asynchronous store into the shared memory of a CTA of the cluster
+// (`addr`), completing 8 bytes on that CTA's barrier `bar` (both addresses
+// in the shared::cluster window of the same CTA).
+__device__ __forceinline__ void st_async_v2f32(uint32_t addr, float x, float y, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];"
+               ::"r"(addr), "f"(x), "f"(y), "r"(bar)
+               : "memory");
+}
+// Release store (cluster scope) of a 32-bit word into the shared memory of a
+// CTA of the cluster.
+__device__ __forceinline__ void st_release_cluster_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.release.cluster.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+// Relaxed load (cluster scope) of a 32-bit word of this CTA's shared memory.
+__device__ __forceinline__ uint32_t ld_relaxed_cluster_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.cluster.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+  return v;
+}
+// Acquire fence (cluster scope) restricted to shared-memory operations: after
+// a relaxed read that observed a release made through this CTA's shared
+// memory by another CTA of the cluster, later shared-memory accesses are
+// ordered after it.  Unlike a full cluster-scope acquire it leaves the L1
+// contents alone.
+__device__ __forceinline__ void fence_acquire_cluster_smem() {
+  asm volatile("fence.acquire.sync_restrict::shared::cluster.cluster;" ::: "memory");
+}
 // Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned)
 // from this CTA's shared memory to global memory, tracked by bulk groups.
 __device__ __forceinline__ void bulk_store_global(void* dst, uint32_t src, uint32_t bytes) {
@@ -246,12 +273,15 @@ __device__ __forceinline__ bool named_and(uint32_t id, uint32_t count, bool v) {
 __device__ __forceinline__ void fence_proxy_async_cluster() {
   asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
 }
-// Wait on a local barrier with acquire semantics at cluster scope (for
-// phases completed by arrivals from other CTAs that publish data).
+// Relaxed test of a local barrier's phase at cluster scope (phases completed
+// by arrivals from other CTAs that publish data); a caller that sees the
+// phase complete closes with fence_acquire_cluster_smem(), which orders its
+// later shared-memory accesses after those CTAs' releases without the L1
+// invalidation of a full cluster-scope acquire.
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.relaxed.cluster.shared::cta.b64 p, [%1], %2;\n"
       " selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
       : "r"(smem_u32(bar)), "r"(parity)

@@ -20,8 +20,9 @@ struct Ctx {
 // Bounded wait for the phase with `parity` of barrier i; also gives up as
 // soon as another role of this CTA, or any CTA of the launch, has recorded
 // an error.  On expiry records RK_ERR_DEVICE_TIMEOUT.
-// CLUSTER: acquire at cluster scope (the phase is completed by arrivals
-// from other CTAs that publish shared-memory data).
+// CLUSTER: the phase is completed by arrivals from other CTAs that publish
+// shared-memory data: relaxed polls at cluster scope, then a shared-memory
+// acquire fence at cluster scope.
 template <bool CLUSTER = false>
 __device__ __forceinline__ bool wait_bar(const Ctx& c, int i, uint32_t parity,
                                          uint64_t limit_ns = WAIT_NS) {
@@ -44,6 +45,35 @@ __device__ __forceinline__ bool wait_bar(const Ctx& c, int i, uint32_t parity,
       }
     }
   }
+  if (CLUSTER) tc::fence_acquire_cluster_smem();
+  return true;
+}
+
+// Bounded wait until the monotonic counter `cnt` (in this CTA's shared
+// memory, written by release stores from other CTAs of the cluster) reaches
+// `need`, polled with relaxed loads and closed by a shared-memory acquire
+// fence; the same give-up rules as wait_bar.
+__device__ __forceinline__ bool wait_count(const Ctx& c, const uint32_t* cnt, uint32_t need,
+                                           uint64_t limit_ns = WAIT_NS) {
+  uint32_t it = 0;
+  uint64_t t0 = 0;
+  while (tc::ld_relaxed_cluster_u32(cnt) < need) {
+    if ((++it & 63u) == 0) {
+      if (*c.abort || *reinterpret_cast<volatile int32_t*>(c.status)) {
+        *c.abort = 1;
+        return false;
+      }
+      const uint64_t now = tc::global_ns();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > limit_ns) {
+        *c.abort = 1;
+        atomicCAS(c.status, 0, static_cast<int32_t>(RK_ERR_DEVICE_TIMEOUT));
+        return false;
+      }
+    }
+  }
+  tc::fence_acquire_cluster_smem();
   return true;
 }
 
