@@ -199,7 +199,10 @@ void rk_seg_attn_plan_destroy(rk_seg_attn_plan_t plan);
 /* Fill *info with the plan's counts.  Host only; errors: RK_ERR_NULL. */
 rk_status_t rk_seg_attn_plan_info(rk_seg_attn_plan_t plan, rk_plan_info_t* info);
 
-/* Bytes of device workspace rk_seg_attn_forward needs (0 if none). */
+/* Bytes of device workspace rk_seg_attn_forward needs (0 if none): the
+ * partial outputs of split decode rows, and for plans on the 4-CTA prefill
+ * kernel (kernel 3) the work queues its persistent clusters claim tile pairs
+ * from (about 166 KB). */
 size_t rk_seg_attn_workspace_bytes(rk_seg_attn_plan_t plan);
 
 /* Segment-relocated attention over the plan's segments (paper,

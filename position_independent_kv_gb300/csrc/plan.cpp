@@ -648,6 +648,7 @@ static rk_status_t build_plan(const rk_seg_attn_desc_t* d, rk_seg_attn_plan_s* p
   info.split_chunks = static_cast<int64_t>(p->chunks.size());
   p->num_parts = parts;
   p->num_mgroups = mgroups;
+  size_t wbytes = 0;
   if (parts) {
     const size_t dv = p->d_v;
     size_t bytes = 0;
@@ -655,8 +656,14 @@ static rk_status_t build_plan(const rk_seg_attn_desc_t* d, rk_seg_attn_plan_s* p
     bytes += static_cast<size_t>(parts) * kSplitHeads * sizeof(float);
     bytes = (bytes + 255) & ~size_t(255);
     bytes += static_cast<size_t>(mgroups) * sizeof(int32_t);
-    p->workspace_bytes = (bytes + 255) & ~size_t(255);
+    wbytes = (bytes + 255) & ~size_t(255);
   }
+  // the 4-CTA kernel's work queues: one per launch that may run at once
+  // (the host-buffer forward launches one per row range)
+  p->queue_off = wbytes;
+  if (p->kernel == 3 && !p->tc_pairs.empty())
+    wbytes += static_cast<size_t>(rk_seg_attn_plan_s::kHostChunks) * rk::kQueueBytes;
+  p->workspace_bytes = wbytes;
   return RK_OK;
 }
 
@@ -800,17 +807,23 @@ namespace rk {
 
 rk_status_t bind_workspace(const rk_seg_attn_plan_s& p, KernelArgs& a, void* workspace,
                            cudaStream_t s) {
-  if (!p.num_parts) return RK_OK;
   char* w = static_cast<char*>(workspace);
-  a.ws_o = reinterpret_cast<float*>(w);
-  size_t off = static_cast<size_t>(p.num_parts) * kSplitHeads * p.d_v * sizeof(float);
-  a.ws_lse = reinterpret_cast<float*>(w + off);
-  off += static_cast<size_t>(p.num_parts) * kSplitHeads * sizeof(float);
-  off = (off + 255) & ~size_t(255);
-  a.ws_ticket = reinterpret_cast<int32_t*>(w + off);
-  return cudaMemsetAsync(a.ws_ticket, 0, p.num_mgroups * sizeof(int32_t), s) == cudaSuccess
-             ? RK_OK
-             : RK_ERR_CUDA;
+  if (p.num_parts) {
+    a.ws_o = reinterpret_cast<float*>(w);
+    size_t off = static_cast<size_t>(p.num_parts) * kSplitHeads * p.d_v * sizeof(float);
+    a.ws_lse = reinterpret_cast<float*>(w + off);
+    off += static_cast<size_t>(p.num_parts) * kSplitHeads * sizeof(float);
+    off = (off + 255) & ~size_t(255);
+    a.ws_ticket = reinterpret_cast<int32_t*>(w + off);
+    if (cudaMemsetAsync(a.ws_ticket, 0, p.num_mgroups * sizeof(int32_t), s) != cudaSuccess)
+      return RK_ERR_CUDA;
+  }
+  if (p.kernel == 3 && !p.tc_pairs.empty()) {
+    a.wq = reinterpret_cast<unsigned long long*>(w + p.queue_off);
+    const size_t qb = static_cast<size_t>(rk_seg_attn_plan_s::kHostChunks) * kQueueBytes;
+    if (cudaMemsetAsync(a.wq, 0, qb, s) != cudaSuccess) return RK_ERR_CUDA;
+  }
+  return RK_OK;
 }
 
 }  // namespace rk
@@ -909,6 +922,7 @@ extern "C" rk_status_t rk_seg_attn_forward_host(rk_seg_attn_plan_t p, const void
         ac.tc_pairs = p->d_tc_pairs_chunked + b;
         ac.num_tc_pairs = e - b;
         ac.num_chunks = 0;
+        if (a.wq) ac.wq = a.wq + static_cast<size_t>(c) * (rk::kQueueBytes / 8);  // a queue per range
         good = ok(p->kernel == 3 ? rk::launch_dense_tc4(*p, ac, q, cs)
                                  : rk::launch_dense_tc2(*p, ac, q, cs));
       }

@@ -99,6 +99,13 @@ struct TcPair {
   int32_t skip;
 };
 
+// Work queue of one launch of the persistent 4-CTA kernel: a claim counter
+// (word 0) and, from word 32 on, a ring of kQueueRing claimed items for each
+// of up to kQueueClusters clusters.
+constexpr int kQueueClusters = 40;
+constexpr int kQueueRing = 64;
+constexpr size_t kQueueBytes = 256 + static_cast<size_t>(kQueueClusters) * kQueueRing * 8;
+
 struct KernelArgs {
   const uint16_t* q;
   uint16_t* out;
@@ -134,6 +141,7 @@ struct KernelArgs {
   int32_t d_v;                // output columns
   const float* pos_cs_hi;     // [T / 256 + 1][d_rope/2][2] cos, sin of 256 a theta   (v_rope)
   const float* pos_cs_lo;     // [256][d_rope/2][2] cos, sin of b theta              (v_rope)
+  unsigned long long* wq;     // work queue of the 4-CTA kernel (kQueueBytes, zeroed)
 };
 
 }  // namespace rk
@@ -188,6 +196,7 @@ struct rk_seg_attn_plan_s {
   uint8_t* d_head_role = nullptr;
   int32_t* d_status = nullptr;
   size_t workspace_bytes = 0;
+  size_t queue_off = 0;       // the 4-CTA kernel's work queues (kHostChunks of kQueueBytes)
   // when a forward has both split chunks and prefill tiles, the tiles run on
   // this plan-owned stream, forked from and joined back to the caller's
   cudaStream_t side = nullptr;

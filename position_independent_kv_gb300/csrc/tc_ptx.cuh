@@ -224,6 +224,15 @@ __device__ __forceinline__ void st_async_v2f32(uint32_t addr, float x, float y, 
 __device__ __forceinline__ void st_release_cluster_u32(uint32_t addr, uint32_t v) {
   asm volatile("st.release.cluster.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
+// Release store / acquire load (device scope) of a 64-bit word of global memory.
+__device__ __forceinline__ void st_release_gpu_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_acquire_gpu_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
 // Relaxed load (cluster scope) of a 32-bit word of this CTA's shared memory.
 __device__ __forceinline__ uint32_t ld_relaxed_cluster_u32(const uint32_t* p) {
   uint32_t v;
@@ -237,6 +246,10 @@ __device__ __forceinline__ uint32_t ld_relaxed_cluster_u32(const uint32_t* p) {
 // contents alone.
 __device__ __forceinline__ void fence_acquire_cluster_smem() {
   asm volatile("fence.acquire.sync_restrict::shared::cluster.cluster;" ::: "memory");
+}
+// Prefetch `bytes` (a multiple of 16, 16-byte aligned) of global memory into L2.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 // Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned)
 // from this CTA's shared memory to global memory, tracked by bulk groups.

@@ -195,7 +195,11 @@ def test_vrope_plan_rules():
     assert pd.info["split_chunks"] == pn.info["split_chunks"] > 0
     parts = pd.info["split_chunks"]
     body = ((parts * 8 * 512 * 4 + parts * 8 * 4 + 255) // 256) * 256
-    assert body < pd.workspace_bytes <= body + 256 + 4 * parts
+    # plus the 4-CTA kernel's work queues (its Local tiles): 8 launches' worth
+    # of a claim counter and 40 clusters' 64-entry rings
+    queue = 8 * (256 + 40 * 64 * 8)
+    assert pd.info["kernel"] == 3
+    assert body + queue < pd.workspace_bytes <= body + 256 + 4 * parts + queue
 
 
 @pytest.mark.parametrize("name", ["edge_sink0_w0", "edge_tiny_decode", "edge_h8", "edge_many_segs"])

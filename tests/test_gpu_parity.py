@@ -154,7 +154,8 @@ def test_plan_reuse_and_stream():
         out, lse = wl.out_init.clone(), wl.lse_init.clone()
         s.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(s):
-            plan.forward(wl.q, out, lse, None, stream=s)
+            ws = torch.empty(max(16, plan.workspace_bytes), dtype=torch.uint8, device="cuda")
+            plan.forward(wl.q, out, lse, ws, stream=s)
         s.synchronize()
         ref = oracle_rows(wl, prot)
         rows = [np.arange(r.q_row_begin, r.T) for r in wl.requests]

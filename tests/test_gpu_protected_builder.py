@@ -108,7 +108,8 @@ def test_plan_takes_the_device_bitmap():
     plan2 = B.SegAttnPlan.from_workload(wl, bitmap=d_bits, flags=B.RK_PLAN_DEVICE_BITMAP)
     out = wl.out_init.clone()
     lse = wl.lse_init.clone()
-    plan2.forward(wl.q, out, lse)
+    ws = torch.empty(max(16, plan2.workspace_bytes), dtype=torch.uint8, device="cuda")
+    plan2.forward(wl.q, out, lse, ws)
     torch.cuda.synchronize()
     assert torch.equal(out, out_h) and torch.equal(lse, lse_h)
     assert plan2.info["protected_local_rows"] == plan.info["protected_local_rows"]
