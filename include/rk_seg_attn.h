@@ -199,6 +199,21 @@ void rk_seg_attn_plan_destroy(rk_seg_attn_plan_t plan);
 /* Fill *info with the plan's counts.  Host only; errors: RK_ERR_NULL. */
 rk_status_t rk_seg_attn_plan_info(rk_seg_attn_plan_t plan, rk_plan_info_t* info);
 
+/* Diagnostics: the tile pairs of a plan on the 4-CTA prefill kernel (kernel
+ * 3), in the plan's order (longest first), RK_PAIR_WORDS int32 per pair:
+ *   [0..7]   tile 0: request, kind (0 Global rows x Global heads, 1 one or
+ *            two protected rows x every head), p0, p1, key_hi, win_lo,
+ *            sink_hi, flags (bit 0: a partner without work)
+ *   [8..15]  tile 1, the same
+ *   [16..18] the pair's key ranges: key_hi, win_lo, sink_hi (keys
+ *            [0, sink_hi) u [win_lo, key_hi), absolute within the request)
+ *   [19]     segment skip: the request's segments [skip & 0xffff, skip >> 16)
+ *            meet neither range (0: none)
+ * Copies min(count, capacity) pairs to `out` (host memory; may be NULL when
+ * capacity is 0) and returns the count, or -1 for a NULL plan.  Host only. */
+#define RK_PAIR_WORDS 20
+int64_t rk_seg_attn_plan_pairs(rk_seg_attn_plan_t plan, int32_t* out, int64_t capacity);
+
 /* Bytes of device workspace rk_seg_attn_forward needs (0 if none): the
  * partial outputs of split decode rows, and for plans on the 4-CTA prefill
  * kernel (kernel 3) the work queues its persistent clusters claim tile pairs

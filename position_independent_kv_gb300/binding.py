@@ -24,6 +24,7 @@ RK_PLAN_V_ROPE = 32
 RK_PROT_NONE = 1
 
 EXPORTS = ["rk_seg_attn_plan", "rk_seg_attn_plan_destroy", "rk_seg_attn_plan_info",
+           "rk_seg_attn_plan_pairs",
            "rk_seg_attn_workspace_bytes", "rk_seg_attn_forward", "rk_lse_merge",
            "rk_seg_attn_last_device_status", "rk_status_string",
            "rk_seg_attn_forward_noalloc", "rk_seg_attn_forward_host",
@@ -120,6 +121,8 @@ def lib() -> C.CDLL:
         L.rk_seg_attn_plan_destroy.restype = None
         L.rk_seg_attn_plan_info.argtypes = [C.c_void_p, C.POINTER(RkPlanInfo)]
         L.rk_seg_attn_plan_info.restype = C.c_int
+        L.rk_seg_attn_plan_pairs.argtypes = [C.c_void_p, C.c_void_p, C.c_int64]
+        L.rk_seg_attn_plan_pairs.restype = C.c_int64
         L.rk_seg_attn_workspace_bytes.argtypes = [C.c_void_p]
         L.rk_seg_attn_workspace_bytes.restype = C.c_size_t
         L.rk_seg_attn_forward.argtypes = [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
@@ -252,6 +255,16 @@ class SegAttnPlan:
         inf = RkPlanInfo()
         _check(lib().rk_seg_attn_plan_info(self._h, C.byref(inf)), "rk_seg_attn_plan_info")
         return inf.as_dict()
+
+    def pairs(self):
+        """rk_seg_attn_plan_pairs: int32 [n, RK_PAIR_WORDS] records of the
+        4-CTA kernel's tile pairs, in the plan's order."""
+        import numpy as np
+        n = int(lib().rk_seg_attn_plan_pairs(self._h, None, 0))
+        buf = np.zeros((max(n, 0), 20), dtype=np.int32)
+        if n > 0:
+            lib().rk_seg_attn_plan_pairs(self._h, buf.ctypes.data, n)
+        return buf
 
     @property
     def workspace_bytes(self) -> int:

@@ -799,6 +799,15 @@ extern "C" rk_status_t rk_seg_attn_plan_info(rk_seg_attn_plan_t p, rk_plan_info_
   return RK_OK;
 }
 
+extern "C" int64_t rk_seg_attn_plan_pairs(rk_seg_attn_plan_t p, int32_t* out, int64_t capacity) {
+  if (!p) return -1;
+  static_assert(sizeof(TcPair) == RK_PAIR_WORDS * sizeof(int32_t), "pair record");
+  const int64_t n = static_cast<int64_t>(p->tc_pairs.size());
+  const int64_t m = std::min(n, std::max<int64_t>(capacity, 0));
+  if (m > 0 && out) std::memcpy(out, p->tc_pairs.data(), static_cast<size_t>(m) * sizeof(TcPair));
+  return n;
+}
+
 extern "C" size_t rk_seg_attn_workspace_bytes(rk_seg_attn_plan_t p) {
   return p ? p->workspace_bytes : 0;
 }
