@@ -83,6 +83,17 @@ typedef enum {
                                    one pair per half of d_v, instead of
                                    4-CTA clusters (scores on one CTA pair,
                                    outputs on the other) */
+#define RK_PLAN_NO_SIDE_PAIRS 64u /* run every tile pair on the 4-CTA
+                                   clusters.  By default, on a GPU whose SMs
+                                   do not divide into 4-CTA clusters, a
+                                   persistent CTA-pair kernel on the SMs the
+                                   clusters leave free (a second stream, forked
+                                   from and joined back to the caller's) takes
+                                   the shortest pairs (at most 8 key tiles)
+                                   from the back of the same work list, with
+                                   the same arithmetic, so the results are the
+                                   same either way.  Set this when other work
+                                   is meant to use those SMs meanwhile. */
 #define RK_PLAN_V_ROPE 32u      /* the value carries a rotary part: V is the
                                    whole packed latent row [c_nope | k_rope]
                                    (d_v = d_k).  Each segment's contribution
@@ -176,6 +187,10 @@ typedef struct {
                                 4 = tcgen05 tiles for small heads (d_nope 128,
                                     d_rope 32), one CTA per tile */
   int32_t d_v;               /* output columns: d_nope, or d_k with RK_PLAN_V_ROPE */
+  int64_t side_pairs;        /* kernel 3: tile pairs at the end of the work list
+                                (at most 8 key tiles each) that the side kernel
+                                beside the 4-CTA clusters may take; 0 with
+                                RK_PLAN_NO_SIDE_PAIRS or RK_PLAN_V_ROPE */
 } rk_plan_info_t;
 
 /* Build an immutable, reusable plan for one request bundle geometry

@@ -21,6 +21,7 @@ RK_PLAN_SINGLE_CTA = 4
 RK_PLAN_CTA_PAIR = 8
 RK_PLAN_DEVICE_BITMAP = 16
 RK_PLAN_V_ROPE = 32
+RK_PLAN_NO_SIDE_PAIRS = 64
 RK_PROT_NONE = 1
 
 EXPORTS = ["rk_seg_attn_plan", "rk_seg_attn_plan_destroy", "rk_seg_attn_plan_info",
@@ -83,7 +84,7 @@ class RkPlanInfo(C.Structure):
                 ("dense_tiles", C.c_int64), ("split_chunks", C.c_int64),
                 ("pairs_global", C.c_int64), ("pairs_local", C.c_int64),
                 ("performed_pairs", C.c_int64), ("latent_bytes", C.c_int64),
-                ("kernel", C.c_int32), ("d_v", C.c_int32)]
+                ("kernel", C.c_int32), ("d_v", C.c_int32), ("side_pairs", C.c_int64)]
 
     def as_dict(self) -> dict:
         return {k: getattr(self, k) for k, _ in self._fields_}

@@ -21,8 +21,8 @@ LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "librk_seg_attn.so")
 
 SOURCES = ["plan.cpp", "dense_mma.cu", "split_decode.cu", "dense_tc.cu", "dense_tc2.cu",
-           "dense_tc4.cu", "dense_tcs.cu", "noalloc.cu", "protected.cu", "project.cu",
-           "seg_paged.cu"]
+           "dense_tc4.cu", "dense_side.cu", "dense_tcs.cu", "noalloc.cu", "protected.cu",
+           "project.cu", "seg_paged.cu"]
 # test-only library: single-CTA checks of the tensor-path building blocks
 SELFTEST_SOURCES = ["tc_selftest.cu"]
 SELFTEST_LIB = os.path.join(LIBDIR, "librk_tc_selftest.so")

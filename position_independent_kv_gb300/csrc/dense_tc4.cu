@@ -143,52 +143,15 @@ __device__ __forceinline__ Item load_item(const KernelArgs& a, int idx, uint32_t
 }
 // Items are claimed dynamically: the score CTA of rank 0 (its TMA producer,
 // which runs ahead of every other role) takes the next pair index from the
-// launch's counter (the plan orders pairs longest first) and publishes it in
-// its cluster's ring as (k + 1) << 32 | index for item k of the walk; every
-// other role reads the ring.  An index >= npairs ends the walk.
+// front of the launch's counter (the plan orders pairs longest first; the
+// side kernel takes pairs from the back) and publishes it in its cluster's
+// ring as (k + 1) << 32 | index for item k of the walk; every other role
+// reads the ring.  An index >= npairs (0xffffffff) ends the walk.
 __device__ __forceinline__ unsigned long long* ring_of(unsigned long long* wq) {
-  return wq + 32 + static_cast<size_t>(blockIdx.x >> 2) * kQueueRing;
-}
-// Pair index of item k of this cluster's walk, -1 past its end (or when the
-// bounded wait gives up, with the status recorded).  Called once per item and
-// role, so kept out of line (the roles' tile loops need their registers).
-__device__ __noinline__ int claimed(const Ctx c, unsigned long long* wq, int k, int npairs) {
-  const unsigned long long* e = ring_of(wq) + (k & (kQueueRing - 1));
-  const unsigned long long tag = static_cast<unsigned long long>(k + 1);
-  uint32_t it = 0;
-  uint64_t t0 = 0;
-  while (true) {
-    const unsigned long long v = tc::ld_acquire_gpu_u64(e);
-    if ((v >> 32) == tag) {
-      const uint32_t idx = static_cast<uint32_t>(v);
-      return idx < static_cast<uint32_t>(npairs) ? static_cast<int>(idx) : -1;
-    }
-    if ((++it & 63u) == 0) {
-      if (*c.abort || *reinterpret_cast<volatile int32_t*>(c.status)) {
-        *c.abort = 1;
-        return -1;
-      }
-      const uint64_t now = tc::global_ns();
-      if (t0 == 0) {
-        t0 = now;
-      } else if (now - t0 > tt::WAIT_NS) {
-        *c.abort = 1;
-        atomicCAS(c.status, 0, static_cast<int32_t>(RK_ERR_DEVICE_TIMEOUT));
-        return -1;
-      }
-    }
-  }
+  return tt::queue_ring<4, 0>(wq);
 }
 __device__ __forceinline__ bool next_tile(KeyTile& kt, const Item& I) {
   return next_key_tile<TNK>(kt, I.segs, I.nseg, 0, I.r0hi, I.r1lo, I.r1hi, I.skip);
-}
-
-// Bit i set for each offset base + i (i < 32) inside [lo, hi).
-__device__ __forceinline__ uint32_t span_bits(int lo, int hi, int base) {
-  const int l = min(max(lo - base, 0), 32), h = min(max(hi - base, 0), 32);
-  const uint32_t mh = h >= 32 ? 0xffffffffu : ((1u << h) - 1u);
-  const uint32_t ml = l >= 32 ? 0xffffffffu : ((1u << l) - 1u);
-  return mh & ~ml;
 }
 
 // Turn the 16 rope pairs held in o[0..31] (32 consecutive output columns:
@@ -308,12 +271,20 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
             // have finished item - 48
             if (item >= 48) ok = wait_count(c, &misc[3], static_cast<uint32_t>(item - 47));
             if (!ok) break;
-            const uint32_t got = atomicAdd(reinterpret_cast<unsigned int*>(a.wq), 1u);
+            // the next pair from the front of the list, unless the side
+            // kernel has taken it from the back (it takes at most the
+            // num_side_pairs shortest ones)
+            const unsigned long long old = atomicAdd(a.wq, 1ull);
+            const uint32_t front = static_cast<uint32_t>(old);
+            const uint32_t back = static_cast<uint32_t>(old >> 32);
+            const uint32_t taken = min(back, static_cast<uint32_t>(a.num_side_pairs));
+            idx = static_cast<uint64_t>(front) + taken < static_cast<uint64_t>(npairs)
+                      ? static_cast<int>(front) : -1;
             tc::st_release_gpu_u64(ring_of(a.wq) + (item & (kQueueRing - 1)),
-                                   (static_cast<unsigned long long>(item + 1) << 32) | got);
-            idx = got < static_cast<uint32_t>(npairs) ? static_cast<int>(got) : -1;
+                                   (static_cast<unsigned long long>(item + 1) << 32) |
+                                       static_cast<uint32_t>(idx));
           } else {
-            idx = claimed(c, a.wq, item, a.num_tc_pairs);
+            idx = tt::claimed<4, 0>(c, a.wq, item, a.num_tc_pairs);
           }
           if (idx < 0) break;
           const Item I = load_item(a, idx, r);
@@ -358,7 +329,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
         int j = 0;
         bool ok = true;
         for (int item = 0; ok; ++item) {
-          const int idx = claimed(c, a.wq, item, a.num_tc_pairs);
+          const int idx = tt::claimed<4, 0>(c, a.wq, item, a.num_tc_pairs);
           if (idx < 0) break;
           const Item I = load_item(a, idx, 0);
           // the item's queries are in tensor memory and its first q_rope' is written
@@ -422,7 +393,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
       const int m0 = 64 * (warp - 6) + lane;
       uint32_t sw_ev = 0;
       for (int item = 0;; ++item) {
-        const int idx = claimed(c, a.wq, item, a.num_tc_pairs);
+        const int idx = tt::claimed<4, 0>(c, a.wq, item, a.num_tc_pairs);
         if (idx < 0) break;
         const Item I = load_item(a, idx, r);
         uint32_t raw[2][32];
@@ -531,7 +502,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
       int j = 0;  // tiles of the walk so far, over all items
       bool ok = true;
       for (int item = 0; ok; ++item) {
-        const int idx = claimed(c, a.wq, item, a.num_tc_pairs);
+        const int idx = tt::claimed<4, 0>(c, a.wq, item, a.num_tc_pairs);
         if (idx < 0) break;
         const Item I = load_item(a, idx, r);
         const tt::RowInfo ri = tt::row_info(a, I.t, I.rq, m);
@@ -605,7 +576,10 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
         while (ok && have) {
           const int b = j & 1;
           KeyTile nx = kt;
-          const bool have_next = next_tile(nx, I);
+          // the next key tile: found while this tile's loads of S are in
+          // flight (the rotary-value kernel, measured slower that way, finds
+          // it first)
+          bool have_next = VROPE ? next_tile(nx, I) : false;
           bool okw = __all_sync(0xffffffffu, wait_bar(c, B_SFULL + b, (j >> 1) & 1));
           uint32_t s[4][32];
           float alpha = 1.f;
@@ -613,58 +587,14 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
             tc::tc_fence_after();
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) tc::tmem_ld32(lt + T_S + 128 * b + 32 * q4, s[q4]);
+            if (!VROPE) have_next = next_tile(nx, I);
             tc::tmem_wait_ld();
             tc::tc_fence_before();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive_cluster(cbar(B_SFREE + b, 0));
 
             // scores are scaled inside the exponent: x = s * scale * log2(e)
-            const int p = ri.p;
-            const bool full = kt.k1 - kt.k0 == TNK && kt.k0 + TNK - 1 <= p &&
-                              (ri.glob || kt.k0 >= p - window || kt.k0 + TNK <= sink);
-            float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-            if (__all_sync(0xffffffffu, full)) {
-#pragma unroll
-              for (int q4 = 0; q4 < 4; ++q4)
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
-                  mx4[i & 3] = fmaxf(mx4[i & 3], __uint_as_float(s[q4][i]));
-            } else {
-              // visible keys as offsets from k0: [0, a_hi) u [b_lo, hi) (a Global
-              // head: [0, hi)), one bit per key of each 32-key group
-              const int hi = min(max(min(kt.k1, p + 1) - kt.k0, 0), TNK);
-              const int a_hi = ri.glob ? hi : min(hi, max(sink - kt.k0, 0));
-              const int b_lo = ri.glob ? hi : max(p - window - kt.k0, 0);
-#pragma unroll
-              for (int q4 = 0; q4 < 4; ++q4) {
-                const uint32_t msk = span_bits(0, a_hi, 32 * q4) | span_bits(b_lo, hi, 32 * q4);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                  const float x = ((msk >> i) & 1u) ? __uint_as_float(s[q4][i]) : -INFINITY;
-                  s[q4][i] = __float_as_uint(x);
-                  mx4[i & 3] = fmaxf(mx4[i & 3], x);
-                }
-              }
-            }
-            const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * sl2;
-            if (mx > m_run + 8.f) {  // lazy rescale: only when the max grows by more than 2^8
-              if (m_run != -INFINITY) alpha = fast_exp2(m_run - mx);
-              m_run = mx;
-            }
-            const float nb = (m_run == -INFINITY) ? 0.f : -m_run;
-            float ls4[4] = {0.f, 0.f, 0.f, 0.f};
-            // P in place: keys 2w, 2w + 1 in word w = 16 q4 + i of s[q4 >> 1]
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-#pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                const float p0 = fast_exp2(fmaf(__uint_as_float(s[q4][2 * i]), sl2, nb));
-                const float p1 = fast_exp2(fmaf(__uint_as_float(s[q4][2 * i + 1]), sl2, nb));
-                ls4[i & 3] += p0 + p1;
-                s[q4 >> 1][16 * (q4 & 1) + i] = pack_bf16x2(p0, p1);
-              }
-            }
-            l_run = l_run * alpha + ((ls4[0] + ls4[1]) + (ls4[2] + ls4[3]));
+            alpha = tt::softmax_tile(s, kt, ri, sink, window, sl2, m_run, l_run);
             // the O pair's P buffer b is free once the output MMAs of tile
             // j - 2 are done
             okw = __all_sync(0xffffffffu, wait_bar(c, B_PEMPTY + b, ((j >> 1) & 1) ^ 1));
@@ -699,7 +629,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
           have = have_next;
         }
         if (ok && ri.store && l_run > 0.f)
-          a.lse[ri.frow * a.H + ri.head] = m_run * 0.6931471805599453f + logf(l_run);
+          a.lse[ri.frow * a.H + ri.head] = tt::lse_of(m_run, l_run);
       }
       // every output MMA has consumed its P before the cluster may exit
       for (int jj = j - 1; ok && jj >= 0 && jj >= j - 2; --jj)
@@ -712,7 +642,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
         uint32_t cnt = 0;
         bool ok = true;
         for (int item = 0; ok; ++item) {
-          const int idx = claimed(c, a.wq, item, a.num_tc_pairs);
+          const int idx = tt::claimed<4, 0>(c, a.wq, item, a.num_tc_pairs);
           if (idx < 0) break;
           const Item I = load_item(a, idx, r);
           KeyTile cur{0, 0, 0, -1};
@@ -744,7 +674,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
         int j = 0;
         bool ok = true;
         for (int item = 0; ok; ++item) {
-          const int idx = claimed(c, a.wq, item, a.num_tc_pairs);
+          const int idx = tt::claimed<4, 0>(c, a.wq, item, a.num_tc_pairs);
           if (idx < 0) break;
           const Item I = load_item(a, idx, 0);
           KeyTile cur{0, 0, 0, -1};
@@ -798,7 +728,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
         const uint32_t cnt = tc::mapa_shared(smem_u32(&misc[2]), crank - 2);
         bool ok = true;
         for (int item = 0; ok; ++item) {
-          const int idx = claimed(c, a.wq, item, a.num_tc_pairs);
+          const int idx = tt::claimed<4, 0>(c, a.wq, item, a.num_tc_pairs);
           if (idx < 0) break;
           const Item I = load_item(a, idx, r);
           KeyTile kt{0, 0, 0, -1};
@@ -824,7 +754,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
       int j = 0;  // tiles of the walk so far, over all items
       bool ok = true;
       for (int item = 0; ok; ++item) {
-        const int idx = claimed(c, a.wq, item, a.num_tc_pairs);
+        const int idx = tt::claimed<4, 0>(c, a.wq, item, a.num_tc_pairs);
         if (idx < 0) break;
         const Item I = load_item(a, idx, r);
         const tt::RowInfo ri = tt::row_info(a, I.t, I.rq, m);
@@ -944,21 +874,21 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
   }
 }
 
+// Clusters of one launch: as many as the device holds at once (asked once
+// per device), never more than there are tile pairs or queue rings.
 template <int NCH, bool VROPE>
-cudaError_t launch_tc4_t(const KernelArgs& a, cudaStream_t s) {
+cudaError_t clusters_t(const KernelArgs& a, int64_t& clusters) {
   auto k = dense_tc4_kernel<NCH, VROPE>;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(SMEM_BYTES));
-  if (e != cudaSuccess) return e;
-  // persistent clusters: as many as the device holds at once (asked once per
-  // device), never more than there are tile pairs; they claim pairs from the
-  // launch's work queue (a.wq, zeroed before the launch)
+  clusters = 0;
   static int resident[64] = {0};
   int dev = 0;
-  e = cudaGetDevice(&dev);
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   int ncl = (dev >= 0 && dev < 64) ? resident[dev] : 0;
   if (ncl <= 0) {
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(SMEM_BYTES));
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(4 * 64);
     cfg.blockDim = dim3(THREADS);
@@ -968,9 +898,22 @@ cudaError_t launch_tc4_t(const KernelArgs& a, cudaStream_t s) {
     if (ncl <= 0) return cudaErrorInvalidConfiguration;
     if (dev >= 0 && dev < 64) resident[dev] = ncl;
   }
+  clusters = std::min<int64_t>(std::min<int64_t>(ncl, kQueueClusters), a.num_tc_pairs);
+  return cudaSuccess;
+}
+
+template <int NCH, bool VROPE>
+cudaError_t launch_tc4_t(const KernelArgs& a, cudaStream_t s) {
+  auto k = dense_tc4_kernel<NCH, VROPE>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(SMEM_BYTES));
+  if (e != cudaSuccess) return e;
+  // persistent clusters that claim pairs from the launch's work queue (a.wq,
+  // zeroed before the launch)
+  int64_t clusters = 0;
+  e = clusters_t<NCH, VROPE>(a, clusters);
+  if (e != cudaSuccess) return e;
   if (!a.wq) return cudaErrorInvalidValue;  // the work queue lives in the workspace
-  const int64_t clusters =
-      std::min<int64_t>(std::min<int64_t>(ncl, kQueueClusters), a.num_tc_pairs);
   if (clusters <= 0) return cudaSuccess;
   k<<<static_cast<unsigned>(4 * clusters), THREADS, SMEM_BYTES, s>>>(a);
   return cudaGetLastError();
@@ -983,6 +926,12 @@ cudaError_t launch_dense_tc4(const rk_seg_attn_plan_s& p, const KernelArgs& a, c
   (void)q;
   if (p.v_rope) return launch_tc4_t<7, true>(a, s);
   return launch_tc4_t<8, false>(a, s);
+}
+
+cudaError_t dense_tc4_clusters(const rk_seg_attn_plan_s& p, const KernelArgs& a,
+                               int64_t& clusters) {
+  if (p.v_rope) return clusters_t<7, true>(a, clusters);
+  return clusters_t<8, false>(a, clusters);
 }
 
 }  // namespace rk

@@ -155,6 +155,7 @@ static rk_status_t build_plan(const rk_seg_attn_desc_t* d, rk_seg_attn_plan_s* p
   if (!(d->softmax_scale > 0.f) || !std::isfinite(d->softmax_scale)) return RK_ERR_INVALID_ARG;
   if (d->sink < 0 || d->window < 0) return RK_ERR_INVALID_ARG;
   if (d->flags & ~(RK_PLAN_HOST_ONLY | RK_PLAN_LEGACY_MMA | RK_PLAN_SINGLE_CTA | RK_PLAN_CTA_PAIR |
+                   RK_PLAN_NO_SIDE_PAIRS |
                    RK_PLAN_DEVICE_BITMAP | RK_PLAN_V_ROPE))
     return RK_ERR_INVALID_ARG;
   if (v_rope && (d->flags & (RK_PLAN_LEGACY_MMA | RK_PLAN_SINGLE_CTA | RK_PLAN_CTA_PAIR)))
@@ -611,6 +612,12 @@ static rk_status_t build_plan(const rk_seg_attn_desc_t* d, rk_seg_attn_plan_s* p
     std::stable_sort(pairs.begin(), pairs.end(),
                      [](const auto& a, const auto& b) { return a.first > b.first; });
     for (auto& pr : pairs) p->tc_pairs.push_back(pr.second);
+    // the short tail that the side kernel beside the 4-CTA clusters may take
+    p->side_pairs = 0;
+    if (p->kernel == 3 && !v_rope && !(d->flags & RK_PLAN_NO_SIDE_PAIRS))
+      for (size_t k = pairs.size(); k > 0 && pairs[k - 1].first <= rk::kSideMaxTiles; --k)
+        ++p->side_pairs;
+    info.side_pairs = p->side_pairs;
     // the same pairs grouped by the row range of their last computed row
     // (a pair spans at most a few hundred rows, so with ranges of >= 1024
     // rows it touches only its own range and the one before)
@@ -750,8 +757,9 @@ extern "C" rk_status_t rk_seg_attn_plan(const rk_seg_attn_desc_t* desc, void* st
       else if (cudaMemsetAsync(p->d_status, 0, sizeof(int32_t), s) != cudaSuccess)
         st = RK_ERR_CUDA;
     }
-    if (st == RK_OK && !p->chunks.empty() &&
-        (!p->tiles.empty() || !p->tc_tiles.empty() || !p->tc_pairs.empty())) {
+    if (st == RK_OK && ((!p->chunks.empty() &&
+                         (!p->tiles.empty() || !p->tc_tiles.empty() || !p->tc_pairs.empty())) ||
+                        p->side_pairs > 0)) {
       if (cudaStreamCreateWithFlags(&p->side, cudaStreamNonBlocking) != cudaSuccess ||
           cudaEventCreateWithFlags(&p->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
           cudaEventCreateWithFlags(&p->ev_join, cudaEventDisableTiming) != cudaSuccess)
@@ -768,6 +776,10 @@ extern "C" rk_status_t rk_seg_attn_plan(const rk_seg_attn_desc_t* desc, void* st
               cudaEventCreateWithFlags(&p->ev_k[c], cudaEventDisableTiming) == cudaSuccess;
       if (!okc) st = RK_ERR_CUDA;
     }
+    // the side kernel is loaded here: a lazy load at the first forward could
+    // wait for the 4-CTA kernel launched just before it to finish
+    if (st == RK_OK && p->side_pairs > 0 && rk::prepare_dense_side() != cudaSuccess)
+      st = RK_ERR_CUDA;
     // host vectors are pageable: make the uploads complete before returning
     if (st == RK_OK && cudaStreamSynchronize(s) != cudaSuccess) st = RK_ERR_CUDA;
     if (st != RK_OK) {
@@ -931,6 +943,7 @@ extern "C" rk_status_t rk_seg_attn_forward_host(rk_seg_attn_plan_t p, const void
         ac.tc_pairs = p->d_tc_pairs_chunked + b;
         ac.num_tc_pairs = e - b;
         ac.num_chunks = 0;
+        ac.num_side_pairs = 0;  // the ranges' pairs run on the 4-CTA clusters alone
         if (a.wq) ac.wq = a.wq + static_cast<size_t>(c) * (rk::kQueueBytes / 8);  // a queue per range
         good = ok(p->kernel == 3 ? rk::launch_dense_tc4(*p, ac, q, cs)
                                  : rk::launch_dense_tc2(*p, ac, q, cs));
@@ -1051,6 +1064,7 @@ void fill_args(const rk_seg_attn_plan_s& p, KernelArgs& a, const void* q, void* 
   a.d_v = p.d_v;
   a.pos_cs_hi = p.d_pos_cs_hi;
   a.pos_cs_lo = p.d_pos_cs_lo;
+  a.num_side_pairs = p.side_pairs;
 }
 
 cudaError_t launch_forward(const rk_seg_attn_plan_s& p, const KernelArgs& a, const void* q,
@@ -1069,9 +1083,25 @@ cudaError_t launch_forward(const rk_seg_attn_plan_s& p, const KernelArgs& a, con
   // beside split chunks (decode) the few short Local tiles run on CTA pairs,
   // which leave more SMs to the split kernel than 4-CTA clusters (the pair
   // kernel has no rotary-value form)
-  if (e == cudaSuccess && a.num_tc_pairs)
-    e = (p.kernel == 3 && (!a.num_chunks || p.v_rope)) ? launch_dense_tc4(p, a, q, ts)
-                                                        : launch_dense_tc2(p, a, q, ts);
+  if (e == cudaSuccess && a.num_tc_pairs) {
+    if (p.kernel == 3 && !a.num_chunks && a.num_side_pairs > 0 && p.side) {
+      // the 4-CTA clusters first, then the side kernel on the plan's stream
+      // (forked before the clusters' launch, so that it runs beside them on
+      // the SMs they leave free)
+      int64_t clusters = 0;
+      e = dense_tc4_clusters(p, a, clusters);
+      if (e == cudaSuccess) e = prepare_dense_side();
+      if (e == cudaSuccess) e = cudaEventRecord(p.ev_fork, s);
+      if (e == cudaSuccess) e = launch_dense_tc4(p, a, q, s);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(p.side, p.ev_fork, 0);
+      if (e == cudaSuccess) e = launch_dense_side(p, a, q, clusters, p.side);
+      if (e == cudaSuccess) e = cudaEventRecord(p.ev_join, p.side);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(s, p.ev_join, 0);
+    } else {
+      e = (p.kernel == 3 && (!a.num_chunks || p.v_rope)) ? launch_dense_tc4(p, a, q, ts)
+                                                          : launch_dense_tc2(p, a, q, ts);
+    }
+  }
   if (e == cudaSuccess && a.num_chunks) e = launch_split_decode(p, a, s);
   if (ts != s) {
     const cudaError_t e1 = cudaEventRecord(p.ev_join, ts);

@@ -99,12 +99,18 @@ struct TcPair {
   int32_t skip;
 };
 
-// Work queue of one launch of the persistent 4-CTA kernel: a claim counter
-// (word 0) and, from word 32 on, a ring of kQueueRing claimed items for each
-// of up to kQueueClusters clusters.
+// Work queue of one launch of the persistent 4-CTA kernel and of the side
+// kernel beside it: a 64-bit claim counter (word 0: the pairs taken from the
+// front of the list in its low half, from the back in its high half) and,
+// from word 32 on, a ring of kQueueRing claimed items for each of up to
+// kQueueClusters 4-CTA clusters and kSideClusters side CTA pairs.
 constexpr int kQueueClusters = 40;
+constexpr int kSideClusters = 8;
 constexpr int kQueueRing = 64;
-constexpr size_t kQueueBytes = 256 + static_cast<size_t>(kQueueClusters) * kQueueRing * 8;
+constexpr size_t kQueueBytes =
+    256 + static_cast<size_t>(kQueueClusters + kSideClusters) * kQueueRing * 8;
+// the side kernel takes only pairs of at most this many key tiles
+constexpr int kSideMaxTiles = 8;
 
 struct KernelArgs {
   const uint16_t* q;
@@ -142,6 +148,7 @@ struct KernelArgs {
   const float* pos_cs_hi;     // [T / 256 + 1][d_rope/2][2] cos, sin of 256 a theta   (v_rope)
   const float* pos_cs_lo;     // [256][d_rope/2][2] cos, sin of b theta              (v_rope)
   unsigned long long* wq;     // work queue of the 4-CTA kernel (kQueueBytes, zeroed)
+  int32_t num_side_pairs;     // the short tail of tc_pairs that the side kernel may take
 };
 
 }  // namespace rk
@@ -197,8 +204,10 @@ struct rk_seg_attn_plan_s {
   int32_t* d_status = nullptr;
   size_t workspace_bytes = 0;
   size_t queue_off = 0;       // the 4-CTA kernel's work queues (kHostChunks of kQueueBytes)
+  int32_t side_pairs = 0;     // pairs at the end of tc_pairs with <= kSideMaxTiles key tiles
   // when a forward has both split chunks and prefill tiles, the tiles run on
-  // this plan-owned stream, forked from and joined back to the caller's
+  // this plan-owned stream, forked from and joined back to the caller's; a
+  // forward on 4-CTA clusters runs the side kernel there
   cudaStream_t side = nullptr;
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
   // forward from host buffers: the computed rows in kHostChunks ranges of
@@ -227,6 +236,18 @@ cudaError_t launch_dense_tc2(const rk_seg_attn_plan_s& plan, const KernelArgs& a
                              const void* q, cudaStream_t stream);
 cudaError_t launch_dense_tc4(const rk_seg_attn_plan_s& plan, const KernelArgs& a,
                              const void* q, cudaStream_t stream);
+// 4-CTA clusters that launch_dense_tc4 starts for these arguments.
+cudaError_t dense_tc4_clusters(const rk_seg_attn_plan_s& plan, const KernelArgs& a,
+                               int64_t& clusters);
+// The side kernel: persistent CTA pairs on the SMs that `tc4_clusters`
+// 4-CTA clusters leave free, taking the short pairs from the back of the
+// same work queue (none launched when no SM pair is free).
+cudaError_t launch_dense_side(const rk_seg_attn_plan_s& plan, const KernelArgs& a,
+                              const void* q, int64_t tc4_clusters, cudaStream_t stream);
+// Sets the side kernel's attributes.  With lazy module loading the first
+// such call loads the kernel, which may wait for the device to go idle, so
+// it is made before the 4-CTA kernel is launched.
+cudaError_t prepare_dense_side();
 cudaError_t launch_dense_tcs(const rk_seg_attn_plan_s& plan, const KernelArgs& a,
                              cudaStream_t stream);
 // Fill the kernel arguments shared by every launch of a forward.

@@ -77,6 +77,48 @@ __device__ __forceinline__ bool wait_count(const Ctx& c, const uint32_t* cnt, ui
   return true;
 }
 
+// Ring of claimed items of this CTA's cluster in the work queue `wq`: ring
+// FIRST + blockIdx.x / CTAS (CTAS: CTAs per cluster).
+template <int CTAS, int FIRST>
+__device__ __forceinline__ unsigned long long* queue_ring(unsigned long long* wq) {
+  return wq + 32 + static_cast<size_t>(FIRST + blockIdx.x / CTAS) * kQueueRing;
+}
+
+// Work item k of a persistent cluster's walk, read from the cluster's ring
+// (entry k mod kQueueRing holds (k + 1) << 32 | pair index, written by the
+// cluster's claimer with a release store): the pair index, or -1 past the
+// walk's end (an index >= npairs) or when the bounded wait gives up (the same
+// give-up rules as wait_bar).  Called once per item and role, so kept out of
+// line (the roles' tile loops need their registers).
+template <int CTAS, int FIRST>
+__device__ __noinline__ int claimed(const Ctx c, unsigned long long* wq, int k, int npairs) {
+  const unsigned long long* e = queue_ring<CTAS, FIRST>(wq) + (k & (kQueueRing - 1));
+  const unsigned long long tag = static_cast<unsigned long long>(k + 1);
+  uint32_t it = 0;
+  uint64_t t0 = 0;
+  while (true) {
+    const unsigned long long v = tc::ld_acquire_gpu_u64(e);
+    if ((v >> 32) == tag) {
+      const uint32_t idx = static_cast<uint32_t>(v);
+      return idx < static_cast<uint32_t>(npairs) ? static_cast<int>(idx) : -1;
+    }
+    if ((++it & 63u) == 0) {
+      if (*c.abort || *reinterpret_cast<volatile int32_t*>(c.status)) {
+        *c.abort = 1;
+        return -1;
+      }
+      const uint64_t now = tc::global_ns();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > WAIT_NS) {
+        *c.abort = 1;
+        atomicCAS(c.status, 0, static_cast<int32_t>(RK_ERR_DEVICE_TIMEOUT));
+        return -1;
+      }
+    }
+  }
+}
+
 // Bounded wait that ignores the abort flag (drains work in flight).
 __device__ __forceinline__ void drain_bar(const Ctx& c, int i, uint32_t parity,
                                           uint64_t limit_ns = WAIT_NS) {
@@ -124,6 +166,84 @@ __device__ __forceinline__ RowInfo row_info(const KernelArgs& a, const TcTile& t
   }
   r.frow = r.p >= 0 ? rq.row_base + (r.p - rq.q_row_begin) : -1;
   return r;
+}
+
+// Bit i set for each offset base + i (i < 32) inside [lo, hi).
+__device__ __forceinline__ uint32_t span_bits(int lo, int hi, int base) {
+  const int l = min(max(lo - base, 0), 32), h = min(max(hi - base, 0), 32);
+  const uint32_t mh = h >= 32 ? 0xffffffffu : ((1u << h) - 1u);
+  const uint32_t ml = l >= 32 ? 0xffffffffu : ((1u << l) - 1u);
+  return mh & ~ml;
+}
+
+// Online softmax of one 128-key tile for one query pair, with its scores
+// s[q4][i] (key k0 + 32 q4 + i, fp32 bits) from tensor memory (RedKnot-MLA
+// paper, RoPE-orthogonality paragraph: the running max, sum and output carry
+// across the key walk).  Keys the pair does not see become -inf (Global: k <=
+// p; Local: sink u [p - w, p], RedKnot blog "Insight 1").  The running max
+// (log2 domain) is raised only when the tile's max exceeds it by more than
+// 2^8; the returned factor alpha (1 otherwise) rescales the earlier sum and
+// output.  P = 2^(s * scale * log2 e - max) is left as bf16 pairs in s[0] and
+// s[1] (keys 2w, 2w + 1 in word w = 16 q4 + i of s[q4 >> 1]).  The 4-CTA
+// kernel and the side kernel beside it both use this, so a pair's P, sum and
+// output are the same whichever of them takes it.
+__device__ __forceinline__ float softmax_tile(uint32_t (&s)[4][32], const KeyTile& kt,
+                                              const RowInfo& ri, int sink, int window,
+                                              float sl2, float& m_run, float& l_run) {
+  constexpr int TNK = 128;
+  const int p = ri.p;
+  const bool full = kt.k1 - kt.k0 == TNK && kt.k0 + TNK - 1 <= p &&
+                    (ri.glob || kt.k0 >= p - window || kt.k0 + TNK <= sink);
+  float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+  if (__all_sync(0xffffffffu, full)) {
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4)
+#pragma unroll
+      for (int i = 0; i < 32; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], __uint_as_float(s[q4][i]));
+  } else {
+    // visible keys as offsets from k0: [0, a_hi) u [b_lo, hi) (a Global
+    // head: [0, hi)), one bit per key of each 32-key group
+    const int hi = min(max(min(kt.k1, p + 1) - kt.k0, 0), TNK);
+    const int a_hi = ri.glob ? hi : min(hi, max(sink - kt.k0, 0));
+    const int b_lo = ri.glob ? hi : max(p - window - kt.k0, 0);
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) {
+      const uint32_t msk = span_bits(0, a_hi, 32 * q4) | span_bits(b_lo, hi, 32 * q4);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float x = ((msk >> i) & 1u) ? __uint_as_float(s[q4][i]) : -INFINITY;
+        s[q4][i] = __float_as_uint(x);
+        mx4[i & 3] = fmaxf(mx4[i & 3], x);
+      }
+    }
+  }
+  const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * sl2;
+  float alpha = 1.f;
+  if (mx > m_run + 8.f) {  // lazy rescale: only when the max grows by more than 2^8
+    if (m_run != -INFINITY) alpha = fast_exp2(m_run - mx);
+    m_run = mx;
+  }
+  const float nb = (m_run == -INFINITY) ? 0.f : -m_run;
+  float ls4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int q4 = 0; q4 < 4; ++q4) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float p0 = fast_exp2(fmaf(__uint_as_float(s[q4][2 * i]), sl2, nb));
+      const float p1 = fast_exp2(fmaf(__uint_as_float(s[q4][2 * i + 1]), sl2, nb));
+      ls4[i & 3] += p0 + p1;
+      s[q4 >> 1][16 * (q4 & 1) + i] = pack_bf16x2(p0, p1);
+    }
+  }
+  // explicit fused multiply-adds here and in lse_of: the kernels that share
+  // this arithmetic get the same roundings whatever the compiler contracts
+  l_run = fmaf(l_run, alpha, (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]));
+  return alpha;
+}
+
+// Natural-log LSE of a query pair from its running max (log2 domain) and sum.
+__device__ __forceinline__ float lse_of(float m_run, float l_run) {
+  return fmaf(m_run, 0.6931471805599453f, logf(l_run));
 }
 
 // q_rope' = R(-delta) q_rope of one row (RedKnot-MLA paper, RoPE-orthogonality

@@ -79,7 +79,7 @@ def test_plan_errors():
     _expect(2, rope_base=1.0)
     _expect(2, softmax_scale=0.0)
     _expect(2, window=-1)
-    _expect(2, flags=B.RK_PLAN_HOST_ONLY | 64)
+    _expect(2, flags=B.RK_PLAN_HOST_ONLY | 128)
     _expect(2, q_row_begin=[576])             # beyond T
     _expect(2, head_role=np.array([0, 0, 0, 0, 0, 0, 0, 2], np.uint8))
     _expect(2, seg_begin=[0, 0])              # empty request
@@ -196,8 +196,8 @@ def test_vrope_plan_rules():
     parts = pd.info["split_chunks"]
     body = ((parts * 8 * 512 * 4 + parts * 8 * 4 + 255) // 256) * 256
     # plus the 4-CTA kernel's work queues (its Local tiles): 8 launches' worth
-    # of a claim counter and 40 clusters' 64-entry rings
-    queue = 8 * (256 + 40 * 64 * 8)
+    # of a claim counter and 64-entry rings for 40 clusters and 8 side pairs
+    queue = 8 * (256 + (40 + 8) * 64 * 8)
     assert pd.info["kernel"] == 3
     assert body + queue < pd.workspace_bytes <= body + 256 + 4 * parts + queue
 

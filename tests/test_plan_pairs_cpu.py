@@ -92,3 +92,31 @@ def test_pairs_cover_tiles_and_skip_only_unneeded_segments(name):
     assert all(a >= b for a, b in zip(costs, costs[1:])), "pairs are ordered longest first"
     if name == "ctx16k":
         assert skipped_any, "Local pairs far from the sink skip segments"
+    # the side kernel's share: the pairs of at most 8 key tiles at the end of
+    # the list (the rotary-value kernel has no side kernel)
+    tail = 0
+    for cst in reversed(costs):
+        if cst > 8:
+            break
+        tail += 1
+    assert plan.info["side_pairs"] == (0 if wl.v_rope else tail)
+    if not wl.v_rope and name in ("ctx16k", "ctx128k_mini", "flash_mini"):
+        assert tail > 0, "Local pairs are short"
+
+
+def test_no_side_pairs_flag():
+    """RK_PLAN_NO_SIDE_PAIRS keeps every pair on the 4-CTA clusters; the pair
+    list itself does not change."""
+    wl, plan = _host_plan("ctx16k")
+    assert plan.info["side_pairs"] > 0
+    bm, _ = build_bitmap(wl)
+    flat, begins = segments_for_abi(wl)
+    segs = [(0x10000000 + i * 0x1000000, s[1], s[2], s[3]) for i, s in enumerate(flat)]
+    off = B.SegAttnPlan(segments=segs, seg_begin=begins,
+                        q_row_begin=[r.q_row_begin for r in wl.requests], num_heads=wl.H,
+                        d_nope=wl.d_nope, d_rope=wl.d_rope, rope_base=wl.rope_base,
+                        softmax_scale=wl.scale, head_role=wl.head_role, sink=wl.sink,
+                        window=wl.window, bitmap=bm,
+                        flags=B.RK_PLAN_HOST_ONLY | B.RK_PLAN_NO_SIDE_PAIRS)
+    assert off.info["side_pairs"] == 0
+    assert np.array_equal(off.pairs(), plan.pairs())
