@@ -83,7 +83,8 @@ KERNEL_SOURCES = {"mma_sync": ["dense_mma.cu", "common.cuh"],
                   "tcgen05_small": ["dense_tcs.cu", "tc_tile.cuh", "tc_ptx.cuh", "common.cuh"],
                   "tcgen05": ["dense_tc.cu", "tc_ptx.cuh", "common.cuh"],
                   "tcgen05_pair": ["dense_tc2.cu", "tc_tile.cuh", "tc_ptx.cuh", "common.cuh"],
-                  "tcgen05_quad": ["dense_tc4.cu", "tc_tile.cuh", "tc_ptx.cuh", "common.cuh"]}
+                  "tcgen05_quad": ["dense_tc4.cu", "dense_side.cu", "tc_tile.cuh", "tc_ptx.cuh",
+                                   "common.cuh"]}
 
 
 def kernel_source_hash(kernel: str) -> str:
