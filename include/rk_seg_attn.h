@@ -231,8 +231,8 @@ int64_t rk_seg_attn_plan_pairs(rk_seg_attn_plan_t plan, int32_t* out, int64_t ca
 
 /* Bytes of device workspace rk_seg_attn_forward needs (0 if none): the
  * partial outputs of split decode rows, and for plans on the 4-CTA prefill
- * kernel (kernel 3) the work queues its persistent clusters claim tile pairs
- * from (about 166 KB). */
+ * kernel (kernel 3) the work queues its persistent clusters, and the side
+ * kernel beside them, claim tile pairs from (about 199 KB). */
 size_t rk_seg_attn_workspace_bytes(rk_seg_attn_plan_t plan);
 
 /* Segment-relocated attention over the plan's segments (paper,
