@@ -189,8 +189,9 @@ typedef struct {
   int32_t d_v;               /* output columns: d_nope, or d_k with RK_PLAN_V_ROPE */
   int64_t side_pairs;        /* kernel 3: tile pairs at the end of the work list
                                 (at most 8 key tiles each) that the side kernel
-                                beside the 4-CTA clusters may take; 0 with
-                                RK_PLAN_NO_SIDE_PAIRS or RK_PLAN_V_ROPE */
+                                beside the 4-CTA clusters may take (prefill
+                                forwards without split decode rows); 0 with
+                                RK_PLAN_NO_SIDE_PAIRS */
 } rk_plan_info_t;
 
 /* Build an immutable, reusable plan for one request bundle geometry

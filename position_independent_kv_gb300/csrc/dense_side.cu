@@ -86,8 +86,10 @@ __device__ __forceinline__ bool next_tile(KeyTile& kt, const TcPair& P, const De
                             static_cast<uint32_t>(P.skip));
 }
 
+template <int NCH, bool VROPE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     dense_side_kernel(const KernelArgs a, const __grid_constant__ tt::QMaps qm) {
+  constexpr int DK = 64 * (NCH + 1);  // latent row: NCH nope chunks + the rope chunk
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
@@ -163,8 +165,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         if (item > 0) ok = wait_bar(c, B_QEMPTY, (item - 1) & 1);
         if (!ok) break;
         // the leader's QFULL counts both CTAs' query bytes
-        if (rank == 0) tc::mbar_arrive_expect_tx(&bar[B_QFULL], 2 * 8 * CHUNK);
-        tt::load_q_tile<true>(a, qm, t, rq, smem_u32(sm + OFF_Q), lbar(B_QFULL));
+        if (rank == 0) tc::mbar_arrive_expect_tx(&bar[B_QFULL], 2 * NCH * CHUNK);
+        tt::load_q_tile<true, NCH>(a, qm, t, rq, smem_u32(sm + OFF_Q), lbar(B_QFULL));
         ++qloads;
         // one box per slot use; the leader arms its FULL barrier with both
         // CTAs' bytes, and both CTAs' copies complete on it
@@ -182,14 +184,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         const int koff = 64 * static_cast<int>(rank);
         for (int half = 0; half < 2 && ok; ++half) {
           // per key tile: the rope chunk, nope chunks 0-3 and 4-7 of this
-          // CTA's 64 keys, then this CTA's two value chunks of the previous
-          // tile (the half's 256 columns: 128 from each CTA)
+          // CTA's 64 keys (with NCH = 7 the second box's last chunk is the
+          // rope chunk, unused), then this CTA's two value chunks of the
+          // previous tile (the half's 256 columns: 128 from each CTA)
           KeyTile cur{0, 0, 0, -1}, prev{0, 0, 0, -1};
           bool have = next_tile(cur, P, segs, nseg);
           bool has_prev = false;
           while (ok && (have || has_prev)) {
             if (have) {
-              ok = load(cur, MAP_R, koff, 8, HCHUNK);
+              ok = load(cur, MAP_R, koff, NCH, HCHUNK);
               if (ok) ok = load(cur, MAP_K4, koff, 0, 4 * HCHUNK);
               if (ok) ok = load(cur, MAP_K4, koff, 4, 4 * HCHUNK);
             }
@@ -268,6 +271,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 #pragma unroll
                 for (int ch = 0; ch < 4; ++ch) {
                   const int cc = 4 * b + ch;
+                  if (cc >= NCH) break;
 #pragma unroll
                   for (int k = 0; k < 4; ++k)
                     tc::mma_ss_2sm(ts, tc::sdesc_sw128(qa + cc * CHUNK + 32 * k, 16, 1024),
@@ -343,7 +347,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       const DevSeg* segs = a.segs + rq.seg_first;
       const int nseg = rq.seg_count;
       const tt::RowInfo ri = tt::row_info(a, t, rq, m);
-      const uint16_t* qrope = ri.p >= 0 ? a.q + (ri.frow * a.H + ri.head) * 576 + 512 : nullptr;
+      const uint16_t* qrope = ri.p >= 0 ? a.q + (ri.frow * a.H + ri.head) * DK + 64 * NCH : nullptr;
       for (int half = 0; half < 2 && ok; ++half) {
         KeyTile kt{0, 0, 0, -1};
         bool have = next_tile(kt, P, segs, nseg);
@@ -354,6 +358,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         tc::tc_fence_before();
         tc::mbar_arrive_cluster(sfree_l);
         float m_run = -INFINITY, l_run = 0.f;
+        // rotary value: the segment whose canonical frame the output's rope
+        // columns are in (value columns 448..511: this CTA pair's columns
+        // 192..255 in the second half)
+        int seg_frame = kt.j;
         while (ok && have) {
           KeyTile nx = kt;
           const bool have_next = next_tile(nx, P, segs, nseg);
@@ -378,17 +386,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           tc::tc_fence_after();
           tc::tmem_st32(lt + T_P, s[0]);
           tc::tmem_st32(lt + T_P + 32, s[1]);
-          if (__any_sync(0xffffffffu, alpha != 1.f)) {
+          const bool scale = __any_sync(0xffffffffu, alpha != 1.f);
+          // a new segment: R(delta_frame - delta_next) moves the rope columns
+          // into the next segment's canonical frame (after the rescale, as
+          // the 4-CTA kernel does)
+          const bool turn = VROPE && half == 1 && kt.j != seg_frame;
+          if (scale || turn) {
+            const float4* ca =
+                reinterpret_cast<const float4*>(a.rope_cs + int64_t(rq.seg_first + seg_frame) * 64);
+            const float4* cb =
+                reinterpret_cast<const float4*>(a.rope_cs + int64_t(rq.seg_first + kt.j) * 64);
 #pragma unroll 1
-            for (int q8 = 0; q8 < 8; ++q8) {
+            for (int q8 = scale ? 0 : 6; q8 < 8; ++q8) {
               uint32_t o[32];
               tc::tmem_ld32(lt + T_O + 32 * q8, o);
               tc::tmem_wait_ld();
+              if (scale) {
 #pragma unroll
-              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+              }
+              if (turn && q8 >= 6) tt::turn16(o, ca, cb, 16 * (q8 - 6));
               tc::tmem_st32(lt + T_O + 32 * q8, o);
             }
           }
+          seg_frame = kt.j;
           tc::tmem_wait_st();
           tc::tc_fence_before();
           tc::mbar_arrive_cluster(pready_l);
@@ -409,6 +430,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             uint32_t o[32];
             tc::tmem_ld32(lt + T_O + 32 * q8, o);
             tc::tmem_wait_ld();
+            if (VROPE && st && half == 1 && q8 >= 6) {
+              // rotary value: R(delta_frame - p) restores the last segment's
+              // output phase and applies the inverse output RoPE at the row's
+              // position p (cos / sin of p theta from the two-level table)
+              const float4* ca =
+                  reinterpret_cast<const float4*>(a.rope_cs + int64_t(rq.seg_first + seg_frame) * 64);
+              const float4* ph = reinterpret_cast<const float4*>(a.pos_cs_hi + int64_t(ri.p >> 8) * 64);
+              const float4* pl = reinterpret_cast<const float4*>(a.pos_cs_lo + int64_t(ri.p & 255) * 64);
+              tt::restore16(o, ca, ph, pl, 16 * (q8 - 6));
+            }
             if (st) {
               uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * q8);
 #pragma unroll
@@ -449,13 +480,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 }  // namespace
 
 cudaError_t prepare_dense_side() {
-  return cudaFuncSetAttribute(dense_side_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(dense_side_kernel<8, false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(SMEM_BYTES));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(dense_side_kernel<7, true>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                               static_cast<int>(SMEM_BYTES));
 }
 
 cudaError_t launch_dense_side(const rk_seg_attn_plan_s& p, const KernelArgs& a, const void* q,
                               int64_t tc4_clusters, cudaStream_t s) {
-  if (p.v_rope || p.d_nope != 512 || p.d_rope != 64 || a.num_side_pairs <= 0 || !a.wq)
+  const bool vr = p.v_rope;
+  if (p.d_rope != 64 || p.d_nope != (vr ? 448 : 512) || a.num_side_pairs <= 0 || !a.wq)
     return cudaSuccess;
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -469,7 +506,11 @@ cudaError_t launch_dense_side(const rk_seg_attn_plan_s& p, const KernelArgs& a, 
   tt::QMaps qm;
   e = tt::make_qmaps(p, a, q, qm);
   if (e != cudaSuccess) return e;
-  dense_side_kernel<<<static_cast<unsigned>(2 * pairs), THREADS, SMEM_BYTES, s>>>(a, qm);
+  const dim3 grid(static_cast<unsigned>(2 * pairs));
+  if (vr)
+    dense_side_kernel<7, true><<<grid, THREADS, SMEM_BYTES, s>>>(a, qm);
+  else
+    dense_side_kernel<8, false><<<grid, THREADS, SMEM_BYTES, s>>>(a, qm);
   return cudaGetLastError();
 }
 

@@ -154,47 +154,6 @@ __device__ __forceinline__ bool next_tile(KeyTile& kt, const Item& I) {
   return next_key_tile<TNK>(kt, I.segs, I.nseg, 0, I.r0hi, I.r1lo, I.r1hi, I.skip);
 }
 
-// Turn the 16 rope pairs held in o[0..31] (32 consecutive output columns:
-// pairs h0 .. h0 + 15 of the rope slice) by R(delta_a - delta_b), from the
-// cos / sin tables of the two frames (float4 k: pairs 2k and 2k + 1).  The
-// angles are formed here, for these 16 pairs only, to keep them out of the
-// registers of the loops around.
-__device__ __forceinline__ void turn16(uint32_t (&o)[32], const float4* ca, const float4* cb, int h0) {
-#pragma unroll
-  for (int u = 0; u < 8; ++u) {
-    const float4 x = __ldg(ca + h0 / 2 + u), y = __ldg(cb + h0 / 2 + u);
-    const float c0 = fmaf(x.x, y.x, x.y * y.y), s0 = fmaf(x.y, y.x, -x.x * y.y);
-    const float c1 = fmaf(x.z, y.z, x.w * y.w), s1 = fmaf(x.w, y.z, -x.z * y.w);
-    const float a0 = __uint_as_float(o[4 * u]), b0 = __uint_as_float(o[4 * u + 1]);
-    const float a1 = __uint_as_float(o[4 * u + 2]), b1 = __uint_as_float(o[4 * u + 3]);
-    o[4 * u] = __float_as_uint(a0 * c0 - b0 * s0);
-    o[4 * u + 1] = __float_as_uint(fmaf(a0, s0, b0 * c0));
-    o[4 * u + 2] = __float_as_uint(a1 * c1 - b1 * s1);
-    o[4 * u + 3] = __float_as_uint(fmaf(a1, s1, b1 * c1));
-  }
-}
-// Turn the same 16 pairs by R(delta_frame - p): the frame's cos / sin table
-// `ca` and the row position p's cos / sin of p theta from the two-level table
-// (ph: the 256-multiple part, pl: the remainder), for the epilogue.
-__device__ __forceinline__ void restore16(uint32_t (&o)[32], const float4* ca, const float4* ph,
-                                          const float4* pl, int h0) {
-#pragma unroll
-  for (int u = 0; u < 8; ++u) {
-    const float4 x = __ldg(ca + h0 / 2 + u), h = __ldg(ph + h0 / 2 + u), l = __ldg(pl + h0 / 2 + u);
-    // cos / sin of p theta for pairs h0 + 2u, + 1
-    const float pc0 = fmaf(h.x, l.x, -h.y * l.y), ps0 = fmaf(h.y, l.x, h.x * l.y);
-    const float pc1 = fmaf(h.z, l.z, -h.w * l.w), ps1 = fmaf(h.w, l.z, h.z * l.w);
-    const float c0 = fmaf(x.x, pc0, x.y * ps0), s0 = fmaf(x.y, pc0, -x.x * ps0);
-    const float c1 = fmaf(x.z, pc1, x.w * ps1), s1 = fmaf(x.w, pc1, -x.z * ps1);
-    const float a0 = __uint_as_float(o[4 * u]), b0 = __uint_as_float(o[4 * u + 1]);
-    const float a1 = __uint_as_float(o[4 * u + 2]), b1 = __uint_as_float(o[4 * u + 3]);
-    o[4 * u] = __float_as_uint(a0 * c0 - b0 * s0);
-    o[4 * u + 1] = __float_as_uint(fmaf(a0, s0, b0 * c0));
-    o[4 * u + 2] = __float_as_uint(a1 * c1 - b1 * s1);
-    o[4 * u + 3] = __float_as_uint(fmaf(a1, s1, b1 * c1));
-  }
-}
-
 template <int NCH, bool VROPE>
 __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
     dense_tc4_kernel(const KernelArgs a) {
@@ -798,7 +757,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
 #pragma unroll
                 for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
               }
-              if (turn && q8 >= 14) turn16(o, ca, cb, 16 * (q8 - 14));
+              if (turn && q8 >= 14) tt::turn16(o, ca, cb, 16 * (q8 - 14));
               tc::tmem_st32(lt + T_O + 32 * q8, o);
             }
             tc::tmem_wait_st();
@@ -831,8 +790,8 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
               const float4* ca = reinterpret_cast<const float4*>(a.rope_cs + int64_t(I.rq.seg_first + seg_frame) * 64);
               const float4* ph = reinterpret_cast<const float4*>(a.pos_cs_hi + int64_t(ri.p >> 8) * 64);
               const float4* pl = reinterpret_cast<const float4*>(a.pos_cs_lo + int64_t(ri.p & 255) * 64);
-              restore16(o[0], ca, ph, pl, 0);
-              restore16(o[1], ca, ph, pl, 16);
+              tt::restore16(o[0], ca, ph, pl, 0);
+              tt::restore16(o[1], ca, ph, pl, 16);
             }
             if (st) {
 #pragma unroll

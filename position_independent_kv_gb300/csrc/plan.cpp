@@ -614,7 +614,7 @@ static rk_status_t build_plan(const rk_seg_attn_desc_t* d, rk_seg_attn_plan_s* p
     for (auto& pr : pairs) p->tc_pairs.push_back(pr.second);
     // the short tail that the side kernel beside the 4-CTA clusters may take
     p->side_pairs = 0;
-    if (p->kernel == 3 && !v_rope && !(d->flags & RK_PLAN_NO_SIDE_PAIRS))
+    if (p->kernel == 3 && !(d->flags & RK_PLAN_NO_SIDE_PAIRS))
       for (size_t k = pairs.size(); k > 0 && pairs[k - 1].first <= rk::kSideMaxTiles; --k)
         ++p->side_pairs;
     info.side_pairs = p->side_pairs;

@@ -246,6 +246,48 @@ __device__ __forceinline__ float lse_of(float m_run, float l_run) {
   return fmaf(m_run, 0.6931471805599453f, logf(l_run));
 }
 
+// Turn the 16 rope pairs held in o[0..31] (32 consecutive output columns:
+// pairs h0 .. h0 + 15 of the rope slice) by R(delta_a - delta_b), from the
+// cos / sin tables of the two frames (float4 k: pairs 2k and 2k + 1).  The
+// angles are formed here, for these 16 pairs only, to keep them out of the
+// registers of the loops around.  Shared by the 4-CTA kernel and the side
+// kernel beside it, so that both turn a pair's output the same way.
+__device__ __forceinline__ void turn16(uint32_t (&o)[32], const float4* ca, const float4* cb, int h0) {
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const float4 x = __ldg(ca + h0 / 2 + u), y = __ldg(cb + h0 / 2 + u);
+    const float c0 = fmaf(x.x, y.x, x.y * y.y), s0 = fmaf(x.y, y.x, -x.x * y.y);
+    const float c1 = fmaf(x.z, y.z, x.w * y.w), s1 = fmaf(x.w, y.z, -x.z * y.w);
+    const float a0 = __uint_as_float(o[4 * u]), b0 = __uint_as_float(o[4 * u + 1]);
+    const float a1 = __uint_as_float(o[4 * u + 2]), b1 = __uint_as_float(o[4 * u + 3]);
+    o[4 * u] = __float_as_uint(a0 * c0 - b0 * s0);
+    o[4 * u + 1] = __float_as_uint(fmaf(a0, s0, b0 * c0));
+    o[4 * u + 2] = __float_as_uint(a1 * c1 - b1 * s1);
+    o[4 * u + 3] = __float_as_uint(fmaf(a1, s1, b1 * c1));
+  }
+}
+// Turn the same 16 pairs by R(delta_frame - p): the frame's cos / sin table
+// `ca` and the row position p's cos / sin of p theta from the two-level table
+// (ph: the 256-multiple part, pl: the remainder), for the epilogue.
+__device__ __forceinline__ void restore16(uint32_t (&o)[32], const float4* ca, const float4* ph,
+                                          const float4* pl, int h0) {
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const float4 x = __ldg(ca + h0 / 2 + u), h = __ldg(ph + h0 / 2 + u), l = __ldg(pl + h0 / 2 + u);
+    // cos / sin of p theta for pairs h0 + 2u, + 1
+    const float pc0 = fmaf(h.x, l.x, -h.y * l.y), ps0 = fmaf(h.y, l.x, h.x * l.y);
+    const float pc1 = fmaf(h.z, l.z, -h.w * l.w), ps1 = fmaf(h.w, l.z, h.z * l.w);
+    const float c0 = fmaf(x.x, pc0, x.y * ps0), s0 = fmaf(x.y, pc0, -x.x * ps0);
+    const float c1 = fmaf(x.z, pc1, x.w * ps1), s1 = fmaf(x.w, pc1, -x.z * ps1);
+    const float a0 = __uint_as_float(o[4 * u]), b0 = __uint_as_float(o[4 * u + 1]);
+    const float a1 = __uint_as_float(o[4 * u + 2]), b1 = __uint_as_float(o[4 * u + 3]);
+    o[4 * u] = __float_as_uint(a0 * c0 - b0 * s0);
+    o[4 * u + 1] = __float_as_uint(fmaf(a0, s0, b0 * c0));
+    o[4 * u + 2] = __float_as_uint(a1 * c1 - b1 * s1);
+    o[4 * u + 3] = __float_as_uint(fmaf(a1, s1, b1 * c1));
+  }
+}
+
 // q_rope' = R(-delta) q_rope of one row (RedKnot-MLA paper, RoPE-orthogonality
 // paragraph: the query turns by -delta_i instead of rewriting the cache) as
 // bf16 hi and lo parts, written to this thread's TMEM lane at columns rh..
@@ -284,50 +326,53 @@ __device__ __forceinline__ void write_rope(uint32_t lane_taddr, uint32_t rh, uin
   tc::tmem_wait_st();
 }
 
-// TMA views of q (bf16 [rows, H, 576]) for loading a tile's nope part
-// chunk-major into shared memory (8 chunks of 128 lanes x 64 dims, 128-byte
-// swizzled).
+// TMA views of q (bf16 [rows, H, d_k], d_k = 64 (NCH + 1): NCH nope chunks
+// then the rope chunk) for loading a tile's nope part chunk-major into shared
+// memory (NCH chunks of 128 lanes x 64 dims, 128-byte swizzled).
 struct QMaps {
-  CUtensorMap g5;   // Global, one Global head per group: (64, rows, groups, 8 chunks, in-group)
-  CUtensorMap g3;   // Global, any roles: (576, H, rows), box (64, 1, R)
-  CUtensorMap l4;   // Local, H = 128: (64, H, 8 chunks, rows), box (64, 128, 8, 1)
-  CUtensorMap l3;   // Local, any H: (576, H, rows), box (64, H, 1)
+  CUtensorMap g5;   // Global, one Global head per group: (64, rows, groups, NCH chunks, in-group)
+  CUtensorMap g3;   // Global, any roles: (d_k, H, rows), box (64, 1, R)
+  CUtensorMap l4;   // Local, H = 128: (64, H, NCH chunks, rows), box (64, 128, NCH, 1)
+  CUtensorMap l3;   // Local, any H: (d_k, H, rows), box (64, H, 1)
 };
 
 inline cudaError_t make_qmaps(const rk_seg_attn_plan_s& p, const KernelArgs& a, const void* q,
                               QMaps& qm) {
   qm = QMaps{};
   const uint64_t H = static_cast<uint64_t>(p.H), rows = static_cast<uint64_t>(p.info.rows);
+  const uint64_t dk = static_cast<uint64_t>(p.d_nope + p.d_rope), rb = 2 * dk;  // row bytes
+  const uint32_t nch = static_cast<uint32_t>(p.d_nope / 64);
   const uint32_t R = static_cast<uint32_t>(a.rows_per_gtile > 0 ? a.rows_per_gtile : 8);
   if (a.g_ingroup >= 0) {  // the whole Global tile in one box
     const uint64_t G = H / 8;
-    const uint64_t dims[5] = {64, rows, G, 8, 8};
-    const uint64_t strides[4] = {H * 1152, 8 * 1152, 128, 1152};
-    const uint32_t box[5] = {64, R, static_cast<uint32_t>(G), 8, 1};
+    const uint64_t dims[5] = {64, rows, G, nch, 8};
+    const uint64_t strides[4] = {H * rb, 8 * rb, 128, rb};
+    const uint32_t box[5] = {64, R, static_cast<uint32_t>(G), nch, 1};
     if (!make_tmap_bf16(&qm.g5, q, 5, dims, strides, box)) return cudaErrorInvalidValue;
   }
   {
-    const uint64_t dims[3] = {576, H, rows};
-    const uint64_t strides[2] = {1152, H * 1152};
+    const uint64_t dims[3] = {dk, H, rows};
+    const uint64_t strides[2] = {rb, H * rb};
     const uint32_t boxg[3] = {64, 1, R};
     const uint32_t boxl[3] = {64, static_cast<uint32_t>(H), 1};
     if (!make_tmap_bf16(&qm.g3, q, 3, dims, strides, boxg)) return cudaErrorInvalidValue;
     if (!make_tmap_bf16(&qm.l3, q, 3, dims, strides, boxl)) return cudaErrorInvalidValue;
   }
   if (H == 128) {
-    const uint64_t dims[4] = {64, H, 8, rows};
-    const uint64_t strides[3] = {1152, 128, H * 1152};
-    const uint32_t box[4] = {64, static_cast<uint32_t>(H), 8, 1};
+    const uint64_t dims[4] = {64, H, nch, rows};
+    const uint64_t strides[3] = {rb, 128, H * rb};
+    const uint32_t box[4] = {64, static_cast<uint32_t>(H), nch, 1};
     if (!make_tmap_bf16(&qm.l4, q, 4, dims, strides, box)) return cudaErrorInvalidValue;
   }
   return cudaSuccess;
 }
 
-// Issue the TMA loads of tile t's queries (128 KB) into `qdst`.  PAIR: the
+// Issue the TMA loads of tile t's queries (NCH x 16 KB) into `qdst`, from
+// maps that make_qmaps built for a plan with d_nope = 64 NCH.  PAIR: the
 // copies complete on the barrier at cluster address `bar` (cta_group::2
 // form, the barrier may be the peer's); otherwise on this CTA's barrier at
 // shared address `bar`.
-template <bool PAIR>
+template <bool PAIR, int NCH = 8>
 __device__ __forceinline__ void load_q_tile(const KernelArgs& a, const QMaps& qm, const TcTile& t,
                                             const DevReq& rq, uint32_t qdst, uint32_t bar) {
   auto ld3 = [&](uint32_t dst, const CUtensorMap* m, int32_t x, int32_t y, int32_t z) {
@@ -345,7 +390,7 @@ __device__ __forceinline__ void load_q_tile(const KernelArgs& a, const QMaps& qm
         tc::tma_load_5d_u32(qdst, &qm.g5, bar, 0, fr, 0, 0, a.g_ingroup);
     } else {
       const int R = a.rows_per_gtile;
-      for (int ch = 0; ch < 8; ++ch)
+      for (int ch = 0; ch < NCH; ++ch)
         for (int hi = 0; hi < a.num_global; ++hi)
           ld3(qdst + ch * 16384 + hi * R * 128, &qm.g3, 64 * ch, a.global_heads[hi], fr);
     }
@@ -357,7 +402,7 @@ __device__ __forceinline__ void load_q_tile(const KernelArgs& a, const QMaps& qm
       tc::tma_load_4d_u32(qdst, &qm.l4, bar, 0, 0, 0, fr);
   } else {
     const int rows_per = 128 / a.H;
-    for (int ch = 0; ch < 8; ++ch)
+    for (int ch = 0; ch < NCH; ++ch)
       for (int ri = 0; ri < rows_per; ++ri) {
         const int pr = (ri == 0 || t.p1 < 0) ? t.p0 : t.p1;
         const int32_t fr = static_cast<int32_t>(rq.row_base + (pr - rq.q_row_begin));

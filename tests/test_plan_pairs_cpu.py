@@ -93,14 +93,14 @@ def test_pairs_cover_tiles_and_skip_only_unneeded_segments(name):
     if name == "ctx16k":
         assert skipped_any, "Local pairs far from the sink skip segments"
     # the side kernel's share: the pairs of at most 8 key tiles at the end of
-    # the list (the rotary-value kernel has no side kernel)
+    # the list
     tail = 0
     for cst in reversed(costs):
         if cst > 8:
             break
         tail += 1
-    assert plan.info["side_pairs"] == (0 if wl.v_rope else tail)
-    if not wl.v_rope and name in ("ctx16k", "ctx128k_mini", "flash_mini"):
+    assert plan.info["side_pairs"] == tail
+    if name in ("ctx16k", "ctx128k_mini", "flash_mini", "ctx128k_vrope_mini"):
         assert tail > 0, "Local pairs are short"
 
 
