@@ -311,19 +311,17 @@ def bench_prefill(args, ws, local, pk):
         h_lat = torch.empty(wl.latent_pool.shape, dtype=wl.latent_pool.dtype, pin_memory=True)
         h_lat.copy_(wl.latent_pool)
         torch.cuda.synchronize(dev)
-        # in: lse, the latents and the queries the kernels read (the Global
-        # heads of every row, one strided copy per row range, and the whole
-        # protected rows); out is not uploaded (no kernel reads it).  Out:
-        # lse and the written elements of out, copied the same way.  The
-        # Global heads of protected rows travel twice (strided copy and
-        # whole row) and are counted twice.
-        q_head = wl.d_k * h_q.element_size()
+        # in: q, lse and the latents (out is not uploaded: no kernel reads
+        # it).  Out: lse and the written elements of out: the Global heads of
+        # every row (one strided copy per row range) and the whole protected
+        # rows, so the Global heads of protected rows travel twice and are
+        # counted twice
+        h2d = sum(t.numel() * t.element_size() for t in (h_q, h_lse, h_lat))
         o_head = wl.d_v * out.element_size()
         if info["num_local_heads"]:
             heads = info["protected_local_rows"] * wl.H + info["rows"] * info["num_global_heads"]
         else:
             heads = info["rows"] * wl.H
-        h2d = heads * q_head + sum(t.numel() * t.element_size() for t in (h_lse, h_lat))
         d2h = heads * o_head + lse.numel() * lse.element_size()
         steps = max(1, min(args.steps, 3))
         # one untimed pass: the first device reads of freshly written host

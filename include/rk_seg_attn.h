@@ -259,9 +259,7 @@ rk_status_t rk_seg_attn_forward(rk_seg_attn_plan_t plan, const void* q, void* ou
 /* The same forward with q, out and lse starting and ending in host memory:
  * the copies to and from the device run inside the call, overlapped with
  * the kernels.  The computed rows are taken in eight consecutive ranges;
- * a range's lse rows and the part of its q rows that the kernels read (the
- * Global heads of every row and the whole protected rows, or every row when
- * all heads are Global) are copied in on a plan-owned stream, its tiles
+ * a range's q and lse rows are copied in on a plan-owned stream, its tiles
  * run as soon as it (and every earlier range) is on the device, alternately
  * on `stream` and on a second plan-owned stream,
  * and its results are copied back on a third plan-owned stream once the
@@ -276,8 +274,7 @@ rk_status_t rk_seg_attn_forward(rk_seg_attn_plan_t plan, const void* q, void* ou
  *            lse.  Page-locked memory lets the copies overlap; pageable
  *            memory is accepted and is copied synchronously.
  * q, out, lse device arrays of the full sizes (as for rk_seg_attn_forward);
- *            lse and the read part of q are overwritten with the host
- *            contents first (q's other elements are left as they were); out
+ *            q and lse are overwritten with the host contents first; out
  *            receives the written elements, its other elements are left
  *            unspecified.
  * workspace  as for rk_seg_attn_forward.

@@ -906,68 +906,20 @@ extern "C" rk_status_t rk_seg_attn_forward_host(rk_seg_attn_plan_t p, const void
   char* qd = static_cast<char*>(q);
   char* od = static_cast<char*>(out);
   char* ld = reinterpret_cast<char*>(lse);
-  const int HG = static_cast<int>(p->global_heads.size());
-  const bool all_global = p->local_heads.empty();
-  // Global heads c0 + s g (g < H / s) are one strided copy per range;
-  // otherwise one copy per run of consecutive Global heads
-  int gstride = 0;
-  if (HG > 0 && !all_global && p->H % HG == 0) {
-    const int sdiv = p->H / HG;
-    bool ev = p->global_heads[0] < sdiv;
-    for (int g = 0; g < HG && ev; ++g) ev = p->global_heads[g] == p->global_heads[0] + sdiv * g;
-    if (ev) gstride = sdiv;
-  }
-  // The Global heads of rows [r0, r1) (bytes `hb` per head, `rb` per row)
-  // between host and device, then whole rows for the protected ones, from
-  // full-row run `run` on (advanced past the runs that end in the range).
-  auto heads_and_full_rows = [&](char* dst, const char* src, size_t rb, size_t hb, int64_t r0,
-                                 int64_t r1, size_t& run, cudaMemcpyKind kind, cudaStream_t cs) {
-    const int64_t n = r1 - r0;
-    bool g = true;
-    if (gstride > 0) {
-      const size_t off = r0 * rb + p->global_heads[0] * hb;
-      g = ok(cudaMemcpy2DAsync(dst + off, gstride * hb, src + off, gstride * hb, hb,
-                               static_cast<size_t>(n) * HG, kind, cs));
-    } else {
-      for (int k = 0; k < HG && g;) {
-        int e = k + 1;
-        while (e < HG && p->global_heads[e] == p->global_heads[e - 1] + 1) ++e;
-        const size_t off = r0 * rb + p->global_heads[k] * hb;
-        g = ok(cudaMemcpy2DAsync(dst + off, rb, src + off, rb, (e - k) * hb, static_cast<size_t>(n),
-                                 kind, cs));
-        k = e;
-      }
-    }
-    while (g && run < p->full_rows.size() && p->full_rows[run].first < r1) {
-      const int64_t f0 = std::max(r0, p->full_rows[run].first);
-      const int64_t f1 = std::min(r1, p->full_rows[run].second);
-      if (f1 > f0) g = ok(cudaMemcpyAsync(dst + f0 * rb, src + f0 * rb, (f1 - f0) * rb, kind, cs));
-      if (p->full_rows[run].second > r1) break;  // continues in the next range
-      ++run;
-    }
-    return g;
-  };
   // the copies start after the caller's earlier work on s
   bool good = ok(cudaEventRecord(p->ev_start, s)) &&
               ok(cudaStreamWaitEvent(p->copy_in, p->ev_start, 0)) &&
               ok(cudaStreamWaitEvent(p->copy_out, p->ev_start, 0));
-  size_t qrun = 0;  // first run of full rows whose queries are not yet copied
   for (int c = 0; c < NC && good; ++c) {
     int64_t r0, r1;
     range(c, r0, r1);
     if (r1 > r0) {
-      // q and lse go in; out does not (no kernel reads it).  Of q only what
-      // the kernels read: the Global heads of every row and the whole
-      // protected rows (a Local tile reads every head of its rows)
+      // q and lse go in; out does not (no kernel reads it)
       const int64_t n = r1 - r0;
-      good = ok(cudaMemcpyAsync(ld + r0 * lrow, lh + r0 * lrow, n * lrow, cudaMemcpyHostToDevice,
+      good = ok(cudaMemcpyAsync(qd + r0 * qrow, qh + r0 * qrow, n * qrow, cudaMemcpyHostToDevice,
+                                p->copy_in)) &&
+             ok(cudaMemcpyAsync(ld + r0 * lrow, lh + r0 * lrow, n * lrow, cudaMemcpyHostToDevice,
                                 p->copy_in));
-      if (all_global)
-        good = good && ok(cudaMemcpyAsync(qd + r0 * qrow, qh + r0 * qrow, n * qrow,
-                                          cudaMemcpyHostToDevice, p->copy_in));
-      else
-        good = good && heads_and_full_rows(qd, qh, qrow, qrow / H, r0, r1, qrun,
-                                           cudaMemcpyHostToDevice, p->copy_in);
     }
     good = good && ok(cudaEventRecord(p->ev_in[c], p->copy_in));
   }
@@ -1015,7 +967,18 @@ extern "C" rk_status_t rk_seg_attn_forward_host(rk_seg_attn_plan_t p, const void
   // head is written (protected rows; every row when all heads are Global)
   // and the Global heads' columns of the other rows; the host keeps the rest
   // of out_host as it was.  lse comes back whole (it went in whole).
+  const int HG = static_cast<int>(p->global_heads.size());
+  const bool all_global = p->local_heads.empty();
   const size_t hbytes = static_cast<size_t>(p->d_v) * 2;
+  // Global heads c0 + s g (g < H / s) are one strided copy per range;
+  // otherwise one copy per run of consecutive Global heads
+  int gstride = 0;
+  if (HG > 0 && !all_global && p->H % HG == 0) {
+    const int sdiv = p->H / HG;
+    bool ev = p->global_heads[0] < sdiv;
+    for (int g = 0; g < HG && ev; ++g) ev = p->global_heads[g] == p->global_heads[0] + sdiv * g;
+    if (ev) gstride = sdiv;
+  }
   size_t run = 0;  // first run of full rows not yet copied
   // range c is final once the kernels of ranges c and c + 1 (and any split
   // chunks) are done
@@ -1034,8 +997,30 @@ extern "C" rk_status_t rk_seg_attn_forward_host(rk_seg_attn_plan_t p, const void
                                         cudaMemcpyDeviceToHost, p->copy_out));
       continue;
     }
-    good = good && heads_and_full_rows(oh, od, orow, hbytes, r0, r1, run, cudaMemcpyDeviceToHost,
-                                       p->copy_out);
+    if (good && gstride > 0) {
+      const size_t off = r0 * orow + p->global_heads[0] * hbytes;
+      good = ok(cudaMemcpy2DAsync(oh + off, gstride * hbytes, od + off, gstride * hbytes, hbytes,
+                                  static_cast<size_t>(n) * HG, cudaMemcpyDeviceToHost,
+                                  p->copy_out));
+    } else {
+      for (int g = 0; g < HG && good;) {
+        int e = g + 1;
+        while (e < HG && p->global_heads[e] == p->global_heads[e - 1] + 1) ++e;
+        const size_t off = r0 * orow + p->global_heads[g] * hbytes;
+        good = ok(cudaMemcpy2DAsync(oh + off, orow, od + off, orow, (e - g) * hbytes,
+                                    static_cast<size_t>(n), cudaMemcpyDeviceToHost, p->copy_out));
+        g = e;
+      }
+    }
+    while (good && run < p->full_rows.size() && p->full_rows[run].first < r1) {
+      const int64_t f0 = std::max(r0, p->full_rows[run].first);
+      const int64_t f1 = std::min(r1, p->full_rows[run].second);
+      if (f1 > f0)
+        good = ok(cudaMemcpyAsync(oh + f0 * orow, od + f0 * orow, (f1 - f0) * orow,
+                                  cudaMemcpyDeviceToHost, p->copy_out));
+      if (p->full_rows[run].second > r1) break;  // continues in the next range
+      ++run;
+    }
   }
   // the caller's stream resumes when everything is back on the host
   good = good && ok(cudaEventRecord(p->ev_done, p->copy_out)) &&
