@@ -15,16 +15,21 @@
 // find the queue empty.
 //
 // A CTA pair holds its two tiles' queries in shared memory (rank r: tile r's
-// 128 lanes x 512 nope dims, loaded once per pair) and computes the output
+// 128 lanes x the nope dims, loaded once per pair) and computes the output
 // one half of d_v per pass over the keys, so the scores are computed twice.
 // The arithmetic is the 4-CTA kernel's step for step, so that a pair's
 // outputs do not depend on which kernel took it: the score chain S = Q K^T
 // (M = 256, N = 128: 64 keys from each CTA's shared memory) takes the rope
-// chunk's q_rope' hi and lo parts first and then the eight nope chunks in
-// order, the query turning by -delta at each segment of the key walk
-// (RedKnot-MLA paper, RoPE-orthogonality paragraph); the online softmax is
-// the shared one; O += P V runs per 16 keys in key order after the rescale;
-// the epilogue divides by the same running sum.
+// chunk's q_rope' hi and lo parts first and then the nope chunks in order,
+// the query turning by -delta at each segment of the key walk (RedKnot-MLA
+// paper, RoPE-orthogonality paragraph); the online softmax is the shared
+// one; O += P V runs per 16 keys in key order after the rescale; the
+// epilogue divides by the same running sum.  Two instantiations, as for the
+// 4-CTA kernel: (d_nope, d_rope) = (512, 64) with V = c_nope, and (448, 64)
+// with V = the whole latent row, whose rope columns (the last 64 of the
+// second half) turn into each new segment's frame at a switch and get the
+// output phase restored in the epilogue (RedKnot-MLA paper: R^-1 in the
+// head-partition paragraph) by the 4-CTA kernel's own helpers.
 // Tensor memory per CTA: O (256 columns) | S (128) | P (64) | q_rope' hi
 // (32) | lo (32).  Every wait is bounded in time; on expiry the CTA records
 // RK_ERR_DEVICE_TIMEOUT, every CTA of both kernels stops, the leader waits
