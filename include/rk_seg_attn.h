@@ -249,9 +249,15 @@ size_t rk_seg_attn_workspace_bytes(rk_seg_attn_plan_t plan);
  *            16-byte aligned (may be NULL when that is 0); its contents on
  *            entry are irrelevant.  Forwards that share a workspace must be
  *            ordered on one stream.
- * Asynchronous on `stream`.  Errors: RK_ERR_NULL, RK_ERR_ALIGNMENT,
- * RK_ERR_WORKSPACE, RK_ERR_PLAN_MISMATCH, RK_ERR_CUDA (launch failure).
- * Device-side wait expiries are reported by rk_seg_attn_last_device_status. */
+ * Asynchronous on `stream`.  A forward with split decode rows beside
+ * prefill tiles, or with the side kernel beside the 4-CTA clusters, forks
+ * part of its work onto a plan-owned stream (recorded events order it after
+ * the work queued on `stream` before the call, and `stream` continues only
+ * after it); forwards on one plan issued from several host threads at once
+ * may therefore wait for one another there.  Errors: RK_ERR_NULL,
+ * RK_ERR_ALIGNMENT, RK_ERR_WORKSPACE, RK_ERR_PLAN_MISMATCH, RK_ERR_CUDA
+ * (launch failure).  Device-side wait expiries are reported by
+ * rk_seg_attn_last_device_status. */
 rk_status_t rk_seg_attn_forward(rk_seg_attn_plan_t plan, const void* q, void* out,
                                 float* lse, void* workspace, size_t workspace_bytes,
                                 void* stream);
