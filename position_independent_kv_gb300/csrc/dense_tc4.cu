@@ -551,6 +551,11 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
             tc::tc_fence_before();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive_cluster(cbar(B_SFREE + b, 0));
+            // the landed-halves count, read before the softmax: the halves of
+            // tile j - 1 have usually landed by then, and the wait below then
+            // needs only its acquire fence (the rotary-value kernel, at its
+            // register limit, polls after the softmax only)
+            const uint32_t landed = (!VROPE && issuer) ? tc::ld_relaxed_cluster_u32(&misc[2]) : 0u;
 
             // scores are scaled inside the exponent: x = s * scale * log2(e)
             alpha = tt::softmax_tile(s, kt, ri, sink, window, sl2, m_run, l_run);
@@ -561,7 +566,12 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
             // copy (half k - 3) must have landed: a shared::cta ->
             // shared::cluster bulk copy completes on the receiver's barrier
             // only, so the output CTA counts the halves that have landed
-            if (okw && issuer && j > 0) okw = wait_count(c, &misc[2], static_cast<uint32_t>(2 * j - 1));
+            if (okw && issuer && j > 0) {
+              if (!VROPE && landed >= static_cast<uint32_t>(2 * j - 1))
+                tc::fence_acquire_cluster_smem();
+              else
+                okw = wait_count(c, &misc[2], static_cast<uint32_t>(2 * j - 1));
+            }
           }
           ok = tc::named_and(1, 128, okw);
           if (!ok) break;
